@@ -1,0 +1,170 @@
+"""Plant plausible mistakes in the oracle and check that some pin catches each.
+
+Each mutation replaces one oracle function (on the CPU, for the duration of one
+test) with a subtly wrong version: a dropped term, a wrong sign or index, a
+transposed operand. The pins in test_oracle_pins.py must then fail.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.dflash_oracle as od
+from tests import test_oracle_pins as pins
+
+
+def _patch(monkeypatch, name, fn):
+    monkeypatch.setattr(od, name, fn)
+    monkeypatch.setattr(oracle, name, fn)
+
+
+def _expect_failure(test_fn):
+    with pytest.raises(AssertionError):
+        test_fn()
+
+
+def test_rope_sign_error_is_caught(monkeypatch):
+    def bad(x, positions, base):
+        n, _, d = x.shape
+        ang = od.rope_angles(positions, d, base)
+        c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+        lo, hi = x[..., : d // 2], x[..., d // 2:]
+        return np.concatenate([lo * c + hi * s, hi * c - lo * s], axis=-1)
+    _patch(monkeypatch, "apply_rope", bad)
+    _expect_failure(pins.test_rope_matches_complex_rotation)
+    _expect_failure(pins.test_draft_pass_matches_scalar_brute_force)
+
+
+def test_rope_interleaved_pairing_is_caught(monkeypatch):
+    def bad(x, positions, base):
+        n, _, d = x.shape
+        ang = od.rope_angles(positions, d, base)
+        c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+        ev, odd = x[..., 0::2], x[..., 1::2]
+        out = np.empty_like(x)
+        out[..., 0::2] = ev * c - odd * s
+        out[..., 1::2] = odd * c + ev * s
+        return out
+    _patch(monkeypatch, "apply_rope", bad)
+    _expect_failure(pins.test_rope_matches_complex_rotation)
+
+
+def test_gqa_head_mapping_error_is_caught(monkeypatch):
+    orig = od.block_attention
+
+    def bad(q, k, v, return_probs=False):
+        n_kv = k.shape[1]
+        g = q.shape[1] // n_kv
+        perm = [h % n_kv for h in range(q.shape[1])]  # modulo instead of integer division
+        kk = k[:, perm, :]
+        vv = v[:, perm, :]
+        return orig(q, kk, vv, return_probs) if g > 1 else orig(q, k, v, return_probs)
+    _patch(monkeypatch, "block_attention", bad)
+    _expect_failure(pins.test_attention_matches_explicit_loops)
+
+
+def test_missing_attention_scale_is_caught(monkeypatch):
+    orig = od.block_attention
+
+    def bad(q, k, v, return_probs=False):
+        return orig(q * math.sqrt(q.shape[-1]), k, v, return_probs)
+    _patch(monkeypatch, "block_attention", bad)
+    _expect_failure(pins.test_attention_matches_explicit_loops)
+
+
+def test_dropped_ffn_residual_is_caught(monkeypatch):
+    def bad(x, layer, k_ctx, v_ctx, pos0, shape):
+        B = x.shape[0]
+        nq, nkv, d = shape.n_heads, shape.n_kv_heads, shape.head_dim
+        pos = pos0 + np.arange(B)
+        h = od.rms_norm(x, layer["g_attn"], shape.rms_eps)
+        q = od.apply_rope((h @ layer["w_q"].T).reshape(B, nq, d), pos, shape.rope_base)
+        k = od.apply_rope((h @ layer["w_k"].T).reshape(B, nkv, d), pos, shape.rope_base)
+        v = (h @ layer["w_v"].T).reshape(B, nkv, d)
+        a = od.block_attention(q, np.concatenate([k_ctx, k]), np.concatenate([v_ctx, v])).reshape(B, nq * d)
+        x = x + a @ layer["w_o"].T
+        h2 = od.rms_norm(x, layer["g_ffn"], shape.rms_eps)
+        return (od.silu(h2 @ layer["w_gate"].T) * (h2 @ layer["w_up"].T)) @ layer["w_down"].T
+    _patch(monkeypatch, "decoder_layer", bad)
+    _expect_failure(pins.test_decoder_B1_C0_is_a_single_step)
+
+
+def test_transposed_output_projection_is_caught(monkeypatch):
+    orig = od.decoder_layer
+
+    def bad(x, layer, k_ctx, v_ctx, pos0, shape):
+        lw = dict(layer)
+        lw["w_o"] = layer["w_o"].T.copy()
+        return orig(x, lw, k_ctx, v_ctx, pos0, shape)
+    _patch(monkeypatch, "decoder_layer", bad)
+    _expect_failure(pins.test_decoder_B1_C0_is_a_single_step)
+
+
+def test_swapped_gate_and_up_is_caught(monkeypatch):
+    orig = od.decoder_layer
+
+    def bad(x, layer, k_ctx, v_ctx, pos0, shape):
+        lw = dict(layer)
+        lw["w_gate"], lw["w_up"] = layer["w_up"], layer["w_gate"]
+        return orig(x, lw, k_ctx, v_ctx, pos0, shape)
+    _patch(monkeypatch, "decoder_layer", bad)
+    _expect_failure(pins.test_decoder_B1_C0_is_a_single_step)
+
+
+def test_fusion_without_norm_is_caught(monkeypatch):
+    def bad(feats, w_c, g_c, eps):
+        return (feats @ w_c.T) * g_c
+    _patch(monkeypatch, "fuse_features", bad)
+    _expect_failure(pins.test_draft_pass_matches_scalar_brute_force)
+
+
+def test_causal_mask_is_caught(monkeypatch):
+    """A causal block (mask positions blind to later positions) is not the
+    non-causal attention the pages describe."""
+    def bad(q, k, v, return_probs=False):
+        B, n_q, d = q.shape
+        T = k.shape[0]
+        g = n_q // k.shape[1]
+        out = np.empty_like(q)
+        for h in range(n_q):
+            s = q[:, h, :] @ k[:, h // g, :].T / math.sqrt(d)
+            for b in range(B):
+                s[b, T - B + b + 1:] = -np.inf
+            s = s - s.max(-1, keepdims=True)
+            p = np.exp(s)
+            p /= p.sum(-1, keepdims=True)
+            out[:, h, :] = p @ v[:, h // g, :]
+        return out
+    _patch(monkeypatch, "block_attention", bad)
+    _expect_failure(pins.test_draft_pass_matches_scalar_brute_force)
+
+
+def test_verify_off_by_one_is_caught(monkeypatch):
+    def bad(drafts, targets):
+        B = len(targets)
+        a = 0
+        while a < B - 1 and int(drafts[a]) == int(targets[a + 1]):
+            a += 1
+        return a + 1, int(targets[a])
+    _patch(monkeypatch, "verify_block", bad)
+    _expect_failure(pins.test_verify_bruteforce_tiny_vocab)
+
+
+def test_verify_without_bonus_is_caught(monkeypatch):
+    def bad(drafts, targets):
+        B = len(targets)
+        a = 0
+        while a < B - 1 and int(drafts[a]) == int(targets[a]):
+            a += 1
+        return max(a, 1), int(targets[a])
+    _patch(monkeypatch, "verify_block", bad)
+    _expect_failure(pins.test_verify_bruteforce_tiny_vocab)
+
+
+def test_mean_len_without_bonus_is_caught(monkeypatch):
+    def bad(accepted, generated, drafts_per_cycle):
+        cycles = generated / drafts_per_cycle
+        return accepted / generated, accepted / cycles
+    _patch(monkeypatch, "acceptance_stats", bad)
+    _expect_failure(pins.test_worked_numbers_from_the_pages)
