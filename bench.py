@@ -1,0 +1,483 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash drafter pass on GB300.
+
+One step is one speculative cycle of the hot path on the Qwen3-8B-shaped
+drafter (5 layers, hidden 4096, 32/8 heads of 128, SwiGLU 12288, vocab 151936,
+5 fused target layers), block B = 16:
+
+  1. dflash_rows_argmax_bf16  target ids = argmax of the target's block logits
+  2. dflash_fuse_ctx          fuse the block's target features, inject K/V (pending)
+  3. dflash_verify            greedy acceptance of the previous drafts, commit/rollback
+  4. dflash_draft             the drafter pass for the next block (anchor = bonus)
+
+The metric is draft-block passes per second (one pass per step). Weights,
+features and logits are synthetic and seeded; every step streams 3.4 GB of
+weights, far more than the 129 MB L2, so no L2 flush is needed.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--block B]
+Under torchrun (N > 1) every rank runs an independent replica (the drafter
+pass has no exchange step) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft-block passes/sec (8B-shaped drafter, B=16) and % of HBM/tensor roofline"
+UNIT = "passes/s"
+
+# name -> (batch, context, context spread (lo, hi) or None)
+WORKLOADS = {
+    "qwen3_8b_b1_ctx4096": (1, 4096, None),
+    "qwen3_8b_b1_ctx32768": (1, 32768, None),
+    "qwen3_8b_b1_ctx262144": (1, 262144, None),
+    "qwen3_8b_b32_ctx1k_8k": (32, None, (1024, 8192)),
+}
+GEMM_CLASSES = ("qkv", "o", "gateup", "down", "lmhead", "fuse_wc", "fuse_kv")
+
+
+# ----------------------------------------------------------------------------
+# ranks
+# ----------------------------------------------------------------------------
+
+def dist_setup(backend: str):
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return rank, local, world
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(steps_per_rank: int, world: int, max_ms: float) -> float:
+    """Weak scaling: every rank runs `steps_per_rank` passes; the job's rate is
+    all passes over the slowest rank's time."""
+    return steps_per_rank * world / (max_ms / 1000.0)
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def gemm_source_hash() -> str:
+    p = os.path.join(ROOT, "block_diffusion_drafter_pass_gb300", "csrc", "gemm_tc.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per step of the projection GEMMs from a committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    try:
+        t = json.load(open(p))
+    except (OSError, ValueError):
+        return None
+    if t.get("gemm_source_hash") != gemm_source_hash():
+        return None
+    return t.get("per_workload", {}).get(workload)
+
+
+class Cycle:
+    """Device-resident inputs and outputs of the benchmarked speculative cycle."""
+
+    def __init__(self, dfl, shape, batch, ctx_lens, B, steps_total, seed, dev, max_fuse=4096):
+        import torch
+        from synth import make_weights_torch
+        self.torch = torch
+        self.dfl = dfl
+        self.shape = shape
+        self.B = B
+        self.dev = dev
+        self.seqs = list(range(batch))
+        width = shape.n_feat_layers * shape.hidden
+        self.weights = make_weights_torch(shape, seed=seed, device=dev)
+        max_ctx = max(ctx_lens) + steps_total * B + 2 * B + 64
+        pages = sum((c + steps_total * B + 2 * B + 63) // 64 + 1 for c in ctx_lens)
+        self.d = dfl.Drafter(shape, self.weights, max_seqs=batch, max_batch=batch, max_block=B,
+                             max_ctx=max_ctx, max_pages=pages, max_fuse_tokens=max_fuse)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed + 1)
+        # fill every sequence's committed context, one chunk at a time
+        for s, c in enumerate(ctx_lens):
+            done = 0
+            while done < c:
+                n = min(max_fuse, c - done)
+                f = torch.randn(n, width, generator=g, device=dev).to(torch.bfloat16)
+                self.d.fuse_ctx([s], [n], f, pending=False)
+                done += n
+                del f
+        # per-step inputs: a ring larger than L2
+        per_step = batch * B * (width + shape.vocab) * 2
+        self.ring = max(4, min(steps_total, math.ceil(400e6 / per_step)))
+        self.feats = torch.randn(self.ring, batch * B, width, generator=g, device=dev).to(torch.bfloat16)
+        logits = torch.empty(self.ring, batch * B, shape.vocab, device=dev, dtype=torch.float32)
+        logits.normal_(0.0, 3.0, generator=g)
+        self.logits = logits.to(torch.bfloat16)
+        del logits
+        self.targets = torch.empty(batch, B, dtype=torch.int32, device=dev)
+        self.drafts = torch.empty(batch, B - 1, dtype=torch.int32, device=dev)
+        self.tau = torch.empty(batch, dtype=torch.int32, device=dev)
+        self.bonus = torch.randint(0, shape.vocab - 1, (batch,), generator=g, device=dev, dtype=torch.int32)
+        torch.cuda.synchronize()
+        # first block so that step 0 has drafts to verify
+        self.d.draft(self.seqs, self.bonus, B, out=self.drafts)
+        torch.cuda.synchronize()
+
+    def step(self, k: int) -> None:
+        r = k % self.ring
+        self.dfl.dflash_rows_argmax_bf16(self.logits[r], out=self.targets.view(-1))
+        self.d.fuse_ctx(self.seqs, [self.B] * len(self.seqs), self.feats[r], pending=True)
+        self.d.verify(self.seqs, self.B, self.drafts, self.targets, tau=self.tau, bonus=self.bonus)
+        self.d.draft(self.seqs, self.bonus, self.B, out=self.drafts)
+
+    def step_e2e(self, k: int, host) -> None:
+        """The same cycle through the public API with host buffers: inputs are
+        copied from pinned host memory, results read back to it."""
+        r = k % host["ring"]
+        self.feats[0].copy_(host["feats"][r], non_blocking=True)
+        self.logits[0].copy_(host["logits"][r], non_blocking=True)
+        self.dfl.dflash_rows_argmax_bf16(self.logits[0], out=self.targets.view(-1))
+        self.d.fuse_ctx(self.seqs, [self.B] * len(self.seqs), self.feats[0], pending=True)
+        self.d.verify(self.seqs, self.B, self.drafts, self.targets, tau=self.tau, bonus=self.bonus)
+        self.d.draft(self.seqs, self.bonus, self.B, out=self.drafts)
+        host["drafts"].copy_(self.drafts, non_blocking=True)
+        host["tau"].copy_(self.tau, non_blocking=True)
+        host["bonus"].copy_(self.bonus, non_blocking=True)
+
+
+def timed(fn, K, world, dev):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(K):
+        fn(k)
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def cpu_baseline(shape, weights_dev, ctx_len: int, B: int, budget_s: float = 20.0):
+    """The oracle as it stands, timed on this host's cores on a bounded
+    sample: full speculative cycles (fuse B features, verify, draft) of the
+    same drafter at the same context length, until `budget_s` has passed."""
+    import numpy as np
+    import oracle
+    from synth import torch_weights_to_np
+    wn = torch_weights_to_np(weights_dev)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    rng = np.random.Generator(np.random.PCG64(7))
+    st = orc._state(0)
+    for l in range(shape.n_layers):   # synthetic committed context (an input, not computed)
+        st["k"][l] = rng.standard_normal((ctx_len, shape.n_kv_heads, shape.head_dim), dtype=np.float32)
+        st["v"][l] = rng.standard_normal((ctx_len, shape.n_kv_heads, shape.head_dim), dtype=np.float32)
+    st["len"] = ctx_len
+    width = shape.n_feat_layers * shape.hidden
+    drafts = np.zeros((1, B - 1), dtype=np.int64)
+    anchor = [1]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        f = rng.standard_normal((B, width), dtype=np.float32)
+        t = rng.integers(0, shape.vocab, size=(1, B))
+        orc.fuse_ctx([0], [B], f, pending=True)
+        _, bonus = orc.verify([0], B, drafts, t)
+        drafts = orc.draft([0], bonus, B)[0]["draft"][None, :]
+        n += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or n >= 50:
+            break
+    return {"value": n / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} full cycles (fuse {B} features + verify + draft, 5 layers, context {ctx_len}, "
+                      f"fp32 numpy) in {el:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    import block_diffusion_drafter_pass_gb300 as dfl
+    from synth import QWEN3_8B, make_serving_lengths
+    rank, local, world = dist_setup("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if local == 0:   # one builder per node; the other ranks wait for it
+        from block_diffusion_drafter_pass_gb300 import _build
+        _build.build()
+    barrier(world)
+    dfl.load_library()
+    batch, ctx, spread = WORKLOADS[args.workload]
+    B = args.block
+    K, W = args.steps, args.warmup
+    total_steps = W + 3 * K + 8
+    if spread:
+        lens = [int(x) for x in make_serving_lengths(batch, spread[0], spread[1], seed=0)]
+    else:
+        lens = [ctx] * batch
+    # start short of the nominal length so the timed region is centred on it
+    start_lens = [max(0, c - W - K // 2) for c in lens]
+    cyc = Cycle(dfl, QWEN3_8B, batch, start_lens, B, total_steps, seed=1000 * rank, dev=dev)
+
+    for k in range(W):
+        cyc.step(k)
+    with ClockSampler(local) as clk:
+        ms = timed(cyc.step, K, world, dev)
+    clocks = clk.summary()
+    max_ms = reduce_max(ms, world, dev)
+    value = whole_job_rate(K, world, max_ms)
+
+    # second pass of K steps with every launch event-timed: per-kernel roofline
+    cyc.d.profile_read()
+    cyc.d.profile(True)
+    ms_prof = timed(lambda k: cyc.step(W + K + k), K, world, dev)
+    cyc.d.profile(False)
+    stats = cyc.d.profile_read()
+
+    # end to end through the public API with pinned host buffers
+    ring = min(16, cyc.ring)
+    host = {
+        "ring": ring,
+        "feats": cyc.feats[:ring].cpu().pin_memory(),
+        "logits": cyc.logits[:ring].cpu().pin_memory(),
+        "drafts": torch.empty_like(cyc.drafts, device="cpu").pin_memory(),
+        "tau": torch.empty_like(cyc.tau, device="cpu").pin_memory(),
+        "bonus": torch.empty_like(cyc.bonus, device="cpu").pin_memory(),
+    }
+    ms_e2e = timed(lambda k: cyc.step_e2e(k, host), K, world, dev)
+    e2e_value = whole_job_rate(K, world, reduce_max(ms_e2e, world, dev))
+    h2d = host["feats"][0].numel() * 2 + host["logits"][0].numel() * 2
+    d2h = (host["drafts"].numel() + host["tau"].numel() + host["bonus"].numel()) * 4
+    len_end = cyc.d.seq_len(0)[0]
+
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    g_ms = sum(stats[c]["ms"] for c in GEMM_CLASSES)
+    g_bytes = sum(stats[c]["bytes"] for c in GEMM_CLASSES)
+    g_launch = sum(stats[c]["launches"] for c in GEMM_CLASSES)
+    achieved = g_bytes / (g_ms / 1e3) / 1e9 if g_ms > 0 else None
+    traffic = ncu_traffic(args.workload)
+    kernels = {}
+    for name, s in stats.items():
+        if not s["launches"]:
+            continue
+        t = s["ms"] / 1e3
+        kernels[name] = {"launches_per_step": s["launches"] / K, "us_per_step": 1e3 * s["ms"] / K,
+                         "share": s["ms"] / ms_prof if ms_prof else None,
+                         "GB_per_step": s["bytes"] / K / 1e9,
+                         "GBps": s["bytes"] / t / 1e9 if t else None,
+                         "TFLOPs": s["flops"] / t / 1e12 if t else None}
+    launches_per_step = sum(s["launches"] for s in stats.values()) / K + 1   # + rows_argmax
+    step_bytes = sum(s["bytes"] for s in stats.values()) / K + batch * B * (QWEN3_8B.vocab * 2 + 4)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) features, N(0,3) target logits)",
+        "config": {"workload": args.workload, "model": "Qwen3-8B-shaped DFlash drafter (5 layers, H 4096, "
+                   "32/8 heads x 128, FFN 12288, V 151936, 5 fused target layers)",
+                   "batch_per_gpu": batch, "block": B,
+                   "context": ctx if ctx else f"U[{spread[0]}, {spread[1]}]",
+                   "context_at_timed_start": start_lens[0] + W, "context_at_end": len_end,
+                   "global_batch": batch * world, "parallelism": f"replicas x{world}",
+                   "step": "rows_argmax(target logits) + fuse_ctx(B, pending) + verify + draft",
+                   "l2": "no flush: each step streams 3.4 GB of weights (> 129 MB L2)"},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(round(launches_per_step * K)),
+        "roofline": {"bound": "hbm", "kernel": "gemm_kernel (all projection launches)",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"] if achieved else None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": g_bytes / g_launch if g_launch else None,
+                     "avg_launch_us": 1e3 * g_ms / g_launch if g_launch else None,
+                     "timing": "CUDA events around every launch on its stream, over a second pass of K steps"},
+        "step_hbm_frac": step_bytes / (max_ms / K / 1e3) / 1e9 / peaks["hbm_gbs"],
+        "step_algorithmic_GB": step_bytes / 1e9,
+        "profiled_ms_per_step": ms_prof / K,
+        "kernels": kernels,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(QWEN3_8B, cyc.weights, lens[0] if batch == 1 else lens[0], B)
+    return out
+
+
+def run_reference(args):
+    """The oracle as it stands, on this host's cores, on the same workload."""
+    import numpy as np
+    import oracle
+    from synth import QWEN3_8B, make_weights_np, make_serving_lengths
+    rank, _, world = dist_setup("gloo")
+    if rank != 0:
+        return None
+    batch, ctx, spread = WORKLOADS[args.workload]
+    B = args.block
+    shape = QWEN3_8B
+    lens = [int(x) for x in make_serving_lengths(batch, *spread, seed=0)] if spread else [ctx] * batch
+    seqs = list(range(batch))
+    t_setup = time.perf_counter()
+    wn = make_weights_np(shape, seed=0)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    rng = np.random.Generator(np.random.PCG64(7))
+    for s, c in zip(seqs, lens):   # synthetic committed context (an input)
+        st = orc._state(s)
+        for l in range(shape.n_layers):
+            st["k"][l] = rng.standard_normal((c, shape.n_kv_heads, shape.head_dim), dtype=np.float32)
+            st["v"][l] = rng.standard_normal((c, shape.n_kv_heads, shape.head_dim), dtype=np.float32)
+        st["len"] = c
+    width = shape.n_feat_layers * shape.hidden
+    drafts = np.zeros((batch, B - 1), dtype=np.int64)
+    anchors = rng.integers(0, shape.vocab - 1, size=batch)
+
+    def step():
+        nonlocal drafts, anchors
+        f = rng.standard_normal((batch * B, width), dtype=np.float32)
+        t = rng.integers(0, shape.vocab, size=(batch, B))
+        orc.fuse_ctx(seqs, [B] * batch, f, pending=True)
+        _, anchors = orc.verify(seqs, B, drafts, t)
+        drafts = np.stack([r["draft"] for r in orc.draft(seqs, anchors, B)])
+
+    setup_s = time.perf_counter() - t_setup
+    t0 = time.perf_counter()
+    step()                                    # one warm-up cycle
+    per = time.perf_counter() - t0
+    budget = 150.0
+    W = min(args.warmup, max(0, int(0.1 * budget / per)))
+    for _ in range(W - 1):
+        step()
+    K = max(1, min(args.steps, int(budget / per)))
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step()
+    el = time.perf_counter() - t0
+    value = K / el
+    sample = (f"{K} of the requested {args.steps} steps (capped to ~{budget:.0f} s): full cycles of the fp32 numpy "
+              f"oracle (fuse {B} features per sequence + verify + draft), batch {batch}")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": 1e3 * el / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "batch_per_gpu": batch, "block": B,
+                   "context": ctx if ctx else f"U[{spread[0]}, {spread[1]}]", "setup_s": setup_s},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_8b_b1_ctx4096")
+    ap.add_argument("--block", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

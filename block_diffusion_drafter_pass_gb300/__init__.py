@@ -1,0 +1,274 @@
+"""Python binding of libdflash (the DFlash drafter pass on GB300).
+
+Argument marshalling only: every step of the drafter pass runs in the CUDA
+kernels behind include/dflash.h. The functions named dflash_* mirror the C
+entry points one to one; `Drafter` bundles a context with the torch tensors
+it borrows. PyTorch supplies device memory and streams.
+
+There is no fallback: if libdflash.so is missing or cannot load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from . import _build
+
+LIB_PATH = _build.LIB
+
+DFLASH_OK, DFLASH_EINVAL, DFLASH_ENOMEM, DFLASH_ECUDA, DFLASH_ETIMEOUT, DFLASH_EDEVICE = range(6)
+_STATUS_NAMES = {0: "OK", 1: "EINVAL", 2: "ENOMEM", 3: "ECUDA", 4: "ETIMEOUT", 5: "EDEVICE"}
+
+# Entry points declared in include/dflash.h.
+EXPORTED = (
+    "dflash_create", "dflash_destroy", "dflash_last_error", "dflash_seq_reset", "dflash_seq_len",
+    "dflash_fuse_ctx", "dflash_draft", "dflash_verify", "dflash_rows_argmax_bf16", "dflash_sync",
+    "dflash_debug_read_kv", "dflash_debug_last_draft", "dflash_debug_gemm", "dflash_debug_profile",
+    "dflash_debug_profile_read",
+)
+
+# Kernel classes of the per-kernel accounting (DFLASH_K_* in include/dflash.h).
+KERNEL_CLASSES = ("qkv", "attn", "attn_combine", "o", "gateup", "down", "lmhead", "fuse_wc", "fuse_kv", "norm",
+                  "verify", "other")
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"dflash {_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class dflash_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("hidden", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
+                                            "n_layers", "n_feat_layers")] + [
+        ("rope_base", ctypes.c_float), ("rms_eps", ctypes.c_float)] + [
+        (n, ctypes.c_int) for n in ("mask_id", "max_seqs", "max_batch", "max_block", "max_ctx", "max_pages",
+                                    "max_fuse_tokens")]
+
+
+class dflash_layer_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down",
+                                               "g_attn", "g_ffn")]
+
+
+class dflash_kernel_stat(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_longlong), ("ms", ctypes.c_double), ("bytes", ctypes.c_double),
+                ("flops", ctypes.c_double)]
+
+
+class dflash_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_c", "g_c", "embed", "lm_head", "g_final")] + [
+        ("layers", ctypes.POINTER(dflash_layer_weights))]
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libdflash.so (built by __graft_entry__.build()). Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise DFlashError(DFLASH_ECUDA, f"{LIB_PATH} is missing; build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, VP = ctypes.POINTER, ctypes.c_int, ctypes.c_void_p
+    i32p = P(ctypes.c_int32)
+    sigs = {
+        "dflash_create": ([P(dflash_config), P(dflash_weights), P(VP)], I),
+        "dflash_destroy": ([VP], I),
+        "dflash_last_error": ([VP], ctypes.c_char_p),
+        "dflash_seq_reset": ([VP, I], I),
+        "dflash_seq_len": ([VP, I, P(I), P(I)], I),
+        "dflash_fuse_ctx": ([VP, i32p, I, i32p, VP, I, VP], I),
+        "dflash_draft": ([VP, i32p, I, VP, I, VP, VP], I),
+        "dflash_verify": ([VP, i32p, I, I, VP, VP, VP, VP, VP], I),
+        "dflash_rows_argmax_bf16": ([VP, I, I, VP, VP], I),
+        "dflash_sync": ([VP], I),
+        "dflash_debug_read_kv": ([VP, I, I, I, I, VP, VP], I),
+        "dflash_debug_last_draft": ([VP, VP, VP], I),
+        "dflash_debug_gemm": ([VP, VP, VP, I, I, I, I, VP], I),
+        "dflash_debug_profile": ([VP, I], I),
+        "dflash_debug_profile_read": ([VP, P(dflash_kernel_stat), I], I),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(status: int, ctx=None) -> None:
+    if status != DFLASH_OK:
+        msg = load_library().dflash_last_error(ctx)
+        raise DFlashError(status, msg.decode() if msg else "")
+
+
+def _i32(seq: Sequence[int]):
+    arr = (ctypes.c_int32 * max(1, len(seq)))(*[int(v) for v in seq])
+    return arr
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+# --- one-to-one wrappers of the C entry points -------------------------------
+
+def dflash_rows_argmax_bf16(logits, out=None, stream=None):
+    """Row argmax of bf16 logits [rows, cols] (lowest index on ties) -> int32 [rows]."""
+    import torch
+    assert logits.dtype == torch.bfloat16 and logits.is_cuda and logits.is_contiguous()
+    rows, cols = logits.shape
+    if out is None:
+        out = torch.empty(rows, dtype=torch.int32, device=logits.device)
+    _check(load_library().dflash_rows_argmax_bf16(_ptr(logits), rows, cols, _ptr(out), _stream(stream)))
+    return out
+
+
+def dflash_debug_gemm(W, X, splits: int = 0, stream=None):
+    """Y = X W^T in fp32 with the library's tcgen05 GEMM (W [N,K], X [M,K] bf16)."""
+    import torch
+    N, K = W.shape
+    M = X.shape[0]
+    Y = torch.empty(M, N, dtype=torch.float32, device=W.device)
+    _check(load_library().dflash_debug_gemm(_ptr(W), _ptr(X), _ptr(Y), N, M, K, splits, _stream(stream)))
+    return Y
+
+
+class Drafter:
+    """A dflash context plus the bf16 device weights it borrows.
+
+    `weights` follows synth.make_weights_torch: w_c, g_c, embed, lm_head,
+    g_final and layers[i] = {w_q, w_k, w_v, w_o, w_gate, w_up, w_down,
+    g_attn, g_ffn}, all contiguous torch.bfloat16 CUDA tensors.
+    """
+
+    def __init__(self, shape, weights, *, max_seqs: int = 4, max_batch: int = 4, max_block: int = 16,
+                 max_ctx: int = 4096, max_pages: Optional[int] = None, max_fuse_tokens: int = 1024):
+        import torch
+        lib = load_library()
+        self.shape = shape
+        self._weights = weights  # keep the borrowed tensors alive
+        for t in [weights[k] for k in ("w_c", "g_c", "embed", "lm_head", "g_final")] + \
+                 [v for lw in weights["layers"] for v in lw.values()]:
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise DFlashError(DFLASH_EINVAL, "weights must be contiguous bf16 CUDA tensors")
+        if max_pages is None:
+            max_pages = max_seqs * ((max_ctx + 63) // 64)
+        self.cfg = dflash_config(shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
+                                 shape.vocab, shape.n_layers, shape.n_feat_layers, shape.rope_base,
+                                 shape.rms_eps, shape.mask_id, max_seqs, max_batch, max_block, max_ctx,
+                                 max_pages, max_fuse_tokens)
+        layers = (dflash_layer_weights * shape.n_layers)()
+        for i, lw in enumerate(weights["layers"]):
+            layers[i] = dflash_layer_weights(*[_ptr(lw[k]) for k in ("w_q", "w_k", "w_v", "w_o", "w_gate",
+                                                                      "w_up", "w_down", "g_attn", "g_ffn")])
+        self._layers = layers
+        w = dflash_weights(_ptr(weights["w_c"]), _ptr(weights["g_c"]), _ptr(weights["embed"]),
+                           _ptr(weights["lm_head"]), _ptr(weights["g_final"]), layers)
+        ctx = ctypes.c_void_p()
+        _check(lib.dflash_create(ctypes.byref(self.cfg), ctypes.byref(w), ctypes.byref(ctx)), None)
+        self.ctx = ctx
+        self.device = weights["w_c"].device
+
+    # lifecycle ---------------------------------------------------------------
+    def close(self) -> None:
+        if getattr(self, "ctx", None):
+            load_library().dflash_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # the hot path ----------------------------------------------------------------
+    def fuse_ctx(self, seq_ids, n_new, feats, pending: bool, stream=None) -> None:
+        import torch
+        assert feats is None or (feats.dtype == torch.bfloat16 and feats.is_cuda and feats.is_contiguous())
+        _check(load_library().dflash_fuse_ctx(self.ctx, _i32(seq_ids), len(seq_ids), _i32(n_new), _ptr(feats),
+                                              1 if pending else 0, _stream(stream)), self.ctx)
+
+    def draft(self, seq_ids, anchor_ids, B: int, out=None, stream=None):
+        import torch
+        n = len(seq_ids)
+        if out is None:
+            out = torch.empty(n, max(B - 1, 0), dtype=torch.int32, device=self.device)
+        assert anchor_ids.dtype == torch.int32 and anchor_ids.is_cuda
+        _check(load_library().dflash_draft(self.ctx, _i32(seq_ids), n, _ptr(anchor_ids), B,
+                                           _ptr(out) if out.numel() else 0, _stream(stream)), self.ctx)
+        return out
+
+    def verify(self, seq_ids, B: int, draft_ids, target_ids, tau=None, bonus=None, stream=None):
+        import torch
+        n = len(seq_ids)
+        if tau is None:
+            tau = torch.empty(n, dtype=torch.int32, device=self.device)
+        if bonus is None:
+            bonus = torch.empty(n, dtype=torch.int32, device=self.device)
+        dptr = _ptr(draft_ids) if draft_ids is not None and draft_ids.numel() else 0
+        _check(load_library().dflash_verify(self.ctx, _i32(seq_ids), n, B, dptr, _ptr(target_ids), _ptr(tau),
+                                            _ptr(bonus), _stream(stream)), self.ctx)
+        return tau, bonus
+
+    # state and inspection ------------------------------------------------------
+    def seq_reset(self, seq: int) -> None:
+        _check(load_library().dflash_seq_reset(self.ctx, seq), self.ctx)
+
+    def seq_len(self, seq: int):
+        c, p = ctypes.c_int(), ctypes.c_int()
+        _check(load_library().dflash_seq_len(self.ctx, seq, ctypes.byref(c), ctypes.byref(p)), self.ctx)
+        return c.value, p.value
+
+    def sync(self) -> None:
+        _check(load_library().dflash_sync(self.ctx), self.ctx)
+
+    def read_kv(self, layer: int, seq: int, pos0: int, n: int):
+        """Cached K, V of `n` positions as float32 arrays [n, n_kv, d]."""
+        import numpy as np
+        sh = self.shape
+        k = np.empty((n, sh.n_kv_heads, sh.head_dim), dtype=np.uint16)
+        v = np.empty_like(k)
+        _check(load_library().dflash_debug_read_kv(self.ctx, layer, seq, pos0, n, k.ctypes.data, v.ctypes.data),
+               self.ctx)
+        f = lambda a: (a.astype(np.uint32) << 16).view(np.float32)
+        return f(k), f(v)
+
+    def profile(self, enable: bool) -> None:
+        """Event-time every kernel launch (on its launch stream) while enabled."""
+        _check(load_library().dflash_debug_profile(self.ctx, 1 if enable else 0), self.ctx)
+
+    def profile_read(self):
+        """Per kernel class: launches, summed ms, algorithmic bytes and flops
+        since the last read (synchronises, then resets the totals)."""
+        n = len(KERNEL_CLASSES)
+        arr = (dflash_kernel_stat * n)()
+        _check(load_library().dflash_debug_profile_read(self.ctx, arr, n), self.ctx)
+        return {name: {"launches": int(a.launches), "ms": float(a.ms), "bytes": float(a.bytes),
+                       "flops": float(a.flops)} for name, a in zip(KERNEL_CLASSES, arr)}
+
+    def last_draft(self, n_seq: int, B: int):
+        """(final residual stream [n_seq*B, H] fp32, winning logits [n_seq*(B-1)] fp32) of the last draft."""
+        import numpy as np
+        hid = np.empty((n_seq * B, self.shape.hidden), dtype=np.float32)
+        top = np.empty(max(1, n_seq * (B - 1)), dtype=np.float32)
+        _check(load_library().dflash_debug_last_draft(self.ctx, hid.ctypes.data, top.ctypes.data), self.ctx)
+        return hid, top[: n_seq * (B - 1)]

@@ -1,0 +1,957 @@
+// runtime.cu - the DFlash drafter context behind the C ABI of dflash.h:
+// validation, the paged KV pool and its host-side page allocator, the RoPE
+// table, TMA descriptors, workspaces, and the call sequences of
+// dflash_fuse_ctx / dflash_draft / dflash_verify.
+//
+// Host/device split of the sequence state: the device holds the exact
+// committed length (verify commits on the device, so no call has to wait for
+// it); the host holds the pending count exactly and an upper bound of the
+// committed length, which sizes page reservations and launch grids. The
+// bound is tightened from an asynchronous snapshot of the device lengths
+// taken after each verify, once that copy has landed.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "dflash.h"
+#include "internal.h"
+
+using namespace dfl;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::string g_create_error = "no error";
+
+bool load_encode() {
+  if (g_encode) return true;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// Row-major [rows, cols] bf16 matrix, box = 64 columns x box_rows rows, 128B swizzle.
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows][heads][d] bf16, box = 64 dims x 1 head x box_rows rows.
+bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t heads, uint64_t d, uint32_t box_rows) {
+  cuuint64_t dims[3] = {d, heads, rows};
+  cuuint64_t strides[2] = {d * 2, heads * d * 2};
+  cuuint32_t box[3] = {64, 1, box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace
+
+struct dflash_ctx {
+  dflash_config cfg{};
+  dflash_weights w{};
+  std::vector<dflash_layer_weights> layers;
+  int num_sms = 0;
+  int pages_per_seq = 0;
+  int rope_positions = 0;
+
+  // device memory
+  uint16_t* pool = nullptr;
+  float2* rope = nullptr;
+  int* d_len = nullptr;
+  int* d_pend = nullptr;
+  int* d_page_table = nullptr;
+  int* d_status = nullptr;
+  float* x = nullptr;        // [max_rows, H] residual stream (fp32)
+  uint16_t* h = nullptr;     // [max_rows, H] normalised layer input
+  uint16_t* q = nullptr;     // [max_rows, n_q*d]
+  uint16_t* kb = nullptr;    // [max_rows, n_kv*d] block keys
+  uint16_t* vb = nullptr;    // [max_rows, n_kv*d] block values
+  uint16_t* attn = nullptr;  // [max_rows, n_q*d]
+  uint16_t* act = nullptr;   // [max_rows, F]
+  uint16_t* hn = nullptr;    // [max_rows, H] final-normed draft rows
+  float* xf = nullptr;       // [max_fuse_tokens, H] fused projection
+  uint16_t* ht = nullptr;    // [max_fuse_tokens, H] H_t
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  int items_cap = 0;
+  float* split_ws = nullptr;
+  size_t split_elems = 0;
+  int* tickets = nullptr;
+  int n_tickets = 0;
+  unsigned long long* keys = nullptr;
+  int* done = nullptr;
+  float* top_logit = nullptr;
+
+  // weight descriptors
+  std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
+  CUtensorMap m_lm{}, m_wc{}, m_pool{};
+  std::map<std::tuple<const void*, int, int, int, int>, CUtensorMap> act_maps;
+
+  // host view of the sequences
+  std::vector<int> free_pages;
+  std::vector<std::vector<int>> pages;
+  std::vector<int> len_ub, pend, added_since;
+  int* h_snap = nullptr;      // pinned copy of d_len
+  cudaEvent_t snap_event = nullptr;
+  bool snap_pending = false;
+
+  int last_rows = 0, last_draft_rows = 0;
+  std::string err = "no error";
+
+  // per-kernel accounting
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_events;
+  size_t prof_next = 0;
+  std::vector<std::pair<int, size_t>> prof_recs;   // (class, first event)
+  dflash_kernel_stat prof_acc[DFLASH_K_COUNT] = {};
+
+  int max_rows() const { return cfg.max_batch * cfg.max_block; }
+};
+
+namespace {
+
+dflash_status fail(dflash_ctx* c, dflash_status s, const std::string& msg) {
+  if (c) c->err = msg;
+  else g_create_error = msg;
+  return s;
+}
+
+#define CK(call)                                                                                   \
+  do {                                                                                             \
+    cudaError_t e_ = (call);                                                                       \
+    if (e_ != cudaSuccess) return fail(ctx, DFLASH_ECUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t count) {
+  return cudaMalloc(reinterpret_cast<void**>(p), std::max<size_t>(count, 1) * sizeof(T));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+const CUtensorMap* act_map(dflash_ctx* ctx, const void* ptr, int rows, int cols, int box_rows) {
+  auto key = std::make_tuple(ptr, rows, cols, box_rows, 2);
+  auto it = ctx->act_maps.find(key);
+  if (it != ctx->act_maps.end()) return &it->second;
+  CUtensorMap m;
+  if (!encode_2d(&m, ptr, rows, cols, box_rows)) return nullptr;
+  if (ctx->act_maps.size() > 4096) ctx->act_maps.clear();
+  return &(ctx->act_maps[key] = m);
+}
+
+const CUtensorMap* blk_map(dflash_ctx* ctx, const void* ptr, int rows, int box_rows) {
+  auto key = std::make_tuple(ptr, rows, ctx->cfg.n_kv_heads, box_rows, 3);
+  auto it = ctx->act_maps.find(key);
+  if (it != ctx->act_maps.end()) return &it->second;
+  CUtensorMap m;
+  if (!encode_3d(&m, ptr, rows, ctx->cfg.n_kv_heads, ctx->cfg.head_dim, box_rows)) return nullptr;
+  return &(ctx->act_maps[key] = m);
+}
+
+// Counts one launch group of class `cls` with its algorithmic bytes/flops and,
+// while profiling is on, brackets it with events on the launch stream.
+struct ProfScope {
+  dflash_ctx* c;
+  int cls;
+  cudaStream_t s;
+  size_t ev = static_cast<size_t>(-1);
+  ProfScope(dflash_ctx* c_, int cls_, cudaStream_t s_, double bytes, double flops, int launches = 1)
+      : c(c_), cls(cls_), s(s_) {
+    c->prof_acc[cls].launches += launches;
+    c->prof_acc[cls].bytes += bytes;
+    c->prof_acc[cls].flops += flops;
+    if (!c->prof_on) return;
+    while (c->prof_next + 2 > c->prof_events.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return;
+      c->prof_events.push_back(e);
+    }
+    ev = c->prof_next;
+    c->prof_next += 2;
+    cudaEventRecord(c->prof_events[ev], s);
+  }
+  ~ProfScope() {
+    if (ev == static_cast<size_t>(-1)) return;
+    cudaEventRecord(c->prof_events[ev + 1], s);
+    c->prof_recs.emplace_back(cls, ev);
+  }
+};
+
+// Algorithmic traffic of OUT[M, n_out] = X[M, K] W[n_w, K]^T with `ob` bytes
+// per output element (read-modify-write outputs count twice).
+double gemm_bytes(double M, double n_w, double K, double n_out, double ob) {
+  return n_w * K * 2 + M * K * 2 + M * n_out * ob;
+}
+
+SeqState seq_state(dflash_ctx* ctx) {
+  SeqState s;
+  s.len = ctx->d_len;
+  s.pend = ctx->d_pend;
+  s.page_table = ctx->d_page_table;
+  s.pages_per_seq = ctx->pages_per_seq;
+  return s;
+}
+
+GemmWork gemm_work(dflash_ctx* ctx) {
+  GemmWork w;
+  w.partial = ctx->split_ws;
+  w.partial_elems = ctx->split_elems;
+  w.tickets = ctx->tickets;
+  w.n_tickets = ctx->n_tickets;
+  return w;
+}
+
+GemmEpi base_epi(dflash_ctx* ctx, int kind) {
+  GemmEpi e;
+  std::memset(&e, 0, sizeof(e));
+  e.kind = kind;
+  e.head_dim = ctx->cfg.head_dim;
+  e.n_q_heads = ctx->cfg.n_heads;
+  e.n_kv_heads = ctx->cfg.n_kv_heads;
+  e.rope = ctx->rope;
+  e.rope_positions = ctx->rope_positions;
+  e.seqs = seq_state(ctx);
+  e.pool = ctx->pool;
+  e.pool_pages = ctx->cfg.max_pages;
+  e.status = ctx->d_status;
+  return e;
+}
+
+ARegions stacked(std::initializer_list<int> rows) {
+  ARegions r;
+  std::memset(&r, 0, sizeof(r));
+  int t = 0, i = 0;
+  for (int n : rows) {
+    r.tile_begin[i++] = t;
+    t += ceil_div(n, 128);
+  }
+  r.tile_begin[i] = t;
+  r.n_regions = i;
+  r.paired = 0;
+  return r;
+}
+
+void release_tail_pages(dflash_ctx* ctx, int s) {
+  const int need = ceil_div(ctx->len_ub[s] + ctx->pend[s], kPage);
+  auto& pg = ctx->pages[s];
+  while (static_cast<int>(pg.size()) > need) {
+    ctx->free_pages.push_back(pg.back());
+    pg.pop_back();
+  }
+}
+
+// Tighten the host's committed-length bounds from a landed snapshot.
+void consume_snapshot(dflash_ctx* ctx, bool force_wait) {
+  if (!ctx->snap_pending) return;
+  if (force_wait) cudaEventSynchronize(ctx->snap_event);
+  else if (cudaEventQuery(ctx->snap_event) != cudaSuccess) return;
+  for (int s = 0; s < ctx->cfg.max_seqs; ++s) {
+    const int exact = ctx->h_snap[s] + ctx->added_since[s];
+    if (exact < ctx->len_ub[s]) {
+      ctx->len_ub[s] = exact;
+      release_tail_pages(ctx, s);
+    }
+    ctx->added_since[s] = 0;
+  }
+  ctx->snap_pending = false;
+}
+
+dflash_status check_seqs(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, SeqMeta* meta) {
+  if (n_seq < 0 || n_seq > ctx->cfg.max_batch) return fail(ctx, DFLASH_EINVAL, "n_seq out of range");
+  if (n_seq > 0 && !seq_ids) return fail(ctx, DFLASH_EINVAL, "seq_ids is null");
+  std::memset(meta, 0, sizeof(*meta));
+  meta->n_seq = n_seq;
+  for (int i = 0; i < n_seq; ++i) {
+    const int s = seq_ids[i];
+    if (s < 0 || s >= ctx->cfg.max_seqs) return fail(ctx, DFLASH_EINVAL, "sequence id out of range");
+    for (int j = 0; j < i; ++j)
+      if (seq_ids[j] == s) return fail(ctx, DFLASH_EINVAL, "duplicate sequence id in one call");
+    meta->slot[i] = s;
+  }
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_last_error(const dflash_ctx* ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
+
+dflash_status dflash_destroy(dflash_ctx* ctx) {
+  if (!ctx) return DFLASH_EINVAL;
+  cudaDeviceSynchronize();
+  void* ptrs[] = {ctx->pool, ctx->rope, ctx->d_len, ctx->d_pend, ctx->d_page_table, ctx->d_status, ctx->x,
+                  ctx->h, ctx->q, ctx->kb, ctx->vb, ctx->attn, ctx->act, ctx->hn, ctx->xf, ctx->ht, ctx->part_o,
+                  ctx->part_ml, ctx->split_ws, ctx->tickets, ctx->keys, ctx->done, ctx->top_logit};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  if (ctx->h_snap) cudaFreeHost(ctx->h_snap);
+  for (cudaEvent_t e : ctx->prof_events) cudaEventDestroy(e);
+  if (ctx->snap_event) cudaEventDestroy(ctx->snap_event);
+  delete ctx;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w, dflash_ctx** out) {
+  dflash_ctx* ctx = nullptr;
+  if (!out) return fail(nullptr, DFLASH_EINVAL, "out is null");
+  *out = nullptr;
+  if (!cfg_in || !w || !w->layers) return fail(nullptr, DFLASH_EINVAL, "null config or weights");
+  const dflash_config c = *cfg_in;
+  const int d = c.head_dim;
+  if (c.hidden < 64 || c.hidden % 64) return fail(nullptr, DFLASH_EINVAL, "hidden must be a positive multiple of 64");
+  if (d != 64 && d != 128) return fail(nullptr, DFLASH_EINVAL, "head_dim must be 64 or 128");
+  if (c.n_kv_heads < 1 || c.n_heads < 1 || c.n_heads % c.n_kv_heads)
+    return fail(nullptr, DFLASH_EINVAL, "n_heads must be a multiple of n_kv_heads");
+  if ((c.n_heads * d) % 128 || (c.n_kv_heads * d) % 128)
+    return fail(nullptr, DFLASH_EINVAL, "n_heads*d and n_kv_heads*d must be multiples of 128");
+  if (c.ffn < 8 || c.ffn % 8) return fail(nullptr, DFLASH_EINVAL, "ffn must be a positive multiple of 8");
+  if (c.vocab < 2 || c.mask_id < 0 || c.mask_id >= c.vocab) return fail(nullptr, DFLASH_EINVAL, "bad vocab/mask_id");
+  if (c.n_layers < 1 || c.n_layers > 16 || c.n_feat_layers < 1 || c.n_feat_layers > 16)
+    return fail(nullptr, DFLASH_EINVAL, "n_layers and n_feat_layers must be in 1..16");
+  if (c.max_batch < 1 || c.max_batch > kMaxBatch) return fail(nullptr, DFLASH_EINVAL, "max_batch must be in 1..64");
+  if (c.max_block < 1 || c.max_block > kMaxBlock) return fail(nullptr, DFLASH_EINVAL, "max_block must be in 1..32");
+  if ((c.n_heads / c.n_kv_heads) * c.max_block > 128)
+    return fail(nullptr, DFLASH_EINVAL, "(n_heads/n_kv_heads)*max_block must be at most 128");
+  if (c.max_seqs < 1 || c.max_ctx < 1 || c.max_pages < 1 || c.max_fuse_tokens < 1)
+    return fail(nullptr, DFLASH_EINVAL, "capacities must be positive");
+  if (!(c.rms_eps >= 0.f) || !(c.rope_base > 1.f)) return fail(nullptr, DFLASH_EINVAL, "bad rms_eps or rope_base");
+  const long long pool_rows = 1LL * c.n_layers * c.max_pages * 2 * c.n_kv_heads * kPage;
+  if (pool_rows >= (1LL << 31)) return fail(nullptr, DFLASH_EINVAL, "KV pool too large for 32-bit TMA coordinates");
+  const void* ptrs[] = {w->w_c, w->g_c, w->embed, w->lm_head, w->g_final};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return fail(nullptr, DFLASH_EINVAL, "weight pointer null or not 16-byte aligned");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = w->layers[l];
+    const void* lp[] = {L.w_q, L.w_k, L.w_v, L.w_o, L.w_gate, L.w_up, L.w_down, L.g_attn, L.g_ffn};
+    for (const void* p : lp)
+      if (!p || !aligned16(p)) return fail(nullptr, DFLASH_EINVAL, "layer weight null or not 16-byte aligned");
+  }
+  if (!load_encode()) return fail(nullptr, DFLASH_ECUDA, "cuTensorMapEncodeTiled unavailable");
+
+  ctx = new dflash_ctx();
+  ctx->cfg = c;
+  ctx->layers.assign(w->layers, w->layers + c.n_layers);
+  ctx->w = *w;
+  ctx->w.layers = ctx->layers.data();
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    g_create_error = std::string("no CUDA device: ") + cudaGetErrorString(e);
+    delete ctx;
+    return DFLASH_ECUDA;
+  }
+  const int H = c.hidden, nq = c.n_heads, nkv = c.n_kv_heads, F = c.ffn;
+  ctx->pages_per_seq = ceil_div(c.max_ctx, kPage);
+  ctx->rope_positions = c.max_ctx + c.max_block;
+  const size_t rows = ctx->max_rows();
+  const int G = nq / nkv;
+  const int rows_pad = 16 * ceil_div(G * c.max_block, 16);
+  ctx->items_cap = 4 * ctx->num_sms + c.max_batch * nkv + 64;
+
+  auto bad = [&](cudaError_t err, const char* what) {
+    g_create_error = std::string(what) + ": " + cudaGetErrorString(err);
+    dflash_destroy(ctx);
+    return err == cudaErrorMemoryAllocation ? DFLASH_ENOMEM : DFLASH_ECUDA;
+  };
+#define CA(call, what)                      \
+  do {                                      \
+    cudaError_t e_ = (call);                \
+    if (e_ != cudaSuccess) return bad(e_, what); \
+  } while (0)
+
+  CA(dalloc(&ctx->pool, static_cast<size_t>(pool_rows) * d), "KV pool");
+  CA(cudaMemset(ctx->pool, 0, static_cast<size_t>(pool_rows) * d * 2), "KV pool");
+  CA(dalloc(&ctx->rope, static_cast<size_t>(ctx->rope_positions) * (d / 2)), "RoPE table");
+  CA(dalloc(&ctx->d_len, c.max_seqs), "lengths");
+  CA(dalloc(&ctx->d_pend, c.max_seqs), "lengths");
+  CA(cudaMemset(ctx->d_len, 0, c.max_seqs * sizeof(int)), "lengths");
+  CA(cudaMemset(ctx->d_pend, 0, c.max_seqs * sizeof(int)), "lengths");
+  CA(dalloc(&ctx->d_page_table, static_cast<size_t>(c.max_seqs) * ctx->pages_per_seq), "page table");
+  CA(cudaMemset(ctx->d_page_table, 0xFF, static_cast<size_t>(c.max_seqs) * ctx->pages_per_seq * sizeof(int)),
+     "page table");
+  CA(dalloc(&ctx->d_status, 1), "status");
+  CA(cudaMemset(ctx->d_status, 0, sizeof(int)), "status");
+  CA(dalloc(&ctx->x, rows * H), "workspace");
+  CA(dalloc(&ctx->h, rows * H), "workspace");
+  CA(dalloc(&ctx->q, rows * nq * d), "workspace");
+  CA(dalloc(&ctx->kb, rows * nkv * d), "workspace");
+  CA(dalloc(&ctx->vb, rows * nkv * d), "workspace");
+  CA(cudaMemset(ctx->kb, 0, rows * nkv * d * 2), "workspace");
+  CA(cudaMemset(ctx->vb, 0, rows * nkv * d * 2), "workspace");
+  CA(dalloc(&ctx->attn, rows * nq * d), "workspace");
+  CA(dalloc(&ctx->act, rows * F), "workspace");
+  CA(dalloc(&ctx->hn, rows * H), "workspace");
+  CA(dalloc(&ctx->xf, static_cast<size_t>(c.max_fuse_tokens) * H), "workspace");
+  CA(dalloc(&ctx->ht, static_cast<size_t>(c.max_fuse_tokens) * H), "workspace");
+  CA(dalloc(&ctx->part_o, static_cast<size_t>(ctx->items_cap) * rows_pad * d), "attention partials");
+  CA(dalloc(&ctx->part_ml, static_cast<size_t>(ctx->items_cap) * rows_pad), "attention partials");
+  ctx->split_elems = static_cast<size_t>(8) << 20;
+  CA(dalloc(&ctx->split_ws, ctx->split_elems), "split-K workspace");
+  ctx->n_tickets = 1 << 16;
+  CA(dalloc(&ctx->tickets, ctx->n_tickets), "tickets");
+  CA(cudaMemset(ctx->tickets, 0, ctx->n_tickets * sizeof(int)), "tickets");
+  CA(dalloc(&ctx->keys, rows), "argmax keys");
+  CA(cudaMemset(ctx->keys, 0, rows * sizeof(unsigned long long)), "argmax keys");
+  CA(dalloc(&ctx->done, 1), "argmax counter");
+  CA(cudaMemset(ctx->done, 0, sizeof(int)), "argmax counter");
+  CA(dalloc(&ctx->top_logit, rows), "top logits");
+  CA(cudaMallocHost(reinterpret_cast<void**>(&ctx->h_snap), c.max_seqs * sizeof(int)), "pinned snapshot");
+  CA(cudaEventCreateWithFlags(&ctx->snap_event, cudaEventDisableTiming), "event");
+
+  // RoPE table: angle pos * base^(-2i/d) in double precision, stored as fp32 (cos, sin).
+  {
+    std::vector<float2> tab(static_cast<size_t>(ctx->rope_positions) * (d / 2));
+    for (int i = 0; i < d / 2; ++i) {
+      const double theta = std::pow(static_cast<double>(c.rope_base), -2.0 * i / d);
+      for (int p = 0; p < ctx->rope_positions; ++p) {
+        const double a = p * theta;
+        tab[static_cast<size_t>(p) * (d / 2) + i] = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+      }
+    }
+    CA(cudaMemcpy(ctx->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice), "RoPE table");
+  }
+
+  // weight descriptors (box 64 K-elements x 64 rows)
+  bool ok = encode_2d(&ctx->m_lm, w->lm_head, c.vocab, H, 64) &&
+            encode_2d(&ctx->m_wc, w->w_c, H, static_cast<uint64_t>(c.n_feat_layers) * H, 64) &&
+            encode_2d(&ctx->m_pool, ctx->pool, pool_rows, d, 64);
+  ctx->m_wq.resize(c.n_layers);
+  ctx->m_wk.resize(c.n_layers);
+  ctx->m_wv.resize(c.n_layers);
+  ctx->m_wo.resize(c.n_layers);
+  ctx->m_wg.resize(c.n_layers);
+  ctx->m_wu.resize(c.n_layers);
+  ctx->m_wd.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers && ok; ++l) {
+    const dflash_layer_weights& L = ctx->layers[l];
+    ok = encode_2d(&ctx->m_wq[l], L.w_q, nq * d, H, 64) && encode_2d(&ctx->m_wk[l], L.w_k, nkv * d, H, 64) &&
+         encode_2d(&ctx->m_wv[l], L.w_v, nkv * d, H, 64) && encode_2d(&ctx->m_wo[l], L.w_o, H, nq * d, 64) &&
+         encode_2d(&ctx->m_wg[l], L.w_gate, F, H, 64) && encode_2d(&ctx->m_wu[l], L.w_up, F, H, 64) &&
+         encode_2d(&ctx->m_wd[l], L.w_down, H, F, 64);
+  }
+  if (!ok) {
+    g_create_error = "cuTensorMapEncodeTiled rejected a weight layout";
+    dflash_destroy(ctx);
+    return DFLASH_EINVAL;
+  }
+  CA(cudaDeviceSynchronize(), "create");
+
+  ctx->free_pages.reserve(c.max_pages);
+  for (int p = c.max_pages - 1; p >= 0; --p) ctx->free_pages.push_back(p);
+  ctx->pages.assign(c.max_seqs, {});
+  ctx->len_ub.assign(c.max_seqs, 0);
+  ctx->pend.assign(c.max_seqs, 0);
+  ctx->added_since.assign(c.max_seqs, 0);
+  *out = ctx;
+#undef CA
+  return DFLASH_OK;
+}
+
+dflash_status dflash_sync(dflash_ctx* ctx) {
+  if (!ctx) return DFLASH_EINVAL;
+  CK(cudaDeviceSynchronize());
+  int st = 0;
+  CK(cudaMemcpy(&st, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (st) {
+    CK(cudaMemset(ctx->d_status, 0, sizeof(int)));
+    if (st & kDevTimeout) return fail(ctx, DFLASH_ETIMEOUT, "a kernel's bounded wait ran out");
+    return fail(ctx, DFLASH_EDEVICE, "a kernel found an index out of range");
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_seq_reset(dflash_ctx* ctx, int seq) {
+  if (!ctx) return DFLASH_EINVAL;
+  if (seq < 0 || seq >= ctx->cfg.max_seqs) return fail(ctx, DFLASH_EINVAL, "sequence id out of range");
+  CK(cudaDeviceSynchronize());
+  consume_snapshot(ctx, true);
+  CK(cudaMemset(ctx->d_len + seq, 0, sizeof(int)));
+  CK(cudaMemset(ctx->d_pend + seq, 0, sizeof(int)));
+  ctx->len_ub[seq] = 0;
+  ctx->pend[seq] = 0;
+  ctx->added_since[seq] = 0;
+  release_tail_pages(ctx, seq);
+  return DFLASH_OK;
+}
+
+dflash_status dflash_seq_len(dflash_ctx* ctx, int seq, int* committed, int* pending) {
+  if (!ctx) return DFLASH_EINVAL;
+  if (seq < 0 || seq >= ctx->cfg.max_seqs) return fail(ctx, DFLASH_EINVAL, "sequence id out of range");
+  CK(cudaDeviceSynchronize());
+  consume_snapshot(ctx, true);
+  std::vector<int> lens(ctx->cfg.max_seqs);
+  CK(cudaMemcpy(lens.data(), ctx->d_len, lens.size() * sizeof(int), cudaMemcpyDeviceToHost));
+  int p = 0;
+  CK(cudaMemcpy(&p, ctx->d_pend + seq, sizeof(int), cudaMemcpyDeviceToHost));
+  for (int s = 0; s < ctx->cfg.max_seqs; ++s) {
+    ctx->len_ub[s] = lens[s];
+    ctx->added_since[s] = 0;
+    release_tail_pages(ctx, s);
+  }
+  if (committed) *committed = lens[seq];
+  if (pending) *pending = p;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* n_new,
+                              const uint16_t* feats, int pending, void* stream_v) {
+  if (!ctx) return DFLASH_EINVAL;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const dflash_config& c = ctx->cfg;
+  SeqMeta meta;
+  dflash_status st = check_seqs(ctx, seq_ids, n_seq, &meta);
+  if (st != DFLASH_OK) return st;
+  if (n_seq > 0 && !n_new) return fail(ctx, DFLASH_EINVAL, "n_new is null");
+  if (pending != 0 && pending != 1) return fail(ctx, DFLASH_EINVAL, "pending must be 0 or 1");
+  long long total = 0;
+  for (int i = 0; i < n_seq; ++i) {
+    if (n_new[i] < 0) return fail(ctx, DFLASH_EINVAL, "n_new must be >= 0");
+    meta.row0[i] = static_cast<int>(total);
+    total += n_new[i];
+  }
+  meta.row0[n_seq] = static_cast<int>(total);
+  if (total > c.max_fuse_tokens) return fail(ctx, DFLASH_EINVAL, "sum(n_new) exceeds max_fuse_tokens");
+  if (total == 0) return DFLASH_OK;
+  if (!feats || !aligned16(feats)) return fail(ctx, DFLASH_EINVAL, "feats null or not 16-byte aligned");
+  consume_snapshot(ctx, false);
+  for (int i = 0; i < n_seq; ++i) {
+    const int s = meta.slot[i];
+    if (!pending && ctx->pend[s]) return fail(ctx, DFLASH_EINVAL, "committed append while tokens are pending");
+    if (ctx->len_ub[s] + ctx->pend[s] + n_new[i] > c.max_ctx) {
+      // the bound may be loose: wait for the snapshot before refusing
+      consume_snapshot(ctx, true);
+      if (ctx->len_ub[s] + ctx->pend[s] + n_new[i] > c.max_ctx)
+        return fail(ctx, DFLASH_EINVAL, "append would exceed max_ctx");
+    }
+  }
+  // reserve pages (all or nothing)
+  int need_total = 0;
+  for (int i = 0; i < n_seq; ++i) {
+    const int s = meta.slot[i];
+    need_total += std::max(0, ceil_div(ctx->len_ub[s] + ctx->pend[s] + n_new[i], kPage) -
+                                  static_cast<int>(ctx->pages[s].size()));
+  }
+  if (need_total > static_cast<int>(ctx->free_pages.size())) {
+    consume_snapshot(ctx, true);
+    need_total = 0;
+    for (int i = 0; i < n_seq; ++i) {
+      const int s = meta.slot[i];
+      need_total += std::max(0, ceil_div(ctx->len_ub[s] + ctx->pend[s] + n_new[i], kPage) -
+                                    static_cast<int>(ctx->pages[s].size()));
+    }
+    if (need_total > static_cast<int>(ctx->free_pages.size()))
+      return fail(ctx, DFLASH_ENOMEM, "KV page pool exhausted");
+  }
+  for (int i = 0; i < n_seq; ++i) {
+    const int s = meta.slot[i];
+    auto& pg = ctx->pages[s];
+    const int have = static_cast<int>(pg.size());
+    const int want = ceil_div(ctx->len_ub[s] + ctx->pend[s] + n_new[i], kPage);
+    if (want <= have) continue;
+    for (int k = have; k < want; ++k) {
+      pg.push_back(ctx->free_pages.back());
+      ctx->free_pages.pop_back();
+    }
+    CK(cudaMemcpyAsync(ctx->d_page_table + static_cast<size_t>(s) * ctx->pages_per_seq + have, pg.data() + have,
+                       (want - have) * sizeof(int), cudaMemcpyHostToDevice, stream));
+  }
+
+  const int H = c.hidden, d = c.head_dim, nkv = c.n_kv_heads;
+  const int M = static_cast<int>(total);
+  const int BN = gemm_token_tile(M);
+  GemmWork work = gemm_work(ctx);
+  // x = X W_c^T (fp32)
+  {
+    AMaps am;
+    am.m[0] = ctx->m_wc;
+    ARegions rg = stacked({H});
+    const CUtensorMap* xm = act_map(ctx, feats, M, c.n_feat_layers * H, BN);
+    if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe feats for TMA");
+    GemmEpi e = base_epi(ctx, EPI_F32_STORE);
+    e.out_f32 = ctx->xf;
+    e.ld_out = H;
+    const double K = 1.0 * c.n_feat_layers * H;
+    ProfScope ps(ctx, DFLASH_K_FUSE_WC, stream, gemm_bytes(M, H, K, H, 4), 2.0 * M * H * K);
+    CK(launch_gemm(am, rg, *xm, M, H, c.n_feat_layers * H, 0, e, work, ctx->num_sms, stream));
+  }
+  // H_t = RMSNorm(x) * g_c
+  {
+    ProfScope ps(ctx, DFLASH_K_NORM, stream, 6.0 * M * H, 0);
+    CK(launch_rmsnorm(ctx->xf, M, H, ctx->w.g_c, c.rms_eps, ctx->ht, 0, stream));
+  }
+  // K/V of every layer from H_t, RoPE on K, scattered into the pages
+  {
+    const CUtensorMap* xm = act_map(ctx, ctx->ht, M, H, BN);
+    if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe H_t for TMA");
+    const int per_launch = kMaxAMaps / 2;
+    for (int l0 = 0; l0 < c.n_layers; l0 += per_launch) {
+      const int nl = std::min(per_launch, c.n_layers - l0);
+      AMaps am;
+      ARegions rg;
+      std::memset(&rg, 0, sizeof(rg));
+      const int tiles = ceil_div(nkv * d, 128);
+      for (int j = 0; j < nl; ++j) {
+        am.m[2 * j] = ctx->m_wk[l0 + j];
+        am.m[2 * j + 1] = ctx->m_wv[l0 + j];
+        rg.tile_begin[2 * j] = 2 * j * tiles;
+        rg.tile_begin[2 * j + 1] = (2 * j + 1) * tiles;
+      }
+      rg.n_regions = 2 * nl;
+      rg.tile_begin[2 * nl] = 2 * nl * tiles;
+      GemmEpi e = base_epi(ctx, EPI_KV_APPEND);
+      e.meta = meta;
+      e.layer0 = l0;
+      const double nw = 2.0 * nl * nkv * d;
+      ProfScope ps(ctx, DFLASH_K_FUSE_KV, stream, gemm_bytes(M, nw, H, nw, 2), 2.0 * M * nw * H);
+      CK(launch_gemm(am, rg, *xm, M, 2 * nl * tiles * 128, H, 0, e, work, ctx->num_sms, stream));
+    }
+  }
+  {
+    ProfScope ps(ctx, DFLASH_K_OTHER, stream, 8.0 * n_seq, 0);
+    CK(launch_fuse_advance(meta, seq_state(ctx), pending, stream));
+  }
+  for (int i = 0; i < n_seq; ++i) {
+    const int s = meta.slot[i];
+    if (pending) ctx->pend[s] += n_new[i];
+    else {
+      ctx->len_ub[s] += n_new[i];
+      ctx->added_since[s] += n_new[i];
+    }
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids, int B,
+                           int32_t* draft_ids, void* stream_v) {
+  if (!ctx) return DFLASH_EINVAL;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const dflash_config& c = ctx->cfg;
+  SeqMeta meta;
+  dflash_status st = check_seqs(ctx, seq_ids, n_seq, &meta);
+  if (st != DFLASH_OK) return st;
+  if (B < 1 || B > c.max_block) return fail(ctx, DFLASH_EINVAL, "B out of range");
+  meta.B = B;
+  if (n_seq == 0) return DFLASH_OK;
+  if (!anchor_ids || (B > 1 && !draft_ids)) return fail(ctx, DFLASH_EINVAL, "null anchor_ids or draft_ids");
+  consume_snapshot(ctx, false);
+
+  const int H = c.hidden, d = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, F = c.ffn;
+  const int M = n_seq * B;
+  const int BN = gemm_token_tile(M);
+  GemmWork work = gemm_work(ctx);
+  const SeqState ss = seq_state(ctx);
+
+  // attention work split from the host's length bounds
+  long long tiles_ub = 0;
+  for (int i = 0; i < n_seq; ++i) tiles_ub += 1LL * nkv * (ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1);
+  const int grid_full = 2 * ctx->num_sms;
+  int chunk = std::max(2, ceil_div(tiles_ub, 2LL * grid_full));
+  auto items_for = [&](int ch) {
+    long long it = 0;
+    for (int i = 0; i < n_seq; ++i) it += 1LL * nkv * ceil_div(ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1, ch);
+    return it;
+  };
+  while (items_for(chunk) > ctx->items_cap) chunk *= 2;
+  const int attn_grid = static_cast<int>(std::min<long long>(items_for(chunk), grid_full));
+
+  const int Bb = attention_block_rows(B);
+  const CUtensorMap* km = blk_map(ctx, ctx->kb, M, Bb);
+  const CUtensorMap* vm = blk_map(ctx, ctx->vb, M, Bb);
+  const CUtensorMap* hmap = act_map(ctx, ctx->h, M, H, BN);
+  const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, BN);
+  const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, BN);
+  if (!km || !vm || !hmap || !amap || !fmap) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+
+  double ctx_tokens = 0, attn_flops = 0;
+  for (int i = 0; i < n_seq; ++i) {
+    ctx_tokens += ctx->len_ub[meta.slot[i]];
+    attn_flops += 4.0 * B * nq * d * (ctx->len_ub[meta.slot[i]] + B);
+  }
+  const double attn_bytes = ctx_tokens * nkv * d * 4 + 1.0 * M * nkv * d * 4 + 1.0 * M * nq * d * 2;
+  {
+    ProfScope ps(ctx, DFLASH_K_NORM, stream, 8.0 * M * H, 0);
+    CK(launch_embed_norm(ctx->w.embed, anchor_ids, c.mask_id, c.vocab, meta, H, ctx->layers[0].g_attn, c.rms_eps,
+                         ctx->x, ctx->h, ctx->d_status, stream));
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = ctx->layers[l];
+    {  // q, k, v with RoPE at positions len .. len+B-1
+      AMaps am;
+      am.m[0] = ctx->m_wq[l];
+      am.m[1] = ctx->m_wk[l];
+      am.m[2] = ctx->m_wv[l];
+      ARegions rg = stacked({nq * d, nkv * d, nkv * d});
+      GemmEpi e = base_epi(ctx, EPI_QKV_ROPE);
+      e.out_q = ctx->q;
+      e.out_k = ctx->kb;
+      e.out_v = ctx->vb;
+      e.meta = meta;
+      const double nw = 1.0 * (nq + 2 * nkv) * d;
+      ProfScope ps(ctx, DFLASH_K_QKV, stream, gemm_bytes(M, nw, H, nw, 2), 2.0 * M * nw * H);
+      CK(launch_gemm(am, rg, *hmap, M, (nq + 2 * nkv) * d, H, 0, e, work, ctx->num_sms, stream));
+    }
+    {  // non-causal attention over the injected context and the block
+      AttnArgs a;
+      std::memset(&a, 0, sizeof(a));
+      a.meta = meta;
+      a.seqs = ss;
+      a.layer = l;
+      a.n_q_heads = nq;
+      a.n_kv_heads = nkv;
+      a.head_dim = d;
+      a.pool_pages = c.max_pages;
+      a.chunk_tiles = chunk;
+      a.items_cap = ctx->items_cap;
+      a.q = ctx->q;
+      a.part_o = ctx->part_o;
+      a.part_ml = ctx->part_ml;
+      a.out = ctx->attn;
+      a.status = ctx->d_status;
+      {
+        ProfScope ps(ctx, DFLASH_K_ATTN, stream, attn_bytes, attn_flops);
+        CK(launch_attention(ctx->m_pool, *km, *vm, a, attn_grid, 0, stream));
+      }
+      {
+        ProfScope ps(ctx, DFLASH_K_ATTN_COMBINE, stream, 2.0 * M * nq * d, 0);
+        CK(launch_attention(ctx->m_pool, *km, *vm, a, attn_grid, 1, stream));
+      }
+    }
+    {  // x += attn W_o^T
+      AMaps am;
+      am.m[0] = ctx->m_wo[l];
+      GemmEpi e = base_epi(ctx, EPI_F32_ADD);
+      e.out_f32 = ctx->x;
+      e.ld_out = H;
+      ProfScope ps(ctx, DFLASH_K_O, stream, gemm_bytes(M, H, nq * d, H, 8), 2.0 * M * H * nq * d);
+      CK(launch_gemm(am, stacked({H}), *amap, M, H, nq * d, 0, e, work, ctx->num_sms, stream));
+    }
+    {
+      ProfScope ps(ctx, DFLASH_K_NORM, stream, 6.0 * M * H, 0);
+      CK(launch_rmsnorm(ctx->x, M, H, L.g_ffn, c.rms_eps, ctx->h, 0, stream));
+    }
+    {  // act = SiLU(h W_gate^T) * (h W_up^T)
+      AMaps am;
+      am.m[0] = ctx->m_wg[l];
+      am.m[1] = ctx->m_wu[l];
+      ARegions rg;
+      std::memset(&rg, 0, sizeof(rg));
+      rg.n_regions = 2;
+      rg.paired = 1;
+      GemmEpi e = base_epi(ctx, EPI_SWIGLU);
+      e.out_act = ctx->act;
+      e.n_valid = F;
+      ProfScope ps(ctx, DFLASH_K_GATEUP, stream, gemm_bytes(M, 2.0 * F, H, F, 2), 4.0 * M * F * H);
+      CK(launch_gemm(am, rg, *hmap, M, ceil_div(F, 64) * 128, H, 0, e, work, ctx->num_sms, stream));
+    }
+    {  // x += act W_down^T
+      AMaps am;
+      am.m[0] = ctx->m_wd[l];
+      GemmEpi e = base_epi(ctx, EPI_F32_ADD);
+      e.out_f32 = ctx->x;
+      e.ld_out = H;
+      ProfScope ps(ctx, DFLASH_K_DOWN, stream, gemm_bytes(M, H, F, H, 8), 2.0 * M * H * F);
+      CK(launch_gemm(am, stacked({H}), *fmap, M, H, F, 0, e, work, ctx->num_sms, stream));
+    }
+    if (l + 1 < c.n_layers) {
+      ProfScope ps(ctx, DFLASH_K_NORM, stream, 6.0 * M * H, 0);
+      CK(launch_rmsnorm(ctx->x, M, H, ctx->layers[l + 1].g_attn, c.rms_eps, ctx->h, 0, stream));
+    }
+  }
+  ctx->last_rows = M;
+  ctx->last_draft_rows = n_seq * (B - 1);
+  if (B > 1) {
+    const int Md = n_seq * (B - 1);
+    {
+      ProfScope ps(ctx, DFLASH_K_NORM, stream, 6.0 * Md * H, 0);
+      CK(launch_rmsnorm(ctx->x, Md, H, ctx->w.g_final, c.rms_eps, ctx->hn, B, stream));
+    }
+    const CUtensorMap* nm = act_map(ctx, ctx->hn, Md, H, gemm_token_tile(Md));
+    if (!nm) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+    AMaps am;
+    am.m[0] = ctx->m_lm;
+    GemmEpi e = base_epi(ctx, EPI_ARGMAX);
+    e.keys = ctx->keys;
+    e.done = ctx->done;
+    e.out_ids = draft_ids;
+    e.out_logit = ctx->top_logit;
+    ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(Md, c.vocab, H, 1, 8), 2.0 * Md * c.vocab * H);
+    CK(launch_gemm(am, stacked({c.vocab}), *nm, Md, c.vocab, H, 1, e, work, ctx->num_sms, stream));
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, int B, const int32_t* draft_ids,
+                            const int32_t* target_ids, int32_t* tau, int32_t* bonus, void* stream_v) {
+  if (!ctx) return DFLASH_EINVAL;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  SeqMeta meta;
+  dflash_status st = check_seqs(ctx, seq_ids, n_seq, &meta);
+  if (st != DFLASH_OK) return st;
+  if (B < 1 || B > ctx->cfg.max_block) return fail(ctx, DFLASH_EINVAL, "B out of range");
+  meta.B = B;
+  if (n_seq == 0) return DFLASH_OK;
+  if ((B > 1 && !draft_ids) || !target_ids || !tau || !bonus) return fail(ctx, DFLASH_EINVAL, "null pointer");
+  {
+    ProfScope ps(ctx, DFLASH_K_VERIFY, stream, 4.0 * n_seq * (2 * B + 2), 0);
+    CK(launch_verify(meta, seq_state(ctx), draft_ids, target_ids, tau, bonus, stream));
+  }
+  bool had_pending = false;
+  for (int i = 0; i < n_seq; ++i) {
+    const int s = meta.slot[i];
+    had_pending |= ctx->pend[s] > 0;
+    ctx->len_ub[s] += ctx->pend[s];
+    ctx->pend[s] = 0;
+  }
+  if (had_pending) {
+    consume_snapshot(ctx, false);
+    if (!ctx->snap_pending) {
+      CK(cudaMemcpyAsync(ctx->h_snap, ctx->d_len, ctx->cfg.max_seqs * sizeof(int), cudaMemcpyDeviceToHost, stream));
+      CK(cudaEventRecord(ctx->snap_event, stream));
+      std::fill(ctx->added_since.begin(), ctx->added_since.end(), 0);
+      ctx->snap_pending = true;
+    }
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, int32_t* out, void* stream) {
+  if (rows < 0 || cols < 1) return DFLASH_EINVAL;
+  if (rows > 0 && (!logits || !out)) return DFLASH_EINVAL;
+  return launch_rows_argmax_bf16(logits, rows, cols, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DFLASH_OK
+             : DFLASH_ECUDA;
+}
+
+dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0, int n, uint16_t* k_out,
+                                   uint16_t* v_out) {
+  if (!ctx) return DFLASH_EINVAL;
+  const dflash_config& c = ctx->cfg;
+  if (layer < 0 || layer >= c.n_layers || seq < 0 || seq >= c.max_seqs || pos0 < 0 || n < 0)
+    return fail(ctx, DFLASH_EINVAL, "argument out of range");
+  CK(cudaDeviceSynchronize());
+  int len = 0, pend = 0;
+  CK(cudaMemcpy(&len, ctx->d_len + seq, sizeof(int), cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(&pend, ctx->d_pend + seq, sizeof(int), cudaMemcpyDeviceToHost));
+  if (pos0 + n > len + pend) return fail(ctx, DFLASH_EINVAL, "positions beyond the cached tokens");
+  const int d = c.head_dim, nkv = c.n_kv_heads;
+  const size_t page_elems = static_cast<size_t>(2) * nkv * kPage * d;
+  std::vector<uint16_t> buf(page_elems);
+  int cur_page = -1;
+  for (int t = 0; t < n; ++t) {
+    const int pos = pos0 + t;
+    const int pi = pos / kPage;
+    if (pi >= static_cast<int>(ctx->pages[seq].size())) return fail(ctx, DFLASH_EINVAL, "position not paged");
+    const int page = ctx->pages[seq][pi];
+    if (page != cur_page) {
+      const size_t off = (static_cast<size_t>(layer) * c.max_pages + page) * page_elems;
+      CK(cudaMemcpy(buf.data(), ctx->pool + off, page_elems * 2, cudaMemcpyDeviceToHost));
+      cur_page = page;
+    }
+    const int slot = pos % kPage;
+    for (int h = 0; h < nkv; ++h) {
+      const uint16_t* ks = buf.data() + ((static_cast<size_t>(0) * nkv + h) * kPage + slot) * d;
+      const uint16_t* vs = buf.data() + ((static_cast<size_t>(1) * nkv + h) * kPage + slot) * d;
+      if (k_out) std::memcpy(k_out + (static_cast<size_t>(t) * nkv + h) * d, ks, d * 2);
+      if (v_out) std::memcpy(v_out + (static_cast<size_t>(t) * nkv + h) * d, vs, d * 2);
+    }
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_debug_last_draft(dflash_ctx* ctx, float* hidden_out, float* top_logit_out) {
+  if (!ctx) return DFLASH_EINVAL;
+  CK(cudaDeviceSynchronize());
+  if (hidden_out)
+    CK(cudaMemcpy(hidden_out, ctx->x, static_cast<size_t>(ctx->last_rows) * ctx->cfg.hidden * sizeof(float),
+                  cudaMemcpyDeviceToHost));
+  if (top_logit_out && ctx->last_draft_rows)
+    CK(cudaMemcpy(top_logit_out, ctx->top_logit, static_cast<size_t>(ctx->last_draft_rows) * sizeof(float),
+                  cudaMemcpyDeviceToHost));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y, int N, int M, int K, int splits,
+                                void* stream_v) {
+  dflash_ctx* ctx = nullptr;
+  if (!W || !X || !Y || N < 1 || M < 1 || K < 8 || K % 8 || splits < 0) return DFLASH_EINVAL;
+  if (!aligned16(W) || !aligned16(X)) return DFLASH_EINVAL;
+  if (!load_encode()) return DFLASH_ECUDA;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  int dev = 0, sms = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int BN = gemm_token_tile(M);
+  AMaps am;
+  CUtensorMap xm;
+  if (!encode_2d(&am.m[0], W, N, K, 64) || !encode_2d(&xm, X, M, K, BN)) return DFLASH_EINVAL;
+  GemmWork work;
+  work.partial_elems = static_cast<size_t>(16) * ceil_div(M, BN) * BN * ceil_div(N, 128) * 128;
+  work.n_tickets = ceil_div(M, BN) * ceil_div(N, 128);
+  int* status = nullptr;
+  CK(cudaMalloc(&work.partial, work.partial_elems * sizeof(float)));
+  CK(cudaMalloc(&work.tickets, work.n_tickets * sizeof(int) + sizeof(int)));
+  CK(cudaMemsetAsync(work.tickets, 0, work.n_tickets * sizeof(int) + sizeof(int), stream));
+  status = work.tickets + work.n_tickets;
+  GemmEpi e;
+  std::memset(&e, 0, sizeof(e));
+  e.kind = EPI_F32_STORE;
+  e.out_f32 = Y;
+  e.ld_out = N;
+  e.status = status;
+  CK(launch_gemm(am, stacked({N}), xm, M, N, K, splits, e, work, sms, stream));
+  int st = 0;
+  CK(cudaStreamSynchronize(stream));
+  CK(cudaMemcpy(&st, status, sizeof(int), cudaMemcpyDeviceToHost));
+  cudaFree(work.partial);
+  cudaFree(work.tickets);
+  if (st & kDevTimeout) return DFLASH_ETIMEOUT;
+  if (st) return DFLASH_EDEVICE;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_debug_profile(dflash_ctx* ctx, int enable) {
+  if (!ctx) return DFLASH_EINVAL;
+  ctx->prof_on = enable != 0;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_debug_profile_read(dflash_ctx* ctx, dflash_kernel_stat* out, int n) {
+  if (!ctx || (n > 0 && !out)) return DFLASH_EINVAL;
+  CK(cudaDeviceSynchronize());
+  for (const auto& r : ctx->prof_recs) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, ctx->prof_events[r.second], ctx->prof_events[r.second + 1]) == cudaSuccess)
+      ctx->prof_acc[r.first].ms += ms;
+  }
+  ctx->prof_recs.clear();
+  ctx->prof_next = 0;
+  for (int i = 0; i < n && i < DFLASH_K_COUNT; ++i) out[i] = ctx->prof_acc[i];
+  for (auto& a : ctx->prof_acc) a = dflash_kernel_stat{};
+  return DFLASH_OK;
+}
+
+}  // extern "C"

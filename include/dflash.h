@@ -1,0 +1,248 @@
+/*
+ * dflash.h - C ABI of the DFlash drafter pass on one NVIDIA GB300 (sm_103a).
+ *
+ * The library implements the data-parallel hot path of DFlash block-diffusion
+ * speculative decoding ("DFlash - Block Diffusion for Flash Speculative
+ * Decoding", notes on the paper, sections 4.2-4.5):
+ *
+ *   dflash_fuse_ctx  fuses the target model's multi-layer hidden features
+ *                    (section 4.2, fusion equation) and injects them as K/V
+ *                    into every drafter layer's context cache (section 4.3,
+ *                    the K_i / V_i equations);
+ *   dflash_draft     runs one non-causal pass over [anchor, MASK x (B-1)] and
+ *                    returns B-1 greedy draft ids (section 4.4);
+ *   dflash_verify    greedy acceptance against the target's argmax ids with
+ *                    the bonus token, then commit / roll back the cache
+ *                    (section 4.5; tau as defined in section 2.2).
+ *
+ * Conventions (all entry points):
+ *  - Every call returns a dflash_status. Nothing throws across the ABI.
+ *    dflash_last_error() describes the last failure of a context.
+ *  - Tensors named "device" are caller-owned device pointers; tensors named
+ *    "host" are caller-owned host pointers. The library never frees either.
+ *  - Floating-point tensors are bf16 (passed as uint16_t bit patterns) or
+ *    fp32 where stated; ids are int32.
+ *  - Matrices are row-major, weights in nn.Linear layout [out, in].
+ *  - Calls that take a cudaStream_t (passed as void*) are asynchronous on that
+ *    stream and never synchronise the host. One context must be driven from
+ *    one stream at a time. Device-side faults that kernels detect (a bounded
+ *    wait that ran out, an index out of range) are latched in a status word
+ *    that dflash_sync() reports.
+ *  - Weights are borrowed: they must stay valid and unchanged for the life of
+ *    the context. The library owns the KV pool, page tables and workspaces it
+ *    allocates in dflash_create().
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DFLASH_OK = 0,
+  DFLASH_EINVAL = 1,   /* bad argument; nothing was enqueued                  */
+  DFLASH_ENOMEM = 2,   /* KV page pool or device memory exhausted              */
+  DFLASH_ECUDA = 3,    /* a CUDA runtime call failed                           */
+  DFLASH_ETIMEOUT = 4, /* a kernel's bounded wait ran out (reported by sync)   */
+  DFLASH_EDEVICE = 5   /* a kernel detected an out-of-range index (by sync)    */
+} dflash_status;
+
+typedef struct dflash_ctx dflash_ctx;
+
+/* Drafter shape and capacity. Shape fields follow the DFlash notes' setup
+ * (5 drafter layers, 5 fused target layers, block size 16) but any values
+ * meeting the stated constraints are accepted. */
+typedef struct {
+  int hidden;          /* H; multiple of 64                                          */
+  int n_heads;         /* query heads; n_heads * head_dim multiple of 128            */
+  int n_kv_heads;      /* kv heads; divides n_heads; n_kv_heads * head_dim mult. 128  */
+  int head_dim;        /* d: 64 or 128                                               */
+  int ffn;             /* F: SwiGLU width; multiple of 8                             */
+  int vocab;           /* V: shared embedding / LM head rows                         */
+  int n_layers;        /* L drafter layers, 1..16                                    */
+  int n_feat_layers;   /* L_f target layers fused by W_c, 1..16                       */
+  float rope_base;     /* RoPE theta base (rotate-half pairing (i, i+d/2))            */
+  float rms_eps;       /* RMSNorm epsilon                                            */
+  int mask_id;         /* id of the MASK token                                       */
+  int max_seqs;        /* sequence slots: seq ids are 0..max_seqs-1                   */
+  int max_batch;       /* most sequences in one call, 1..64                          */
+  int max_block;       /* largest block B, 1..32                                     */
+  int max_ctx;         /* most cached tokens per sequence (committed + pending)      */
+  int max_pages;       /* KV pool size in 64-token pages (shared by all sequences)   */
+  int max_fuse_tokens; /* most feature rows in one dflash_fuse_ctx call               */
+} dflash_config;
+
+/* One drafter layer's weights, device pointers to bf16 (nn.Linear layout). */
+typedef struct {
+  const uint16_t* w_q;    /* [n_heads*d,    H]                      */
+  const uint16_t* w_k;    /* [n_kv_heads*d, H]  also projects H_t   */
+  const uint16_t* w_v;    /* [n_kv_heads*d, H]  also projects H_t   */
+  const uint16_t* w_o;    /* [H, n_heads*d]                         */
+  const uint16_t* w_gate; /* [F, H]                                 */
+  const uint16_t* w_up;   /* [F, H]                                 */
+  const uint16_t* w_down; /* [H, F]                                 */
+  const uint16_t* g_attn; /* [H] input RMSNorm gain                 */
+  const uint16_t* g_ffn;  /* [H] post-attention RMSNorm gain        */
+} dflash_layer_weights;
+
+/* All drafter weights, device pointers to bf16. `layers` is a HOST array of
+ * n_layers entries (copied by dflash_create). */
+typedef struct {
+  const uint16_t* w_c;     /* [H, L_f*H] shared fusion projection W_c        */
+  const uint16_t* g_c;     /* [H] fusion RMSNorm gain                        */
+  const uint16_t* embed;   /* [V, H] shared token embedding                  */
+  const uint16_t* lm_head; /* [V, H] shared LM head                          */
+  const uint16_t* g_final; /* [H] final RMSNorm gain                         */
+  const dflash_layer_weights* layers;
+} dflash_weights;
+
+/* Create a context on the current CUDA device: validates the config,
+ * allocates the KV pool (n_layers * max_pages * 2 * n_kv_heads * 64 * d bf16,
+ * zero-filled), page tables, RoPE table and workspaces, and encodes TMA
+ * descriptors for the weights. Synchronises the device.
+ * Errors: EINVAL (config out of range, null pointer, weight not 16-byte
+ * aligned), ENOMEM, ECUDA. On error *out is NULL. */
+dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_ctx** out);
+
+/* Synchronise the device and free everything the context allocated. */
+dflash_status dflash_destroy(dflash_ctx* ctx);
+
+/* Static description of the last error of ctx (or of the last failed
+ * dflash_create when ctx is NULL). Never NULL. */
+const char* dflash_last_error(const dflash_ctx* ctx);
+
+/* Forget sequence `seq`: committed and pending lengths become 0 and its pages
+ * return to the pool. Synchronises the device. EINVAL if seq is out of range. */
+dflash_status dflash_seq_reset(dflash_ctx* ctx, int seq);
+
+/* Exact committed and pending lengths of `seq`. Synchronises the device.
+ * Either output pointer may be NULL. */
+dflash_status dflash_seq_len(dflash_ctx* ctx, int seq, int* committed, int* pending);
+
+/* Append fused target features to the drafter's context cache (KV injection).
+ *
+ * DFlash notes 4.2-4.3: H_t = RMSNorm(W_c [H^(l1); ...; H^(lLf)]) per token,
+ * then for every layer i: K_i = RoPE(W_i^K H_t), V_i = W_i^V H_t, written to
+ * the paged cache at the token's absolute position.
+ *
+ *  seq_ids  host  [n_seq]       distinct sequence slots
+ *  n_new    host  [n_seq]       tokens appended per sequence (>= 0)
+ *  feats    device [sum(n_new), L_f*H] bf16, rows grouped by sequence in
+ *           seq_ids order; each row is the target's hidden states of L_f
+ *           layers, layer-major (shallow to deep).
+ *  pending  0: the tokens are committed at once (sequence must have no pending
+ *              tokens); 1: the tokens are speculative until the next
+ *              dflash_verify, which commits the first tau of them.
+ * Positions: the i-th new token of a sequence goes to position
+ * committed + pending + i. Errors: EINVAL (n_seq > max_batch, sum(n_new) >
+ * max_fuse_tokens, length would exceed max_ctx, duplicate seq, committed
+ * append with pending tokens), ENOMEM (page pool exhausted; nothing enqueued).
+ */
+dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq,
+                              const int32_t* n_new, const uint16_t* feats, int pending,
+                              void* stream);
+
+/* One parallel drafting pass (DFlash notes 4.4): for each sequence the block
+ * [anchor, MASK x (B-1)] at positions committed .. committed+B-1 runs once
+ * through every drafter layer, attending without a causal mask to itself and
+ * to the sequence's committed injected context; the final RMSNorm and the
+ * shared LM head score every masked position and the greedy (argmax, lowest
+ * index on ties) id is returned. Pending tokens are not attended.
+ *
+ *  seq_ids    host   [n_seq]
+ *  anchor_ids device [n_seq] int32, the last verified token of each sequence
+ *  B          1..max_block (B = 1 runs the layers and returns no ids)
+ *  draft_ids  device [n_seq, B-1] int32 output
+ * Errors: EINVAL. */
+dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq,
+                           const int32_t* anchor_ids, int B, int32_t* draft_ids,
+                           void* stream);
+
+/* Greedy verify and commit (DFlash notes 4.5): per sequence,
+ * a = number of leading j in 0..B-2 with draft[j] == target[j] (draft[j] is
+ * the drafter's id for block position j+1, target[j] the target's greedy id
+ * after block position j); tau = a + 1, bonus = target[a]. Then the first
+ * min(tau, pending) pending tokens are committed and the rest discarded.
+ *
+ *  draft_ids  device [n_seq, B-1] int32
+ *  target_ids device [n_seq, B]   int32
+ *  tau, bonus device [n_seq]      int32 outputs
+ * Errors: EINVAL. */
+dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, int B,
+                            const int32_t* draft_ids, const int32_t* target_ids,
+                            int32_t* tau, int32_t* bonus, void* stream);
+
+/* Row-wise argmax of bf16 logits (lowest index on ties): the target's greedy
+ * ids that dflash_verify consumes. Stateless.
+ *  logits device [rows, cols] bf16 (row pitch = cols); out device [rows] int32.
+ * Errors: EINVAL (rows < 0, cols < 1, null pointer when rows > 0). */
+dflash_status dflash_rows_argmax_bf16(const uint16_t* logits, int rows, int cols,
+                                      int32_t* out, void* stream);
+
+/* Wait for all work on the device, then report and clear the context's
+ * device status word: OK, ETIMEOUT or EDEVICE. */
+dflash_status dflash_sync(dflash_ctx* ctx);
+
+/* ---- inspection hooks (used by the parity tests; they synchronise) ---- */
+
+/* Copy `n` cached tokens of layer `layer` of `seq`, starting at position
+ * `pos0`, to host buffers k_out / v_out, each [n, n_kv_heads, d] bf16.
+ * Positions may reach into the pending tokens. */
+dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0, int n,
+                                   uint16_t* k_out, uint16_t* v_out);
+
+/* State of the last dflash_draft call: the final residual stream
+ * [n_seq*B, H] fp32 (before the final RMSNorm), and the winning logit of each
+ * draft row [n_seq*(B-1)] fp32. Host outputs; either may be NULL. */
+dflash_status dflash_debug_last_draft(dflash_ctx* ctx, float* hidden_out, float* top_logit_out);
+
+/* Y[M, N] (fp32) = X[M, K] * W[N, K]^T with the library's tensor-core GEMM,
+ * all device pointers (W, X bf16; K multiple of 8). splits = split-K factor
+ * (0 = library's choice). For kernel-level tests. */
+dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y,
+                                int N, int M, int K, int splits, void* stream);
+
+/* ---- per-kernel accounting (used by the benchmark) ----
+ * Every kernel launch of a context is counted in one of these classes. While
+ * profiling is enabled, each launch is also bracketed by two CUDA events
+ * recorded on the launch stream, and the algorithmic bytes and flops of the
+ * launch (what the operation must read, write and compute; not including
+ * split-K or attention partials) are accumulated. */
+enum {
+  DFLASH_K_QKV = 0,       /* q/k/v projection + RoPE                    */
+  DFLASH_K_ATTN,          /* block attention over context chunks        */
+  DFLASH_K_ATTN_COMBINE,  /* merge of the attention chunks              */
+  DFLASH_K_O,             /* output projection + residual               */
+  DFLASH_K_GATEUP,        /* gate/up projection + SwiGLU                */
+  DFLASH_K_DOWN,          /* down projection + residual                 */
+  DFLASH_K_LMHEAD,        /* LM head + argmax                           */
+  DFLASH_K_FUSE_WC,       /* fusion projection W_c                      */
+  DFLASH_K_FUSE_KV,       /* context K/V projection + RoPE + append     */
+  DFLASH_K_NORM,          /* embedding and RMSNorm rows                 */
+  DFLASH_K_VERIFY,        /* verify + commit                            */
+  DFLASH_K_OTHER,         /* bookkeeping kernels                        */
+  DFLASH_K_COUNT
+};
+
+typedef struct {
+  long long launches; /* kernels launched                                 */
+  double ms;          /* summed event-timed duration (profiling enabled)  */
+  double bytes;       /* summed algorithmic bytes                          */
+  double flops;       /* summed algorithmic flops                          */
+} dflash_kernel_stat;
+
+/* Enable (1) or disable (0) event timing of every launch of ctx. Counts and
+ * algorithmic totals are kept in either case. */
+dflash_status dflash_debug_profile(dflash_ctx* ctx, int enable);
+
+/* Synchronise, copy min(n, DFLASH_K_COUNT) class totals to `out` (host), and
+ * reset the totals. */
+dflash_status dflash_debug_profile_read(dflash_ctx* ctx, dflash_kernel_stat* out, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

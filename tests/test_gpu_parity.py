@@ -1,0 +1,192 @@
+"""CUDA path against the CPU oracle through the C ABI.
+
+Tiny drafter (oracle in fp64): cached K/V after fusion, draft ids / residual
+stream / winning logits, verify + commit + rollback over several cycles,
+ragged and empty contexts, B = 1..8, several sequences per call.
+Qwen3-8B-shaped drafter (oracle in fp32): reduced depth at ragged contexts,
+and the full 5-layer pass at context 4096, B = 16 (the benchmarked shape).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import (TINY, QWEN3_8B, make_weights_np, make_features_np, make_anchor_ids_np,
+                   make_weights_torch, torch_weights_to_np)
+from tests.gpu_util import (np_weights_to_device, bf16_dev, i32_dev, assert_close, compare_draft, GAP,
+                            ROW_REL_HIGH_GAIN)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def dfl():
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_diffusion_drafter_pass_gb300 as m
+    return m
+
+
+def _check_kv(d, orc, seqs, layers, what, row_rel=None):
+    for s in seqs:
+        n = orc.seq_len(s)[0] + orc.seq_len(s)[1]
+        if n == 0:
+            continue
+        st = orc.seqs[s]
+        for l in layers:
+            k, v = d.read_kv(l, s, 0, n)
+            assert_close(k, st["k"][l][:n], f"{what}: K layer {l} seq {s}", row_rel=row_rel)
+            assert_close(v, st["v"][l][:n], f"{what}: V layer {l} seq {s}", row_rel=row_rel)
+
+
+def _draft_and_compare(d, orc, seqs, anchors, B, what, row_rel=None):
+    ids = d.draft(seqs, i32_dev(anchors, DEV), B)
+    d.sync()
+    ref = orc.draft(seqs, anchors, B)
+    hid, top = d.last_draft(len(seqs), B)
+    got = ids.cpu().numpy()
+    checked = 0
+    for i in range(len(seqs)):
+        checked += compare_draft(got[i] if B > 1 else [], hid[i * B:(i + 1) * B],
+                                 top[i * (B - 1):(i + 1) * (B - 1)], ref[i], B, f"{what} seq {seqs[i]}",
+                                 row_rel=row_rel)
+    return got, ref, checked
+
+
+@pytest.mark.parametrize("std", [0.02, 0.1])
+def test_tiny_fuse_draft_parity(dfl, std):
+    row_rel = None if std == 0.02 else ROW_REL_HIGH_GAIN
+    sh = TINY
+    wn = make_weights_np(sh, seed=21, gamma="jitter", std=std)
+    orc = oracle.OracleDrafter(sh, wn)
+    width = sh.n_feat_layers * sh.hidden
+    with dfl.Drafter(sh, np_weights_to_device(wn, DEV), max_seqs=6, max_batch=4, max_block=8, max_ctx=512,
+                     max_fuse_tokens=512) as d:
+        # seq 0: one full page; seq 1: ragged; seq 2: empty; seq 3: three chunks crossing pages
+        plan = {0: [64], 1: [100], 2: [], 3: [30, 70, 100]}
+        rng_seed = 100
+        for s, chunks in plan.items():
+            for n in chunks:
+                f = make_features_np(n, width, seed=rng_seed)
+                rng_seed += 1
+                d.fuse_ctx([s], [n], bf16_dev(f, DEV), pending=False)
+                orc.fuse_ctx([s], [n], f, pending=False)
+        d.sync()
+        _check_kv(d, orc, [0, 1, 3], range(sh.n_layers), "tiny fuse", row_rel)
+        seqs = [0, 1, 2, 3]
+        anchors = make_anchor_ids_np(4, sh.vocab, seed=7)
+        total = 0
+        for B in (4, 1, 2, 8):
+            _, _, c = _draft_and_compare(d, orc, seqs, anchors, B, f"tiny std={std} B={B}", row_rel)
+            total += c
+        # a multi-sequence fuse call with rows grouped per sequence
+        f = make_features_np(3 + 5, width, seed=999)
+        d.fuse_ctx([2, 1], [3, 5], bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx([2, 1], [3, 5], f, pending=False)
+        _check_kv(d, orc, [1, 2], range(sh.n_layers), "tiny multi-seq fuse", row_rel)
+        _, _, c = _draft_and_compare(d, orc, [2, 1], anchors[:2], 4, "tiny after multi-seq fuse", row_rel)
+        total += c
+        assert total > 0
+
+
+def test_tiny_speculative_cycles_commit_and_rollback(dfl):
+    """Draft -> fuse the block's features as pending -> verify against target
+    ids that agree for a seeded number of positions -> commit tau, roll back
+    the rest; repeated, with the caches compared after every cycle."""
+    sh = TINY
+    wn = make_weights_np(sh, seed=31, gamma="jitter", std=0.1)
+    orc = oracle.OracleDrafter(sh, wn)
+    width = sh.n_feat_layers * sh.hidden
+    B = 6
+    seqs = [0, 1, 2]
+    rng = np.random.Generator(np.random.PCG64(32))
+    with dfl.Drafter(sh, np_weights_to_device(wn, DEV), max_seqs=3, max_batch=3, max_block=B, max_ctx=1024,
+                     max_fuse_tokens=512) as d:
+        ctx = [70, 5, 128]
+        f = make_features_np(sum(ctx), width, seed=33)
+        d.fuse_ctx(seqs, ctx, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(seqs, ctx, f, pending=False)
+        anchors = make_anchor_ids_np(3, sh.vocab, seed=34)
+        taus = []
+        for cyc in range(6):
+            got, ref, _ = _draft_and_compare(d, orc, seqs, anchors, B, f"cycle {cyc}", ROW_REL_HIGH_GAIN)
+            drafts = np.stack([r["draft"] for r in ref]).astype(np.int32)
+            # targets agree with the oracle's drafts for m positions, then differ
+            t = rng.integers(0, sh.vocab, size=(3, B)).astype(np.int32)
+            for i in range(3):
+                m = int(rng.integers(0, B))
+                t[i, :m] = drafts[i, :m]
+                if m < B - 1:
+                    t[i, m] = (drafts[i, m] + 1) % sh.vocab
+            fb = make_features_np(3 * B, width, seed=200 + cyc)
+            d.fuse_ctx(seqs, [B] * 3, bf16_dev(fb, DEV), pending=True)
+            orc.fuse_ctx(seqs, [B] * 3, fb, pending=True)
+            tau, bonus = d.verify(seqs, B, i32_dev(drafts, DEV), i32_dev(t, DEV))
+            rt, rb = orc.verify(seqs, B, drafts, t)
+            d.sync()
+            np.testing.assert_array_equal(tau.cpu().numpy(), rt)
+            np.testing.assert_array_equal(bonus.cpu().numpy(), rb)
+            taus += list(rt)
+            for s in seqs:
+                assert d.seq_len(s) == orc.seq_len(s)
+            _check_kv(d, orc, seqs, [0], f"cycle {cyc}", ROW_REL_HIGH_GAIN)
+            anchors = rb.astype(np.int32)
+        assert max(taus) > 1 and min(taus) < B
+
+
+def _big_setup(n_layers, seed):
+    shape = QWEN3_8B.with_layers(n_layers)
+    wt = make_weights_torch(shape, seed=seed, device=DEV, gamma="jitter")
+    wn = torch_weights_to_np(wt)
+    return shape, wt, wn
+
+
+def test_qwen3_8b_shape_two_layers_ragged(dfl):
+    """8B width, 2 layers: two sequences with ragged contexts (300 and 1000
+    tokens, appended in uneven chunks), B = 16 and B = 8."""
+    shape, wt, wn = _big_setup(2, seed=41)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    width = shape.n_feat_layers * shape.hidden
+    with dfl.Drafter(shape, wt, max_seqs=2, max_batch=2, max_block=16, max_ctx=2048,
+                     max_fuse_tokens=1024) as d:
+        f = make_features_np(1300, width, seed=42)
+        d.fuse_ctx([0, 1], [300, 700], bf16_dev(f[:1000], DEV), pending=False)
+        orc.fuse_ctx([0, 1], [300, 700], f[:1000], pending=False)
+        d.fuse_ctx([1], [300], bf16_dev(f[1000:], DEV), pending=False)
+        orc.fuse_ctx([1], [300], f[1000:], pending=False)
+        d.sync()
+        for s in (0, 1):
+            n = orc.seq_len(s)[0]
+            for l in range(2):
+                k, v = d.read_kv(l, s, 0, n)
+                kr, vr = orc.context(s, l)
+                assert_close(k, kr, f"8B K layer {l} seq {s}")
+                assert_close(v, vr, f"8B V layer {l} seq {s}")
+        anchors = make_anchor_ids_np(2, shape.vocab, seed=43)
+        for B in (16, 8):
+            _, _, checked = _draft_and_compare(d, orc, [0, 1], anchors, B, f"8B 2-layer B={B}")
+            assert checked > 0
+
+
+def test_qwen3_8b_full_depth_context_4096(dfl):
+    """The benchmarked workload: 5 layers, batch 1, context 4096, B = 16."""
+    shape, wt, wn = _big_setup(5, seed=0)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    width = shape.n_feat_layers * shape.hidden
+    with dfl.Drafter(shape, wt, max_seqs=1, max_batch=1, max_block=16, max_ctx=4096 + 64,
+                     max_fuse_tokens=4096) as d:
+        f = make_features_np(4096, width, seed=1)
+        d.fuse_ctx([0], [4096], bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx([0], [4096], f, pending=False)
+        d.sync()
+        # sampled cache rows: first, page boundaries, last
+        for l in (0, 4):
+            for p0 in (0, 63, 64, 2047, 4095):
+                k, v = d.read_kv(l, 0, p0, 1)
+                st = orc.seqs[0]
+                assert_close(k, st["k"][l][p0:p0 + 1], f"8B K layer {l} pos {p0}")
+                assert_close(v, st["v"][l][p0:p0 + 1], f"8B V layer {l} pos {p0}")
+        anchors = make_anchor_ids_np(1, shape.vocab, seed=2)
+        _, ref, checked = _draft_and_compare(d, orc, [0], anchors, 16, "8B full depth C=4096")
+        assert checked >= 5, f"only {checked} rows with gap > {GAP}"
