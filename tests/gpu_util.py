@@ -34,6 +34,25 @@ def assert_close(got, ref, what, rtol=RTOL, atol=ATOL, row_rel=None):
     assert ok, f"{what}: max abs error {worst:.4g} outside {crit}"
 
 
+# Hidden states (residual stream) of a bf16-storage pass differ from an exact
+# pass by ~1% of the row's norm: numpy emulation of the library's rounding
+# points gives 1.0% per-row relative L2 error at the Qwen3-8B shape (2
+# layers) and a worst element of 0.150 on rows of magnitude up to 13, so an
+# elementwise 5e-2 + 2e-2|x| bound fails for ~2% of elements even for an
+# exact emulation (tests/test_tolerance_derivation.py). The stated "2e-2
+# relative" is therefore applied to each row's L2 norm, with an elementwise
+# guard of ATOL + RTOL * max|row|.
+HID_REL_L2 = 2e-2
+
+
+def assert_hidden_close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rel = np.linalg.norm(got - ref, axis=-1) / np.maximum(np.linalg.norm(ref, axis=-1), 1e-30)
+    assert float(rel.max()) <= HID_REL_L2, f"{what}: row relative L2 error {rel.max():.4g} > {HID_REL_L2}"
+    assert_close(got, ref, what, row_rel=RTOL)
+
+
 def np_weights_to_device(wn, device):
     import torch
     cv = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).to(device)
@@ -54,7 +73,7 @@ def i32_dev(a, device):
 
 def compare_draft(got_ids, got_hidden, got_top, ref, B, what, row_rel=None):
     """Compare one sequence's draft against the oracle's result dict."""
-    assert_close(got_hidden, ref["hidden"], f"{what}: final residual stream", row_rel=row_rel)
+    assert_hidden_close(got_hidden, ref["hidden"], f"{what}: final residual stream")
     if B > 1:
         assert_close(got_top, ref["top1"], f"{what}: winning logits", row_rel=row_rel)
         sure = ref["gap"] > GAP
