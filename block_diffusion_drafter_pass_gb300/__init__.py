@@ -26,7 +26,7 @@ EXPORTED = (
     "dflash_create", "dflash_destroy", "dflash_last_error", "dflash_seq_reset", "dflash_seq_len",
     "dflash_fuse_ctx", "dflash_draft", "dflash_verify", "dflash_rows_argmax_bf16", "dflash_sync",
     "dflash_debug_read_kv", "dflash_debug_last_draft", "dflash_debug_gemm", "dflash_debug_profile",
-    "dflash_debug_profile_read",
+    "dflash_debug_profile_read", "dflash_gemm_noalloc",
 )
 
 # Kernel classes of the per-kernel accounting (DFLASH_K_* in include/dflash.h).
@@ -92,6 +92,7 @@ def load_library() -> ctypes.CDLL:
         "dflash_debug_gemm": ([VP, VP, VP, I, I, I, I, VP], I),
         "dflash_debug_profile": ([VP, I], I),
         "dflash_debug_profile_read": ([VP, P(dflash_kernel_stat), I], I),
+        "dflash_gemm_noalloc": ([VP, VP, VP, I, I, I, I, VP], I),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -143,6 +144,19 @@ def dflash_debug_gemm(W, X, splits: int = 0, stream=None):
     M = X.shape[0]
     Y = torch.empty(M, N, dtype=torch.float32, device=W.device)
     _check(load_library().dflash_debug_gemm(_ptr(W), _ptr(X), _ptr(Y), N, M, K, splits, _stream(stream)))
+    return Y
+
+
+def dflash_gemm_noalloc(W, X, Y=None, splits: int = 0, stream=None):
+    """Y = X W^T (fp32) with no device allocation inside the library; the
+    split-K scratch is a fixed array the library keeps on each GPU. Pass Y
+    (fp32 [M, N], preallocated) when the caller itself cannot allocate."""
+    import torch
+    N, K = W.shape
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty(M, N, dtype=torch.float32, device=W.device)
+    _check(load_library().dflash_gemm_noalloc(_ptr(W), _ptr(X), _ptr(Y), N, M, K, splits, _stream(stream)))
     return Y
 
 

@@ -104,6 +104,11 @@ cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUten
 // height must equal it.
 int gemm_token_tile(int M);
 
+// Row-major [rows, cols] bf16 TMA descriptor (box 64 x box_rows, 128B swizzle).
+bool encode_matrix_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// Message returned by dflash_last_error(NULL).
+void set_unattached_error(const char* msg);
+
 // ----------------------------------------------------------------------------
 // Block attention (split over context chunks) + combine
 // ----------------------------------------------------------------------------

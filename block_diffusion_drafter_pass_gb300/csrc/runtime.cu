@@ -68,6 +68,15 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 
 }  // namespace
 
+namespace dfl {
+// Descriptor helpers and the context-free error string, for entry points
+// defined in other translation units.
+bool encode_matrix_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return load_encode() && encode_2d(m, ptr, rows, cols, box_rows);
+}
+void set_unattached_error(const char* msg) { g_create_error = msg; }
+}  // namespace dfl
+
 struct dflash_ctx {
   dflash_config cfg{};
   dflash_weights w{};

@@ -205,6 +205,29 @@ dflash_status dflash_debug_last_draft(dflash_ctx* ctx, float* hidden_out, float*
 dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y,
                                 int N, int M, int K, int splits, void* stream);
 
+/* Y[M, N] (fp32) = X[M, K] * W[N, K]^T, like dflash_debug_gemm, but without
+ * allocating any device memory. The pages have no counterpart: this serves
+ * callers that cannot call cudaMalloc, e.g. a loop that must not risk the
+ * implicit device synchronisation of cudaMalloc/cudaFree, a process whose
+ * free device memory is held by a caching allocator, or code running while
+ * another thread has a global-mode stream capture in progress.
+ * The split-K workspace, tile tickets and status word live in one fixed
+ * 8 MiB + 16 KiB device array inside the library, which every GPU that loads
+ * the library holds until the process exits. The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress); make that
+ * first call before starting any stream capture. Every call shares the
+ * array: the tickets and status are cleared at the start of each call, and
+ * calls that overlap on the GPU (other threads or streams) race on it.
+ * The call waits for its stream before returning.
+ * W, X, Y: device pointers (W, X bf16, 16-byte aligned; K a multiple of 8).
+ * splits: split-K factor, 0 = chosen to fit the array.
+ * Errors: EINVAL for bad arguments or when an explicit `splits` needs more
+ * than the fixed scratch (splits x roundup(M) x roundup(N, 128) floats above
+ * 2^21, or more than 4096 output tiles); ECUDA; ETIMEOUT/EDEVICE as reported
+ * by the kernel. Messages via dflash_last_error(NULL). */
+dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* X, float* Y,
+                                  int N, int M, int K, int splits, void* stream);
+
 /* ---- per-kernel accounting (used by the benchmark) ----
  * Every kernel launch of a context is counted in one of these classes. While
  * profiling is enabled, each launch is also bracketed by two CUDA events
