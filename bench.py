@@ -315,7 +315,8 @@ def run_ours(args):
         lens = [ctx] * batch
     # start short of the nominal length so the timed region is centred on it
     start_lens = [max(0, c - W - K // 2) for c in lens]
-    cyc = Cycle(dfl, QWEN3_8B, batch, start_lens, B, total_steps, seed=1000 * rank, dev=dev)
+    shape = QWEN3_8B.with_layers(args.layers)
+    cyc = Cycle(dfl, shape, batch, start_lens, B, total_steps, seed=1000 * rank, dev=dev)
 
     for k in range(W):
         cyc.step(k)
@@ -372,7 +373,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) features, N(0,3) target logits)",
-        "config": {"workload": args.workload, "model": "Qwen3-8B-shaped DFlash drafter (5 layers, H 4096, "
+        "config": {"workload": args.workload, "model": f"Qwen3-8B-shaped DFlash drafter ({args.layers} layers, H 4096, "
                    "32/8 heads x 128, FFN 12288, V 151936, 5 fused target layers)",
                    "batch_per_gpu": batch, "block": B,
                    "context": ctx if ctx else f"U[{spread[0]}, {spread[1]}]",
@@ -396,7 +397,7 @@ def run_ours(args):
         "kernels": kernels,
     }
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(QWEN3_8B, cyc.weights, lens[0] if batch == 1 else lens[0], B)
+        out["cpu_baseline"] = cpu_baseline(shape, cyc.weights, lens[0], B)
     return out
 
 
@@ -470,6 +471,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_8b_b1_ctx4096")
     ap.add_argument("--block", type=int, default=16)
+    ap.add_argument("--layers", type=int, default=5,
+                    help="drafter depth (5 = the benchmarked drafter; fewer only for small profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

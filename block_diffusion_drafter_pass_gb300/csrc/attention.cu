@@ -122,6 +122,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     s_prefix[n_seq] = acc;
   }
   __syncthreads();
+  grid_dep_launch();
   const int total = s_prefix[n_seq];
 
   if (warp == NCW) {
@@ -331,39 +332,81 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     }
   }
   __syncthreads();
-  grid_dep_launch();
 }
 
-// Merge the chunks of one (sequence, query head): grid (n_q heads, n_seq),
-// one thread per head dimension.
+// Merge the chunks of each row: grid (n_q heads, n_seq, ceil(B/4)), one warp
+// per (head, block row). Lanes split the chunks for the running max and sum,
+// then read each chunk's partial row as one coalesced 16-byte-per-lane load
+// (D = 128) and accumulate it with its weight exp2(m_c - M).
+constexpr int kCombineWarps = 4;
+constexpr int kCombineMaxChunks = 2048;
+
 template <int D, int NCW>
-__global__ void __launch_bounds__(D) attn_combine_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int kRowsPad = 16 * NCW;
+  constexpr int kPer = D / 32;                 // dims per lane: 4 (D = 128) or 2 (D = 64)
+  __shared__ float wsm[kCombineWarps][kCombineMaxChunks];
   grid_dep_wait();
-  const int hq = blockIdx.x, i = blockIdx.y, dim = threadIdx.x;
+  grid_dep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hq = blockIdx.x, i = blockIdx.y;
+  const int j = blockIdx.z * kCombineWarps + warp;
+  const int B = a.meta.B;
   const int nkv = a.n_kv_heads, G = a.n_q_heads / nkv;
   const int kvh = hq / G, gh = hq - kvh * G;
-  const int B = a.meta.B;
   int base = 0;
   for (int s = 0; s < i; ++s) base += nkv * seq_split(a, s).n_chunks;
   const int nch = seq_split(a, i).n_chunks;
   base += kvh * nch;
-  if (base + nch > a.items_cap) return;
-  for (int j = 0; j < B; ++j) {
-    const int r = gh * B + j;
-    float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, a.part_ml[static_cast<size_t>(base + c) * kRowsPad + r].x);
-    float L = 0.f, acc = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const float2 ml = a.part_ml[static_cast<size_t>(base + c) * kRowsPad + r];
-      const float w = exp2f(ml.x - M);
-      L += w * ml.y;
-      acc += w * a.part_o[(static_cast<size_t>(base + c) * kRowsPad + r) * D + dim];
-    }
-    a.out[static_cast<size_t>(i * B + j) * a.n_q_heads * D + static_cast<size_t>(hq) * D + dim] =
-        f32_to_bf16(acc / L);
+  if (j >= B || base + nch > a.items_cap || nch > kCombineMaxChunks) {
+    if (j < B && lane == 0) latch_status(a.status, kDevBounds);
+    return;
   }
-  grid_dep_launch();
+  const int r = gh * B + j;
+  float M = -INFINITY;
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.part_ml[static_cast<size_t>(base + c) * kRowsPad + r].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = 0.f;
+  for (int c = lane; c < nch; c += 32) {
+    const float2 ml = a.part_ml[static_cast<size_t>(base + c) * kRowsPad + r];
+    const float w = exp2f(ml.x - M);
+    wsm[warp][c] = w;
+    L += w * ml.y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  __syncwarp();
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  const float* po = a.part_o + (static_cast<size_t>(base) * kRowsPad + r) * D + lane * kPer;
+  const size_t stride = static_cast<size_t>(kRowsPad) * D;
+  int c = 0;
+  for (; c + 4 <= nch; c += 4) {
+    float v[4][kPer];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if constexpr (kPer == 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(po + (c + u) * stride));
+        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+      } else {
+        const float2 t = __ldcg(reinterpret_cast<const float2*>(po + (c + u) * stride));
+        v[u][0] = t.x; v[u][1] = t.y;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] += wsm[warp][c + u] * v[u][e];
+  }
+  for (; c < nch; ++c)
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] += wsm[warp][c] * __ldcg(po + c * stride + e);
+  const float inv = 1.f / L;
+  uint16_t* out = a.out + static_cast<size_t>(i * B + j) * a.n_q_heads * D + static_cast<size_t>(hq) * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) out[e] = f32_to_bf16(acc[e] * inv);
 }
 
 template <int D, int NCW>
@@ -378,16 +421,36 @@ cudaError_t launch_dn(const CUtensorMap& pm, const CUtensorMap& km, const CUtens
       if (e != cudaSuccess) return e;
       attr_set = true;
     }
-    attn_kernel<D, NCW><<<grid, (NCW + 1) * 32, C::kSmem, stream>>>(pm, km, vm, a);
-  } else {
-    attn_combine_kernel<D, NCW><<<dim3(a.n_q_heads, a.meta.n_seq), D, 0, stream>>>(a);
+    return launch_pdl(attn_kernel<D, NCW>, dim3(grid), dim3((NCW + 1) * 32), C::kSmem, stream, pm, km, vm, a);
   }
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel<D, NCW>,
+                    dim3(a.n_q_heads, a.meta.n_seq, (a.meta.B + kCombineWarps - 1) / kCombineWarps),
+                    dim3(32 * kCombineWarps), 0, stream, a);
 }
 
 }  // namespace
 
 int attention_block_rows(int B) { return block_rows(B); }
+
+int attention_ctas_per_sm(int head_dim, int ncw) {
+  int n = 0;
+  auto q = [&](auto kern, int threads, int smem) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) n = 1;
+  };
+  if (head_dim == 128) {
+    if (ncw <= 1) q(attn_kernel<128, 1>, 64, ACfg<128>::kSmem);
+    else if (ncw <= 2) q(attn_kernel<128, 2>, 96, ACfg<128>::kSmem);
+    else if (ncw <= 4) q(attn_kernel<128, 4>, 160, ACfg<128>::kSmem);
+    else q(attn_kernel<128, 8>, 288, ACfg<128>::kSmem);
+  } else {
+    if (ncw <= 1) q(attn_kernel<64, 1>, 64, ACfg<64>::kSmem);
+    else if (ncw <= 2) q(attn_kernel<64, 2>, 96, ACfg<64>::kSmem);
+    else if (ncw <= 4) q(attn_kernel<64, 4>, 160, ACfg<64>::kSmem);
+    else q(attn_kernel<64, 8>, 288, ACfg<64>::kSmem);
+  }
+  return n < 1 ? 1 : n;
+}
 
 cudaError_t launch_attention(const CUtensorMap& pool_map, const CUtensorMap& kblk_map, const CUtensorMap& vblk_map,
                              const AttnArgs& a, int grid, int part, cudaStream_t stream) {

@@ -8,6 +8,25 @@
 
 namespace dfl {
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes; every kernel of this library
+// executes griddepcontrol.wait before it touches data another kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 constexpr int kPage = 64;          // tokens per KV page
 constexpr int kMaxBatch = 64;      // sequences per call
 constexpr int kMaxBlock = 32;      // block size B
@@ -43,7 +62,9 @@ enum EpiKind : int {
   EPI_QKV_ROPE = 2,    // regions q|k|v -> bf16, RoPE on q and k
   EPI_SWIGLU = 3,      // paired gate|up -> bf16 SiLU(g) * u
   EPI_KV_APPEND = 4,   // regions (K_l, V_l)* -> RoPE(K), write to paged pool
-  EPI_ARGMAX = 5       // per activation row: argmax over n (lowest index on ties)
+  EPI_ARGMAX = 5,      // per activation row: argmax over n (lowest index on ties)
+  EPI_RESID = 6,       // x += acc; also bf16(x * gain) and per-tile sums of x^2 (next RMSNorm)
+  EPI_NORMSRC = 7      // bf16(acc * gain) and per-tile sums of acc^2 (fusion projection)
 };
 
 struct AMaps {
@@ -83,11 +104,23 @@ struct GemmEpi {
   int* done;                        // CTA completion counter (zero between calls)
   int32_t* out_ids;                 // [M]
   float* out_logit;                 // [M] (may be null)
+  int argmax_skip_B;                // > 0: rows m % B == 0 are skipped; row i*B+j -> out i*(B-1)+j-1
   int* status;
+  // RMSNorm folded into the GEMM. Consumer side: the activation rows X hold
+  // bf16(x * gain); each output column m is scaled by
+  // rsqrt(sum_p in_ss[p][m] * inv_hidden + eps) before the epilogue op.
+  const float* in_ss;               // [in_ss_parts][in_ss_ld], null = no scaling
+  int in_ss_parts, in_ss_ld;
+  float inv_hidden, eps;
+  // Producer side (EPI_RESID / EPI_NORMSRC).
+  uint16_t* out_hg;                 // [M][ld_out] bf16(x * gain)
+  const uint16_t* gain;             // [N]
+  float* out_ss;                    // [n_tiles][out_ss_ld] sum of x^2 over the tile's 128 features
+  int out_ss_ld;
 };
 
 struct GemmWork {
-  float* partial;     // split-K partials
+  float* partial;     // stream-K partial tiles: 2 slots of 128 x BN floats per CTA
   size_t partial_elems;
   int* tickets;       // per output tile, zero between calls
   int n_tickets;
@@ -103,6 +136,9 @@ cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUten
 // BN (token tile) the GEMM uses for M rows; the activation tensor map's box
 // height must equal it.
 int gemm_token_tile(int M);
+// CTAs the GEMM runs with: num_sms stream-K workers (splits = 0) or
+// tiles * splits, reduced until 2 partial tiles per CTA fit partial_elems.
+int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms);
 
 // Row-major [rows, cols] bf16 TMA descriptor (box 64 x box_rows, 128B swizzle).
 bool encode_matrix_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
@@ -131,16 +167,14 @@ struct AttnArgs {
 cudaError_t launch_attention(const CUtensorMap& pool_map, const CUtensorMap& kblk_map, const CUtensorMap& vblk_map,
                              const AttnArgs& a, int grid, int part, cudaStream_t stream);
 int attention_block_rows(int B);   // key-box height used for the block's own keys
+int attention_ctas_per_sm(int head_dim, int ncw);   // resident attention CTAs per SM
 
 // ----------------------------------------------------------------------------
 // Small kernels
 // ----------------------------------------------------------------------------
-cudaError_t launch_embed_norm(const uint16_t* embed, const int32_t* anchors, int mask_id, int vocab,
-                              const SeqMeta& meta, int H, const uint16_t* gain, float eps, float* x, uint16_t* h,
-                              int* status, cudaStream_t s);
-// skip_B > 1: drop row 0 of every block of skip_B rows (rows is then n_seq*(skip_B-1)).
-cudaError_t launch_rmsnorm(const float* x, int rows, int H, const uint16_t* gain, float eps, uint16_t* out,
-                           int skip_B, cudaStream_t s);
+// Block embedding: x (fp32), hg = bf16(x * gain), ss[m] = sum(x^2).
+cudaError_t launch_embed(const uint16_t* embed, const int32_t* anchors, int mask_id, int vocab, const SeqMeta& meta,
+                         int H, const uint16_t* gain, float* x, uint16_t* hg, float* ss, int* status, cudaStream_t s);
 cudaError_t launch_verify(const SeqMeta& meta, SeqState st, const int32_t* drafts, const int32_t* targets,
                           int32_t* tau, int32_t* bonus, cudaStream_t s);
 cudaError_t launch_fuse_advance(const SeqMeta& meta, SeqState st, int pending, cudaStream_t s);

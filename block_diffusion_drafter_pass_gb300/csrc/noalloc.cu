@@ -12,6 +12,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -67,14 +68,19 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
     return DFLASH_EINVAL;
   }
   const int BN = gemm_token_tile(M);
-  const int m_tiles = ceil_div(M, BN), n_tiles = ceil_div(N, 128), k_blocks = ceil_div(K, 64);
-  if (splits > 1) {
-    const int per = ceil_div(k_blocks, splits);
-    const int eff = ceil_div(k_blocks, per);
-    const size_t need = static_cast<size_t>(eff) * m_tiles * BN * n_tiles * 128;
-    if (eff > 1 && (need > kPartialFloats || static_cast<long long>(m_tiles) * n_tiles > kTickets)) {
+  const long long tiles = static_cast<long long>(ceil_div(M, BN)) * ceil_div(N, 128);
+  const int k_blocks = ceil_div(K, 64);
+  if (tiles > kTickets) {
+    set_unattached_error("dflash_gemm_noalloc: more than 4096 output tiles of 128 x 16..256");
+    return DFLASH_EINVAL;
+  }
+  if (splits > 0) {
+    // an explicit split factor runs tiles x splits CTAs with two 128 x BN partial slots each
+    const long long ctas = std::min(tiles * std::min(splits, k_blocks), tiles * k_blocks);
+    const long long need = 2 * ctas * 128 * BN;
+    if (ctas > 1 && tiles % ctas != 0 && need > static_cast<long long>(kPartialFloats)) {
       set_unattached_error("dflash_gemm_noalloc: split-K partials exceed the fixed 8 MiB scratch "
-                           "(splits x roundup(M) x roundup(N,128) floats) or 4096 output tiles; use fewer splits");
+                           "(2 x splits x roundup(M) x roundup(N,128) floats); use fewer splits");
       return DFLASH_EINVAL;
     }
   }
@@ -117,7 +123,7 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
   ARegions rg;
   std::memset(&rg, 0, sizeof(rg));
   rg.n_regions = 1;
-  rg.tile_begin[1] = n_tiles;
+  rg.tile_begin[1] = ceil_div(N, 128);
   if (launch_gemm(am, rg, xm, M, N, K, splits, ep, work, sms, stream) != cudaSuccess) {
     set_unattached_error("dflash_gemm_noalloc: kernel launch failed");
     return DFLASH_ECUDA;

@@ -93,15 +93,16 @@ struct dflash_ctx {
   int* d_page_table = nullptr;
   int* d_status = nullptr;
   float* x = nullptr;        // [max_rows, H] residual stream (fp32)
-  uint16_t* h = nullptr;     // [max_rows, H] normalised layer input
+  uint16_t* hg = nullptr;    // [max_rows, H] bf16(x * gain of the next RMSNorm)
+  float* ssA = nullptr;      // [parts][max_rows] partial sums of x^2 (embed / down producers)
+  float* ssB = nullptr;      // [parts][max_rows] partial sums of x^2 (O producer)
   uint16_t* q = nullptr;     // [max_rows, n_q*d]
   uint16_t* kb = nullptr;    // [max_rows, n_kv*d] block keys
   uint16_t* vb = nullptr;    // [max_rows, n_kv*d] block values
   uint16_t* attn = nullptr;  // [max_rows, n_q*d]
   uint16_t* act = nullptr;   // [max_rows, F]
-  uint16_t* hn = nullptr;    // [max_rows, H] final-normed draft rows
-  float* xf = nullptr;       // [max_fuse_tokens, H] fused projection
-  uint16_t* ht = nullptr;    // [max_fuse_tokens, H] H_t
+  uint16_t* htg = nullptr;   // [max_fuse_tokens, H] bf16(W_c X * g_c)
+  float* ssF = nullptr;      // [parts][max_fuse_tokens] partial sums of (W_c X)^2
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   int items_cap = 0;
@@ -127,6 +128,7 @@ struct dflash_ctx {
   bool snap_pending = false;
 
   int last_rows = 0, last_draft_rows = 0;
+  int attn_ctas_per_sm[9] = {};   // by compute-warp count
   std::string err = "no error";
 
   // per-kernel accounting
@@ -245,6 +247,8 @@ GemmEpi base_epi(dflash_ctx* ctx, int kind) {
   e.pool = ctx->pool;
   e.pool_pages = ctx->cfg.max_pages;
   e.status = ctx->d_status;
+  e.inv_hidden = 1.0f / ctx->cfg.hidden;
+  e.eps = ctx->cfg.rms_eps;
   return e;
 }
 
@@ -312,8 +316,8 @@ dflash_status dflash_destroy(dflash_ctx* ctx) {
   if (!ctx) return DFLASH_EINVAL;
   cudaDeviceSynchronize();
   void* ptrs[] = {ctx->pool, ctx->rope, ctx->d_len, ctx->d_pend, ctx->d_page_table, ctx->d_status, ctx->x,
-                  ctx->h, ctx->q, ctx->kb, ctx->vb, ctx->attn, ctx->act, ctx->hn, ctx->xf, ctx->ht, ctx->part_o,
-                  ctx->part_ml, ctx->split_ws, ctx->tickets, ctx->keys, ctx->done, ctx->top_logit};
+                  ctx->hg, ctx->ssA, ctx->ssB, ctx->q, ctx->kb, ctx->vb, ctx->attn, ctx->act, ctx->htg, ctx->ssF,
+                  ctx->part_o, ctx->part_ml, ctx->split_ws, ctx->tickets, ctx->keys, ctx->done, ctx->top_logit};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (ctx->h_snap) cudaFreeHost(ctx->h_snap);
@@ -404,8 +408,11 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
      "page table");
   CA(dalloc(&ctx->d_status, 1), "status");
   CA(cudaMemset(ctx->d_status, 0, sizeof(int)), "status");
+  const int parts = ceil_div(H, 128);
   CA(dalloc(&ctx->x, rows * H), "workspace");
-  CA(dalloc(&ctx->h, rows * H), "workspace");
+  CA(dalloc(&ctx->hg, rows * H), "workspace");
+  CA(dalloc(&ctx->ssA, rows * parts), "workspace");
+  CA(dalloc(&ctx->ssB, rows * parts), "workspace");
   CA(dalloc(&ctx->q, rows * nq * d), "workspace");
   CA(dalloc(&ctx->kb, rows * nkv * d), "workspace");
   CA(dalloc(&ctx->vb, rows * nkv * d), "workspace");
@@ -413,12 +420,11 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
   CA(cudaMemset(ctx->vb, 0, rows * nkv * d * 2), "workspace");
   CA(dalloc(&ctx->attn, rows * nq * d), "workspace");
   CA(dalloc(&ctx->act, rows * F), "workspace");
-  CA(dalloc(&ctx->hn, rows * H), "workspace");
-  CA(dalloc(&ctx->xf, static_cast<size_t>(c.max_fuse_tokens) * H), "workspace");
-  CA(dalloc(&ctx->ht, static_cast<size_t>(c.max_fuse_tokens) * H), "workspace");
+  CA(dalloc(&ctx->htg, static_cast<size_t>(c.max_fuse_tokens) * H), "workspace");
+  CA(dalloc(&ctx->ssF, static_cast<size_t>(c.max_fuse_tokens) * parts), "workspace");
   CA(dalloc(&ctx->part_o, static_cast<size_t>(ctx->items_cap) * rows_pad * d), "attention partials");
   CA(dalloc(&ctx->part_ml, static_cast<size_t>(ctx->items_cap) * rows_pad), "attention partials");
-  ctx->split_elems = static_cast<size_t>(8) << 20;
+  ctx->split_elems = static_cast<size_t>(16) << 20;   // 2 slots of 128 x 256 floats for 256 CTAs
   CA(dalloc(&ctx->split_ws, ctx->split_elems), "split-K workspace");
   ctx->n_tickets = 1 << 16;
   CA(dalloc(&ctx->tickets, ctx->n_tickets), "tickets");
@@ -593,28 +599,28 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
   const int M = static_cast<int>(total);
   const int BN = gemm_token_tile(M);
   GemmWork work = gemm_work(ctx);
-  // x = X W_c^T (fp32)
+  const int parts = ceil_div(H, 128);
+  // x = X W_c^T, kept as bf16(x * g_c) plus per-tile sums of x^2: the
+  // fusion RMSNorm is applied as a per-token scale by the next GEMM
   {
     AMaps am;
     am.m[0] = ctx->m_wc;
     ARegions rg = stacked({H});
     const CUtensorMap* xm = act_map(ctx, feats, M, c.n_feat_layers * H, BN);
     if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe feats for TMA");
-    GemmEpi e = base_epi(ctx, EPI_F32_STORE);
-    e.out_f32 = ctx->xf;
+    GemmEpi e = base_epi(ctx, EPI_NORMSRC);
+    e.out_hg = ctx->htg;
     e.ld_out = H;
+    e.gain = ctx->w.g_c;
+    e.out_ss = ctx->ssF;
+    e.out_ss_ld = c.max_fuse_tokens;
     const double K = 1.0 * c.n_feat_layers * H;
-    ProfScope ps(ctx, DFLASH_K_FUSE_WC, stream, gemm_bytes(M, H, K, H, 4), 2.0 * M * H * K);
+    ProfScope ps(ctx, DFLASH_K_FUSE_WC, stream, gemm_bytes(M, H, K, H, 2), 2.0 * M * H * K);
     CK(launch_gemm(am, rg, *xm, M, H, c.n_feat_layers * H, 0, e, work, ctx->num_sms, stream));
   }
-  // H_t = RMSNorm(x) * g_c
+  // K/V of every layer from H_t = x / rms(x) * g_c, RoPE on K, scattered into the pages
   {
-    ProfScope ps(ctx, DFLASH_K_NORM, stream, 6.0 * M * H, 0);
-    CK(launch_rmsnorm(ctx->xf, M, H, ctx->w.g_c, c.rms_eps, ctx->ht, 0, stream));
-  }
-  // K/V of every layer from H_t, RoPE on K, scattered into the pages
-  {
-    const CUtensorMap* xm = act_map(ctx, ctx->ht, M, H, BN);
+    const CUtensorMap* xm = act_map(ctx, ctx->htg, M, H, BN);
     if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe H_t for TMA");
     const int per_launch = kMaxAMaps / 2;
     for (int l0 = 0; l0 < c.n_layers; l0 += per_launch) {
@@ -634,6 +640,9 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
       GemmEpi e = base_epi(ctx, EPI_KV_APPEND);
       e.meta = meta;
       e.layer0 = l0;
+      e.in_ss = ctx->ssF;
+      e.in_ss_parts = parts;
+      e.in_ss_ld = c.max_fuse_tokens;
       const double nw = 2.0 * nl * nkv * d;
       ProfScope ps(ctx, DFLASH_K_FUSE_KV, stream, gemm_bytes(M, nw, H, nw, 2), 2.0 * M * nw * H);
       CK(launch_gemm(am, rg, *xm, M, 2 * nl * tiles * 128, H, 0, e, work, ctx->num_sms, stream));
@@ -677,8 +686,12 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   // attention work split from the host's length bounds
   long long tiles_ub = 0;
   for (int i = 0; i < n_seq; ++i) tiles_ub += 1LL * nkv * (ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1);
-  const int grid_full = 2 * ctx->num_sms;
-  int chunk = std::max(2, ceil_div(tiles_ub, 2LL * grid_full));
+  // one wave of resident attention CTAs, each with about one chunk of tiles
+  const int ncw = ceil_div((nq / nkv) * B, 16);
+  int& per_sm = ctx->attn_ctas_per_sm[ncw];
+  if (per_sm == 0) per_sm = attention_ctas_per_sm(d, ncw);
+  const int grid_full = per_sm * ctx->num_sms;
+  int chunk = std::max(2, ceil_div(tiles_ub, grid_full));
   auto items_for = [&](int ch) {
     long long it = 0;
     for (int i = 0; i < n_seq; ++i) it += 1LL * nkv * ceil_div(ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1, ch);
@@ -690,7 +703,9 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   const int Bb = attention_block_rows(B);
   const CUtensorMap* km = blk_map(ctx, ctx->kb, M, Bb);
   const CUtensorMap* vm = blk_map(ctx, ctx->vb, M, Bb);
-  const CUtensorMap* hmap = act_map(ctx, ctx->h, M, H, BN);
+  const CUtensorMap* hmap = act_map(ctx, ctx->hg, M, H, BN);
+  const int parts = ceil_div(H, 128);
+  const int rows_ld = ctx->max_rows();
   const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, BN);
   const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, BN);
   if (!km || !vm || !hmap || !amap || !fmap) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
@@ -703,8 +718,8 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   const double attn_bytes = ctx_tokens * nkv * d * 4 + 1.0 * M * nkv * d * 4 + 1.0 * M * nq * d * 2;
   {
     ProfScope ps(ctx, DFLASH_K_NORM, stream, 8.0 * M * H, 0);
-    CK(launch_embed_norm(ctx->w.embed, anchor_ids, c.mask_id, c.vocab, meta, H, ctx->layers[0].g_attn, c.rms_eps,
-                         ctx->x, ctx->h, ctx->d_status, stream));
+    CK(launch_embed(ctx->w.embed, anchor_ids, c.mask_id, c.vocab, meta, H, ctx->layers[0].g_attn, ctx->x, ctx->hg,
+                    ctx->ssA, ctx->d_status, stream));
   }
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = ctx->layers[l];
@@ -719,6 +734,9 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       e.out_k = ctx->kb;
       e.out_v = ctx->vb;
       e.meta = meta;
+      e.in_ss = ctx->ssA;
+      e.in_ss_parts = l == 0 ? 1 : parts;
+      e.in_ss_ld = rows_ld;
       const double nw = 1.0 * (nq + 2 * nkv) * d;
       ProfScope ps(ctx, DFLASH_K_QKV, stream, gemm_bytes(M, nw, H, nw, 2), 2.0 * M * nw * H);
       CK(launch_gemm(am, rg, *hmap, M, (nq + 2 * nkv) * d, H, 0, e, work, ctx->num_sms, stream));
@@ -749,18 +767,18 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
         CK(launch_attention(ctx->m_pool, *km, *vm, a, attn_grid, 1, stream));
       }
     }
-    {  // x += attn W_o^T
+    {  // x += attn W_o^T; the FFN's RMSNorm input is folded into the epilogue
       AMaps am;
       am.m[0] = ctx->m_wo[l];
-      GemmEpi e = base_epi(ctx, EPI_F32_ADD);
+      GemmEpi e = base_epi(ctx, EPI_RESID);
       e.out_f32 = ctx->x;
       e.ld_out = H;
-      ProfScope ps(ctx, DFLASH_K_O, stream, gemm_bytes(M, H, nq * d, H, 8), 2.0 * M * H * nq * d);
+      e.out_hg = ctx->hg;
+      e.gain = L.g_ffn;
+      e.out_ss = ctx->ssB;
+      e.out_ss_ld = rows_ld;
+      ProfScope ps(ctx, DFLASH_K_O, stream, gemm_bytes(M, H, nq * d, H, 10), 2.0 * M * H * nq * d);
       CK(launch_gemm(am, stacked({H}), *amap, M, H, nq * d, 0, e, work, ctx->num_sms, stream));
-    }
-    {
-      ProfScope ps(ctx, DFLASH_K_NORM, stream, 6.0 * M * H, 0);
-      CK(launch_rmsnorm(ctx->x, M, H, L.g_ffn, c.rms_eps, ctx->h, 0, stream));
     }
     {  // act = SiLU(h W_gate^T) * (h W_up^T)
       AMaps am;
@@ -773,33 +791,33 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       GemmEpi e = base_epi(ctx, EPI_SWIGLU);
       e.out_act = ctx->act;
       e.n_valid = F;
+      e.in_ss = ctx->ssB;
+      e.in_ss_parts = parts;
+      e.in_ss_ld = rows_ld;
       ProfScope ps(ctx, DFLASH_K_GATEUP, stream, gemm_bytes(M, 2.0 * F, H, F, 2), 4.0 * M * F * H);
       CK(launch_gemm(am, rg, *hmap, M, ceil_div(F, 64) * 128, H, 0, e, work, ctx->num_sms, stream));
     }
-    {  // x += act W_down^T
+    {  // x += act W_down^T; the next RMSNorm (next layer's input, or the final norm) is folded in
       AMaps am;
       am.m[0] = ctx->m_wd[l];
-      GemmEpi e = base_epi(ctx, EPI_F32_ADD);
+      GemmEpi e = base_epi(ctx, EPI_RESID);
       e.out_f32 = ctx->x;
       e.ld_out = H;
-      ProfScope ps(ctx, DFLASH_K_DOWN, stream, gemm_bytes(M, H, F, H, 8), 2.0 * M * H * F);
+      e.out_hg = ctx->hg;
+      e.gain = l + 1 < c.n_layers ? ctx->layers[l + 1].g_attn : ctx->w.g_final;
+      e.out_ss = ctx->ssA;
+      e.out_ss_ld = rows_ld;
+      ProfScope ps(ctx, DFLASH_K_DOWN, stream, gemm_bytes(M, H, F, H, 10), 2.0 * M * H * F);
       CK(launch_gemm(am, stacked({H}), *fmap, M, H, F, 0, e, work, ctx->num_sms, stream));
-    }
-    if (l + 1 < c.n_layers) {
-      ProfScope ps(ctx, DFLASH_K_NORM, stream, 6.0 * M * H, 0);
-      CK(launch_rmsnorm(ctx->x, M, H, ctx->layers[l + 1].g_attn, c.rms_eps, ctx->h, 0, stream));
     }
   }
   ctx->last_rows = M;
   ctx->last_draft_rows = n_seq * (B - 1);
   if (B > 1) {
+    // LM head over all block rows (the anchor rows are skipped in the epilogue),
+    // final RMSNorm folded in: the argmax is taken on the unscaled logits (a
+    // positive per-row scale does not move it) and the winning logit is scaled.
     const int Md = n_seq * (B - 1);
-    {
-      ProfScope ps(ctx, DFLASH_K_NORM, stream, 6.0 * Md * H, 0);
-      CK(launch_rmsnorm(ctx->x, Md, H, ctx->w.g_final, c.rms_eps, ctx->hn, B, stream));
-    }
-    const CUtensorMap* nm = act_map(ctx, ctx->hn, Md, H, gemm_token_tile(Md));
-    if (!nm) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
     AMaps am;
     am.m[0] = ctx->m_lm;
     GemmEpi e = base_epi(ctx, EPI_ARGMAX);
@@ -807,8 +825,12 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
     e.done = ctx->done;
     e.out_ids = draft_ids;
     e.out_logit = ctx->top_logit;
+    e.argmax_skip_B = B;
+    e.in_ss = ctx->ssA;
+    e.in_ss_parts = parts;
+    e.in_ss_ld = rows_ld;
     ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(Md, c.vocab, H, 1, 8), 2.0 * Md * c.vocab * H);
-    CK(launch_gemm(am, stacked({c.vocab}), *nm, Md, c.vocab, H, 1, e, work, ctx->num_sms, stream));
+    CK(launch_gemm(am, stacked({c.vocab}), *hmap, M, c.vocab, H, 0, e, work, ctx->num_sms, stream));
   }
   return DFLASH_OK;
 }
@@ -918,7 +940,8 @@ dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y, 
   CUtensorMap xm;
   if (!encode_2d(&am.m[0], W, N, K, 64) || !encode_2d(&xm, X, M, K, BN)) return DFLASH_EINVAL;
   GemmWork work;
-  work.partial_elems = static_cast<size_t>(16) * ceil_div(M, BN) * BN * ceil_div(N, 128) * 128;
+  const int G = gemm_grid(M, N, K, splits, static_cast<size_t>(1) << 40, sms);
+  work.partial_elems = static_cast<size_t>(2) * G * 128 * BN;
   work.n_tickets = ceil_div(M, BN) * ceil_div(N, 128);
   int* status = nullptr;
   CK(cudaMalloc(&work.partial, work.partial_elems * sizeof(float)));

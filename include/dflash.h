@@ -221,10 +221,11 @@ dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y,
  * The call waits for its stream before returning.
  * W, X, Y: device pointers (W, X bf16, 16-byte aligned; K a multiple of 8).
  * splits: split-K factor, 0 = chosen to fit the array.
- * Errors: EINVAL for bad arguments or when an explicit `splits` needs more
- * than the fixed scratch (splits x roundup(M) x roundup(N, 128) floats above
- * 2^21, or more than 4096 output tiles); ECUDA; ETIMEOUT/EDEVICE as reported
- * by the kernel. Messages via dflash_last_error(NULL). */
+ * Errors: EINVAL for bad arguments, more than 4096 output tiles, or an
+ * explicit `splits` whose partial tiles exceed the fixed scratch
+ * (2 x splits x roundup(M) x roundup(N, 128) floats above 2^21); ECUDA;
+ * ETIMEOUT/EDEVICE as reported by the kernel. Messages via
+ * dflash_last_error(NULL). */
 dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* X, float* Y,
                                   int N, int M, int K, int splits, void* stream);
 
