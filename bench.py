@@ -347,6 +347,9 @@ def run_ours(args):
     e2e_value = whole_job_rate(K, world, reduce_max(ms_e2e, world, dev))
     h2d = host["feats"][0].numel() * 2 + host["logits"][0].numel() * 2
     d2h = (host["drafts"].numel() + host["tau"].numel() + host["bonus"].numel()) * 4
+    # the drafter pass alone (anchor + B-1 masks through all layers and the LM head)
+    kd = min(K, 200)
+    ms_draft = timed(lambda k: cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts), kd, world, dev)
     len_end = cyc.d.seq_len(0)[0]
 
     if rank != 0:
@@ -394,11 +397,179 @@ def run_ours(args):
         "step_hbm_frac": step_bytes / (max_ms / K / 1e3) / 1e9 / peaks["hbm_gbs"],
         "step_algorithmic_GB": step_bytes / 1e9,
         "profiled_ms_per_step": ms_prof / K,
+        "draft_only": {"passes_per_s": whole_job_rate(kd, world, reduce_max(ms_draft, world, dev)),
+                       "ms_per_pass": ms_draft / kd},
+        "latency_model": latency_model(ms_draft / kd, max_ms / K, peaks["hbm_gbs"], B),
         "kernels": kernels,
     }
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(shape, cyc.weights, lens[0], B)
     return out
+
+
+def latency_model(t_draft_ms: float, t_cycle_ms: float, hbm_gbs: float, B: int):
+    """L = (T_draft + T_verify) / tau and eta = L_target / L (DFlash notes, 2.2).
+    T_draft is measured here; there is no target model, so L_target and
+    T_verify are supplied estimates: one memory-bound decode step of a bf16
+    Qwen3-8B target (16.4 GB of weights at the measured HBM bandwidth), a
+    B-token verify pass costing the same; tau = 6.49, the paper's Qwen3-8B
+    DFlash(16) acceptance length."""
+    l_target = 16.4e9 / (hbm_gbs * 1e9) * 1e3
+    t_verify = l_target
+    tau = 6.49 if B == 16 else None
+    out = {"T_draft_ms": t_draft_ms, "T_cycle_drafter_side_ms": t_cycle_ms,
+           "L_target_ms_estimate": l_target, "T_verify_ms_estimate": t_verify, "tau_assumed": tau}
+    if tau:
+        L = (t_cycle_ms + t_verify) / tau
+        out.update({"L_ms": L, "eta": l_target / L,
+                    "note": "T_verify, L_target and tau are supplied estimates, not measurements"})
+    return out
+
+
+def run_verify(args):
+    """Verify/accept + commit at batch 64, B = 16, vocab 151936: target ids are
+    the argmax of bf16 N(0, 3) logits (rows_argmax, timed), drafts agree with
+    them up to a geometric(0.3) mismatch; verify commits tau of 16 pending
+    slots per sequence. Pending slots are appended outside the timed region."""
+    import numpy as np
+    import torch
+    import block_diffusion_drafter_pass_gb300 as dfl
+    from synth import TINY, make_weights_torch, make_verify_case_np
+    from block_diffusion_drafter_pass_gb300 import _build
+    _build.build()
+    dfl.load_library()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    b, B, V = 64, 16, 151936
+    K, W = args.steps, args.warmup
+    ring = 8
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    logits = torch.empty(ring, b * B, V, device=dev, dtype=torch.float32)
+    logits.normal_(0.0, 3.0, generator=g)
+    logits = logits.to(torch.bfloat16)
+    targets = logits.float().argmax(dim=-1).to(torch.int32).view(ring, b, B)   # first index of the max
+    drafts = torch.stack([torch.from_numpy(make_verify_case_np(targets[r].cpu().numpy(), V, seed=r)[0])
+                          for r in range(ring)]).to(dev)
+    width = TINY.n_feat_layers * TINY.hidden
+    wt = make_weights_torch(TINY, seed=1, device=dev)
+    steps = W + K
+    d = dfl.Drafter(TINY, wt, max_seqs=b, max_batch=b, max_block=B, max_ctx=(steps + 2) * B + 64,
+                    max_fuse_tokens=b * B)
+    feats = torch.randn(b * B, width, generator=g, device=dev).to(torch.bfloat16)
+    seqs = list(range(b))
+    t_out = torch.empty(b * B, dtype=torch.int32, device=dev)
+    tau = torch.empty(b, dtype=torch.int32, device=dev)
+    bonus = torch.empty(b, dtype=torch.int32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps):
+        d.fuse_ctx(seqs, [B] * b, feats, pending=True)
+        e0, e1, e2 = ev[k]
+        e0.record()
+        dfl.dflash_rows_argmax_bf16(logits[k % ring], out=t_out)
+        e1.record()
+        d.verify(seqs, B, drafts[k % ring], t_out.view(b, B), tau=tau, bonus=bonus)
+        e2.record()
+    torch.cuda.synchronize()
+    am = [ev[k][0].elapsed_time(ev[k][1]) for k in range(W, steps)]
+    vf = [ev[k][1].elapsed_time(ev[k][2]) for k in range(W, steps)]
+    peaks, kind = measured_peaks()
+    am_us = 1e3 * sum(am) / K
+    vf_us = 1e3 * sum(vf) / K
+    bytes_am = b * B * V * 2
+    return {"metric": "verify/accept + commit latency (batch 64, B = 16, vocab 151936)", "value": am_us + vf_us,
+            "unit": "us", "higher_is_better": False, "n_gpus": 1, "steps": K, "warmup": W, "dtype": "bf16 -> int32",
+            "data": "synthetic (N(0,3) bf16 logits, geometric(0.3) agreement)",
+            "config": {"workload": "verify_b64", "batch": b, "block": B, "vocab": V},
+            "argmax_us": am_us, "verify_commit_us": vf_us,
+            "roofline": {"bound": "hbm", "kernel": "rows_argmax_bf16_kernel", "achieved": bytes_am / (am_us * 1e3),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": bytes_am / (am_us * 1e3) / peaks["hbm_gbs"], "peak_source": f"{kind} hbm_gbs"}}
+
+
+def run_fill(args):
+    """Context fill: dflash_fuse_ctx of 4096 committed target-feature rows per
+    call (fusion projection + every layer's K/V + RoPE + paged append)."""
+    import torch
+    import block_diffusion_drafter_pass_gb300 as dfl
+    from synth import QWEN3_8B, make_weights_torch
+    from block_diffusion_drafter_pass_gb300 import _build
+    _build.build()
+    dfl.load_library()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    n = 4096
+    K, W = args.steps, args.warmup
+    sh = QWEN3_8B.with_layers(args.layers)
+    wt = make_weights_torch(sh, seed=0, device=dev)
+    width = sh.n_feat_layers * sh.hidden
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    feats = torch.randn(n, width, generator=g, device=dev).to(torch.bfloat16)
+    d = dfl.Drafter(sh, wt, max_seqs=1, max_batch=1, max_block=16, max_ctx=(W + K) * n + 64,
+                    max_fuse_tokens=n)
+    for _ in range(W):
+        d.fuse_ctx([0], [n], feats, pending=False)
+    ms = timed(lambda k: d.fuse_ctx([0], [n], feats, pending=False), K, 1, dev)
+    flops = 2.0 * n * width * sh.hidden + 2.0 * n * sh.hidden * (2 * sh.n_layers * sh.n_kv_heads * sh.head_dim)
+    peaks, kind = measured_peaks()
+    tf = flops / (ms / K * 1e-3) / 1e12
+    return {"metric": "context fill tokens/s (fuse_ctx, 4096 tokens per call)", "value": n * K / (ms / 1e3),
+            "unit": "tokens/s", "higher_is_better": True, "n_gpus": 1, "steps": K, "warmup": W,
+            "ms_per_step": ms / K, "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": "fill_4096", "layers": sh.n_layers},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "peak_source": f"{kind} bf16_tflops"}}
+
+
+def run_reference_aux(args):
+    """Oracle timings for the verify and context-fill workloads."""
+    import numpy as np
+    import oracle
+    from synth import QWEN3_8B, TINY, make_target_logits_bf16_np, bits_to_f32, make_verify_case_np, \
+        make_weights_np, make_features_np
+    if args.workload == "verify_b64":
+        b, B, V = 64, 16, 151936
+        logits = bits_to_f32(make_target_logits_bf16_np(b * B, V, seed=5))
+        orc = oracle.OracleDrafter(TINY, make_weights_np(TINY, seed=1))
+        feats = make_features_np(b * B, TINY.n_feat_layers * TINY.hidden, seed=2)
+        K = max(1, min(args.steps, 20))
+        t_am = t_vf = 0.0
+        for _ in range(K):
+            orc.fuse_ctx(list(range(b)), [B] * b, feats, pending=True)
+            t0 = time.perf_counter()
+            t = oracle.rows_argmax(logits).reshape(b, B)
+            t1 = time.perf_counter()
+            drafts, _ = make_verify_case_np(t, V, seed=0)
+            t2 = time.perf_counter()
+            orc.verify(list(range(b)), B, drafts, t)
+            t3 = time.perf_counter()
+            t_am += t1 - t0
+            t_vf += t3 - t2
+        us = 1e6 * (t_am + t_vf) / K
+        return {"impl": "reference", "metric": "verify/accept + commit latency (batch 64, B = 16, vocab 151936)",
+                "value": us, "unit": "us", "higher_is_better": False, "n_gpus": 1, "steps": K, "warmup": 0,
+                "config": {"workload": "verify_b64"},
+                "cpu_baseline": {"value": us, "unit": "us", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": f"{K} verify steps of the numpy oracle"},
+                "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    n = 4096
+    sh = QWEN3_8B.with_layers(args.layers)
+    orc = oracle.OracleDrafter(sh, make_weights_np(sh, seed=0), dtype=np.float32)
+    feats = make_features_np(n, sh.n_feat_layers * sh.hidden, seed=3)
+    K = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(K):
+        orc.fuse_ctx([0], [n], feats, pending=False)
+    el = time.perf_counter() - t0
+    v = n * K / el
+    return {"impl": "reference", "metric": "context fill tokens/s (fuse_ctx, 4096 tokens per call)", "value": v,
+            "unit": "tokens/s", "higher_is_better": True, "n_gpus": 1, "steps": K, "warmup": 0,
+            "config": {"workload": "fill_4096", "layers": sh.n_layers},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{K} fills of 4096 tokens by the fp32 numpy oracle"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def run_reference(args):
@@ -409,6 +580,8 @@ def run_reference(args):
     rank, _, world = dist_setup("gloo")
     if rank != 0:
         return None
+    if args.workload not in WORKLOADS:
+        return run_reference_aux(args)
     batch, ctx, spread = WORKLOADS[args.workload]
     B = args.block
     shape = QWEN3_8B
@@ -469,7 +642,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_8b_b1_ctx4096")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["verify_b64", "fill_4096"],
+                    default="qwen3_8b_b1_ctx4096")
     ap.add_argument("--block", type=int, default=16)
     ap.add_argument("--layers", type=int, default=5,
                     help="drafter depth (5 = the benchmarked drafter; fewer only for small profiling captures)")
@@ -477,7 +651,14 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.impl == "reference":
+        out = run_reference(args)
+    elif args.workload == "verify_b64":
+        out = run_verify(args)
+    elif args.workload == "fill_4096":
+        out = run_fill(args)
+    else:
+        out = run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 

@@ -80,7 +80,7 @@ __device__ __forceinline__ SeqSplit seq_split(const AttnArgs& a, int i) {
 }
 
 template <int D, int NCW>
-__global__ void __launch_bounds__((NCW + 1) * 32)
+__global__ void __launch_bounds__((NCW + 1) * 32, NCW <= 4 ? 2 : 1)
     attn_kernel(const __grid_constant__ CUtensorMap pool_map, const __grid_constant__ CUtensorMap kblk_map,
                 const __grid_constant__ CUtensorMap vblk_map, const __grid_constant__ AttnArgs a) {
   using C = ACfg<D>;

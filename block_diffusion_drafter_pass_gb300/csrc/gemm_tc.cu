@@ -7,17 +7,26 @@
 // tokens still fills the 128-row tensor-core tile and the kernel streams
 // weights at HBM speed; with 512 tokens the same kernel is compute bound.
 //
-// CTA = 6 warps: warp 0 issues TMA loads into a STAGES-deep ring of shared
-// memory stages, warp 1 owns TMEM and issues the MMAs (one elected thread),
-// warps 2-5 drain the accumulator (tcgen05.ld) and run the fused epilogue:
-//   EPI_F32_STORE  plain fp32 output (fusion projection W_c, tests)
-//   EPI_F32_ADD    residual add (attention output and FFN down projections)
+// Persistent stream-K: one CTA per SM streams an equal, contiguous range of
+// (tile, 64-wide k-block) units through a STAGES-deep TMA ring. CTA = 6 warps:
+// warp 0 issues the TMA loads, warp 1 owns TMEM and issues the MMAs (one
+// thread) into one of two accumulator buffers, warps 2-5 drain the other
+// buffer (tcgen05.ld) and run the fused epilogue:
+//   EPI_F32_STORE  plain fp32 output (tests)
+//   EPI_RESID      x += acc, then bf16(x * g) and sum(x^2) for the next RMSNorm
+//   EPI_NORMSRC    bf16(acc * g) and sum(acc^2) (fusion projection W_c)
 //   EPI_QKV_ROPE   q/k/v split with rotate-half RoPE on q and k
 //   EPI_SWIGLU     SiLU(gate) * up from paired gate/up weight rows
 //   EPI_KV_APPEND  KV injection: RoPE(W_K H_t), W_V H_t scattered to pages
 //   EPI_ARGMAX     LM head with the per-row argmax fused; logits never stored
-// Split-K: each split writes an fp32 partial; the last CTA of a tile (atomic
-// ticket, no spinning) sums them and runs the epilogue.
+// A tile split over several CTAs is finished by the last one to arrive (an
+// atomic ticket; nothing spins): it adds the others' partial tiles to its own
+// accumulator and runs the epilogue.
+//
+// RoPE and SwiGLU pair tile row r with row r ^ P (P = d/2 for RoPE, 64 for
+// gate/up rows); those live in another warp's TMEM lanes, so the pair is
+// exchanged through a double-buffered shared-memory stage, one named barrier
+// per 16-column chunk.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -40,7 +49,7 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = BN <= 64 ? 8 : (BN <= 128 ? 6 : 4);
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;     // two accumulator buffers
-  static constexpr int kStgBytes = 128 * 17 * 4;                    // epilogue staging
+  static constexpr int kStgBytes = 2 * 128 * 17 * 4;                // pair-exchange stage (x2)
   static constexpr int kSmem = kStages * kStageBytes + kStgBytes + 1024;
 };
 
@@ -57,13 +66,38 @@ struct GemmArgs {
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 struct EpiShared {
-  unsigned long long cand[4][16];
-  int row_pos[256];     // QKV_ROPE / KV_APPEND: absolute position of each tile row
-  int row_dst[256];     // KV_APPEND: pool row index of (page, slot) without layer/kv/head
-  float row_scale[256]; // folded RMSNorm scale of each tile row
-  float red[4][16];     // per-warp column sums of squares
+  unsigned long long cand[4][256];   // per-warp argmax candidates per column
+  float red[4][256];                 // per-warp column sums of squares
+  int row_pos[256];                  // QKV_ROPE / KV_APPEND: absolute position of each column
+  int row_dst[256];                  // KV_APPEND: (page, slot) part of the pool row index
+  float row_scale[256];              // folded RMSNorm scale of each column
   int flag;
 };
+
+__device__ __forceinline__ int region_of(const ARegions& rg, int tile) {
+  int r = 0;
+  while (r + 1 < rg.n_regions && tile >= rg.tile_begin[r + 1]) ++r;
+  return r;
+}
+
+// TMA sources of the tile's two 64-row halves: stacked regions read 128
+// consecutive rows of one matrix; paired tiles read 64 gate rows and the same
+// 64 up rows.
+__device__ __forceinline__ void weight_rows(const ARegions& rg, int tile_n, int& map_lo, int& row_lo, int& map_hi,
+                                            int& row_hi) {
+  if (rg.paired) {
+    map_lo = 0;
+    map_hi = 1;
+    row_lo = row_hi = tile_n * 64;
+  } else {
+    const int reg = region_of(rg, tile_n);
+    map_lo = map_hi = reg;
+    row_lo = (tile_n - rg.tile_begin[reg]) * kTileN;
+    row_hi = row_lo + 64;
+  }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // Folded RMSNorm scale of activation row m: 8 independent partial loads per
 // batch so the sum costs a few memory latencies, not one per partial.
@@ -79,14 +113,15 @@ __device__ __forceinline__ float norm_scale(const GemmEpi& e, int m) {
   return rsqrtf(ss * e.inv_hidden + e.eps);
 }
 
-// Per-row metadata of one output tile (rows m0 .. m0+BN-1), computed once by
-// all 128 epilogue threads before the tile's chunks are processed.
+// Per-column metadata of one output tile (columns m0 .. m0+BN-1), computed
+// once by all 128 epilogue threads before the tile is drained.
 template <int BN>
-__device__ __forceinline__ void tile_rows_prepare(const GemmArgs& a, const GemmEpi& e, int m0, int r, EpiShared& sh) {
+__device__ __forceinline__ void tile_cols_prepare(const GemmArgs& a, const GemmEpi& e, int m0, int r,
+                                                  EpiShared& sh) {
   const int kind = e.kind;
-  for (int row = r; row < BN; row += 128) {
-    const int m = m0 + row;
-    float sc = 0.f;
+  for (int col = r; col < BN; col += 128) {
+    const int m = m0 + col;
+    float sc = 1.f;
     int pos = -1, dst = -1;
     if (m < a.M) {
       if (e.in_ss) sc = norm_scale(e, m);
@@ -111,180 +146,240 @@ __device__ __forceinline__ void tile_rows_prepare(const GemmArgs& a, const GemmE
         dst = -1;
       }
     }
-    sh.row_scale[row] = sc;
-    sh.row_pos[row] = pos;
-    sh.row_dst[row] = dst;
+    sh.row_scale[col] = sc;
+    sh.row_pos[col] = pos;
+    sh.row_dst[col] = dst;
   }
   epi_bar();
 }
 
+// Inputs of one 16-column chunk that live in global memory, loaded one chunk
+// ahead of use so the chunk loop pays about one memory latency in total.
+struct ChunkAux {
+  float d[32];     // EPI_RESID: residual in d[0..15]; RoPE kinds: cos in d[0..15], sin in d[16..31]
+};
 
-__device__ __forceinline__ int region_of(const ARegions& rg, int tile) {
-  int r = 0;
-  while (r + 1 < rg.n_regions && tile >= rg.tile_begin[r + 1]) ++r;
-  return r;
-}
-
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
-
-// Final values of one 16-column chunk: v[c] for output feature (tile row) r
-// and token m0 + c0 + c. Staging area `stg` holds 128 x 17 floats.
-template <int BN>
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int tile_n,
-                                               int m0, int c0, int r, float (&v)[16], float* stg, EpiShared& sh) {
-  const int q = r >> 5;
-  const int lane = r & 31;
-  const int kind = e.kind;
-  if (e.in_ss && kind != EPI_ARGMAX) {
-    // folded RMSNorm of the input rows: scale each token column
-#pragma unroll
-    for (int c = 0; c < 16; ++c) v[c] *= sh.row_scale[c0 + c];
-  }
-  if (kind == EPI_RESID || kind == EPI_NORMSRC) {
-    const int n = tile_n * kTileN + r;
-    const bool nv = n < a.N;
-    const float g = nv ? bf16_to_f32(e.gain[n]) : 0.f;
-    float xo[16];
-    if (kind == EPI_RESID) {   // all residual loads in flight at once
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int m = m0 + c0 + c;
-        xo[c] = (nv && m < a.M) ? e.out_f32[static_cast<size_t>(m) * e.ld_out + n] : 0.f;
-      }
-    }
+__device__ __forceinline__ void load_aux(const GemmArgs& a, const GemmEpi& e, const EpiShared& sh, int m0, int c0,
+                                         int n, bool rope, int fi, int half, ChunkAux& x) {
+  if (e.kind == EPI_RESID) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int m = m0 + c0 + c;
-      float xn = 0.f;
-      if (nv && m < a.M) {
-        const size_t off = static_cast<size_t>(m) * e.ld_out + n;
-        xn = v[c];
-        if (kind == EPI_RESID) {
-          xn += xo[c];
-          e.out_f32[off] = xn;
-        }
-        e.out_hg[off] = f32_to_bf16(xn * g);
-      }
-      float sq = xn * xn;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      if (lane == 0) sh.red[q][c] = sq;
+      x.d[c] = (n < a.N && m < a.M) ? e.out_f32[static_cast<size_t>(m) * e.ld_out + n] : 0.f;
     }
-    epi_bar();
-    if (r < 16) {
-      const int m = m0 + c0 + r;
-      if (m < a.M)
-        e.out_ss[static_cast<size_t>(tile_n) * e.out_ss_ld + m] = sh.red[0][r] + sh.red[1][r] + sh.red[2][r] + sh.red[3][r];
-    }
-    epi_bar();
-    return;
   }
-  if (kind == EPI_F32_STORE || kind == EPI_F32_ADD) {
-    const int n = tile_n * kTileN + r;
-    if (n < a.N) {
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int m = m0 + c0 + c;
-        if (m < a.M) {
-          float* p = e.out_f32 + static_cast<size_t>(m) * e.ld_out + n;
-          if (kind == EPI_F32_ADD) *p += v[c]; else *p = v[c];
-        }
-      }
-    }
-    return;
-  }
-  if (kind == EPI_ARGMAX) {
-    const int n = tile_n * kTileN + r;
+  if (rope) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const int m = m0 + c0 + c;
-      const bool ok = (n < a.N) && (m < a.M) && !(e.argmax_skip_B > 0 && m % e.argmax_skip_B == 0);
-      const uint32_t key = ok ? ordered_key(v[c]) : 0u;
-      const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-      const uint32_t hit = __ballot_sync(0xffffffffu, ok && key == mx);
-      if (lane == 0) {
-        unsigned long long cand = 0ull;
-        if (hit) {
-          const uint32_t idx = static_cast<uint32_t>(tile_n * kTileN + q * 32 + (__ffs(hit) - 1));
-          cand = (static_cast<unsigned long long>(mx) << 32) | (0xFFFFFFFFu - idx);
-        }
-        sh.cand[q][c] = cand;
-      }
-    }
-    epi_bar();
-    if (r < 16) {
-      unsigned long long best = sh.cand[0][r];
-#pragma unroll
-      for (int w = 1; w < 4; ++w) best = sh.cand[w][r] > best ? sh.cand[w][r] : best;
-      const int m = m0 + c0 + r;
-      if (m < a.M && best) atomicMax(e.keys + m, best);
-    }
-    epi_bar();
-    return;
-  }
-
-  // Remaining kinds pair rows of the tile: stage it in shared memory.
-#pragma unroll
-  for (int c = 0; c < 16; ++c) stg[r * 17 + c] = v[c];
-  epi_bar();
-
-  if (kind == EPI_SWIGLU) {
-    const int rr = r & 63;
-    const int f = tile_n * 64 + rr;
-    if (f < e.n_valid) {
-      for (int c = r >> 6; c < 16; c += 2) {
-        const int m = m0 + c0 + c;
-        if (m < a.M) {
-          const float g = stg[rr * 17 + c];
-          const float u = stg[(rr + 64) * 17 + c];
-          e.out_act[static_cast<size_t>(m) * e.n_valid + f] = f32_to_bf16(silu_f(g) * u);
-        }
-      }
-    }
-  } else {
-    // QKV_ROPE or KV_APPEND
-    const int reg = region_of(rg, tile_n);
-    const int f = (tile_n - rg.tile_begin[reg]) * kTileN + r;   // feature within the region's matrix
-    const int d = e.head_dim, half = d >> 1;
-    const int head = f / d, i = f - head * d;
-    bool rope;
-    uint16_t* base;
-    size_t ld;
-    int layer = 0, kv = 0;
-    if (kind == EPI_QKV_ROPE) {
-      rope = reg < 2;
-      base = reg == 0 ? e.out_q : (reg == 1 ? e.out_k : e.out_v);
-      ld = static_cast<size_t>(reg == 0 ? e.n_q_heads : e.n_kv_heads) * d;
-    } else {
-      layer = e.layer0 + (reg >> 1);
-      kv = reg & 1;
-      rope = kv == 0;
-      base = e.pool;
-      ld = 0;
-    }
-    const int partner = i < half ? r + half : r - half;
-    const int fi = i < half ? i : i - half;
-#pragma unroll 4
-    for (int c = 0; c < 16; ++c) {
-      const int m = m0 + c0 + c;
       const int pos = sh.row_pos[c0 + c];
-      if (m >= a.M || pos < 0) continue;
-      float x = stg[r * 17 + c];
-      if (rope) {
-        const float2 cs = e.rope[static_cast<size_t>(pos) * half + fi];
-        const float p = stg[partner * 17 + c];
-        x = i < half ? (x * cs.x - p * cs.y) : (x * cs.x + p * cs.y);
+      const float2 cs = pos >= 0 ? e.rope[static_cast<size_t>(pos) * half + fi] : make_float2(1.f, 0.f);
+      x.d[c] = cs.x;
+      x.d[16 + c] = cs.y;
+    }
+  }
+}
+
+// Drain one finished tile from TMEM (plus the other CTAs' partial tiles) and
+// run the epilogue. r = TMEM lane of this thread (0..127).
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int g,
+                                              int tile, int first, int last, uint32_t tb, int r, EpiShared& sh,
+                                              float* stg) {
+  const int kind = e.kind;
+  const int q = r >> 5, lane = r & 31;
+  const int tn = tile / a.m_tiles, tm = tile - tn * a.m_tiles;
+  const int m0 = tm * BN;
+  const int P = rg.pair;
+  const int f = r;                              // row of this lane within the tile
+  const size_t slot_elems = static_cast<size_t>(kTileN) * BN;
+  tile_cols_prepare<BN>(a, e, m0, r, sh);
+
+  // kind-specific constants of this lane
+  int reg = 0, rf = f;                          // region and row within the region's matrix
+  if (!rg.paired) {
+    reg = region_of(rg, tn);
+    rf = (tn - rg.tile_begin[reg]) * kTileN + f;
+  }
+  const int n = tn * kTileN + f;                // output feature (plain kinds)
+  const int d = e.head_dim > 0 ? e.head_dim : 1, half = d >> 1;
+  const int hd = rf / d, di = rf - hd * d;
+  const bool lo = (r & P) == 0;                 // lower member of the row pair (r, r ^ P)
+  const bool paired_kind = kind == EPI_SWIGLU || kind == EPI_QKV_ROPE || kind == EPI_KV_APPEND;
+  bool rope = false;
+  if (kind == EPI_QKV_ROPE) rope = reg < 2;
+  if (kind == EPI_KV_APPEND) rope = (reg & 1) == 0;
+  const int fi = lo ? di : di - half;           // RoPE frequency index of the pair
+  const float gain = (kind == EPI_RESID || kind == EPI_NORMSRC) && n < a.N ? bf16_to_f32(e.gain[n]) : 0.f;
+
+  // Sum of the other CTAs' partial tiles for one chunk; loads are issued two
+  // CTAs at a time.
+  auto partial_src = [&](int o) {
+    const int side = (static_cast<long long>(o) * a.units / a.grid) / a.k_blocks == tile ? 0 : 1;
+    return a.partial + (static_cast<size_t>(o) * 2 + side) * slot_elems + r;
+  };
+  auto partial_sum = [&](int c0, float (&ps)[16]) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) ps[c] = 0.f;
+    int o = first;
+    while (o <= last) {
+      if (o == g) ++o;
+      if (o > last) break;
+      int o2 = o + 1;
+      if (o2 == g) ++o2;
+      const float* s0 = partial_src(o);
+      const bool two = o2 <= last;
+      const float* s1 = two ? partial_src(o2) : s0;
+      float t0[16], t1[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        t0[c] = __ldcg(s0 + static_cast<size_t>(c0 + c) * kTileN);
+        t1[c] = two ? __ldcg(s1 + static_cast<size_t>(c0 + c) * kTileN) : 0.f;
       }
-      if (kind == EPI_QKV_ROPE) {
-        base[static_cast<size_t>(m) * ld + f] = f32_to_bf16(x);
-      } else {
-        const int dst = sh.row_dst[c0 + c];
-        if (dst < 0) continue;
-        // pool row = ((layer*P + page)*2 + kv)*n_kv + head)*64 + slot
-        const size_t row = static_cast<size_t>(layer) * e.pool_pages * 2 * e.n_kv_heads * kPage +
-                           static_cast<size_t>(dst) + static_cast<size_t>(kv * e.n_kv_heads + head) * kPage;
-        base[row * d + i] = f32_to_bf16(x);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) ps[c] += t0[c] + t1[c];
+      o = two ? o2 + 1 : o2;
+    }
+  };
+  const bool split = first != last;
+  ChunkAux cur;
+  load_aux(a, e, sh, m0, 0, n, rope, fi, half, cur);
+  float pcur[16];
+  if (split) partial_sum(0, pcur);
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    ChunkAux nxt;
+    float pnxt[16];
+    if (c0 + 16 < BN) {
+      load_aux(a, e, sh, m0, c0 + 16, n, rope, fi, half, nxt);
+      if (split) partial_sum(c0 + 16, pnxt);
+    }
+    float v[16];
+    tmem_ld16(tb + c0, v);
+    if (split) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] += pcur[c];
+    }
+    if (e.in_ss && kind != EPI_ARGMAX) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] *= sh.row_scale[c0 + c];
+    }
+    float other[16];
+    if (paired_kind) {   // exchange with row r ^ P through the chunk's staging buffer
+      float* sb = stg + ((c0 >> 4) & 1) * (128 * 17);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sb[r * 17 + c] = v[c];
+      epi_bar();
+      const int pr = r ^ P;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) other[c] = sb[pr * 17 + c];
+    }
+
+    if (kind == EPI_F32_STORE || kind == EPI_F32_ADD) {
+      if (n < a.N) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int m = m0 + c0 + c;
+          if (m < a.M) {
+            float* p = e.out_f32 + static_cast<size_t>(m) * e.ld_out + n;
+            if (kind == EPI_F32_ADD) *p += v[c]; else *p = v[c];
+          }
+        }
       }
+    } else if (kind == EPI_RESID || kind == EPI_NORMSRC) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        float xn = 0.f;
+        if (n < a.N && m < a.M) {
+          const size_t off = static_cast<size_t>(m) * e.ld_out + n;
+          xn = v[c];
+          if (kind == EPI_RESID) {
+            xn += cur.d[c];
+            e.out_f32[off] = xn;
+          }
+          e.out_hg[off] = f32_to_bf16(xn * gain);
+        }
+        float sq = xn * xn;
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, s);
+        if (lane == 0) sh.red[q][c0 + c] = sq;
+      }
+    } else if (kind == EPI_ARGMAX) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        const bool ok = (n < a.N) && (m < a.M) && !(e.argmax_skip_B > 0 && m % e.argmax_skip_B == 0);
+        const uint32_t key = ok ? ordered_key(v[c]) : 0u;
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+        const uint32_t hit = __ballot_sync(0xffffffffu, ok && key == mx);
+        if (lane == 0) {
+          unsigned long long cand = 0ull;
+          if (hit) {   // the lowest lane is the lowest index
+            const uint32_t idx = static_cast<uint32_t>(tn * kTileN + q * 32 + __ffs(hit) - 1);
+            cand = (static_cast<unsigned long long>(mx) << 32) | (0xFFFFFFFFu - idx);
+          }
+          sh.cand[q][c0 + c] = cand;
+        }
+      }
+    } else if (kind == EPI_SWIGLU) {
+      // rows < 64 hold gate rows, rows >= 64 the up rows of the same features;
+      // each member of a pair writes half of the columns
+      const int fint = tn * 64 + (f & 63);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        if ((c < 8) == lo && fint < e.n_valid && m < a.M) {
+          const float gt = lo ? v[c] : other[c], up = lo ? other[c] : v[c];
+          e.out_act[static_cast<size_t>(m) * e.n_valid + fint] = f32_to_bf16(silu_f(gt) * up);
+        }
+      }
+    } else {   // EPI_QKV_ROPE or EPI_KV_APPEND
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        const int pos = sh.row_pos[c0 + c];
+        if (m >= a.M || pos < 0) continue;
+        float x = v[c];
+        if (rope) {
+          const float cc = cur.d[c], sn = cur.d[16 + c];
+          x = lo ? (x * cc - other[c] * sn) : (x * cc + other[c] * sn);
+        }
+        if (kind == EPI_QKV_ROPE) {
+          uint16_t* base = reg == 0 ? e.out_q : (reg == 1 ? e.out_k : e.out_v);
+          const size_t ld = static_cast<size_t>(reg == 0 ? e.n_q_heads : e.n_kv_heads) * d;
+          base[static_cast<size_t>(m) * ld + rf] = f32_to_bf16(x);
+        } else {
+          const int dst = sh.row_dst[c0 + c];
+          if (dst < 0) continue;
+          const int layer = e.layer0 + (reg >> 1), kv = reg & 1;
+          // pool row = ((layer*P + page)*2 + kv)*n_kv + head)*64 + slot
+          const size_t row = static_cast<size_t>(layer) * e.pool_pages * 2 * e.n_kv_heads * kPage +
+                             static_cast<size_t>(dst) + static_cast<size_t>(kv * e.n_kv_heads + hd) * kPage;
+          e.pool[row * d + di] = f32_to_bf16(x);
+        }
+      }
+    }
+    cur = nxt;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) pcur[c] = pnxt[c];
+  }
+
+  if (kind == EPI_RESID || kind == EPI_NORMSRC) {
+    epi_bar();
+    for (int col = r; col < BN; col += 128) {
+      const int m = m0 + col;
+      if (m < a.M)
+        e.out_ss[static_cast<size_t>(tn) * e.out_ss_ld + m] =
+            (sh.red[0][col] + sh.red[1][col]) + (sh.red[2][col] + sh.red[3][col]);
+    }
+  } else if (kind == EPI_ARGMAX) {
+    epi_bar();
+    for (int col = r; col < BN; col += 128) {
+      unsigned long long best = sh.cand[0][col];
+#pragma unroll
+      for (int w = 1; w < 4; ++w) best = sh.cand[w][col] > best ? sh.cand[w][col] : best;
+      const int m = m0 + col;
+      if (m < a.M && best) atomicMax(e.keys + m, best);
     }
   }
   epi_bar();
@@ -303,26 +398,6 @@ __device__ __forceinline__ int cta_of(long long u, const GemmArgs& a) {
   return static_cast<int>(g);
 }
 
-__device__ __forceinline__ void weight_rows(const ARegions& rg, int tile_n, int& map_lo, int& row_lo, int& map_hi,
-                                            int& row_hi) {
-  if (rg.paired) {
-    map_lo = 0;
-    map_hi = 1;
-    row_lo = row_hi = tile_n * 64;
-  } else {
-    const int reg = region_of(rg, tile_n);
-    map_lo = map_hi = reg;
-    row_lo = (tile_n - rg.tile_begin[reg]) * kTileN;
-    row_hi = row_lo + 64;
-  }
-}
-
-// Persistent, stream-K tcgen05 GEMM. One CTA per SM; each streams its unit
-// range through a STAGES-deep TMA ring. Warp 1 accumulates each tile segment
-// in one of two TMEM buffers while warps 2-5 drain the other: a segment that
-// covers a whole tile goes straight to the epilogue; a partial segment is
-// written to the CTA's partial slot and the last CTA to finish a tile (atomic
-// ticket) adds the other slots to its own accumulator and runs the epilogue.
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ AMaps amaps, const __grid_constant__ CUtensorMap xmap,
@@ -331,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* stg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);   // 128 x 17 floats
+  float* stg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
   __shared__ __align__(8) uint64_t full[C::kStages];
   __shared__ __align__(8) uint64_t empty[C::kStages];
   __shared__ __align__(8) uint64_t acc_full[2];
@@ -478,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps ----------------
     grid_dep_wait();
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int r = q * 32 + lane;            // tile row = output feature
+    const int r = q * 32 + lane;            // TMEM lane = tile row slot
     const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const size_t slot_elems = static_cast<size_t>(kTileN) * BN;
     int seg = 0;
@@ -487,8 +562,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long seg_end = min(u1, static_cast<long long>(t + 1) * kb);
       const bool whole = (u == static_cast<long long>(t) * kb) && (seg_end == static_cast<long long>(t + 1) * kb);
       const int buf = seg & 1;
-      const int tn = t / a.m_tiles, tm = t - tn * a.m_tiles;
-      const int m0 = tm * BN;
       if (!mbar_wait(&acc_full[buf], (seg >> 1) & 1, &abort_flag)) {
         abort_flag = 1;
         latch_status(a.status, kDevTimeout);
@@ -525,19 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (finish) __threadfence();
       }
       if (finish) {
-        tile_rows_prepare<BN>(a, e, m0, r, esh);
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          float v[16];
-          tmem_ld16(tb + c0, v);
-          for (int o = first; o <= last; ++o) {
-            if (o == g) continue;
-            const int side_o = (unit_begin(o, a) / kb == t) ? 0 : 1;
-            const float* src = a.partial + (static_cast<size_t>(o) * 2 + side_o) * slot_elems + r;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] += __ldcg(src + static_cast<size_t>(c0 + c) * kTileN);
-          }
-          epilogue_chunk<BN>(a, rg, e, tn, m0, c0, r, v, stg, esh);
-        }
+        epilogue_tile<BN>(a, rg, e, g, t, first, last, tb, r, esh, stg);
         if (e.kind == EPI_ARGMAX) {
           // the CTA that finishes the last tile decodes the winning keys and resets them
           __threadfence();
@@ -590,17 +651,7 @@ cudaError_t launch_bn(const AMaps& amaps, const ARegions& rg, const CUtensorMap&
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, amaps, xmap, a, rg, e);
+  return launch_pdl(gemm_kernel<BN>, dim3(a.grid), dim3(kThreads), C::kSmem, stream, amaps, xmap, a, rg, e);
 }
 
 }  // namespace
@@ -634,6 +685,7 @@ int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms
 cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUtensorMap& xmap, int M, int N, int K,
                         int splits, const GemmEpi& epi, const GemmWork& work, int num_sms, cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
+  if (regions.pair != 32 && regions.pair != 64) return cudaErrorInvalidValue;
   const int BN = gemm_token_tile(M);
   GemmArgs a{};
   a.M = M;

@@ -74,8 +74,13 @@ struct AMaps {
 struct ARegions {
   int n_regions;
   int paired;                       // 1: tile t reads rows 64t.. of maps 0 and 1
+  int pair;                         // row-pair distance: d/2 for RoPE, 64 for gate/up (32 or 64)
   int tile_begin[kMaxAMaps + 1];    // stacked: region r covers tiles [b_r, b_{r+1})
 };
+
+// Weight descriptors are encoded with boxes of this many rows (the GEMM loads
+// each 128-row tile as two 64-row halves).
+constexpr int kWeightBoxRows = 64;
 
 struct GemmEpi {
   int kind;

@@ -98,7 +98,7 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
   }
   AMaps am;
   CUtensorMap xm;
-  if (!encode_matrix_map(&am.m[0], W, N, K, 64) || !encode_matrix_map(&xm, X, M, K, BN)) {
+  if (!encode_matrix_map(&am.m[0], W, N, K, kWeightBoxRows) || !encode_matrix_map(&xm, X, M, K, BN)) {
     set_unattached_error("dflash_gemm_noalloc: cannot describe W or X for TMA");
     return DFLASH_EINVAL;
   }
@@ -123,6 +123,7 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
   ARegions rg;
   std::memset(&rg, 0, sizeof(rg));
   rg.n_regions = 1;
+  rg.pair = 64;
   rg.tile_begin[1] = ceil_div(N, 128);
   if (launch_gemm(am, rg, xm, M, N, K, splits, ep, work, sms, stream) != cudaSuccess) {
     set_unattached_error("dflash_gemm_noalloc: kernel launch failed");

@@ -263,6 +263,7 @@ ARegions stacked(std::initializer_list<int> rows) {
   r.tile_begin[i] = t;
   r.n_regions = i;
   r.paired = 0;
+  r.pair = 64;
   return r;
 }
 
@@ -451,8 +452,9 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
   }
 
   // weight descriptors (box 64 K-elements x 64 rows)
-  bool ok = encode_2d(&ctx->m_lm, w->lm_head, c.vocab, H, 64) &&
-            encode_2d(&ctx->m_wc, w->w_c, H, static_cast<uint64_t>(c.n_feat_layers) * H, 64) &&
+  const int wb = kWeightBoxRows;
+  bool ok = encode_2d(&ctx->m_lm, w->lm_head, c.vocab, H, wb) &&
+            encode_2d(&ctx->m_wc, w->w_c, H, static_cast<uint64_t>(c.n_feat_layers) * H, wb) &&
             encode_2d(&ctx->m_pool, ctx->pool, pool_rows, d, 64);
   ctx->m_wq.resize(c.n_layers);
   ctx->m_wk.resize(c.n_layers);
@@ -463,10 +465,10 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
   ctx->m_wd.resize(c.n_layers);
   for (int l = 0; l < c.n_layers && ok; ++l) {
     const dflash_layer_weights& L = ctx->layers[l];
-    ok = encode_2d(&ctx->m_wq[l], L.w_q, nq * d, H, 64) && encode_2d(&ctx->m_wk[l], L.w_k, nkv * d, H, 64) &&
-         encode_2d(&ctx->m_wv[l], L.w_v, nkv * d, H, 64) && encode_2d(&ctx->m_wo[l], L.w_o, H, nq * d, 64) &&
-         encode_2d(&ctx->m_wg[l], L.w_gate, F, H, 64) && encode_2d(&ctx->m_wu[l], L.w_up, F, H, 64) &&
-         encode_2d(&ctx->m_wd[l], L.w_down, H, F, 64);
+    ok = encode_2d(&ctx->m_wq[l], L.w_q, nq * d, H, wb) && encode_2d(&ctx->m_wk[l], L.w_k, nkv * d, H, wb) &&
+         encode_2d(&ctx->m_wv[l], L.w_v, nkv * d, H, wb) && encode_2d(&ctx->m_wo[l], L.w_o, H, nq * d, wb) &&
+         encode_2d(&ctx->m_wg[l], L.w_gate, F, H, wb) && encode_2d(&ctx->m_wu[l], L.w_up, F, H, wb) &&
+         encode_2d(&ctx->m_wd[l], L.w_down, H, F, wb);
   }
   if (!ok) {
     g_create_error = "cuTensorMapEncodeTiled rejected a weight layout";
@@ -636,6 +638,7 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
         rg.tile_begin[2 * j + 1] = (2 * j + 1) * tiles;
       }
       rg.n_regions = 2 * nl;
+      rg.pair = d / 2;
       rg.tile_begin[2 * nl] = 2 * nl * tiles;
       GemmEpi e = base_epi(ctx, EPI_KV_APPEND);
       e.meta = meta;
@@ -729,6 +732,7 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       am.m[1] = ctx->m_wk[l];
       am.m[2] = ctx->m_wv[l];
       ARegions rg = stacked({nq * d, nkv * d, nkv * d});
+      rg.pair = d / 2;
       GemmEpi e = base_epi(ctx, EPI_QKV_ROPE);
       e.out_q = ctx->q;
       e.out_k = ctx->kb;
@@ -788,6 +792,7 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       std::memset(&rg, 0, sizeof(rg));
       rg.n_regions = 2;
       rg.paired = 1;
+      rg.pair = 64;
       GemmEpi e = base_epi(ctx, EPI_SWIGLU);
       e.out_act = ctx->act;
       e.n_valid = F;
@@ -938,7 +943,7 @@ dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y, 
   const int BN = gemm_token_tile(M);
   AMaps am;
   CUtensorMap xm;
-  if (!encode_2d(&am.m[0], W, N, K, 64) || !encode_2d(&xm, X, M, K, BN)) return DFLASH_EINVAL;
+  if (!encode_2d(&am.m[0], W, N, K, kWeightBoxRows) || !encode_2d(&xm, X, M, K, BN)) return DFLASH_EINVAL;
   GemmWork work;
   const int G = gemm_grid(M, N, K, splits, static_cast<size_t>(1) << 40, sms);
   work.partial_elems = static_cast<size_t>(2) * G * 128 * BN;
