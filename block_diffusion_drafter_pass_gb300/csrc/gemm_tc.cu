@@ -345,17 +345,25 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
           x = lo ? (x * cc - other[c] * sn) : (x * cc + other[c] * sn);
         }
         if (kind == EPI_QKV_ROPE) {
-          uint16_t* base = reg == 0 ? e.out_q : (reg == 1 ? e.out_k : e.out_v);
-          const size_t ld = static_cast<size_t>(reg == 0 ? e.n_q_heads : e.n_kv_heads) * d;
-          base[static_cast<size_t>(m) * ld + rf] = f32_to_bf16(x);
+          if (reg == 2) {   // values transposed per (sequence, head): [d][64 slots]
+            const int i = m / e.meta.B, j = m - i * e.meta.B;
+            e.out_v[((static_cast<size_t>(i) * e.n_kv_heads + hd) * d + di) * kPage + j] = f32_to_bf16(x);
+          } else {
+            uint16_t* base = reg == 0 ? e.out_q : e.out_k;
+            const size_t ld = static_cast<size_t>(reg == 0 ? e.n_q_heads : e.n_kv_heads) * d;
+            base[static_cast<size_t>(m) * ld + rf] = f32_to_bf16(x);
+          }
         } else {
           const int dst = sh.row_dst[c0 + c];
           if (dst < 0) continue;
-          const int layer = e.layer0 + (reg >> 1), kv = reg & 1;
-          // pool row = ((layer*P + page)*2 + kv)*n_kv + head)*64 + slot
-          const size_t row = static_cast<size_t>(layer) * e.pool_pages * 2 * e.n_kv_heads * kPage +
-                             static_cast<size_t>(dst) + static_cast<size_t>(kv * e.n_kv_heads + hd) * kPage;
-          e.pool[row * d + di] = f32_to_bf16(x);
+          const int layer = e.layer0 + (reg >> 1), slot = dst & (kPage - 1);
+          // elements of (layer, page): keys [n_kv][64][d], then values [n_kv][d][64]
+          const size_t lp = (static_cast<size_t>(layer) * e.pool_pages * 2 * e.n_kv_heads * kPage +
+                             static_cast<size_t>(dst - slot)) * d;
+          const size_t off = (reg & 1) ? static_cast<size_t>(e.n_kv_heads) * kPage * d +
+                                             (static_cast<size_t>(hd) * d + di) * kPage + slot
+                                       : (static_cast<size_t>(hd) * kPage + slot) * d + di;
+          e.pool[lp + off] = f32_to_bf16(x);
         }
       }
     }

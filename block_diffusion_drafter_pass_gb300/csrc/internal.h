@@ -88,9 +88,9 @@ struct GemmEpi {
   float* out_f32;
   int ld_out;
   // QKV_ROPE / SWIGLU / KV_APPEND
-  uint16_t* out_q;
-  uint16_t* out_k;
-  uint16_t* out_v;
+  uint16_t* out_q;                  // [M][n_q*d]
+  uint16_t* out_k;                  // [M][n_kv*d]
+  uint16_t* out_v;                  // transposed: [n_seq][n_kv][d][64 slots], slot = block position
   uint16_t* out_act;
   int n_valid;                      // SWIGLU: F (features beyond are padding)
   int head_dim;
@@ -100,7 +100,8 @@ struct GemmEpi {
   int rope_positions;
   SeqState seqs;
   SeqMeta meta;
-  // KV_APPEND
+  // KV_APPEND. Pool layout per (layer, page): keys [n_kv][64 slots][d], then
+  // values transposed [n_kv][d][64 slots].
   uint16_t* pool;
   int pool_pages;
   int layer0;                       // layer of region 0
@@ -161,18 +162,33 @@ struct AttnArgs {
   int pool_pages;
   int chunk_tiles;           // context chunk in 64-key tiles
   int items_cap;             // partial-buffer capacity in work items
-  const uint16_t* q;         // [n_seq*B][n_q*d] bf16
+  int rows_pad;              // row stride of the partial buffers (>= G*B)
+  int q_group_heads;         // > 0: query rows spread 16 per TMEM lane quarter, loaded in
+                             // boxes of q_group_heads heads x 16/q_group_heads positions
   float* part_o;             // [items][rows_pad][d]
   float2* part_ml;           // [items][rows_pad] (max, sum)
   uint16_t* out;             // [n_seq*B][n_q*d] bf16
   int* status;
 };
 
+// Tensor maps the attention kernel reads through (all bf16, 128-byte swizzle):
+//   pool_k  the pool as rows of d elements: key rows of (layer, page, head)
+//   pool_vt the pool as rows of 64 elements: transposed value rows [dim][slot]
+//   q       the block's queries, 3D (d, n_q, tokens), box (64, G, B), or with
+//           q_group_heads = gG > 0 box (64, gG, 16/gG)
+//   kblk    the block's keys, 3D (d, n_kv, tokens), box (64, 1, block_rows(B))
+//   vblk    the block's transposed values [seq][n_kv][d][64 slots], rows of 64
+struct AttnMaps {
+  CUtensorMap pool_k, pool_vt, q, kblk, vblk;
+};
+
 // part 0: the chunked attention kernel; part 1: the combine kernel.
-cudaError_t launch_attention(const CUtensorMap& pool_map, const CUtensorMap& kblk_map, const CUtensorMap& vblk_map,
-                             const AttnArgs& a, int grid, int part, cudaStream_t stream);
+cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& a, int grid, int part, cudaStream_t stream);
 int attention_block_rows(int B);   // key-box height used for the block's own keys
-int attention_ctas_per_sm(int head_dim, int ncw);   // resident attention CTAs per SM
+// Heads per 16-row query group when G*B <= 64 rows can be spread over the four
+// TMEM lane quarters (G divides 16 or 16 divides G); 0 otherwise.
+int attention_spread_group(int G, int B);
+int attention_ctas_per_sm(int head_dim);   // resident attention CTAs per SM
 
 // ----------------------------------------------------------------------------
 // Small kernels

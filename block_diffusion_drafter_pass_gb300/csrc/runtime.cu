@@ -53,11 +53,12 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, ui
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][heads][d] bf16, box = 64 dims x 1 head x box_rows rows.
-bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t heads, uint64_t d, uint32_t box_rows) {
+// [rows][heads][d] bf16, box = 64 dims x box_heads heads x box_rows rows.
+bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t heads, uint64_t d, uint32_t box_rows,
+               uint32_t box_heads = 1) {
   cuuint64_t dims[3] = {d, heads, rows};
   cuuint64_t strides[2] = {d * 2, heads * d * 2};
-  cuuint32_t box[3] = {64, 1, box_rows};
+  cuuint32_t box[3] = {64, box_heads, box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -98,7 +99,7 @@ struct dflash_ctx {
   float* ssB = nullptr;      // [parts][max_rows] partial sums of x^2 (O producer)
   uint16_t* q = nullptr;     // [max_rows, n_q*d]
   uint16_t* kb = nullptr;    // [max_rows, n_kv*d] block keys
-  uint16_t* vb = nullptr;    // [max_rows, n_kv*d] block values
+  uint16_t* vb = nullptr;    // [max_batch][n_kv][d][64 slots] block values, transposed
   uint16_t* attn = nullptr;  // [max_rows, n_q*d]
   uint16_t* act = nullptr;   // [max_rows, F]
   uint16_t* htg = nullptr;   // [max_fuse_tokens, H] bf16(W_c X * g_c)
@@ -116,7 +117,7 @@ struct dflash_ctx {
 
   // weight descriptors
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
-  CUtensorMap m_lm{}, m_wc{}, m_pool{};
+  CUtensorMap m_lm{}, m_wc{}, m_pool{}, m_pool_vt{}, m_vblk{};
   std::map<std::tuple<const void*, int, int, int, int>, CUtensorMap> act_maps;
 
   // host view of the sequences
@@ -128,7 +129,7 @@ struct dflash_ctx {
   bool snap_pending = false;
 
   int last_rows = 0, last_draft_rows = 0;
-  int attn_ctas_per_sm[9] = {};   // by compute-warp count
+  int attn_ctas_per_sm = 0;
   std::string err = "no error";
 
   // per-kernel accounting
@@ -169,6 +170,19 @@ const CUtensorMap* act_map(dflash_ctx* ctx, const void* ptr, int rows, int cols,
   CUtensorMap m;
   if (!encode_2d(&m, ptr, rows, cols, box_rows)) return nullptr;
   if (ctx->act_maps.size() > 4096) ctx->act_maps.clear();
+  return &(ctx->act_maps[key] = m);
+}
+
+// The block's queries [rows][n_q][d], box = 64 dims x G heads x B rows: the
+// G*B query rows of one (sequence, kv head) in one copy.
+// box_heads x box_rows = G x B (all rows of an item), or gG x 16/gG (one
+// 16-row group).
+const CUtensorMap* q_map(dflash_ctx* ctx, int box_heads, int box_rows) {
+  auto key = std::make_tuple(static_cast<const void*>(ctx->q), ctx->max_rows(), box_heads, box_rows, 4);
+  auto it = ctx->act_maps.find(key);
+  if (it != ctx->act_maps.end()) return &it->second;
+  CUtensorMap m;
+  if (!encode_3d(&m, ctx->q, ctx->max_rows(), ctx->cfg.n_heads, ctx->cfg.head_dim, box_rows, box_heads)) return nullptr;
   return &(ctx->act_maps[key] = m);
 }
 
@@ -353,7 +367,9 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
     return fail(nullptr, DFLASH_EINVAL, "capacities must be positive");
   if (!(c.rms_eps >= 0.f) || !(c.rope_base > 1.f)) return fail(nullptr, DFLASH_EINVAL, "bad rms_eps or rope_base");
   const long long pool_rows = 1LL * c.n_layers * c.max_pages * 2 * c.n_kv_heads * kPage;
-  if (pool_rows >= (1LL << 31)) return fail(nullptr, DFLASH_EINVAL, "KV pool too large for 32-bit TMA coordinates");
+  // the pool is also read as rows of 64 elements (transposed values)
+  if (pool_rows * (d / 64) >= (1LL << 31))
+    return fail(nullptr, DFLASH_EINVAL, "KV pool too large for 32-bit TMA coordinates");
   const void* ptrs[] = {w->w_c, w->g_c, w->embed, w->lm_head, w->g_final};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return fail(nullptr, DFLASH_EINVAL, "weight pointer null or not 16-byte aligned");
@@ -416,9 +432,10 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
   CA(dalloc(&ctx->ssB, rows * parts), "workspace");
   CA(dalloc(&ctx->q, rows * nq * d), "workspace");
   CA(dalloc(&ctx->kb, rows * nkv * d), "workspace");
-  CA(dalloc(&ctx->vb, rows * nkv * d), "workspace");
+  const size_t vb_elems = static_cast<size_t>(c.max_batch) * nkv * d * kPage;
+  CA(dalloc(&ctx->vb, vb_elems), "workspace");
   CA(cudaMemset(ctx->kb, 0, rows * nkv * d * 2), "workspace");
-  CA(cudaMemset(ctx->vb, 0, rows * nkv * d * 2), "workspace");
+  CA(cudaMemset(ctx->vb, 0, vb_elems * 2), "workspace");
   CA(dalloc(&ctx->attn, rows * nq * d), "workspace");
   CA(dalloc(&ctx->act, rows * F), "workspace");
   CA(dalloc(&ctx->htg, static_cast<size_t>(c.max_fuse_tokens) * H), "workspace");
@@ -455,7 +472,9 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
   const int wb = kWeightBoxRows;
   bool ok = encode_2d(&ctx->m_lm, w->lm_head, c.vocab, H, wb) &&
             encode_2d(&ctx->m_wc, w->w_c, H, static_cast<uint64_t>(c.n_feat_layers) * H, wb) &&
-            encode_2d(&ctx->m_pool, ctx->pool, pool_rows, d, 64);
+            encode_2d(&ctx->m_pool, ctx->pool, pool_rows, d, 64) &&
+            encode_2d(&ctx->m_pool_vt, ctx->pool, static_cast<uint64_t>(pool_rows) * (d / 64), 64, 64) &&
+            encode_2d(&ctx->m_vblk, ctx->vb, static_cast<uint64_t>(c.max_batch) * nkv * d, 64, 64);
   ctx->m_wq.resize(c.n_layers);
   ctx->m_wk.resize(c.n_layers);
   ctx->m_wv.resize(c.n_layers);
@@ -690,9 +709,8 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   long long tiles_ub = 0;
   for (int i = 0; i < n_seq; ++i) tiles_ub += 1LL * nkv * (ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1);
   // one wave of resident attention CTAs, each with about one chunk of tiles
-  const int ncw = ceil_div((nq / nkv) * B, 16);
-  int& per_sm = ctx->attn_ctas_per_sm[ncw];
-  if (per_sm == 0) per_sm = attention_ctas_per_sm(d, ncw);
+  int& per_sm = ctx->attn_ctas_per_sm;
+  if (per_sm == 0) per_sm = attention_ctas_per_sm(d);
   const int grid_full = per_sm * ctx->num_sms;
   int chunk = std::max(2, ceil_div(tiles_ub, grid_full));
   auto items_for = [&](int ch) {
@@ -705,13 +723,20 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
 
   const int Bb = attention_block_rows(B);
   const CUtensorMap* km = blk_map(ctx, ctx->kb, M, Bb);
-  const CUtensorMap* vm = blk_map(ctx, ctx->vb, M, Bb);
+  const int q_group = attention_spread_group(nq / nkv, B);
+  const CUtensorMap* qm = q_group > 0 ? q_map(ctx, q_group, 16 / q_group) : q_map(ctx, nq / nkv, B);
   const CUtensorMap* hmap = act_map(ctx, ctx->hg, M, H, BN);
   const int parts = ceil_div(H, 128);
   const int rows_ld = ctx->max_rows();
   const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, BN);
   const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, BN);
-  if (!km || !vm || !hmap || !amap || !fmap) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+  if (!km || !qm || !hmap || !amap || !fmap) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+  AttnMaps attn_maps;
+  attn_maps.pool_k = ctx->m_pool;
+  attn_maps.pool_vt = ctx->m_pool_vt;
+  attn_maps.q = *qm;
+  attn_maps.kblk = *km;
+  attn_maps.vblk = ctx->m_vblk;
 
   double ctx_tokens = 0, attn_flops = 0;
   for (int i = 0; i < n_seq; ++i) {
@@ -757,18 +782,19 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       a.pool_pages = c.max_pages;
       a.chunk_tiles = chunk;
       a.items_cap = ctx->items_cap;
-      a.q = ctx->q;
+      a.rows_pad = 16 * ceil_div((nq / nkv) * B, 16);
+      a.q_group_heads = q_group;
       a.part_o = ctx->part_o;
       a.part_ml = ctx->part_ml;
       a.out = ctx->attn;
       a.status = ctx->d_status;
       {
         ProfScope ps(ctx, DFLASH_K_ATTN, stream, attn_bytes, attn_flops);
-        CK(launch_attention(ctx->m_pool, *km, *vm, a, attn_grid, 0, stream));
+        CK(launch_attention(attn_maps, a, attn_grid, 0, stream));
       }
       {
         ProfScope ps(ctx, DFLASH_K_ATTN_COMBINE, stream, 2.0 * M * nq * d, 0);
-        CK(launch_attention(ctx->m_pool, *km, *vm, a, attn_grid, 1, stream));
+        CK(launch_attention(attn_maps, a, attn_grid, 1, stream));
       }
     }
     {  // x += attn W_o^T; the FFN's RMSNorm input is folded into the epilogue
@@ -909,10 +935,12 @@ dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0
     }
     const int slot = pos % kPage;
     for (int h = 0; h < nkv; ++h) {
-      const uint16_t* ks = buf.data() + ((static_cast<size_t>(0) * nkv + h) * kPage + slot) * d;
-      const uint16_t* vs = buf.data() + ((static_cast<size_t>(1) * nkv + h) * kPage + slot) * d;
+      // keys [n_kv][64 slots][d], then values transposed [n_kv][d][64 slots]
+      const uint16_t* ks = buf.data() + (static_cast<size_t>(h) * kPage + slot) * d;
+      const uint16_t* vs = buf.data() + static_cast<size_t>(nkv) * kPage * d + static_cast<size_t>(h) * d * kPage + slot;
       if (k_out) std::memcpy(k_out + (static_cast<size_t>(t) * nkv + h) * d, ks, d * 2);
-      if (v_out) std::memcpy(v_out + (static_cast<size_t>(t) * nkv + h) * d, vs, d * 2);
+      if (v_out)
+        for (int di = 0; di < d; ++di) v_out[(static_cast<size_t>(t) * nkv + h) * d + di] = vs[static_cast<size_t>(di) * kPage];
     }
   }
   return DFLASH_OK;

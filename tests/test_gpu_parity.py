@@ -190,3 +190,28 @@ def test_qwen3_8b_full_depth_context_4096(dfl):
         anchors = make_anchor_ids_np(1, shape.vocab, seed=2)
         _, ref, checked = _draft_and_compare(d, orc, [0], anchors, 16, "8B full depth C=4096")
         assert checked >= 5, f"only {checked} rows with gap > {GAP}"
+
+
+@pytest.mark.parametrize("n_heads,n_kv,blocks", [(8, 2, (32, 16, 5)), (6, 2, (32, 8, 1))])
+def test_gqa_group_layouts(dfl, n_heads, n_kv, blocks):
+    """Query-row layouts of the attention kernel: G = 4 with G*B = 128 (one
+    thread per row), 64 and 20 (rows spread over the four TMEM lane
+    quarters); G = 3 (16 not a multiple of G: one thread per row at every B)."""
+    from dataclasses import replace
+    sh = replace(TINY, n_heads=n_heads, n_kv_heads=n_kv)
+    wn = make_weights_np(sh, seed=51, gamma="jitter", std=0.05)
+    orc = oracle.OracleDrafter(sh, wn)
+    width = sh.n_feat_layers * sh.hidden
+    with dfl.Drafter(sh, np_weights_to_device(wn, DEV), max_seqs=3, max_batch=3, max_block=32, max_ctx=1024,
+                     max_fuse_tokens=512) as d:
+        ctx = [200, 64, 7]
+        f = make_features_np(sum(ctx), width, seed=52)
+        d.fuse_ctx([0, 1, 2], ctx, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx([0, 1, 2], ctx, f, pending=False)
+        anchors = make_anchor_ids_np(3, sh.vocab, seed=53)
+        total = 0
+        for B in blocks:
+            _, _, c = _draft_and_compare(d, orc, [0, 1, 2], anchors, B, f"G={n_heads // n_kv} B={B}",
+                                         ROW_REL_HIGH_GAIN)
+            total += c
+        assert total > 0
