@@ -17,6 +17,7 @@
 //              thread: S = Q K^T (M = 128 query rows, N = 64 keys) into one of
 //              two TMEM S buffers, then O += P V (N = d) into the item's TMEM
 //              O buffer, with P read from shared memory;
+//   warp 6     L2 prefetch of the context pages a few steps ahead of warp 0;
 //   warps 2-5  one query row per thread (the TMEM lane quarter of the warp):
 //              online softmax in the log2 domain on S read from TMEM, P
 //              written to shared memory as bf16, O rescaled in TMEM only when
@@ -38,25 +39,45 @@ namespace {
 
 constexpr int kKeyTile = 64;
 constexpr float kRescaleLog2 = 8.f;   // rescale O when the row max grows by more than 2^8
+constexpr int kThreads = 224;         // producer, MMA, 4 softmax warps, L2 prefetch warp
+constexpr int kPrefetchSteps = 4;     // the prefetch warp runs this many steps ahead of the producer
 
 // Rows of the block's own key box: B rounded up to 16 or 32.
 __host__ __device__ __forceinline__ int block_rows(int B) { return B <= 16 ? 16 : 32; }
 
 template <int D>
 struct ACfg {
-  static constexpr int kStages = D == 128 ? 4 : 6;
-  static constexpr int kBox = 64 * 128;                   // 64 rows x 128 bytes
-  static constexpr int kKBytes = (D / 64) * kBox;         // keys [64][D]
-  static constexpr int kVBytes = (D / 64) * kBox;         // values transposed [D][64]
-  static constexpr int kStageBytes = kKBytes + kVBytes;
-  static constexpr int kQBox = 128 * 128;                 // 128 query rows x 64 dims
-  static constexpr int kQBytes = (D / 64) * kQBox;
-  static constexpr int kPBytes = 128 * 128;               // P [128 rows][64 keys] bf16
-  static constexpr int kSmem = kStages * kStageBytes + 2 * kQBytes + 2 * kPBytes + 1024;
-  static constexpr uint32_t kTmemCols = D == 128 ? 512 : 256;   // S 2x64 + O 2xD
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, kKeyTile);
+  // One pipeline stage holds one step: two 64-key units (context pages or the
+  // block) as [K dim-box 0: 128 keys x 128 B]...[K dim-box D/64-1][V^T unit 0]
+  // [V^T unit 1], so S = Q K^T of a step is one N = 128 product per K slice.
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kUnitBox = 64 * 128;               // 64 rows x 128 bytes
+  static constexpr int kKBox = 2 * kUnitBox;              // 128 key rows of one 64-dim slice
+  static constexpr int kKBytes = (D / 64) * kKBox;
+  static constexpr int kVUnit = (D / 64) * kUnitBox;      // values transposed [D][64] of one unit
+  static constexpr int kStageBytes = kKBytes + 2 * kVUnit;
+  static constexpr int kSmem = kStages * kStageBytes + 1024;
+  // TMEM columns: S buffers at 0 and 128 (P overwrites the first 64 columns
+  // of its own S as packed bf16), Q at 256 (D/2 columns of packed bf16), O after it.
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSCols = 2 * kKeyTile;
+  static constexpr uint32_t kQCol = 2 * kSCols;
+  static constexpr uint32_t kOCol = kQCol + D / 2;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 2 * kKeyTile);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D);
 };
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M rows in TMEM lanes, K packed two bf16
+// per 32-bit column), B from a shared-memory descriptor. One thread issues.
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -128,6 +149,29 @@ __device__ __forceinline__ void tmem_ld_half32(uint32_t taddr, float (&v)[32]) {
 }
 
 template <int SPLIT>
+__device__ __forceinline__ void tmem_ld_half64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64], %65;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "n"(SPLIT)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int SPLIT>
 __device__ __forceinline__ void tmem_st_half32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %33, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -136,6 +180,48 @@ __device__ __forceinline__ void tmem_st_half32(uint32_t taddr, const float (&v)[
       "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
       "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
       "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31]), "n"(SPLIT)
+      : "memory");
+}
+
+// 32x32b stores of packed words (one lane per thread), x16 / x32 columns.
+__device__ __forceinline__ void tmem_st_u16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_u32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+// 16x32bx2 stores of packed words: threads 0-15 to columns [c, c+n), threads
+// 16-31 to [c+SPLIT, c+SPLIT+n) of the same 16 lanes.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st_half_u16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %17, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "n"(SPLIT)
+      : "memory");
+}
+template <int SPLIT>
+__device__ __forceinline__ void tmem_st_half_u32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %33, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]), "n"(SPLIT)
       : "memory");
 }
 
@@ -177,31 +263,34 @@ __device__ __forceinline__ SeqSplit seq_split(const AttnArgs& a, int i) {
 }
 
 struct Item {
-  int i, kvh, tb, te;   // sequence index, kv head, tiles [tb, te)
+  int i, kvh, tb, te;   // sequence index, kv head, units [tb, te)
 };
 
 // SPREAD (G*B <= 64): query row r sits in TMEM lane 32*(r/16) + r%16, so all
 // four lane quarters (and the four SM sub-partitions that own them) carry 16
-// rows, and two threads share a row (32 keys each). Otherwise one thread per
-// row, row r in lane r.
+// rows, and two threads share a row (64 keys of a step each). Otherwise one
+// thread per row, row r in lane r.
+//
+// Units are 64-key tiles: context pages 0 .. n_ctx-1, then the block (unit
+// n_ctx). An item covers units [tb, te) with tb even; a step takes units
+// (tb + 2j, tb + 2j + 1), the second possibly absent.
 template <int D, bool SPREAD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ AttnArgs a) {
   using C = ACfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + S * C::kStageBytes;
-  uint8_t* sP = sQ + 2 * C::kQBytes;   // queries double-buffered by item
   __shared__ __align__(8) uint64_t kv_full[S], kv_empty[S];
-  __shared__ __align__(8) uint64_t q_full[2], q_empty[2], mma_done;
-  __shared__ __align__(8) uint64_t s_full[2], p_full[2], pv_done[2], o_full[2], o_free[2];
+  __shared__ __align__(8) uint64_t q_ready, mma_done, o_full, o_free;
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int s_prefix[kMaxBatch + 1];
   __shared__ int s_len[kMaxBatch];
   __shared__ int s_nctx[kMaxBatch];
   __shared__ int s_nch[kMaxBatch];
   __shared__ volatile int abort_flag;
+  __shared__ volatile int s_issued;   // steps whose copies the producer has issued
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_seq = a.meta.n_seq, B = a.meta.B;
@@ -213,17 +302,14 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(&q_full[0], 1);
-    mbar_init(&q_full[1], 1);
-    mbar_init(&q_empty[0], 1);
-    mbar_init(&q_empty[1], 1);
+    mbar_init(&q_ready, 4);
     mbar_init(&mma_done, 1);
+    mbar_init(&o_full, 1);
+    s_issued = 0;
+    mbar_init(&o_free, 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 4);
-      mbar_init(&pv_done[b], 1);
-      mbar_init(&o_full[b], 1);
-      mbar_init(&o_free[b], 4);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -231,12 +317,18 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&maps.pool_k);
     tma_prefetch_desc(&maps.pool_vt);
-    tma_prefetch_desc(&maps.q);
     tma_prefetch_desc(&maps.kblk);
     tma_prefetch_desc(&maps.vblk);
   }
   if (warp == 1) tmem_alloc(&tmem_slot, C::kTmemCols);
-  grid_dep_wait();
+  // Dependencies: every launch sequence of the library puts a kernel that
+  // waits for its predecessor before it lets its dependents start (the block
+  // embedding, the previous layer's combine) between the last writer of the
+  // KV pool, page table and lengths and this kernel. They are final when this
+  // kernel starts, so the context pages stream before griddepcontrol.wait;
+  // only q and the block's own keys and values, written by the projection
+  // kernel just before, are read after it (producer: block unit; softmax
+  // warps: q).
   if (threadIdx.x == 0) {
     int acc = 0;
     for (int i = 0; i < n_seq; ++i) {
@@ -277,160 +369,243 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const int Bb = block_rows(B);
-      int n = 0, k = 0;
-      bool dead = false;
-      for (int item = blockIdx.x; item < total && !dead; item += gridDim.x, ++k) {
+      int q = 0;
+      bool dead = false, waited = false;
+      for (int item = blockIdx.x; item < total && !dead; item += gridDim.x) {
         const Item it = decode(item);
-        const int qb = k & 1;
-        if (!mbar_wait(&q_empty[qb], ((k >> 1) & 1) ^ 1, &abort_flag)) {
-          give_up();
-          break;
-        }
-        uint8_t* qdst = sQ + qb * C::kQBytes;
-        if constexpr (SPREAD) {
-          // groups of 16 rows (gB positions x gG heads) to smem rows 32k .. 32k+15
-          const int gG = a.q_group_heads, gB = 16 / gG, ng = (R + 15) / 16;
-          mbar_arrive_expect_tx(&q_full[qb], ng * (D / 64) * 16 * 128);
-          for (int g = 0; g < ng; ++g) {
-            const int hpg = G / gG;                        // groups per block position
-            const int j = g / hpg * gB, h0 = (g % hpg) * gG;
-#pragma unroll
-            for (int bx = 0; bx < D / 64; ++bx)
-              tma_load_3d(qdst + bx * C::kQBox + g * 32 * 128, &maps.q, &q_full[qb], bx * 64, it.kvh * G + h0,
-                          it.i * B + j);
-          }
-        } else {
-          mbar_arrive_expect_tx(&q_full[qb], (D / 64) * R * 128);
-#pragma unroll
-          for (int bx = 0; bx < D / 64; ++bx)
-            tma_load_3d(qdst + bx * C::kQBox, &maps.q, &q_full[qb], bx * 64, it.kvh * G, it.i * B);
-        }
-        const int slot = a.meta.slot[it.i];
-        for (int t = it.tb; t < it.te; ++t, ++n) {
-          const int s = n % S;
-          if (!mbar_wait(&kv_empty[s], ((n / S) & 1) ^ 1, &abort_flag)) {
+        const int slot = a.meta.slot[it.i], nctx = s_nctx[it.i];
+        const int* ptab = a.seqs.page_table + static_cast<size_t>(slot) * a.seqs.pages_per_seq;
+        auto page_of = [&](int t) {   // -1 (latched below) if the table is too short
+          return t < nctx ? (t < a.seqs.pages_per_seq ? ptab[t] : -1) : 0;
+        };
+        int cur0 = page_of(it.tb), cur1 = it.tb + 1 < it.te ? page_of(it.tb + 1) : 0;
+        for (int t0 = it.tb; t0 < it.te; t0 += 2, ++q) {
+          // page ids of the next step are in flight during the wait below
+          const int nxt0 = t0 + 2 < it.te ? page_of(t0 + 2) : 0;
+          const int nxt1 = t0 + 3 < it.te ? page_of(t0 + 3) : 0;
+          const int s = q % S;
+          if (!mbar_wait(&kv_empty[s], ((q / S) & 1) ^ 1, &abort_flag)) {
             give_up();
             dead = true;
             break;
           }
-          uint8_t* ks = smem + s * C::kStageBytes;
-          uint8_t* vs = ks + C::kKBytes;
-          if (t < s_nctx[it.i]) {
-            int page = -1;
-            if (t < a.seqs.pages_per_seq) page = a.seqs.page_table[static_cast<size_t>(slot) * a.seqs.pages_per_seq + t];
-            if (page < 0 || page >= a.pool_pages) {
-              latch_status(a.status, kDevBounds);
-              page = 0;
-            }
-            const int lp = a.layer * a.pool_pages + page;
-            const int rowk = (lp * 2 * nkv + it.kvh) * kKeyTile;        // rows of d elements
-            const int rowv = ((lp * 2 + 1) * nkv + it.kvh) * D;         // rows of 64 elements
-            mbar_arrive_expect_tx(&kv_full[s], C::kStageBytes);
+          uint8_t* st = smem + s * C::kStageBytes;
+          const int nu = min(2, it.te - t0);
+          uint32_t bytes = 0;
+          for (int u = 0; u < nu; ++u) bytes += (t0 + u < nctx ? C::kVUnit : (D / 64) * Bb * 128) + C::kVUnit;
+          mbar_arrive_expect_tx(&kv_full[s], bytes);
+          for (int u = 0; u < nu; ++u) {
+            const int t = t0 + u;
+            uint8_t* ku = st + u * C::kUnitBox;
+            uint8_t* vu = st + C::kKBytes + u * C::kVUnit;
+            if (t < nctx) {
+              int page = u == 0 ? cur0 : cur1;
+              if (page < 0 || page >= a.pool_pages) {
+                latch_status(a.status, kDevBounds);
+                page = 0;
+              }
+              const int lp = a.layer * a.pool_pages + page;
+              const int rowk = (lp * 2 * nkv + it.kvh) * kKeyTile;   // rows of d elements
+              const int rowv = ((lp * 2 + 1) * nkv + it.kvh) * D;    // rows of 64 elements
 #pragma unroll
-            for (int bx = 0; bx < D / 64; ++bx) {
-              tma_load_2d(ks + bx * C::kBox, &maps.pool_k, &kv_full[s], bx * 64, rowk);
-              tma_load_2d(vs + bx * C::kBox, &maps.pool_vt, &kv_full[s], 0, rowv + bx * 64);
-            }
-          } else {
-            mbar_arrive_expect_tx(&kv_full[s], (D / 64) * Bb * 128 + C::kVBytes);
+              for (int bx = 0; bx < D / 64; ++bx) {
+                tma_load_2d(ku + bx * C::kKBox, &maps.pool_k, &kv_full[s], bx * 64, rowk);
+                tma_load_2d(vu + bx * C::kUnitBox, &maps.pool_vt, &kv_full[s], 0, rowv + bx * 64);
+              }
+            } else {
+              if (!waited) {   // the block's keys and values come from the projection kernel
+                grid_dep_wait();
+                waited = true;
+              }
 #pragma unroll
-            for (int bx = 0; bx < D / 64; ++bx) {
-              tma_load_3d(ks + bx * C::kBox, &maps.kblk, &kv_full[s], bx * 64, it.kvh, it.i * B);
-              tma_load_2d(vs + bx * C::kBox, &maps.vblk, &kv_full[s], 0, (it.i * nkv + it.kvh) * D + bx * 64);
+              for (int bx = 0; bx < D / 64; ++bx) {
+                tma_load_3d(ku + bx * C::kKBox, &maps.kblk, &kv_full[s], bx * 64, it.kvh, it.i * B);
+                tma_load_2d(vu + bx * C::kUnitBox, &maps.vblk, &kv_full[s], 0,
+                            (it.i * nkv + it.kvh) * D + bx * 64);
+              }
             }
           }
+          s_issued = q + 1;
+          cur0 = nxt0;
+          cur1 = nxt1;
         }
       }
       // copies still in flight complete before shared memory is released
-      for (int j = max(0, n - S); j < n; ++j) mbar_wait(&kv_full[j % S], (j / S) & 1);
-      for (int j = max(0, k - 2); j < k; ++j) mbar_wait(&q_full[j & 1], (j >> 1) & 1);
+      for (int j = max(0, q - S); j < q; ++j) mbar_wait(&kv_full[j % S], (j / S) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // Per step q: S_{q+1} is issued before PV_q, so S of the next step
+    // overlaps the softmax of this one. P_q lives in S buffer q&1; S_{q+2}
+    // overwrites it only after PV_q, which precedes it in issue order.
     if (lane == 0) {
-      const uint32_t q_base = smem_u32(sQ), p_base = smem_u32(sP), kv_base = smem_u32(smem);
-      auto issue_s = [&](int m, int qb) {   // S[m & 1] = Q K_m^T
-        const uint32_t kb = kv_base + (m % S) * C::kStageBytes;
-        const uint32_t qs = q_base + qb * C::kQBytes;
-        const uint32_t d_tmem = tmem + (m & 1) * kKeyTile;
+      const uint32_t kv_base = smem_u32(smem);
+      auto issue_s = [&](int q) {   // S[q & 1] = Q K^T over the step's 128 keys
+        const uint32_t kb = kv_base + (q % S) * C::kStageBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;   // 16 elements along K inside the 128-byte row
-          tc_mma_bf16(d_tmem, sdesc_kmajor_sw128(qs + (kk >> 2) * C::kQBox + off),
-                      sdesc_kmajor_sw128(kb + (kk >> 2) * C::kBox + off), C::kIdescS, kk > 0);
-        }
-        tc_commit(&s_full[m & 1]);
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_bf16_ts(tmem + (q & 1) * C::kSCols, tmem + C::kQCol + kk * 8,
+                         sdesc_kmajor_sw128(kb + (kk >> 2) * C::kKBox + (kk & 3) * 32), C::kIdescS, kk > 0);
+        tc_commit(&s_full[q & 1]);
       };
-      int n = 0, k = 0;
+      auto issue_pv = [&](int q, int j, const Item& it) {   // O += P V over the step's units
+        const int nu = min(2, it.te - (it.tb + 2 * j));
+        const uint32_t vb = kv_base + (q % S) * C::kStageBytes + C::kKBytes;
+        for (int u = 0; u < nu; ++u) {
+#pragma unroll
+          for (int kk = 0; kk < kKeyTile / 16; ++kk)
+            tc_mma_bf16_ts(tmem + C::kOCol, tmem + (q & 1) * C::kSCols + u * 32 + kk * 8,
+                           sdesc_kmajor_sw128(vb + u * C::kVUnit + kk * 32), C::kIdescO,
+                           (j > 0 || u > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&kv_empty[q % S]);
+      };
+      int q = 0, k = 0;
       bool dead = false;
       for (int item = blockIdx.x; item < total && !dead; item += gridDim.x, ++k) {
         const Item it = decode(item);
-        const int nt = it.te - it.tb;
-        const int ob = k & 1;
-        const uint32_t o_tmem = tmem + 2 * kKeyTile + ob * D;
-        const int qb = k & 1;
-        if (!mbar_wait(&q_full[qb], (k >> 1) & 1, &abort_flag) ||
-            !mbar_wait(&kv_full[n % S], (n / S) & 1, &abort_flag)) {
+        const int ns = (it.te - it.tb + 1) >> 1;
+        if (!mbar_wait(&q_ready, k & 1, &abort_flag)) {
           give_up();
           break;
         }
-        tc_fence_after();
-        issue_s(n, qb);
-        if (nt == 1) tc_commit(&q_empty[qb]);
-        for (int lt = 0; lt < nt; ++lt) {
-          const int m = n + lt;
-          if (lt + 1 < nt) {
-            if (!mbar_wait(&kv_full[(m + 1) % S], ((m + 1) / S) & 1, &abort_flag)) {
-              give_up();
-              dead = true;
-              break;
-            }
+        // Issue whichever product is ready, PV first (it frees a stage):
+        // S_x needs its keys and PV_{x-2} issued (P_{x-2} lives in S buffer
+        // x&1); PV_y needs P_y (and, first in the item, O read out).
+        int ns_done = 0, npv = 0;
+        unsigned long long t0 = global_ns();
+        while (npv < ns) {
+          bool moved = false;
+          if (npv < ns_done && mbar_test_wait(&p_full[(q + npv) & 1], ((q + npv) >> 1) & 1) &&
+              (npv > 0 || mbar_test_wait(&o_free, (k & 1) ^ 1))) {
             tc_fence_after();
-            issue_s(m + 1, qb);
-            if (lt + 2 == nt) tc_commit(&q_empty[qb]);
+            issue_pv(q + npv, npv, it);
+            ++npv;
+            moved = true;
           }
-          if (!mbar_wait(&p_full[m & 1], (m >> 1) & 1, &abort_flag) ||
-              (lt == 0 && !mbar_wait(&o_free[ob], ((k >> 1) & 1) ^ 1, &abort_flag))) {
+          if (ns_done < ns && ns_done <= npv + 1 &&
+              mbar_test_wait(&kv_full[(q + ns_done) % S], ((q + ns_done) / S) & 1)) {
+            tc_fence_after();
+            issue_s(q + ns_done);
+            ++ns_done;
+            moved = true;
+          }
+          if (moved) {
+            t0 = global_ns();
+          } else if (abort_flag || global_ns() - t0 > kWaitLimitNs) {
             give_up();
             dead = true;
             break;
           }
-          tc_fence_after();
-          const uint32_t vb = kv_base + (m % S) * C::kStageBytes + C::kKBytes;
-          const uint32_t pb = p_base + (m & 1) * C::kPBytes;
-#pragma unroll
-          for (int kk = 0; kk < kKeyTile / 16; ++kk)
-            tc_mma_bf16(o_tmem, sdesc_kmajor_sw128(pb + kk * 32), sdesc_kmajor_sw128(vb + kk * 32), C::kIdescO,
-                        (lt > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&kv_empty[m % S]);
-          tc_commit(&pv_done[m & 1]);
         }
         if (dead) break;
-        tc_commit(&o_full[ob]);
-        n += nt;
+        tc_commit(&o_full);
+        q += ns;
       }
       // every issued MMA completes before TMEM and shared memory are released
       tc_commit(&mma_done);
       mbar_wait(&mma_done, 0);
     }
+  } else if (warp == 6) {
+    // ---------------- L2 prefetch ----------------
+    // Walks the same steps as the producer, at most kPrefetchSteps ahead of
+    // it, and pulls their context pages into L2 with plain prefetches (one
+    // 128-byte line per lane), so the producer's copies hit L2.
+    int q = 0;
+    bool stop = false;
+    for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
+      const Item it = decode(item);
+      const int slot = a.meta.slot[it.i], nctx = s_nctx[it.i];
+      const int* ptab = a.seqs.page_table + static_cast<size_t>(slot) * a.seqs.pages_per_seq;
+      for (int t0 = it.tb; t0 < it.te && !stop; t0 += 2, ++q) {
+        if (s_issued + kPrefetchSteps <= q) {
+          const unsigned long long w0 = global_ns();
+          while (s_issued + kPrefetchSteps <= q) {
+            if (abort_flag || global_ns() - w0 > kWaitLimitNs) {
+              stop = true;
+              break;
+            }
+            __nanosleep(200);
+          }
+          if (stop) break;
+        }
+        for (int u = 0; u < 2; ++u) {
+          const int t = t0 + u;
+          if (t >= it.te || t >= nctx || t >= a.seqs.pages_per_seq) continue;
+          const int page = ptab[t];
+          if (page < 0 || page >= a.pool_pages) continue;
+          const size_t lp = static_cast<size_t>(a.layer) * a.pool_pages + page;
+          const uint16_t* kp = a.pool + ((lp * 2 * nkv + it.kvh) * kKeyTile) * D;
+          const uint16_t* vp = a.pool + (((lp * 2 + 1) * nkv + it.kvh) * D) * kKeyTile;
+#pragma unroll
+          for (int l = lane; l < kKeyTile * D * 2 / 128; l += 32) {   // 128-byte lines of a 64 x D tile
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(kp + l * 64));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(vp + l * 64));
+          }
+        }
+      }
+    }
   } else {
     // ---------------- softmax / output warps ----------------
-    constexpr int kCols = SPREAD ? 32 : 64;                // S columns per thread
     const int quarter = warp & 3;                          // TMEM lanes 32*quarter .. +31
-    const int half = SPREAD ? (lane >> 4) : 0;             // which 32 keys of the row (SPREAD)
-    const int tlane = quarter * 32 + (SPREAD ? (lane & 15) : lane);   // TMEM lane = Q/P smem row
-    const int row = SPREAD ? quarter * 16 + (lane & 15) : tlane;      // query row r
-    const bool active = (SPREAD ? quarter * 16 : quarter * 32) < R;   // warp-uniform
+    const int half = SPREAD ? (lane >> 4) : 0;             // which unit of the step (SPREAD)
+    const int row = SPREAD ? quarter * 16 + (lane & 15) : quarter * 32 + lane;   // query row r
+    const bool active = (SPREAD ? quarter * 16 : quarter * 32) < R;              // warp-uniform
     const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t o_tmem = lane_tmem + C::kOCol;
     const float sl2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));   // log2(e)/sqrt(d)
-    uint8_t* p_row = sP + tlane * 128;
     // waits taken by all 32 lanes together, so the warp-collective TMEM
     // accesses after them never diverge (also when a wait runs out)
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, &abort_flag));
     };
+    // Q rows of an item into TMEM (packed bf16 pairs): the thread's row,
+    // all D dims (one thread per row) or D/2 dims (SPREAD, by half).
+    auto load_q = [&](const Item& it) {
+      if (active) {
+        constexpr int kW = SPREAD ? D / 4 : D / 2;       // 32-bit words per thread
+        uint32_t qv[kW];
+        if (row < R) {
+          const int j = row / G, g = row - j * G;
+          const uint4* src = reinterpret_cast<const uint4*>(
+              a.q + (static_cast<size_t>(it.i * B + j) * a.n_q_heads + it.kvh * G + g) * D + half * (D / 2));
+#pragma unroll
+          for (int c = 0; c < kW / 4; ++c) {
+            const uint4 v4 = __ldcg(src + c);
+            qv[4 * c] = v4.x;
+            qv[4 * c + 1] = v4.y;
+            qv[4 * c + 2] = v4.z;
+            qv[4 * c + 3] = v4.w;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kW; ++c) qv[c] = 0u;
+        }
+        if constexpr (SPREAD) {
+          if constexpr (D == 128) tmem_st_half_u32<32>(lane_tmem + C::kQCol, qv);
+          else tmem_st_half_u16<16>(lane_tmem + C::kQCol, qv);
+        } else {
+          if constexpr (D == 128) {
+            uint32_t lo[32], hi[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              lo[c] = qv[c];
+              hi[c] = qv[32 + c];
+            }
+            tmem_st_u32(lane_tmem + C::kQCol, lo);
+            tmem_st_u32(lane_tmem + C::kQCol + 32, hi);
+          } else {
+            tmem_st_u32(lane_tmem + C::kQCol, qv);
+          }
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready);
+    };
     // O row of this thread: D columns (one thread per row) or D/2 (SPREAD)
-    auto o_scale = [&](uint32_t o_tmem, float alpha) {
+    auto o_scale = [&](float alpha) {
 #pragma unroll
       for (int c0 = 0; c0 < (SPREAD ? D / 2 : D); c0 += 32) {
         float ov[32];
@@ -443,42 +618,76 @@ __global__ void __launch_bounds__(192, 1)
       }
       tmem_wait_st();
     };
-    int n = 0, k = 0;
+    // 64 S values of unit u (one thread per row) or of this thread's unit (SPREAD)
+    auto load_s = [&](uint32_t s_tmem, int u, float (&sv)[64]) {
+      if constexpr (SPREAD) tmem_ld_half64<64>(s_tmem, sv);
+      else tmem_ld64(s_tmem + u * kKeyTile, sv);
+    };
+    auto mask = [&](float (&sv)[64], int nvalid) {
+      if (nvalid < kKeyTile) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sv[c] = c < nvalid ? sv[c] : -INFINITY;
+      }
+    };
+    // p = 2^(s*sl2 - m), packed to bf16 pairs; returns the sum of p
+    auto exp_pack = [&](const float (&sv)[64], float m, uint32_t (&pk)[32]) {
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(sv[2 * c], sl2, -m));
+        const float p1 = ex2(fmaf(sv[2 * c + 1], sl2, -m));
+        s4[c & 3] += p0 + p1;
+        pk[c] = pack_bf16(p0, p1);
+      }
+      return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    };
+    int q = 0, k = 0;
     bool dead = false;
+    grid_dep_wait();   // q comes from the projection kernel
+    if (blockIdx.x < total) load_q(decode(blockIdx.x));
     for (int item = blockIdx.x; item < total && !dead; item += gridDim.x, ++k) {
       const Item it = decode(item);
-      const int nt = it.te - it.tb;
-      const int ob = k & 1;
-      const uint32_t o_tmem = lane_tmem + 2 * kKeyTile + ob * D;
-      const int len = s_len[it.i];
+      const int ns = (it.te - it.tb + 1) >> 1;
+      const int len = s_len[it.i], nctx = s_nctx[it.i];
+      auto unit_valid = [&](int t) {   // valid keys of unit t (0 if absent)
+        return t >= it.te ? 0 : (t < nctx ? min(kKeyTile, len - t * kKeyTile) : B);
+      };
       float m_run = -INFINITY, l_run = 0.f;   // l_run: this thread's share of the row sum
-      for (int lt = 0; lt < nt; ++lt) {
-        const int m = n + lt, b = m & 1;
-        const int t = it.tb + lt;
-        if (!warp_wait(&s_full[b], (m >> 1) & 1)) {
+      for (int j = 0; j < ns; ++j) {
+        const int qq = q + j, b = qq & 1;
+        const uint32_t s_tmem = lane_tmem + b * C::kSCols;
+        const int t0 = it.tb + 2 * j;
+        const int n0 = unit_valid(t0), n1 = unit_valid(t0 + 1);
+        if (!warp_wait(&s_full[b], (qq >> 1) & 1)) {
           give_up();
           dead = true;
           break;
         }
         tc_fence_after();
         if (active) {
-          float sv[kCols];
-          if constexpr (SPREAD) tmem_ld_half32<32>(lane_tmem + b * kKeyTile, sv);
-          else tmem_ld64(lane_tmem + b * kKeyTile, sv);
-          const int nvalid = t < s_nctx[it.i] ? min(kKeyTile, len - t * kKeyTile) : B;
-          if (nvalid < kKeyTile) {   // warp-uniform: only a ragged last page or the block tile
-            const int col0 = half * 32;
-#pragma unroll
-            for (int c = 0; c < kCols; ++c) sv[c] = col0 + c < nvalid ? sv[c] : -INFINITY;
+          float sv[64];
+          float mx;
+          if constexpr (SPREAD) {
+            load_s(s_tmem, 0, sv);
+            mask(sv, half ? n1 : n0);
+            mx = row_max(sv);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          } else {
+            load_s(s_tmem, 0, sv);
+            mask(sv, n0);
+            mx = row_max(sv);
+            if (n1 > 0) {
+              load_s(s_tmem, 1, sv);
+              mask(sv, n1);
+              mx = fmaxf(mx, row_max(sv));
+            }
           }
-          float mx = row_max(sv);
-          if constexpr (SPREAD) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           mx *= sl2;   // log2 units
-          if (lt == 0) {
+          if (j == 0) {
             m_run = mx;
           } else if (__any_sync(0xffffffffu, row < R && mx > m_run + kRescaleLog2)) {
-            // O holds the products up to tile m-1: wait for them, then rescale
-            if (!warp_wait(&pv_done[(m - 1) & 1], ((m - 1) >> 1) & 1)) {
+            // O holds the products up to step qq-1: wait for them, then rescale
+            if (!warp_wait(&kv_empty[(qq - 1) % S], ((qq - 1) / S) & 1)) {
               give_up();
               dead = true;
             }
@@ -487,31 +696,27 @@ __global__ void __launch_bounds__(192, 1)
             const float alpha = ex2(m_run - nm);
             l_run *= alpha;
             m_run = nm;
-            if (!dead) o_scale(o_tmem, alpha);
+            if (!dead) o_scale(alpha);
           }
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t pk[kCols / 2];
-#pragma unroll
-          for (int c = 0; c < kCols / 2; ++c) {
-            const float p0 = ex2(fmaf(sv[2 * c], sl2, -m_run));
-            const float p1 = ex2(fmaf(sv[2 * c + 1], sl2, -m_run));
-            s4[c & 3] += p0 + p1;
-            pk[c] = pack_bf16(p0, p1);
+          uint32_t pk[32];
+          if constexpr (SPREAD) {
+            // sv still holds this thread's unit; P of unit `half` -> columns 32*half ..
+            l_run += exp_pack(sv, m_run, pk);
+            tmem_st_half_u32<32>(s_tmem, pk);
+          } else {
+            // P of unit 1 goes to columns 32..63, which still hold S of unit
+            // 0: both units are read before either P is stored
+            uint32_t pk1[32];
+            if (n1 > 0) {   // sv holds unit 1
+              l_run += exp_pack(sv, m_run, pk1);
+              load_s(s_tmem, 0, sv);
+              mask(sv, n0);
+            }
+            l_run += exp_pack(sv, m_run, pk);
+            tmem_st_u32(s_tmem, pk);
+            if (n1 > 0) tmem_st_u32(s_tmem + 32, pk1);
           }
-          l_run += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-          // P buffer b was last read by the products of tile m-2
-          if (!dead && !warp_wait(&pv_done[b], ((m >> 1) & 1) ^ 1)) {
-            give_up();
-            dead = true;
-          }
-          uint8_t* pr = p_row + b * C::kPBytes;
-#pragma unroll
-          for (int cc = 0; cc < kCols / 8; ++cc) {
-            const int ch = half * 4 + cc;   // 16-byte chunk (8 keys) of the 128-byte P row
-            *reinterpret_cast<uint4*>(pr + ((ch ^ (tlane & 7)) << 4)) =
-                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-          }
-          fence_proxy_async_smem();
+          tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
@@ -519,7 +724,9 @@ __global__ void __launch_bounds__(192, 1)
         if (dead) break;
       }
       if (dead) break;
-      if (!warp_wait(&o_full[ob], (k >> 1) & 1)) {
+      // every S of this item has completed: Q's TMEM columns are free for the next item
+      if (item + static_cast<int>(gridDim.x) < total) load_q(decode(item + gridDim.x));
+      if (!warp_wait(&o_full, k & 1)) {
         give_up();
         break;
       }
@@ -544,8 +751,8 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[ob]);
-      n += nt;
+      if (lane == 0) mbar_arrive(&o_free);
+      q += ns;
     }
   }
   tc_fence_before();
@@ -641,13 +848,13 @@ cudaError_t launch_main(const AttnMaps& maps, const AttnArgs& a, int grid, cudaS
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(attn_kernel<D, SPREAD>, dim3(grid), dim3(192), C::kSmem, stream, maps, a);
+  return launch_pdl(attn_kernel<D, SPREAD>, dim3(grid), dim3(kThreads), C::kSmem, stream, maps, a);
 }
 
 template <int D>
 cudaError_t launch_d(const AttnMaps& maps, const AttnArgs& a, int grid, int part, cudaStream_t stream) {
   if (part == 0)
-    return a.q_group_heads > 0 ? launch_main<D, true>(maps, a, grid, stream) : launch_main<D, false>(maps, a, grid, stream);
+    return a.spread ? launch_main<D, true>(maps, a, grid, stream) : launch_main<D, false>(maps, a, grid, stream);
   return launch_pdl(attn_combine_kernel<D>,
                     dim3(a.n_q_heads, a.meta.n_seq, (a.meta.B + kCombineWarps - 1) / kCombineWarps),
                     dim3(32 * kCombineWarps), 0, stream, a);
@@ -657,18 +864,11 @@ cudaError_t launch_d(const AttnMaps& maps, const AttnArgs& a, int grid, int part
 
 int attention_block_rows(int B) { return block_rows(B); }
 
-int attention_spread_group(int G, int B) {
-  if (G * B > 64) return 0;
-  if (16 % G == 0) return G;
-  if (G % 16 == 0) return 16;
-  return 0;
-}
-
 int attention_ctas_per_sm(int head_dim) {
   int n = 0;
   auto q = [&](auto kern, int smem) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 192, smem) != cudaSuccess) n = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess) n = 1;
   };
   if (head_dim == 128) q(attn_kernel<128, true>, ACfg<128>::kSmem);
   else q(attn_kernel<64, true>, ACfg<64>::kSmem);
@@ -678,8 +878,7 @@ int attention_ctas_per_sm(int head_dim) {
 cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& a, int grid, int part, cudaStream_t stream) {
   const int G = a.n_q_heads / a.n_kv_heads, R = G * a.meta.B;
   if (R > 128 || a.rows_pad < R) return cudaErrorInvalidValue;
-  if (a.q_group_heads > 0 && (R > 64 || attention_spread_group(G, a.meta.B) != a.q_group_heads))
-    return cudaErrorInvalidValue;
+  if (a.spread && R > 64) return cudaErrorInvalidValue;
   if (a.head_dim == 128) return launch_d<128>(maps, a, grid, part, stream);
   if (a.head_dim == 64) return launch_d<64>(maps, a, grid, part, stream);
   return cudaErrorInvalidValue;

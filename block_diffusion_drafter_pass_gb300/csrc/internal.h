@@ -163,8 +163,9 @@ struct AttnArgs {
   int chunk_tiles;           // context chunk in 64-key tiles
   int items_cap;             // partial-buffer capacity in work items
   int rows_pad;              // row stride of the partial buffers (>= G*B)
-  int q_group_heads;         // > 0: query rows spread 16 per TMEM lane quarter, loaded in
-                             // boxes of q_group_heads heads x 16/q_group_heads positions
+  int spread;                // 1: G*B <= 64, query rows spread 16 per TMEM lane quarter
+  const uint16_t* q;         // [n_seq*B][n_q*d] bf16 (RoPE applied)
+  const uint16_t* pool;      // the KV pool (read directly only for L2 prefetches)
   float* part_o;             // [items][rows_pad][d]
   float2* part_ml;           // [items][rows_pad] (max, sum)
   uint16_t* out;             // [n_seq*B][n_q*d] bf16
@@ -174,20 +175,15 @@ struct AttnArgs {
 // Tensor maps the attention kernel reads through (all bf16, 128-byte swizzle):
 //   pool_k  the pool as rows of d elements: key rows of (layer, page, head)
 //   pool_vt the pool as rows of 64 elements: transposed value rows [dim][slot]
-//   q       the block's queries, 3D (d, n_q, tokens), box (64, G, B), or with
-//           q_group_heads = gG > 0 box (64, gG, 16/gG)
 //   kblk    the block's keys, 3D (d, n_kv, tokens), box (64, 1, block_rows(B))
 //   vblk    the block's transposed values [seq][n_kv][d][64 slots], rows of 64
 struct AttnMaps {
-  CUtensorMap pool_k, pool_vt, q, kblk, vblk;
+  CUtensorMap pool_k, pool_vt, kblk, vblk;
 };
 
 // part 0: the chunked attention kernel; part 1: the combine kernel.
 cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& a, int grid, int part, cudaStream_t stream);
 int attention_block_rows(int B);   // key-box height used for the block's own keys
-// Heads per 16-row query group when G*B <= 64 rows can be spread over the four
-// TMEM lane quarters (G divides 16 or 16 divides G); 0 otherwise.
-int attention_spread_group(int G, int B);
 int attention_ctas_per_sm(int head_dim);   // resident attention CTAs per SM
 
 // ----------------------------------------------------------------------------

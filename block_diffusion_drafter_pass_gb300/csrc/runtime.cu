@@ -53,12 +53,11 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, ui
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][heads][d] bf16, box = 64 dims x box_heads heads x box_rows rows.
-bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t heads, uint64_t d, uint32_t box_rows,
-               uint32_t box_heads = 1) {
+// [rows][heads][d] bf16, box = 64 dims x 1 head x box_rows rows.
+bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t heads, uint64_t d, uint32_t box_rows) {
   cuuint64_t dims[3] = {d, heads, rows};
   cuuint64_t strides[2] = {d * 2, heads * d * 2};
-  cuuint32_t box[3] = {64, box_heads, box_rows};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -175,17 +174,6 @@ const CUtensorMap* act_map(dflash_ctx* ctx, const void* ptr, int rows, int cols,
 
 // The block's queries [rows][n_q][d], box = 64 dims x G heads x B rows: the
 // G*B query rows of one (sequence, kv head) in one copy.
-// box_heads x box_rows = G x B (all rows of an item), or gG x 16/gG (one
-// 16-row group).
-const CUtensorMap* q_map(dflash_ctx* ctx, int box_heads, int box_rows) {
-  auto key = std::make_tuple(static_cast<const void*>(ctx->q), ctx->max_rows(), box_heads, box_rows, 4);
-  auto it = ctx->act_maps.find(key);
-  if (it != ctx->act_maps.end()) return &it->second;
-  CUtensorMap m;
-  if (!encode_3d(&m, ctx->q, ctx->max_rows(), ctx->cfg.n_heads, ctx->cfg.head_dim, box_rows, box_heads)) return nullptr;
-  return &(ctx->act_maps[key] = m);
-}
-
 const CUtensorMap* blk_map(dflash_ctx* ctx, const void* ptr, int rows, int box_rows) {
   auto key = std::make_tuple(ptr, rows, ctx->cfg.n_kv_heads, box_rows, 3);
   auto it = ctx->act_maps.find(key);
@@ -718,23 +706,21 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
     for (int i = 0; i < n_seq; ++i) it += 1LL * nkv * ceil_div(ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1, ch);
     return it;
   };
+  chunk += chunk & 1;   // items start at even units: the kernel consumes units in pairs
   while (items_for(chunk) > ctx->items_cap) chunk *= 2;
   const int attn_grid = static_cast<int>(std::min<long long>(items_for(chunk), grid_full));
 
   const int Bb = attention_block_rows(B);
   const CUtensorMap* km = blk_map(ctx, ctx->kb, M, Bb);
-  const int q_group = attention_spread_group(nq / nkv, B);
-  const CUtensorMap* qm = q_group > 0 ? q_map(ctx, q_group, 16 / q_group) : q_map(ctx, nq / nkv, B);
   const CUtensorMap* hmap = act_map(ctx, ctx->hg, M, H, BN);
   const int parts = ceil_div(H, 128);
   const int rows_ld = ctx->max_rows();
   const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, BN);
   const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, BN);
-  if (!km || !qm || !hmap || !amap || !fmap) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+  if (!km || !hmap || !amap || !fmap) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
   AttnMaps attn_maps;
   attn_maps.pool_k = ctx->m_pool;
   attn_maps.pool_vt = ctx->m_pool_vt;
-  attn_maps.q = *qm;
   attn_maps.kblk = *km;
   attn_maps.vblk = ctx->m_vblk;
 
@@ -783,7 +769,9 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       a.chunk_tiles = chunk;
       a.items_cap = ctx->items_cap;
       a.rows_pad = 16 * ceil_div((nq / nkv) * B, 16);
-      a.q_group_heads = q_group;
+      a.spread = (nq / nkv) * B <= 64;
+      a.q = ctx->q;
+      a.pool = ctx->pool;
       a.part_o = ctx->part_o;
       a.part_ml = ctx->part_ml;
       a.out = ctx->attn;

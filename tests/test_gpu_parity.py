@@ -194,9 +194,9 @@ def test_qwen3_8b_full_depth_context_4096(dfl):
 
 @pytest.mark.parametrize("n_heads,n_kv,blocks", [(8, 2, (32, 16, 5)), (6, 2, (32, 8, 1))])
 def test_gqa_group_layouts(dfl, n_heads, n_kv, blocks):
-    """Query-row layouts of the attention kernel: G = 4 with G*B = 128 (one
-    thread per row), 64 and 20 (rows spread over the four TMEM lane
-    quarters); G = 3 (16 not a multiple of G: one thread per row at every B)."""
+    """Query-row layouts of the attention kernel: G*B = 128 and 96 (one thread
+    per row, row r in TMEM lane r), G*B <= 64 (rows spread 16 per TMEM lane
+    quarter, two threads per row), for G = 4 and G = 3, B = 1 .. 32."""
     from dataclasses import replace
     sh = replace(TINY, n_heads=n_heads, n_kv_heads=n_kv)
     wn = make_weights_np(sh, seed=51, gamma="jitter", std=0.05)
