@@ -318,8 +318,12 @@ def run_ours(args):
     shape = QWEN3_8B.with_layers(args.layers)
     cyc = Cycle(dfl, shape, batch, start_lens, B, total_steps, seed=1000 * rank, dev=dev)
 
+    # NVTX range names let a profiler select the warm-up steps
+    # (ncu --nvtx --nvtx-include "warmup/")
+    torch.cuda.nvtx.range_push("warmup")
     for k in range(W):
         cyc.step(k)
+    torch.cuda.nvtx.range_pop()
     with ClockSampler(local) as clk:
         ms = timed(cyc.step, K, world, dev)
     clocks = clk.summary()

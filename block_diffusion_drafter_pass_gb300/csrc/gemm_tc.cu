@@ -65,9 +65,12 @@ struct GemmArgs {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Reductions over the tile's 128 rows go through shared memory: a 16-column
+// chunk is staged as [128 rows][17], thread t reduces rows 16*(t>>4) .. +15
+// of column t&15, and 16 threads combine the 8 row groups.
 struct EpiShared {
-  unsigned long long cand[4][256];   // per-warp argmax candidates per column
-  float red[4][256];                 // per-warp column sums of squares
+  unsigned long long cand8[2][8][16];  // argmax candidate per (row group, column), per chunk parity
+  float red8[2][8][16];                // sum of squares per (row group, column), per chunk parity
   int row_pos[256];                  // QKV_ROPE / KV_APPEND: absolute position of each column
   int row_dst[256];                  // KV_APPEND: (page, slot) part of the pool row index
   float row_scale[256];              // folded RMSNorm scale of each column
@@ -211,53 +214,49 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   const int fi = lo ? di : di - half;           // RoPE frequency index of the pair
   const float gain = (kind == EPI_RESID || kind == EPI_NORMSRC) && n < a.N ? bf16_to_f32(e.gain[n]) : 0.f;
 
-  // Sum of the other CTAs' partial tiles for one chunk; loads are issued two
-  // CTAs at a time.
+  // Other CTAs holding partial sums of this tile: one is read a chunk ahead
+  // into registers; any further ones are read on use.
   auto partial_src = [&](int o) {
     const int side = (static_cast<long long>(o) * a.units / a.grid) / a.k_blocks == tile ? 0 : 1;
     return a.partial + (static_cast<size_t>(o) * 2 + side) * slot_elems + r;
   };
-  auto partial_sum = [&](int c0, float (&ps)[16]) {
+  int oth0 = -1;
+  bool more = false;
+  for (int o = first; o <= last; ++o) {
+    if (o == g) continue;
+    if (oth0 < 0) oth0 = o;
+    else more = true;
+  }
+  const float* ps0 = oth0 >= 0 ? partial_src(oth0) : nullptr;
+  auto partial_load = [&](int c0, float (&p0)[16]) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) ps[c] = 0.f;
-    int o = first;
-    while (o <= last) {
-      if (o == g) ++o;
-      if (o > last) break;
-      int o2 = o + 1;
-      if (o2 == g) ++o2;
-      const float* s0 = partial_src(o);
-      const bool two = o2 <= last;
-      const float* s1 = two ? partial_src(o2) : s0;
-      float t0[16], t1[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        t0[c] = __ldcg(s0 + static_cast<size_t>(c0 + c) * kTileN);
-        t1[c] = two ? __ldcg(s1 + static_cast<size_t>(c0 + c) * kTileN) : 0.f;
-      }
-#pragma unroll
-      for (int c = 0; c < 16; ++c) ps[c] += t0[c] + t1[c];
-      o = two ? o2 + 1 : o2;
-    }
+    for (int c = 0; c < 16; ++c) p0[c] = ps0 ? __ldcg(ps0 + static_cast<size_t>(c0 + c) * kTileN) : 0.f;
   };
-  const bool split = first != last;
   ChunkAux cur;
   load_aux(a, e, sh, m0, 0, n, rope, fi, half, cur);
-  float pcur[16];
-  if (split) partial_sum(0, pcur);
+  float pc0[16];
+  partial_load(0, pc0);
 #pragma unroll 1
   for (int c0 = 0; c0 < BN; c0 += 16) {
+    const int buf = (c0 >> 4) & 1;
+    float* sb = stg + buf * (128 * 17);
     ChunkAux nxt;
-    float pnxt[16];
+    float pn0[16];
     if (c0 + 16 < BN) {
       load_aux(a, e, sh, m0, c0 + 16, n, rope, fi, half, nxt);
-      if (split) partial_sum(c0 + 16, pnxt);
+      partial_load(c0 + 16, pn0);
     }
     float v[16];
     tmem_ld16(tb + c0, v);
-    if (split) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) v[c] += pcur[c];
+    for (int c = 0; c < 16; ++c) v[c] += pc0[c];
+    if (more) {
+      for (int o = first; o <= last; ++o) {
+        if (o == g || o == oth0) continue;
+        const float* src = partial_src(o);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] += __ldcg(src + static_cast<size_t>(c0 + c) * kTileN);
+      }
     }
     if (e.in_ss && kind != EPI_ARGMAX) {
 #pragma unroll
@@ -265,7 +264,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
     }
     float other[16];
     if (paired_kind) {   // exchange with row r ^ P through the chunk's staging buffer
-      float* sb = stg + ((c0 >> 4) & 1) * (128 * 17);
 #pragma unroll
       for (int c = 0; c < 16; ++c) sb[r * 17 + c] = v[c];
       epi_bar();
@@ -299,27 +297,49 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
           }
           e.out_hg[off] = f32_to_bf16(xn * gain);
         }
-        float sq = xn * xn;
+        sb[r * 17 + c] = xn * xn;
+      }
+      // column sums of squares over the tile's 128 rows
+      epi_bar();
+      const int cc = r & 15, gq = r >> 4;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int s = 16; s > 0; s >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, s);
-        if (lane == 0) sh.red[q][c0 + c] = sq;
+      for (int i = 0; i < 16; ++i) s4[i & 3] += sb[(gq * 16 + i) * 17 + cc];
+      sh.red8[buf][gq][cc] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      epi_bar();
+      if (r < 16) {
+        const int m = m0 + c0 + r;
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t += sh.red8[buf][k][r];
+        if (m < a.M) e.out_ss[static_cast<size_t>(tn) * e.out_ss_ld + m] = t;
       }
     } else if (kind == EPI_ARGMAX) {
+      // per column: highest logit over the tile's rows, lowest row on ties,
+      // packed as (ordered key << 32) | ~row so one 64-bit max decides
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int m = m0 + c0 + c;
-        const bool ok = (n < a.N) && (m < a.M) && !(e.argmax_skip_B > 0 && m % e.argmax_skip_B == 0);
-        const uint32_t key = ok ? ordered_key(v[c]) : 0u;
-        const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-        const uint32_t hit = __ballot_sync(0xffffffffu, ok && key == mx);
-        if (lane == 0) {
-          unsigned long long cand = 0ull;
-          if (hit) {   // the lowest lane is the lowest index
-            const uint32_t idx = static_cast<uint32_t>(tn * kTileN + q * 32 + __ffs(hit) - 1);
-            cand = (static_cast<unsigned long long>(mx) << 32) | (0xFFFFFFFFu - idx);
-          }
-          sh.cand[q][c0 + c] = cand;
+      for (int c = 0; c < 16; ++c) sb[r * 17 + c] = v[c];
+      epi_bar();
+      const int cc = r & 15, gq = r >> 4;
+      const int m = m0 + c0 + cc;
+      unsigned long long best = 0ull;
+      if (m < a.M && !(e.argmax_skip_B > 0 && m % e.argmax_skip_B == 0)) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int row = gq * 16 + i;
+          const uint32_t idx = static_cast<uint32_t>(tn * kTileN + row);
+          const unsigned long long cand =
+              (static_cast<unsigned long long>(ordered_key(sb[row * 17 + cc])) << 32) | (0xFFFFFFFFu - idx);
+          best = (static_cast<int>(idx) < a.N && cand > best) ? cand : best;
         }
+      }
+      sh.cand8[buf][gq][cc] = best;
+      epi_bar();
+      if (r < 16) {
+        unsigned long long b8 = sh.cand8[buf][0][r];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) b8 = sh.cand8[buf][k][r] > b8 ? sh.cand8[buf][k][r] : b8;
+        if (b8) atomicMax(e.keys + (m0 + c0 + r), b8);
       }
     } else if (kind == EPI_SWIGLU) {
       // rows < 64 hold gate rows, rows >= 64 the up rows of the same features;
@@ -333,6 +353,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
           e.out_act[static_cast<size_t>(m) * e.n_valid + fint] = f32_to_bf16(silu_f(gt) * up);
         }
       }
+    } else if (kind == EPI_QKV_ROPE && reg == 2 && e.meta.B % 16 == 0 && m0 + c0 + 16 <= a.M &&
+               sh.row_pos[c0] >= 0 && sh.row_pos[c0 + 15] >= 0) {
+      // values, transposed: the chunk's 16 tokens are 16 consecutive slots of
+      // one sequence, written as two 16-byte stores
+      const int i = (m0 + c0) / e.meta.B, j0 = (m0 + c0) - i * e.meta.B;
+      uint32_t w[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        w[c] = static_cast<uint32_t>(f32_to_bf16(v[2 * c])) | (static_cast<uint32_t>(f32_to_bf16(v[2 * c + 1])) << 16);
+      uint4* dstv = reinterpret_cast<uint4*>(
+          e.out_v + ((static_cast<size_t>(i) * e.n_kv_heads + hd) * d + di) * kPage + j0);
+      dstv[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dstv[1] = make_uint4(w[4], w[5], w[6], w[7]);
     } else {   // EPI_QKV_ROPE or EPI_KV_APPEND
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
@@ -369,26 +402,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
     }
     cur = nxt;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) pcur[c] = pnxt[c];
-  }
-
-  if (kind == EPI_RESID || kind == EPI_NORMSRC) {
-    epi_bar();
-    for (int col = r; col < BN; col += 128) {
-      const int m = m0 + col;
-      if (m < a.M)
-        e.out_ss[static_cast<size_t>(tn) * e.out_ss_ld + m] =
-            (sh.red[0][col] + sh.red[1][col]) + (sh.red[2][col] + sh.red[3][col]);
-    }
-  } else if (kind == EPI_ARGMAX) {
-    epi_bar();
-    for (int col = r; col < BN; col += 128) {
-      unsigned long long best = sh.cand[0][col];
-#pragma unroll
-      for (int w = 1; w < 4; ++w) best = sh.cand[w][col] > best ? sh.cand[w][col] : best;
-      const int m = m0 + col;
-      if (m < a.M && best) atomicMax(e.keys + m, best);
-    }
+    for (int c = 0; c < 16; ++c) pc0[c] = pn0[c];
   }
   epi_bar();
 }
