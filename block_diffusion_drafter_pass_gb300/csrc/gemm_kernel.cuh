@@ -1,0 +1,754 @@
+// gemm_kernel.cuh - the drafter's dense contractions on the 5th-generation tensor
+// cores (tcgen05.mma, fp32 accumulators in TMEM, operands staged by TMA).
+//
+// Every projection of the drafter pass is OUT^T[N, M] = W[N, K] * X[M, K]^T:
+// the weight rows are the UMMA "A" operand (M_mma = 128 rows per tile) and
+// the tokens the "B" operand (N_mma = BN, 16..256), so a batch-1 block of 16
+// tokens still fills the 128-row tensor-core tile and the kernel streams
+// weights at HBM speed; with 512 tokens the same kernel is compute bound.
+//
+// Persistent stream-K: one CTA per SM streams an equal, contiguous range of
+// (tile, 64-wide k-block) units through a STAGES-deep TMA ring. CTA = 6 warps:
+// warp 0 issues the TMA loads, warp 1 owns TMEM and issues the MMAs (one
+// thread) into one of two accumulator buffers, warps 2-5 drain the other
+// buffer (tcgen05.ld) and run the fused epilogue:
+//   EPI_F32_STORE  plain fp32 output (tests)
+//   EPI_RESID      x += acc, then bf16(x * g) and sum(x^2) for the next RMSNorm
+//   EPI_NORMSRC    bf16(acc * g) and sum(acc^2) (fusion projection W_c)
+//   EPI_QKV_ROPE   q/k/v split with rotate-half RoPE on q and k
+//   EPI_SWIGLU     SiLU(gate) * up from paired gate/up weight rows
+//   EPI_KV_APPEND  KV injection: RoPE(W_K H_t), W_V H_t scattered to pages
+//   EPI_ARGMAX     LM head with the per-row argmax fused; logits never stored
+// A tile split over several CTAs is finished by the last one to arrive (an
+// atomic ticket; nothing spins): it adds the others' partial tiles to its own
+// accumulator and runs the epilogue.
+//
+// RoPE and SwiGLU pair tile row r with row r ^ P (P = d/2 for RoPE, 64 for
+// gate/up rows); those live in another warp's TMEM lanes, so the pair is
+// exchanged through a double-buffered shared-memory stage, one named barrier
+// per 16-column chunk.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfl {
+namespace gk {
+
+// Epilogue classes: each kernel instantiation carries the code of one class
+// only, so the kind is a compile-time constant (or one of two) and the
+// chunk loop stays small.
+enum : int { kEcF32 = 0, kEcNorm = 1, kEcRope = 2, kEcSwiglu = 3, kEcArgmax = 4 };
+
+__host__ __device__ constexpr int epilogue_class(int kind) {
+  return kind == EPI_RESID || kind == EPI_NORMSRC       ? kEcNorm
+         : kind == EPI_QKV_ROPE || kind == EPI_KV_APPEND ? kEcRope
+         : kind == EPI_SWIGLU                            ? kEcSwiglu
+         : kind == EPI_ARGMAX                            ? kEcArgmax
+                                                         : kEcF32;
+}
+
+// The run-time kind narrowed to the kinds of class EC.
+template <int EC>
+__device__ __forceinline__ int class_kind(int kind) {
+  if constexpr (EC == kEcNorm) return kind == EPI_NORMSRC ? EPI_NORMSRC : EPI_RESID;
+  else if constexpr (EC == kEcRope) return kind == EPI_KV_APPEND ? EPI_KV_APPEND : EPI_QKV_ROPE;
+  else if constexpr (EC == kEcSwiglu) return EPI_SWIGLU;
+  else if constexpr (EC == kEcArgmax) return EPI_ARGMAX;
+  else return kind == EPI_F32_ADD ? EPI_F32_ADD : EPI_F32_STORE;
+}
+
+constexpr int kThreads = 192;
+constexpr int kTileN = 128;     // weight rows per tile (UMMA M)
+constexpr int kTileK = 64;      // K per stage (one 128-byte swizzle row)
+constexpr int kABytes = kTileN * kTileK * 2;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kBBytes = BN * kTileK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = BN <= 64 ? 8 : (BN <= 128 ? 6 : 4);
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;     // two accumulator buffers
+  static constexpr int kStgBytes = 2 * 128 * 17 * 4;                // pair-exchange stage (x2)
+  static constexpr int kSmem = kStages * kStageBytes + kStgBytes + 1024;
+};
+
+struct GemmArgs {
+  int M, N, K;
+  int k_blocks, n_tiles, m_tiles;
+  long long units;     // tiles * k_blocks
+  int grid;            // CTAs (stream-K workers)
+  float* partial;      // [grid][2][128 * BN] partial tiles
+  int* tickets;        // [tiles], zero between launches
+  int* status;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Reductions over the tile's 128 rows go through shared memory: a 16-column
+// chunk is staged as [128 rows][17], thread t reduces rows 16*(t>>4) .. +15
+// of column t&15, and 16 threads combine the 8 row groups.
+struct EpiShared {
+  unsigned long long cand8[2][8][16];  // argmax candidate per (row group, column), per chunk parity
+  float red8[2][8][16];                // sum of squares per (row group, column), per chunk parity
+  int row_pos[256];                  // QKV_ROPE / KV_APPEND: absolute position of each column
+  int row_dst[256];                  // KV_APPEND: (page, slot) part of the pool row index
+  float row_scale[256];              // folded RMSNorm scale of each column
+  float2 rope_base[16][64];          // RoPE (cos, sin) at each chunk's first position, per frequency
+  int flag;
+};
+
+__device__ __forceinline__ int region_of(const ARegions& rg, int tile) {
+  int r = 0;
+  while (r + 1 < rg.n_regions && tile >= rg.tile_begin[r + 1]) ++r;
+  return r;
+}
+
+// TMA sources of the tile's two 64-row halves: stacked regions read 128
+// consecutive rows of one matrix; paired tiles read 64 gate rows and the same
+// 64 up rows.
+__device__ __forceinline__ void weight_rows(const ARegions& rg, int tile_n, int& map_lo, int& row_lo, int& map_hi,
+                                            int& row_hi) {
+  if (rg.paired) {
+    map_lo = 0;
+    map_hi = 1;
+    row_lo = row_hi = tile_n * 64;
+  } else {
+    const int reg = region_of(rg, tile_n);
+    map_lo = map_hi = reg;
+    row_lo = (tile_n - rg.tile_begin[reg]) * kTileN;
+    row_hi = row_lo + 64;
+  }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Folded RMSNorm scale of activation row m: 8 independent partial loads per
+// batch so the sum costs a few memory latencies, not one per partial.
+__device__ __forceinline__ float norm_scale(const GemmEpi& e, int m) {
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int p = 0;
+  for (; p + 8 <= e.in_ss_parts; p += 8) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] += __ldcg(e.in_ss + static_cast<size_t>(p + q) * e.in_ss_ld + m);
+  }
+  for (; p < e.in_ss_parts; ++p) acc[0] += __ldcg(e.in_ss + static_cast<size_t>(p) * e.in_ss_ld + m);
+  const float ss = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  return rsqrtf(ss * e.inv_hidden + e.eps);
+}
+
+// Per-column metadata of one output tile (columns m0 .. m0+BN-1), computed
+// once by all 128 epilogue threads before the tile is drained.
+template <int BN, int EC>
+__device__ __forceinline__ void tile_cols_prepare(const GemmArgs& a, const GemmEpi& e, int m0, int r,
+                                                  EpiShared& sh) {
+  const int kind = class_kind<EC>(e.kind);
+  for (int col = r; col < BN; col += 128) {
+    const int m = m0 + col;
+    float sc = 1.f;
+    int pos = -1, dst = -1;
+    if (m < a.M) {
+      if (e.in_ss) sc = norm_scale(e, m);
+      if (kind == EPI_QKV_ROPE) {
+        const int i = m / e.meta.B, j = m - i * e.meta.B;
+        pos = e.seqs.len[e.meta.slot[i]] + j;
+      } else if (kind == EPI_KV_APPEND) {
+        int i = 0;
+        while (i + 1 < e.meta.n_seq && m >= e.meta.row0[i + 1]) ++i;
+        const int slot = e.meta.slot[i];
+        pos = e.seqs.len[slot] + e.seqs.pend[slot] + (m - e.meta.row0[i]);
+        const int pg_idx = pos / kPage;
+        if (pg_idx < e.seqs.pages_per_seq) {
+          const int page = e.seqs.page_table[static_cast<size_t>(slot) * e.seqs.pages_per_seq + pg_idx];
+          if (page >= 0 && page < e.pool_pages) dst = page * 2 * e.n_kv_heads * kPage + (pos % kPage);
+        }
+        if (dst < 0) latch_status(e.status, kDevBounds);
+      }
+      if (pos >= e.rope_positions) {
+        latch_status(e.status, kDevBounds);
+        pos = -1;
+        dst = -1;
+      }
+    }
+    sh.row_scale[col] = sc;
+    sh.row_pos[col] = pos;
+    sh.row_dst[col] = dst;
+  }
+  epi_bar();
+  // RoPE bases of every chunk: one round of loads for the whole tile
+  if (kind == EPI_QKV_ROPE || kind == EPI_KV_APPEND) {
+    const int half = e.head_dim >> 1;
+    for (int k = r; k < (BN / 16) * half; k += 128) {
+      const int ch = k / half, fi = k - ch * half;
+      const int pos = sh.row_pos[ch * 16];
+      sh.rope_base[ch][fi] = pos >= 0 ? e.rope[static_cast<size_t>(pos) * half + fi] : make_float2(1.f, 0.f);
+    }
+    epi_bar();
+  }
+}
+
+// Residual inputs of one 16-column chunk (EPI_RESID); the chunk loop keeps
+// them two chunks ahead of use.
+__device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, int m0, int c0, int n,
+                                           float (&x)[16]) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const int m = m0 + c0 + c;
+    x[c] = (n < a.N && m < a.M && c0 < a.M) ? __ldcg(e.out_f32 + static_cast<size_t>(m) * e.ld_out + n) : 0.f;
+  }
+}
+
+// Drain one finished tile from TMEM (plus the other CTAs' partial tiles) and
+// run the epilogue. r = TMEM lane of this thread (0..127).
+template <int BN, int EC>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int g,
+                                              int tile, int first, int last, uint32_t tb, int r, EpiShared& sh,
+                                              float* stg) {
+  const int kind = class_kind<EC>(e.kind);
+  const int q = r >> 5, lane = r & 31;
+  const int tn = tile / a.m_tiles, tm = tile - tn * a.m_tiles;
+  const int m0 = tm * BN;
+  const int P = rg.pair;
+  const int f = r;                              // row of this lane within the tile
+  const size_t slot_elems = static_cast<size_t>(kTileN) * BN;
+  tile_cols_prepare<BN, EC>(a, e, m0, r, sh);
+
+  // kind-specific constants of this lane
+  int reg = 0, rf = f;                          // region and row within the region's matrix
+  if (!rg.paired) {
+    reg = region_of(rg, tn);
+    rf = (tn - rg.tile_begin[reg]) * kTileN + f;
+  }
+  const int n = tn * kTileN + f;                // output feature (plain kinds)
+  const int d = e.head_dim > 0 ? e.head_dim : 1, half = d >> 1;
+  const int hd = rf / d, di = rf - hd * d;
+  const bool lo = (r & P) == 0;                 // lower member of the row pair (r, r ^ P)
+  const bool paired_kind = kind == EPI_SWIGLU || kind == EPI_QKV_ROPE || kind == EPI_KV_APPEND;
+  bool rope = false;
+  if (kind == EPI_QKV_ROPE) rope = reg < 2;
+  if (kind == EPI_KV_APPEND) rope = (reg & 1) == 0;
+  const int fi = lo ? di : di - half;           // RoPE frequency index of the pair
+  const float gain = (kind == EPI_RESID || kind == EPI_NORMSRC) && n < a.N ? bf16_to_f32(e.gain[n]) : 0.f;
+
+  // Other CTAs holding partial sums of this tile: one is read a chunk ahead
+  // into registers; any further ones are read on use.
+  auto partial_src = [&](int o) {
+    const int side = (static_cast<long long>(o) * a.units / a.grid) / a.k_blocks == tile ? 0 : 1;
+    return a.partial + (static_cast<size_t>(o) * 2 + side) * slot_elems + r;
+  };
+  int oth0 = -1;
+  bool more = false;
+  for (int o = first; o <= last; ++o) {
+    if (o == g) continue;
+    if (oth0 < 0) oth0 = o;
+    else more = true;
+  }
+  const float* ps0 = oth0 >= 0 ? partial_src(oth0) : nullptr;
+  auto partial_load = [&](int c0, float (&p0)[16]) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) p0[c] = ps0 ? __ldcg(ps0 + static_cast<size_t>(c0 + c) * kTileN) : 0.f;
+  };
+  // RoPE: when a chunk's 16 positions are consecutive (one sequence's block),
+  // (cos, sin) is read once at its first position and advanced by the row's
+  // rotation R = (cos, sin) of its frequency (the table's position 1) with a
+  // complex multiply per column; otherwise it is read per column.
+  const bool resid = kind == EPI_RESID;
+  float ra[16], rb[16];
+  float2 rot = make_float2(1.f, 0.f);
+  if (resid) {
+    load_resid(a, e, m0, 0, n, ra);
+    load_resid(a, e, m0, 16, n, rb);
+  }
+  if (rope) rot = e.rope[half + fi];
+  float pc0[16];
+  partial_load(0, pc0);
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    const int buf = (c0 >> 4) & 1;
+    float* sb = stg + buf * (128 * 17);
+    float rc[16];
+    if (resid && c0 + 32 < BN) load_resid(a, e, m0, c0 + 32, n, rc);
+    float pn0[16];
+    if (c0 + 16 < BN) partial_load(c0 + 16, pn0);
+    float v[16];
+    tmem_ld16(tb + c0, v);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) v[c] += pc0[c];
+    if (more) {
+      for (int o = first; o <= last; ++o) {
+        if (o == g || o == oth0) continue;
+        const float* src = partial_src(o);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] += __ldcg(src + static_cast<size_t>(c0 + c) * kTileN);
+      }
+    }
+    if (e.in_ss && kind != EPI_ARGMAX) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] *= sh.row_scale[c0 + c];
+    }
+    float other[16];
+    if (paired_kind) {   // exchange with row r ^ P through the chunk's staging buffer
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sb[r * 17 + c] = v[c];
+      epi_bar();
+      const int pr = r ^ P;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) other[c] = sb[pr * 17 + c];
+    }
+
+    if (kind == EPI_F32_STORE || kind == EPI_F32_ADD) {
+      if (n < a.N) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int m = m0 + c0 + c;
+          if (m < a.M) {
+            float* p = e.out_f32 + static_cast<size_t>(m) * e.ld_out + n;
+            if (kind == EPI_F32_ADD) *p += v[c]; else *p = v[c];
+          }
+        }
+      }
+    } else if (kind == EPI_RESID || kind == EPI_NORMSRC) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        float xn = 0.f;
+        if (n < a.N && m < a.M) {
+          const size_t off = static_cast<size_t>(m) * e.ld_out + n;
+          xn = v[c];
+          if (kind == EPI_RESID) {
+            xn += ra[c];
+            e.out_f32[off] = xn;
+          }
+          e.out_hg[off] = f32_to_bf16(xn * gain);
+        }
+        sb[r * 17 + c] = xn * xn;
+      }
+      // column sums of squares over the tile's 128 rows
+      epi_bar();
+      const int cc = r & 15, gq = r >> 4;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) s4[i & 3] += sb[(gq * 16 + i) * 17 + cc];
+      sh.red8[buf][gq][cc] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      epi_bar();
+      if (r < 16) {
+        const int m = m0 + c0 + r;
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t += sh.red8[buf][k][r];
+        if (m < a.M) e.out_ss[static_cast<size_t>(tn) * e.out_ss_ld + m] = t;
+      }
+    } else if (kind == EPI_ARGMAX) {
+      // per column: highest logit over the tile's rows, lowest row on ties,
+      // packed as (ordered key << 32) | ~row so one 64-bit max decides
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sb[r * 17 + c] = v[c];
+      epi_bar();
+      const int cc = r & 15, gq = r >> 4;
+      const int m = m0 + c0 + cc;
+      unsigned long long best = 0ull;
+      if (m < a.M && !(e.argmax_skip_B > 0 && m % e.argmax_skip_B == 0)) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int row = gq * 16 + i;
+          const uint32_t idx = static_cast<uint32_t>(tn * kTileN + row);
+          const unsigned long long cand =
+              (static_cast<unsigned long long>(ordered_key(sb[row * 17 + cc])) << 32) | (0xFFFFFFFFu - idx);
+          best = (static_cast<int>(idx) < a.N && cand > best) ? cand : best;
+        }
+      }
+      sh.cand8[buf][gq][cc] = best;
+      epi_bar();
+      if (r < 16) {
+        unsigned long long b8 = sh.cand8[buf][0][r];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) b8 = sh.cand8[buf][k][r] > b8 ? sh.cand8[buf][k][r] : b8;
+        if (b8) atomicMax(e.keys + (m0 + c0 + r), b8);
+      }
+    } else if (kind == EPI_SWIGLU) {
+      // rows < 64 hold gate rows, rows >= 64 the up rows of the same features;
+      // each member of a pair writes half of the columns
+      const int fint = tn * 64 + (f & 63);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        if ((c < 8) == lo && fint < e.n_valid && m < a.M) {
+          const float gt = lo ? v[c] : other[c], up = lo ? other[c] : v[c];
+          e.out_act[static_cast<size_t>(m) * e.n_valid + fint] = f32_to_bf16(silu_f(gt) * up);
+        }
+      }
+    } else if (kind == EPI_QKV_ROPE && reg == 2 && e.meta.B % 16 == 0 && m0 + c0 + 16 <= a.M &&
+               sh.row_pos[c0] >= 0 && sh.row_pos[c0 + 15] >= 0) {
+      // values, transposed: the chunk's 16 tokens are 16 consecutive slots of
+      // one sequence, written as two 16-byte stores
+      const int i = (m0 + c0) / e.meta.B, j0 = (m0 + c0) - i * e.meta.B;
+      uint32_t w[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        w[c] = static_cast<uint32_t>(f32_to_bf16(v[2 * c])) | (static_cast<uint32_t>(f32_to_bf16(v[2 * c + 1])) << 16);
+      uint4* dstv = reinterpret_cast<uint4*>(
+          e.out_v + ((static_cast<size_t>(i) * e.n_kv_heads + hd) * d + di) * kPage + j0);
+      dstv[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dstv[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {   // EPI_QKV_ROPE or EPI_KV_APPEND
+      // Every shared-memory input of the chunk is read, and every output
+      // value computed, before the chunk's first global store: loads placed
+      // after a store would wait for it.
+      int posv[16], dstv[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        posv[c] = sh.row_pos[c0 + c];
+        dstv[c] = kind == EPI_KV_APPEND ? sh.row_dst[c0 + c] : 0;
+      }
+      bool run = rope && posv[0] >= 0;   // all 16 positions consecutive
+#pragma unroll
+      for (int c = 1; c < 16; ++c) run = run && posv[c] == posv[0] + c;
+      float2 cs = rope ? sh.rope_base[c0 >> 4][fi] : make_float2(1.f, 0.f);
+      uint16_t ov[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        float x = v[c];
+        if (rope) {
+          const int pos = posv[c];
+          const float2 t = run ? cs : (pos >= 0 ? e.rope[static_cast<size_t>(pos) * half + fi] : make_float2(1.f, 0.f));
+          x = lo ? (x * t.x - other[c] * t.y) : (x * t.x + other[c] * t.y);
+          cs = make_float2(cs.x * rot.x - cs.y * rot.y, cs.y * rot.x + cs.x * rot.y);
+        }
+        ov[c] = f32_to_bf16(x);
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int m = m0 + c0 + c;
+        if (m >= a.M || posv[c] < 0) continue;
+        if (kind == EPI_QKV_ROPE) {
+          if (reg == 2) {   // values transposed per (sequence, head): [d][64 slots]
+            const int i = m / e.meta.B, j = m - i * e.meta.B;
+            e.out_v[((static_cast<size_t>(i) * e.n_kv_heads + hd) * d + di) * kPage + j] = ov[c];
+          } else {
+            uint16_t* base = reg == 0 ? e.out_q : e.out_k;
+            const size_t ld = static_cast<size_t>(reg == 0 ? e.n_q_heads : e.n_kv_heads) * d;
+            base[static_cast<size_t>(m) * ld + rf] = ov[c];
+          }
+        } else {
+          const int dst = dstv[c];
+          if (dst < 0) continue;
+          const int layer = e.layer0 + (reg >> 1), slot = dst & (kPage - 1);
+          // elements of (layer, page): keys [n_kv][64][d], then values [n_kv][d][64]
+          const size_t lp = (static_cast<size_t>(layer) * e.pool_pages * 2 * e.n_kv_heads * kPage +
+                             static_cast<size_t>(dst - slot)) * d;
+          const size_t off = (reg & 1) ? static_cast<size_t>(e.n_kv_heads) * kPage * d +
+                                             (static_cast<size_t>(hd) * d + di) * kPage + slot
+                                       : (static_cast<size_t>(hd) * kPage + slot) * d + di;
+          e.pool[lp + off] = ov[c];
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      pc0[c] = pn0[c];
+      ra[c] = rb[c];
+      rb[c] = rc[c];
+    }
+  }
+  epi_bar();
+}
+
+// Stream-K partition: CTA g owns the contiguous range of (tile, k-block)
+// units [unit_begin(g), unit_begin(g + 1)); tiles are ordered so that the m
+// tiles of one weight tile are consecutive (weights reused from L2).
+__device__ __forceinline__ long long unit_begin(int g, const GemmArgs& a) {
+  return static_cast<long long>(g) * a.units / a.grid;
+}
+__device__ __forceinline__ int cta_of(long long u, const GemmArgs& a) {
+  long long g = u * a.grid / a.units;
+  while (g + 1 < a.grid && unit_begin(static_cast<int>(g + 1), a) <= u) ++g;
+  while (g > 0 && unit_begin(static_cast<int>(g), a) > u) --g;
+  return static_cast<int>(g);
+}
+
+template <int BN, int EC>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ AMaps amaps, const __grid_constant__ CUtensorMap xmap,
+                const __grid_constant__ GemmArgs a, const __grid_constant__ ARegions rg,
+                const __grid_constant__ GemmEpi e) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* stg = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  __shared__ __align__(8) uint64_t full[C::kStages];
+  __shared__ __align__(8) uint64_t empty[C::kStages];
+  __shared__ __align__(8) uint64_t acc_full[2];
+  __shared__ __align__(8) uint64_t acc_empty[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ EpiShared esh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = blockIdx.x;
+  const long long u0 = unit_begin(g, a), u1 = unit_begin(g + 1, a);
+  const int n_units = static_cast<int>(u1 - u0);
+  const int kb = a.k_blocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&xmap);
+    for (int i = 0; i < rg.n_regions && i < kMaxAMaps; ++i) tma_prefetch_desc(&amaps.m[i]);
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  grid_dep_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      // Walks its (tile, k-block) units incrementally: the weight rows and
+      // token rows are recomputed only when the tile changes.
+      const uint64_t wpol = policy_evict_first();
+      struct Cursor {
+        int t, k, ml, rl, mh, rh, brow;
+      };
+      auto at_tile = [&](Cursor& c) {
+        const int tn = c.t / a.m_tiles;
+        weight_rows(rg, tn, c.ml, c.rl, c.mh, c.rh);
+        c.brow = (c.t - tn * a.m_tiles) * BN;
+      };
+      auto advance = [&](Cursor& c) {
+        if (++c.k == kb) {
+          c.k = 0;
+          ++c.t;
+          at_tile(c);
+        }
+      };
+      Cursor ca;
+      ca.t = static_cast<int>(u0 / kb);
+      ca.k = static_cast<int>(u0 - static_cast<long long>(ca.t) * kb);
+      at_tile(ca);
+      Cursor cb = ca;
+      auto load_a = [&](int i, const Cursor& c) {
+        uint8_t* sa = smem + (i % C::kStages) * C::kStageBytes;
+        tma_load_2d_hint(sa, &amaps.m[c.ml], &full[i % C::kStages], c.k * kTileK, c.rl, wpol);
+        tma_load_2d_hint(sa + kABytes / 2, &amaps.m[c.mh], &full[i % C::kStages], c.k * kTileK, c.rh, wpol);
+      };
+      auto load_b = [&](int i, const Cursor& c) {
+        uint8_t* sb = smem + (i % C::kStages) * C::kStageBytes + kABytes;
+        tma_load_2d(sb, &xmap, &full[i % C::kStages], c.k * kTileK, c.brow);
+      };
+      // Weights do not depend on the previous kernel: start streaming them
+      // before waiting for it (programmatic dependent launch).
+      const int pre = min(n_units, C::kStages);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], C::kStageBytes);
+        load_a(i, ca);
+        advance(ca);
+      }
+      grid_dep_wait();
+      for (int i = 0; i < pre; ++i) {
+        load_b(i, cb);
+        advance(cb);
+      }
+      int issued = pre;
+      for (int i = pre; i < n_units; ++i) {
+        const int s = i % C::kStages;
+        if (!mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, &abort_flag)) {
+          abort_flag = 1;
+          latch_status(a.status, kDevTimeout);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        load_a(i, ca);
+        load_b(i, ca);
+        advance(ca);
+        ++issued;
+      }
+      if (abort_flag) {  // drain copies still in flight before shared memory is released
+        for (int i = max(0, issued - C::kStages); i < issued; ++i)
+          mbar_wait(&full[i % C::kStages], (i / C::kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileN, BN);
+      grid_dep_wait();
+      int i = 0, seg = 0;
+      for (long long u = u0; u < u1 && !abort_flag; ++seg) {
+        const long long t = u / kb;
+        const long long seg_end = min(u1, (t + 1) * kb);
+        const int buf = seg & 1;
+        if (!mbar_wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, &abort_flag)) {
+          abort_flag = 1;
+          latch_status(a.status, kDevTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * BN;
+        for (long long v = u; v < seg_end; ++v, ++i) {
+          const int s = i % C::kStages;
+          if (!mbar_wait(&full[s], (i / C::kStages) & 1, &abort_flag)) {
+            abort_flag = 1;
+            latch_status(a.status, kDevTimeout);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * C::kStageBytes);
+          const uint64_t ad = sdesc_kmajor_sw128(sa);
+          const uint64_t bd = sdesc_kmajor_sw128(sa + kABytes);
+#pragma unroll
+          for (int k = 0; k < kTileK / 16; ++k)
+            tc_mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (v != u || k != 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
+        }
+        tc_commit(&acc_full[buf]);
+        u = seg_end;
+      }
+    }
+  } else {
+    // ---------------- epilogue warps ----------------
+    grid_dep_wait();
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;            // TMEM lane = tile row slot
+    const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const size_t slot_elems = static_cast<size_t>(kTileN) * BN;
+    int seg = 0;
+    for (long long u = u0; u < u1; ++seg) {
+      const int t = static_cast<int>(u / kb);
+      const long long seg_end = min(u1, static_cast<long long>(t + 1) * kb);
+      const bool whole = (u == static_cast<long long>(t) * kb) && (seg_end == static_cast<long long>(t + 1) * kb);
+      const int buf = seg & 1;
+      if (!mbar_wait(&acc_full[buf], (seg >> 1) & 1, &abort_flag)) {
+        abort_flag = 1;
+        latch_status(a.status, kDevTimeout);
+      }
+      epi_bar();
+      if (r == 0) esh.flag = abort_flag;   // one reader, so all epilogue threads agree
+      epi_bar();
+      if (esh.flag) break;
+      tc_fence_after();
+      const uint32_t tb = trow + buf * BN;
+      bool finish = whole;
+      int first = g, last = g;
+      if (!whole) {
+        // park this segment's partial sum in the CTA's slot, then take a ticket
+        const int side = (u == u0) ? 0 : 1;
+        float* dst = a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems + r;
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(tb + c0, v);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) dst[static_cast<size_t>(c0 + c) * kTileN] = v[c];
+        }
+        first = cta_of(static_cast<long long>(t) * kb, a);
+        last = cta_of(static_cast<long long>(t + 1) * kb - 1, a);
+        __threadfence();
+        epi_bar();
+        if (r == 0) {
+          const int tk = atomicAdd(a.tickets + t, 1);
+          esh.flag = (tk == last - first);
+          if (tk == last - first) a.tickets[t] = 0;
+        }
+        epi_bar();
+        finish = esh.flag != 0;
+        if (finish) __threadfence();
+      }
+      if (finish) {
+        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg);
+        if constexpr (EC == kEcArgmax) {
+          // the CTA that finishes the last tile decodes the winning keys and resets them
+          __threadfence();
+          epi_bar();
+          if (r == 0) {
+            const int dn = atomicAdd(e.done, 1);
+            esh.flag = (dn == a.n_tiles * a.m_tiles - 1);
+          }
+          epi_bar();
+          if (esh.flag) {
+            __threadfence();
+            const int sb = e.argmax_skip_B;
+            for (int m = r; m < a.M; m += 128) {
+              if (sb > 0 && m % sb == 0) continue;
+              const int o = sb > 0 ? (m / sb) * (sb - 1) + (m % sb) - 1 : m;
+              const unsigned long long k = atomicExch(e.keys + m, 0ull);
+              e.out_ids[o] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+              if (e.out_logit) {
+                const float raw = ordered_key_inv(static_cast<uint32_t>(k >> 32));
+                e.out_logit[o] = e.in_ss ? raw * norm_scale(e, m) : raw;
+              }
+            }
+            if (r == 0) *e.done = 0;
+          }
+          epi_bar();
+        }
+      }
+      // hand the TMEM buffer back to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      u = seg_end;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int BN, int EC>
+cudaError_t launch_bn(const AMaps& amaps, const ARegions& rg, const CUtensorMap& xmap, const GemmArgs& a,
+                      const GemmEpi& e, cudaStream_t stream) {
+  using C = Cfg<BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t err = cudaFuncSetAttribute(gemm_kernel<BN, EC>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  return launch_pdl(gemm_kernel<BN, EC>, dim3(a.grid), dim3(kThreads), C::kSmem, stream, amaps, xmap, a, rg, e);
+}
+
+template <int EC>
+cudaError_t launch_class_bn(const AMaps& amaps, const ARegions& rg, const CUtensorMap& xmap, const GemmArgs& a,
+                            const GemmEpi& e, int BN, cudaStream_t stream) {
+  switch (BN) {
+    case 16: return launch_bn<16, EC>(amaps, rg, xmap, a, e, stream);
+    case 32: return launch_bn<32, EC>(amaps, rg, xmap, a, e, stream);
+    case 64: return launch_bn<64, EC>(amaps, rg, xmap, a, e, stream);
+    case 128: return launch_bn<128, EC>(amaps, rg, xmap, a, e, stream);
+    default: return launch_bn<256, EC>(amaps, rg, xmap, a, e, stream);
+  }
+}
+
+// One translation unit per class (gemm_ec_*.cu) defines its launcher.
+cudaError_t launch_ec_f32(const AMaps&, const ARegions&, const CUtensorMap&, const GemmArgs&, const GemmEpi&, int,
+                          cudaStream_t);
+cudaError_t launch_ec_norm(const AMaps&, const ARegions&, const CUtensorMap&, const GemmArgs&, const GemmEpi&, int,
+                           cudaStream_t);
+cudaError_t launch_ec_rope(const AMaps&, const ARegions&, const CUtensorMap&, const GemmArgs&, const GemmEpi&, int,
+                           cudaStream_t);
+cudaError_t launch_ec_swiglu(const AMaps&, const ARegions&, const CUtensorMap&, const GemmArgs&, const GemmEpi&, int,
+                             cudaStream_t);
+cudaError_t launch_ec_argmax(const AMaps&, const ARegions&, const CUtensorMap&, const GemmArgs&, const GemmEpi&, int,
+                             cudaStream_t);
+
+}  // namespace gk
+}  // namespace dfl
