@@ -125,7 +125,7 @@ __device__ __forceinline__ void weight_rows(const ARegions& rg, int tile_n, int&
   }
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Folded RMSNorm scale of activation row m: 8 independent partial loads per
 // batch so the sum costs a few memory latencies, not one per partial.
@@ -301,7 +301,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
     }
 
     if (kind == EPI_F32_STORE || kind == EPI_F32_ADD) {
-      if (n < a.N) {
+      if (n < a.N && m0 + c0 + 16 <= a.M) {
+        float* p = e.out_f32 + static_cast<size_t>(m0 + c0) * e.ld_out + n;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (kind == EPI_F32_ADD) *p += v[c]; else *p = v[c];
+          p += e.ld_out;
+        }
+      } else if (n < a.N) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const int m = m0 + c0 + c;
@@ -312,20 +319,38 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         }
       }
     } else if (kind == EPI_RESID || kind == EPI_NORMSRC) {
+      if (n < a.N && m0 + c0 + 16 <= a.M) {   // whole chunk: pointers advance by the row stride
+        const size_t ld = e.ld_out;
+        float* px = e.out_f32 + static_cast<size_t>(m0 + c0) * ld + n;
+        uint16_t* ph = e.out_hg + static_cast<size_t>(m0 + c0) * ld + n;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int m = m0 + c0 + c;
-        float xn = 0.f;
-        if (n < a.N && m < a.M) {
-          const size_t off = static_cast<size_t>(m) * e.ld_out + n;
-          xn = v[c];
+        for (int c = 0; c < 16; ++c) {
+          float xn = v[c];
           if (kind == EPI_RESID) {
             xn += ra[c];
-            e.out_f32[off] = xn;
+            *px = xn;
+            px += ld;
           }
-          e.out_hg[off] = f32_to_bf16(xn * gain);
+          *ph = f32_to_bf16(xn * gain);
+          ph += ld;
+          sb[r * 17 + c] = xn * xn;
         }
-        sb[r * 17 + c] = xn * xn;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int m = m0 + c0 + c;
+          float xn = 0.f;
+          if (n < a.N && m < a.M) {
+            const size_t off = static_cast<size_t>(m) * e.ld_out + n;
+            xn = v[c];
+            if (kind == EPI_RESID) {
+              xn += ra[c];
+              e.out_f32[off] = xn;
+            }
+            e.out_hg[off] = f32_to_bf16(xn * gain);
+          }
+          sb[r * 17 + c] = xn * xn;
+        }
       }
       // column sums of squares over the tile's 128 rows
       epi_bar();
@@ -373,12 +398,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
       // rows < 64 hold gate rows, rows >= 64 the up rows of the same features;
       // each member of a pair writes half of the columns
       const int fint = tn * 64 + (f & 63);
+      if (fint < e.n_valid && m0 + c0 + 16 <= a.M) {   // whole chunk
+        const size_t ld = e.n_valid;
+        uint16_t* p = e.out_act + static_cast<size_t>(m0 + c0 + (lo ? 0 : 8)) * ld + fint;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int m = m0 + c0 + c;
-        if ((c < 8) == lo && fint < e.n_valid && m < a.M) {
-          const float gt = lo ? v[c] : other[c], up = lo ? other[c] : v[c];
-          e.out_act[static_cast<size_t>(m) * e.n_valid + fint] = f32_to_bf16(silu_f(gt) * up);
+        for (int c = 0; c < 8; ++c) {
+          const float gt = lo ? v[c] : other[c + 8], up = lo ? other[c] : v[c + 8];
+          *p = f32_to_bf16(silu_f(gt) * up);
+          p += ld;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int m = m0 + c0 + c;
+          if ((c < 8) == lo && fint < e.n_valid && m < a.M) {
+            const float gt = lo ? v[c] : other[c], up = lo ? other[c] : v[c];
+            e.out_act[static_cast<size_t>(m) * e.n_valid + fint] = f32_to_bf16(silu_f(gt) * up);
+          }
         }
       }
     } else if (kind == EPI_QKV_ROPE && reg == 2 && e.meta.B % 16 == 0 && m0 + c0 + 16 <= a.M &&
@@ -399,27 +435,46 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
       // value computed, before the chunk's first global store: loads placed
       // after a store would wait for it.
       int posv[16], dstv[16];
+      bool allpos = true;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         posv[c] = sh.row_pos[c0 + c];
         dstv[c] = kind == EPI_KV_APPEND ? sh.row_dst[c0 + c] : 0;
+        allpos = allpos && posv[c] >= 0;
       }
       bool run = rope && posv[0] >= 0;   // all 16 positions consecutive
 #pragma unroll
       for (int c = 1; c < 16; ++c) run = run && posv[c] == posv[0] + c;
       float2 cs = rope ? sh.rope_base[c0 >> 4][fi] : make_float2(1.f, 0.f);
       uint16_t ov[16];
+      const float sg = lo ? -1.f : 1.f;   // rotate-half sign of this row
+      if (run) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float x = v[c];
-        if (rope) {
-          const int pos = posv[c];
-          const float2 t = run ? cs : (pos >= 0 ? e.rope[static_cast<size_t>(pos) * half + fi] : make_float2(1.f, 0.f));
-          x = lo ? (x * t.x - other[c] * t.y) : (x * t.x + other[c] * t.y);
+        for (int c = 0; c < 16; ++c) {
+          ov[c] = f32_to_bf16(fmaf(sg * other[c], cs.y, v[c] * cs.x));
           cs = make_float2(cs.x * rot.x - cs.y * rot.y, cs.y * rot.x + cs.x * rot.y);
         }
-        ov[c] = f32_to_bf16(x);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float x = v[c];
+          if (rope) {
+            const int pos = posv[c];
+            const float2 t = pos >= 0 ? e.rope[static_cast<size_t>(pos) * half + fi] : make_float2(1.f, 0.f);
+            x = fmaf(sg * other[c], t.y, x * t.x);
+          }
+          ov[c] = f32_to_bf16(x);
+        }
       }
+      if (kind == EPI_QKV_ROPE && reg != 2 && allpos && m0 + c0 + 16 <= a.M) {   // whole chunk of q or k
+        const size_t ld = static_cast<size_t>(reg == 0 ? e.n_q_heads : e.n_kv_heads) * d;
+        uint16_t* p = (reg == 0 ? e.out_q : e.out_k) + static_cast<size_t>(m0 + c0) * ld + rf;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          *p = ov[c];
+          p += ld;
+        }
+      } else
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const int m = m0 + c0 + c;
