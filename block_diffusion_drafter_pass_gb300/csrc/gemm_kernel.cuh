@@ -191,6 +191,21 @@ __device__ __forceinline__ void tile_cols_prepare(const GemmArgs& a, const GemmE
   }
 }
 
+// 32 consecutive TMEM columns of this thread's lane (32x32b shape);
+// completes with tcgen05.wait::st.
+__device__ __forceinline__ void tmem_store32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+      "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+      "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
+      "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st_gk() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Residual inputs of one 16-column chunk (EPI_RESID); the chunk loop keeps
 // them two chunks ahead of use.
 __device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, int m0, int c0, int n,
@@ -207,7 +222,7 @@ __device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, 
 template <int BN, int EC>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int g,
                                               int tile, int first, int last, uint32_t tb, int r, EpiShared& sh,
-                                              float* stg) {
+                                              float* stg, uint32_t pre) {
   const int kind = class_kind<EC>(e.kind);
   const int q = r >> 5, lane = r & 31;
   const int tn = tile / a.m_tiles, tm = tile - tn * a.m_tiles;
@@ -235,17 +250,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   const float gain = (kind == EPI_RESID || kind == EPI_NORMSRC) && n < a.N ? bf16_to_f32(e.gain[n]) : 0.f;
 
   // Other CTAs holding partial sums of this tile: one is read a chunk ahead
-  // into registers; any further ones are read on use.
+  // into registers; any further ones are read on use. The pieces are added
+  // in CTA order whichever CTA finishes the tile, so the result is the same
+  // from run to run.
   auto partial_src = [&](int o) {
     const int side = (static_cast<long long>(o) * a.units / a.grid) / a.k_blocks == tile ? 0 : 1;
     return a.partial + (static_cast<size_t>(o) * 2 + side) * slot_elems + r;
   };
   int oth0 = -1;
-  bool more = false;
   for (int o = first; o <= last; ++o) {
-    if (o == g) continue;
-    if (oth0 < 0) oth0 = o;
-    else more = true;
+    if (o != g && oth0 < 0) oth0 = o;
   }
   const float* ps0 = oth0 >= 0 ? partial_src(oth0) : nullptr;
   auto partial_load = [&](int c0, float (&p0)[16]) {
@@ -259,7 +273,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   const bool resid = kind == EPI_RESID;
   float ra[16], rb[16];
   float2 rot = make_float2(1.f, 0.f);
-  if (resid) {
+  // pre != 0: the residual tile already sits in TMEM at `pre` (loaded while
+  // the MMAs ran); otherwise it is read two chunks ahead
+  if (resid && !pre) {
     load_resid(a, e, m0, 0, n, ra);
     load_resid(a, e, m0, 16, n, rb);
   }
@@ -271,20 +287,39 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
     const int buf = (c0 >> 4) & 1;
     float* sb = stg + buf * (128 * 17);
     float rc[16];
-    if (resid && c0 + 32 < BN) load_resid(a, e, m0, c0 + 32, n, rc);
+    if (resid && !pre && c0 + 32 < BN) load_resid(a, e, m0, c0 + 32, n, rc);
+    float rx[16];
+    if (resid) {
+      if (pre) {
+        tmem_ld16(pre + c0, rx);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) rx[c] = ra[c];
+      }
+    }
     float pn0[16];
     if (c0 + 16 < BN) partial_load(c0 + 16, pn0);
     float v[16];
     tmem_ld16(tb + c0, v);
+    if (first != last) {
+      float sum[16];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) v[c] += pc0[c];
-    if (more) {
+      for (int c = 0; c < 16; ++c) sum[c] = 0.f;
       for (int o = first; o <= last; ++o) {
-        if (o == g || o == oth0) continue;
-        const float* src = partial_src(o);
+        if (o == g) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] += __ldcg(src + static_cast<size_t>(c0 + c) * kTileN);
+          for (int c = 0; c < 16; ++c) sum[c] += v[c];
+        } else if (o == oth0) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) sum[c] += pc0[c];
+        } else {
+          const float* src = partial_src(o);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) sum[c] += __ldcg(src + static_cast<size_t>(c0 + c) * kTileN);
+        }
       }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] = sum[c];
     }
     if (e.in_ss && kind != EPI_ARGMAX) {
 #pragma unroll
@@ -327,7 +362,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         for (int c = 0; c < 16; ++c) {
           float xn = v[c];
           if (kind == EPI_RESID) {
-            xn += ra[c];
+            xn += rx[c];
             *px = xn;
             px += ld;
           }
@@ -344,7 +379,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
             const size_t off = static_cast<size_t>(m) * e.ld_out + n;
             xn = v[c];
             if (kind == EPI_RESID) {
-              xn += ra[c];
+              xn += rx[c];
               e.out_f32[off] = xn;
             }
             e.out_hg[off] = f32_to_bf16(xn * gain);
@@ -689,6 +724,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long seg_end = min(u1, static_cast<long long>(t + 1) * kb);
       const bool whole = (u == static_cast<long long>(t) * kb) && (seg_end == static_cast<long long>(t + 1) * kb);
       const int buf = seg & 1;
+      // A CTA that owns exactly one whole tile leaves the other accumulator
+      // buffer unused: the residual add's input tile is loaded into it while
+      // the MMAs run, so the epilogue reads it from TMEM.
+      uint32_t pre = 0;
+      if constexpr (EC == kEcNorm) {
+        if (e.kind == EPI_RESID && whole && u0 == u && u1 == seg_end) {
+          const int tn = t / a.m_tiles, m0 = (t - tn * a.m_tiles) * BN, n = tn * kTileN + r;
+          pre = trow + (buf ^ 1) * BN;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            float xv[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int m = m0 + c0 + c;
+              xv[c] = (n < a.N && m < a.M) ? __ldcg(e.out_f32 + static_cast<size_t>(m) * e.ld_out + n) : 0.f;
+            }
+            tmem_store32(pre + c0, xv);
+          }
+          tmem_wait_st_gk();
+        }
+      }
       if (!mbar_wait(&acc_full[buf], (seg >> 1) & 1, &abort_flag)) {
         abort_flag = 1;
         latch_status(a.status, kDevTimeout);
@@ -725,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (finish) __threadfence();
       }
       if (finish) {
-        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg);
+        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre);
         if constexpr (EC == kEcArgmax) {
           // the CTA that finishes the last tile decodes the winning keys and resets them
           __threadfence();

@@ -7,16 +7,24 @@
 namespace dfl {
 using namespace gk;
 
-int gemm_token_tile(int M) {
+int gemm_token_tile(int M, int N, int num_sms) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128) return 128;
-  return 256;
+  // 256-token tiles, unless 128-token tiles keep clearly more SMs busy (a
+  // tile count well under one wave)
+  const long long nt = (N + kTileN - 1) / kTileN;
+  auto busy = [&](int bn) {
+    const long long t = nt * ((M + bn - 1) / bn);
+    const long long waves = (t + num_sms - 1) / num_sms;
+    return static_cast<double>(t) / static_cast<double>(waves * num_sms);
+  };
+  return busy(128) > busy(256) + 0.05 ? 128 : 256;
 }
 
 int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms) {
-  const int BN = gemm_token_tile(M);
+  const int BN = gemm_token_tile(M, N, num_sms);
   const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + BN - 1) / BN);
   const int kb = (K + kTileK - 1) / kTileK;
   const long long units = tiles * kb;
@@ -42,7 +50,7 @@ cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUten
                         int splits, const GemmEpi& epi, const GemmWork& work, int num_sms, cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
   if (regions.pair != 32 && regions.pair != 64) return cudaErrorInvalidValue;
-  const int BN = gemm_token_tile(M);
+  const int BN = gemm_token_tile(M, N, num_sms);
   GemmArgs a{};
   a.M = M;
   a.N = N;

@@ -139,9 +139,9 @@ cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUten
                         int K, int splits, const GemmEpi& epi, const GemmWork& work, int num_sms,
                         cudaStream_t stream);
 
-// BN (token tile) the GEMM uses for M rows; the activation tensor map's box
-// height must equal it.
-int gemm_token_tile(int M);
+// BN (token tile) the GEMM uses for M rows and N output features on num_sms
+// SMs; the activation tensor map's box height must equal it.
+int gemm_token_tile(int M, int N, int num_sms);
 // CTAs the GEMM runs with: num_sms stream-K workers (splits = 0) or
 // tiles * splits, reduced until 2 partial tiles per CTA fit partial_elems.
 int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms);

@@ -67,7 +67,12 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
     set_unattached_error("dflash_gemm_noalloc: W and X must be 16-byte aligned");
     return DFLASH_EINVAL;
   }
-  const int BN = gemm_token_tile(M);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    set_unattached_error("dflash_gemm_noalloc: no CUDA device");
+    return DFLASH_ECUDA;
+  }
+  const int BN = gemm_token_tile(M, N, sms);
   const long long tiles = static_cast<long long>(ceil_div(M, BN)) * ceil_div(N, 128);
   const int k_blocks = ceil_div(K, 64);
   if (tiles > kTickets) {
@@ -89,11 +94,6 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
   cudaError_t e = scratch_on_current_device(&base);
   if (e != cudaSuccess) {
     set_unattached_error("dflash_gemm_noalloc: cudaGetSymbolAddress of the scratch array failed");
-    return DFLASH_ECUDA;
-  }
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    set_unattached_error("dflash_gemm_noalloc: no CUDA device");
     return DFLASH_ECUDA;
   }
   AMaps am;

@@ -606,7 +606,6 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
 
   const int H = c.hidden, d = c.head_dim, nkv = c.n_kv_heads;
   const int M = static_cast<int>(total);
-  const int BN = gemm_token_tile(M);
   GemmWork work = gemm_work(ctx);
   const int parts = ceil_div(H, 128);
   // x = X W_c^T, kept as bf16(x * g_c) plus per-tile sums of x^2: the
@@ -615,7 +614,7 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
     AMaps am;
     am.m[0] = ctx->m_wc;
     ARegions rg = stacked({H});
-    const CUtensorMap* xm = act_map(ctx, feats, M, c.n_feat_layers * H, BN);
+    const CUtensorMap* xm = act_map(ctx, feats, M, c.n_feat_layers * H, gemm_token_tile(M, H, ctx->num_sms));
     if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe feats for TMA");
     GemmEpi e = base_epi(ctx, EPI_NORMSRC);
     e.out_hg = ctx->htg;
@@ -629,11 +628,12 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
   }
   // K/V of every layer from H_t = x / rms(x) * g_c, RoPE on K, scattered into the pages
   {
-    const CUtensorMap* xm = act_map(ctx, ctx->htg, M, H, BN);
-    if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe H_t for TMA");
     const int per_launch = kMaxAMaps / 2;
     for (int l0 = 0; l0 < c.n_layers; l0 += per_launch) {
       const int nl = std::min(per_launch, c.n_layers - l0);
+      const CUtensorMap* xm =
+          act_map(ctx, ctx->htg, M, H, gemm_token_tile(M, 2 * nl * ceil_div(nkv * d, 128) * 128, ctx->num_sms));
+      if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe H_t for TMA");
       AMaps am;
       ARegions rg;
       std::memset(&rg, 0, sizeof(rg));
@@ -689,7 +689,6 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
 
   const int H = c.hidden, d = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, F = c.ffn;
   const int M = n_seq * B;
-  const int BN = gemm_token_tile(M);
   GemmWork work = gemm_work(ctx);
   const SeqState ss = seq_state(ctx);
 
@@ -712,12 +711,18 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
 
   const int Bb = attention_block_rows(B);
   const CUtensorMap* km = blk_map(ctx, ctx->kb, M, Bb);
-  const CUtensorMap* hmap = act_map(ctx, ctx->hg, M, H, BN);
+  // activation descriptors: the box height is the token tile each GEMM uses
+  const int sms = ctx->num_sms;
+  const int n_qkv = (nq + 2 * nkv) * d, n_gu = ceil_div(F, 64) * 128;
+  const CUtensorMap* hmap_qkv = act_map(ctx, ctx->hg, M, H, gemm_token_tile(M, n_qkv, sms));
+  const CUtensorMap* hmap_gu = act_map(ctx, ctx->hg, M, H, gemm_token_tile(M, n_gu, sms));
+  const CUtensorMap* hmap_lm = act_map(ctx, ctx->hg, M, H, gemm_token_tile(M, c.vocab, sms));
   const int parts = ceil_div(H, 128);
   const int rows_ld = ctx->max_rows();
-  const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, BN);
-  const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, BN);
-  if (!km || !hmap || !amap || !fmap) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+  const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, gemm_token_tile(M, H, sms));
+  const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, gemm_token_tile(M, H, sms));
+  if (!km || !hmap_qkv || !hmap_gu || !hmap_lm || !amap || !fmap)
+    return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
   AttnMaps attn_maps;
   attn_maps.pool_k = ctx->m_pool;
   attn_maps.pool_vt = ctx->m_pool_vt;
@@ -754,7 +759,7 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       e.in_ss_ld = rows_ld;
       const double nw = 1.0 * (nq + 2 * nkv) * d;
       ProfScope ps(ctx, DFLASH_K_QKV, stream, gemm_bytes(M, nw, H, nw, 2), 2.0 * M * nw * H);
-      CK(launch_gemm(am, rg, *hmap, M, (nq + 2 * nkv) * d, H, 0, e, work, ctx->num_sms, stream));
+      CK(launch_gemm(am, rg, *hmap_qkv, M, n_qkv, H, 0, e, work, ctx->num_sms, stream));
     }
     {  // non-causal attention over the injected context and the block
       AttnArgs a;
@@ -814,7 +819,7 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       e.in_ss_parts = parts;
       e.in_ss_ld = rows_ld;
       ProfScope ps(ctx, DFLASH_K_GATEUP, stream, gemm_bytes(M, 2.0 * F, H, F, 2), 4.0 * M * F * H);
-      CK(launch_gemm(am, rg, *hmap, M, ceil_div(F, 64) * 128, H, 0, e, work, ctx->num_sms, stream));
+      CK(launch_gemm(am, rg, *hmap_gu, M, n_gu, H, 0, e, work, ctx->num_sms, stream));
     }
     {  // x += act W_down^T; the next RMSNorm (next layer's input, or the final norm) is folded in
       AMaps am;
@@ -849,7 +854,7 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
     e.in_ss_parts = parts;
     e.in_ss_ld = rows_ld;
     ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(Md, c.vocab, H, 1, 8), 2.0 * Md * c.vocab * H);
-    CK(launch_gemm(am, stacked({c.vocab}), *hmap, M, c.vocab, H, 0, e, work, ctx->num_sms, stream));
+    CK(launch_gemm(am, stacked({c.vocab}), *hmap_lm, M, c.vocab, H, 0, e, work, ctx->num_sms, stream));
   }
   return DFLASH_OK;
 }
@@ -956,7 +961,7 @@ dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y, 
   int dev = 0, sms = 0;
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int BN = gemm_token_tile(M);
+  const int BN = gemm_token_tile(M, N, sms);
   AMaps am;
   CUtensorMap xm;
   if (!encode_2d(&am.m[0], W, N, K, kWeightBoxRows) || !encode_2d(&xm, X, M, K, BN)) return DFLASH_EINVAL;

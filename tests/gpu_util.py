@@ -71,9 +71,26 @@ def i32_dev(a, device):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
 
 
-def compare_draft(got_ids, got_hidden, got_top, ref, B, what, row_rel=None):
+def assert_hidden_like_bf16_storage(got, ref, emu, what, factor=1.5):
+    """Deep passes: the stated 2e-2 relative bound on each row's L2 norm, and
+    no element further from the exact pass than `factor` times the worst
+    element of an exact bf16-storage pass `emu` (tests/emulate.py), plus ATOL."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    emu = np.asarray(emu, dtype=np.float64)
+    rel = np.linalg.norm(got - ref, axis=-1) / np.maximum(np.linalg.norm(ref, axis=-1), 1e-30)
+    assert float(rel.max()) <= HID_REL_L2, f"{what}: row relative L2 error {rel.max():.4g} > {HID_REL_L2}"
+    worst, worst_emu = float(np.abs(got - ref).max()), float(np.abs(emu - ref).max())
+    assert worst <= factor * worst_emu + ATOL, (
+        f"{what}: worst element error {worst:.4g} > {factor} x bf16-storage emulation's {worst_emu:.4g} + {ATOL}")
+
+
+def compare_draft(got_ids, got_hidden, got_top, ref, B, what, row_rel=None, emu_hidden=None):
     """Compare one sequence's draft against the oracle's result dict."""
-    assert_hidden_close(got_hidden, ref["hidden"], f"{what}: final residual stream")
+    if emu_hidden is None:
+        assert_hidden_close(got_hidden, ref["hidden"], f"{what}: final residual stream")
+    else:
+        assert_hidden_like_bf16_storage(got_hidden, ref["hidden"], emu_hidden, f"{what}: final residual stream")
     if B > 1:
         assert_close(got_top, ref["top1"], f"{what}: winning logits", row_rel=row_rel)
         sure = ref["gap"] > GAP

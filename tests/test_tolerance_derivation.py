@@ -13,30 +13,11 @@ reading (tests/gpu_util.py). No CUDA code is involved.
 import numpy as np
 
 import oracle.dflash_oracle as od
-from synth import DrafterShape, make_weights_np, make_features_np, bf16_round
+from synth import DrafterShape, make_weights_np, make_features_np
+from tests.emulate import bf16_context, bf16_storage_hidden
 
 SHAPE = DrafterShape(hidden=1024, n_heads=8, n_kv_heads=2, head_dim=128, ffn=3072, vocab=512, n_layers=2,
                      n_feat_layers=5, rope_base=1e6, rms_eps=1e-6, mask_id=511)
-
-
-def _r(x):
-    return bf16_round(np.asarray(x, dtype=np.float32)).astype(np.float64)
-
-
-def _bf16_storage_pass(w, sh, anchor, kc, vc, B):
-    C = kc[0].shape[0]
-    x = w["embed"][[anchor] + [sh.mask_id] * (B - 1)].copy()
-    for lw, k_ctx, v_ctx in zip(w["layers"], kc, vc):
-        pos = C + np.arange(B)
-        h = _r(od.rms_norm(x, lw["g_attn"], sh.rms_eps))
-        q = _r(od.apply_rope((h @ lw["w_q"].T).reshape(B, sh.n_heads, sh.head_dim), pos, sh.rope_base))
-        k = _r(od.apply_rope((h @ lw["w_k"].T).reshape(B, sh.n_kv_heads, sh.head_dim), pos, sh.rope_base))
-        v = _r((h @ lw["w_v"].T).reshape(B, sh.n_kv_heads, sh.head_dim))
-        a = _r(od.block_attention(q, np.concatenate([k_ctx, k]), np.concatenate([v_ctx, v])).reshape(B, -1))
-        x = x + a @ lw["w_o"].T
-        h2 = _r(od.rms_norm(x, lw["g_ffn"], sh.rms_eps))
-        x = x + _r(od.silu(h2 @ lw["w_gate"].T) * (h2 @ lw["w_up"].T)) @ lw["w_down"].T
-    return x
 
 
 def test_bf16_storage_error_fits_the_row_relative_reading():
@@ -47,16 +28,14 @@ def test_bf16_storage_error_fits_the_row_relative_reading():
     C, B = 200, 16
     f = make_features_np(C, sh.n_feat_layers * sh.hidden, seed=6).astype(np.float64)
     ht = od.fuse_features(f, w["w_c"], w["g_c"], sh.rms_eps)
-    kc, vc, kb, vb = [], [], [], []
+    kc, vc = [], []
     for lw in w["layers"]:
         k, v = od.context_kv(ht, lw, np.arange(C), sh.n_kv_heads, sh.head_dim, sh.rope_base)
         kc.append(k)
         vc.append(v)
-        k, v = od.context_kv(_r(ht), lw, np.arange(C), sh.n_kv_heads, sh.head_dim, sh.rope_base)
-        kb.append(_r(k))
-        vb.append(_r(v))
+    kb, vb = bf16_context(w, sh, f)
     ref = od.draft_block(w, sh, 3, kc, vc, B)["hidden"]
-    emu = _bf16_storage_pass(w, sh, 3, kb, vb, B)
+    emu = bf16_storage_hidden(w, sh, 3, kb, vb, B)
     rel = np.linalg.norm(emu - ref, axis=1) / np.linalg.norm(ref, axis=1)
     assert rel.max() < 0.6 * 2e-2                     # the per-row reading holds with margin
     err = np.abs(emu - ref)
