@@ -156,9 +156,15 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+GEMM_SOURCES = ("gemm_kernel.cuh", "gemm_tc.cu", "gemm_ec_f32.cu", "gemm_ec_norm.cu", "gemm_ec_rope.cu",
+                "gemm_ec_swiglu.cu", "gemm_ec_argmax.cu", "ptx.cuh", "internal.h")
+
+
 def gemm_source_hash() -> str:
-    p = os.path.join(ROOT, "block_diffusion_drafter_pass_gb300", "csrc", "gemm_tc.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        h.update(open(os.path.join(ROOT, "block_diffusion_drafter_pass_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
