@@ -792,6 +792,50 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
   }
   const int r = j * G + gh;
   const size_t rp = static_cast<size_t>(a.rows_pad);
+  uint16_t* out = a.out + static_cast<size_t>(i * B + j) * a.n_q_heads * D + static_cast<size_t>(hq) * D + lane * kPer;
+  if (nch <= 32) {
+    // Every chunk in flight at once: lane c holds chunk c's (max, sum), and
+    // every lane loads its dims of all partial rows before the weights are
+    // known, so the merge costs about one memory latency.
+    const float2 ml = lane < nch ? __ldcg(a.part_ml + (base + lane) * rp + r) : make_float2(-INFINITY, 0.f);
+    const float* po = a.part_o + (static_cast<size_t>(base) * rp + r) * D + lane * kPer;
+    float v[32][kPer];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if (c < nch) {
+        if constexpr (kPer == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(po + c * rp * D));
+          v[c][0] = t.x; v[c][1] = t.y; v[c][2] = t.z; v[c][3] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(po + c * rp * D));
+          v[c][0] = t.x; v[c][1] = t.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) v[c][e] = 0.f;
+      }
+    }
+    float M = ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = lane < nch ? exp2f(ml.x - M) : 0.f;
+    float L = w * ml.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float wc = __shfl_sync(0xffffffffu, w, c);
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] += wc * v[c][e];
+    }
+    const float inv = 1.f / L;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) out[e] = f32_to_bf16(acc[e] * inv);
+    return;
+  }
   float M = -INFINITY;
   for (int c = lane; c < nch; c += 32) M = fmaxf(M, a.part_ml[(base + c) * rp + r].x);
 #pragma unroll
@@ -833,7 +877,6 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] += wsm[warp][c] * __ldcg(po + c * stride + e);
   const float inv = 1.f / L;
-  uint16_t* out = a.out + static_cast<size_t>(i * B + j) * a.n_q_heads * D + static_cast<size_t>(hq) * D + lane * kPer;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) out[e] = f32_to_bf16(acc[e] * inv);
 }
