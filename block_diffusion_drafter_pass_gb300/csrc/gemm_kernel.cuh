@@ -208,6 +208,24 @@ __device__ __forceinline__ void tmem_wait_st_gk() { asm volatile("tcgen05.wait::
 
 // Residual inputs of one 16-column chunk (EPI_RESID); the chunk loop keeps
 // them two chunks ahead of use.
+// Stream-K partition: CTA g owns the contiguous range of (tile, k-block)
+// units [unit_begin(g), unit_begin(g + 1)); tiles are ordered so that the m
+// tiles of one weight tile are consecutive (weights reused from L2).
+// floor(x / y) for x >= 0, y > 0; a 32-bit division whenever both fit
+// (a 64-bit division is a long dependent instruction sequence)
+__device__ __forceinline__ long long div_floor(long long x, long long y) {
+  if (((x | y) >> 32) == 0) return static_cast<long long>(static_cast<uint32_t>(x) / static_cast<uint32_t>(y));
+  return x / y;
+}
+__device__ __forceinline__ long long unit_begin(int g, const GemmArgs& a) {
+  return div_floor(static_cast<long long>(g) * a.units, a.grid);
+}
+// The CTA whose range holds unit u: the largest g with floor(g U / G) <= u,
+// i.e. g U < (u + 1) G, which is floor(((u + 1) G - 1) / U).
+__device__ __forceinline__ int cta_of(long long u, const GemmArgs& a) {
+  return static_cast<int>(div_floor((u + 1) * a.grid - 1, a.units));
+}
+
 __device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, int m0, int c0, int n,
                                            float (&x)[16]) {
 #pragma unroll
@@ -222,7 +240,7 @@ __device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, 
 template <int BN, int EC>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int g,
                                               int tile, int first, int last, uint32_t tb, int r, EpiShared& sh,
-                                              float* stg, uint32_t pre) {
+                                              float* stg, uint32_t pre, const float (&rpre)[16]) {
   const int kind = class_kind<EC>(e.kind);
   const int q = r >> 5, lane = r & 31;
   const int tn = tile / a.m_tiles, tm = tile - tn * a.m_tiles;
@@ -230,7 +248,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   const int P = rg.pair;
   const int f = r;                              // row of this lane within the tile
   const size_t slot_elems = static_cast<size_t>(kTileN) * BN;
-  tile_cols_prepare<BN, EC>(a, e, m0, r, sh);
 
   // kind-specific constants of this lane
   int reg = 0, rf = f;                          // region and row within the region's matrix
@@ -249,12 +266,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   const int fi = lo ? di : di - half;           // RoPE frequency index of the pair
   const float gain = (kind == EPI_RESID || kind == EPI_NORMSRC) && n < a.N ? bf16_to_f32(e.gain[n]) : 0.f;
 
-  // Other CTAs holding partial sums of this tile: one is read a chunk ahead
-  // into registers; any further ones are read on use. The pieces are added
-  // in CTA order whichever CTA finishes the tile, so the result is the same
-  // from run to run.
+  // Other CTAs holding partial sums of this tile. A one-chunk tile reads up
+  // to kRound of them in one round of loads; wider tiles read one a chunk
+  // ahead into registers. Any further pieces are read on use. The pieces are
+  // added in CTA order whichever CTA finishes the tile, so the result is the
+  // same from run to run. Every CTA after the tile's first one starts inside
+  // the tile, so its piece is its first segment (slot 0); the first CTA's
+  // piece is in slot 1 when that CTA began in an earlier tile.
+  const bool first_in_slot1 = unit_begin(first, a) < static_cast<long long>(tile) * a.k_blocks;
   auto partial_src = [&](int o) {
-    const int side = (static_cast<long long>(o) * a.units / a.grid) / a.k_blocks == tile ? 0 : 1;
+    const int side = (o == first && first_in_slot1) ? 1 : 0;
     return a.partial + (static_cast<size_t>(o) * 2 + side) * slot_elems + r;
   };
   int oth0 = -1;
@@ -276,12 +297,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   // pre != 0: the residual tile already sits in TMEM at `pre` (loaded while
   // the MMAs ran); otherwise it is read two chunks ahead
   if (resid && !pre) {
-    load_resid(a, e, m0, 0, n, ra);
-    load_resid(a, e, m0, 16, n, rb);
+    if constexpr (BN == 16) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        ra[c] = rpre[c];
+        rb[c] = 0.f;
+      }
+    } else {
+      load_resid(a, e, m0, 0, n, ra);
+      load_resid(a, e, m0, 16, n, rb);
+    }
   }
   if (rope) rot = e.rope[half + fi];
   float pc0[16];
-  partial_load(0, pc0);
+  if constexpr (BN > 16) partial_load(0, pc0);
 #pragma unroll 1
   for (int c0 = 0; c0 < BN; c0 += 16) {
     const int buf = (c0 >> 4) & 1;
@@ -298,10 +327,38 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
       }
     }
     float pn0[16];
-    if (c0 + 16 < BN) partial_load(c0 + 16, pn0);
+    if constexpr (BN > 16) {
+      if (c0 + 16 < BN) partial_load(c0 + 16, pn0);
+    }
     float v[16];
     tmem_ld16(tb + c0, v);
-    if (first != last) {
+    constexpr int kRound = 7;
+    if (BN == 16 && first != last && last - first <= kRound) {
+      // the other pieces in CTA order: k-th other CTA is first + k, skipping g
+      float pv[kRound][16];
+#pragma unroll
+      for (int k = 0; k < kRound; ++k) {
+        const int o = first + k + (first + k >= g ? 1 : 0);
+        const float* src = o <= last ? partial_src(o) : nullptr;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pv[k][c] = src ? __ldcg(src + static_cast<size_t>(c) * kTileN) : 0.f;
+      }
+      float sum[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sum[c] = 0.f;
+#pragma unroll
+      for (int p = 0; p <= kRound; ++p) {
+        const int o = first + p;
+        if (o <= last) {
+          // position p is this CTA's own piece, or other piece p (before g) or p - 1 (after g)
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            sum[c] += o == g ? v[c] : (o < g ? pv[p < kRound ? p : kRound - 1][c] : pv[p > 0 ? p - 1 : 0][c]);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] = sum[c];
+    } else if (first != last) {
       float sum[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) sum[c] = 0.f;
@@ -309,7 +366,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         if (o == g) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) sum[c] += v[c];
-        } else if (o == oth0) {
+        } else if (BN > 16 && o == oth0) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) sum[c] += pc0[c];
         } else {
@@ -547,18 +604,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   epi_bar();
 }
 
-// Stream-K partition: CTA g owns the contiguous range of (tile, k-block)
-// units [unit_begin(g), unit_begin(g + 1)); tiles are ordered so that the m
-// tiles of one weight tile are consecutive (weights reused from L2).
-__device__ __forceinline__ long long unit_begin(int g, const GemmArgs& a) {
-  return static_cast<long long>(g) * a.units / a.grid;
-}
-__device__ __forceinline__ int cta_of(long long u, const GemmArgs& a) {
-  long long g = u * a.grid / a.units;
-  while (g + 1 < a.grid && unit_begin(static_cast<int>(g + 1), a) <= u) ++g;
-  while (g > 0 && unit_begin(static_cast<int>(g), a) > u) --g;
-  return static_cast<int>(g);
-}
 
 template <int BN, int EC>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -724,13 +769,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long seg_end = min(u1, static_cast<long long>(t + 1) * kb);
       const bool whole = (u == static_cast<long long>(t) * kb) && (seg_end == static_cast<long long>(t + 1) * kb);
       const int buf = seg & 1;
+      // Column constants (RMSNorm scales, positions, RoPE bases) and a
+      // one-chunk tile's residual input do not depend on the accumulator:
+      // they are fetched while the MMAs run, whether or not this CTA ends up
+      // finishing the tile.
+      const int tn0 = t / a.m_tiles, m0 = (t - tn0 * a.m_tiles) * BN;
+      tile_cols_prepare<BN, EC>(a, e, m0, r, esh);
+      float rpre[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) rpre[c] = 0.f;
       // A CTA that owns exactly one whole tile leaves the other accumulator
       // buffer unused: the residual add's input tile is loaded into it while
       // the MMAs run, so the epilogue reads it from TMEM.
       uint32_t pre = 0;
       if constexpr (EC == kEcNorm) {
         if (e.kind == EPI_RESID && whole && u0 == u && u1 == seg_end) {
-          const int tn = t / a.m_tiles, m0 = (t - tn * a.m_tiles) * BN, n = tn * kTileN + r;
+          const int n = tn0 * kTileN + r;
           pre = trow + (buf ^ 1) * BN;
 #pragma unroll 1
           for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -743,6 +797,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_store32(pre + c0, xv);
           }
           tmem_wait_st_gk();
+        } else if (BN == 16 && e.kind == EPI_RESID) {
+          load_resid(a, e, m0, 0, tn0 * kTileN + r, rpre);
         }
       }
       if (!mbar_wait(&acc_full[buf], (seg >> 1) & 1, &abort_flag)) {
@@ -781,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (finish) __threadfence();
       }
       if (finish) {
-        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre);
+        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre, rpre);
         if constexpr (EC == kEcArgmax) {
           // the CTA that finishes the last tile decodes the winning keys and resets them
           __threadfence();
