@@ -195,6 +195,18 @@ cudaError_t launch_embed(const uint16_t* embed, const int32_t* anchors, int mask
 cudaError_t launch_verify(const SeqMeta& meta, SeqState st, const int32_t* drafts, const int32_t* targets,
                           int32_t* tau, int32_t* bonus, cudaStream_t s);
 cudaError_t launch_fuse_advance(const SeqMeta& meta, SeqState st, int pending, cudaStream_t s);
+
+// Page-table entries to set, table[idx[k]] = page[k], carried in the launch's
+// parameter block: no host buffer has to outlive the call, and the stream
+// holds only kernels, so neither the host nor the programmatic launch chain
+// waits for a copy.
+constexpr int kPageUpdMax = 1000;
+struct PageUpdates {
+  int n;
+  int idx[kPageUpdMax];
+  int page[kPageUpdMax];
+};
+cudaError_t launch_page_updates(const PageUpdates& u, int* table, cudaStream_t s);
 cudaError_t launch_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, int32_t* out, cudaStream_t s);
 
 }  // namespace dfl

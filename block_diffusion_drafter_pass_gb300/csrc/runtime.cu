@@ -17,6 +17,7 @@
 #include <cmath>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -124,6 +125,7 @@ struct dflash_ctx {
   std::vector<std::vector<int>> pages;
   std::vector<int> len_ub, pend, added_since;
   int* h_snap = nullptr;      // pinned copy of d_len
+  std::unique_ptr<PageUpdates> page_upd{new PageUpdates()};   // staging of one append's new pages
   cudaEvent_t snap_event = nullptr;
   bool snap_pending = false;
 
@@ -590,19 +592,25 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
     if (need_total > static_cast<int>(ctx->free_pages.size()))
       return fail(ctx, DFLASH_ENOMEM, "KV page pool exhausted");
   }
+  PageUpdates& upd = *ctx->page_upd;
+  upd.n = 0;
   for (int i = 0; i < n_seq; ++i) {
     const int s = meta.slot[i];
     auto& pg = ctx->pages[s];
     const int have = static_cast<int>(pg.size());
     const int want = ceil_div(ctx->len_ub[s] + ctx->pend[s] + n_new[i], kPage);
-    if (want <= have) continue;
     for (int k = have; k < want; ++k) {
       pg.push_back(ctx->free_pages.back());
       ctx->free_pages.pop_back();
+      upd.idx[upd.n] = s * ctx->pages_per_seq + k;
+      upd.page[upd.n] = pg.back();
+      if (++upd.n == kPageUpdMax) {
+        CK(launch_page_updates(upd, ctx->d_page_table, stream));
+        upd.n = 0;
+      }
     }
-    CK(cudaMemcpyAsync(ctx->d_page_table + static_cast<size_t>(s) * ctx->pages_per_seq + have, pg.data() + have,
-                       (want - have) * sizeof(int), cudaMemcpyHostToDevice, stream));
   }
+  CK(launch_page_updates(upd, ctx->d_page_table, stream));
 
   const int H = c.hidden, d = c.head_dim, nkv = c.n_kv_heads;
   const int M = static_cast<int>(total);

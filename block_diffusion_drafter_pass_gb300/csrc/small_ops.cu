@@ -120,6 +120,16 @@ __global__ void fuse_advance_kernel(const __grid_constant__ SeqMeta meta, SeqSta
   else st.len[slot] += n;
 }
 
+// Dependents may start at once (none reads the page table before its own
+// wait; the attention kernel's early reads sit behind the draft's embedding
+// kernel). The entries are written after the wait, when every earlier reader
+// of the table has completed.
+__global__ void page_table_update_kernel(const __grid_constant__ PageUpdates u, int* table) {
+  grid_dep_launch();
+  grid_dep_wait();
+  for (int k = threadIdx.x; k < u.n; k += blockDim.x) table[u.idx[k]] = u.page[k];
+}
+
 // Row argmax of bf16 logits, lowest index on ties: the per-thread best is kept
 // as a 64-bit key (ordered value << 32 | ~index) so one max picks both.
 // Each row is split over a cluster of kArgCluster CTAs; their partial keys
@@ -231,6 +241,11 @@ cudaError_t launch_verify(const SeqMeta& meta, SeqState st, const int32_t* draft
 cudaError_t launch_fuse_advance(const SeqMeta& meta, SeqState st, int pending, cudaStream_t s) {
   if (meta.n_seq == 0) return cudaSuccess;
   return launch_pdl(fuse_advance_kernel, dim3(1), dim3(kMaxBatch), 0, s, meta, st, pending);
+}
+
+cudaError_t launch_page_updates(const PageUpdates& u, int* table, cudaStream_t s) {
+  if (u.n <= 0) return cudaSuccess;
+  return launch_pdl(page_table_update_kernel, dim3(1), dim3(256), 0, s, u, table);
 }
 
 cudaError_t launch_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, int32_t* out, cudaStream_t s) {

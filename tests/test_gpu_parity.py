@@ -226,6 +226,33 @@ def test_gqa_group_layouts(dfl, n_heads, n_kv, blocks):
         assert total > 0
 
 
+def test_mqa_long_context_many_chunks(dfl):
+    """One key/value head (d = 128, two query heads) over a 6000-token
+    context: the attention work is split into 2-unit chunks (94 pages plus the
+    block per row on 152 SMs), so one (sequence, head) row has 48 chunk
+    partials and the combine kernel takes its general path (more than 32
+    chunks, weights recomputed per chunk). A second, short sequence shares the
+    call."""
+    from dataclasses import replace
+    sh = replace(TINY, n_heads=2, n_kv_heads=1, head_dim=128)
+    wn = make_weights_np(sh, seed=71, gamma="jitter", std=0.05)
+    orc = oracle.OracleDrafter(sh, wn)
+    width = sh.n_feat_layers * sh.hidden
+    with dfl.Drafter(sh, np_weights_to_device(wn, DEV), max_seqs=2, max_batch=2, max_block=16, max_ctx=6400,
+                     max_fuse_tokens=2048) as d:
+        for part, n in enumerate((2000, 2000, 1700, 300)):
+            f = make_features_np(n, width, seed=72 + part)
+            d.fuse_ctx([0], [n], bf16_dev(f, DEV), pending=False)
+            orc.fuse_ctx([0], [n], f, pending=False)
+        f = make_features_np(300, width, seed=79)
+        d.fuse_ctx([1], [300], bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx([1], [300], f, pending=False)
+        assert orc.seq_len(0)[0] == 6000
+        anchors = make_anchor_ids_np(2, sh.vocab, seed=80)
+        _, _, c = _draft_and_compare(d, orc, [0, 1], anchors, 16, "MQA C=6000", ROW_REL_HIGH_GAIN)
+        assert c > 0
+
+
 def test_draft_is_bit_reproducible(dfl):
     """Repeated drafts over the same cache give bit-identical ids, logits and
     residual streams: split GEMM tiles are summed in a fixed order, whichever
