@@ -82,6 +82,7 @@ struct GemmArgs {
   int k_blocks, n_tiles, m_tiles;
   long long units;     // tiles * k_blocks
   int grid;            // CTAs (stream-K workers)
+  int csplit;          // 1: CTAs 2t and 2t+1 form a cluster splitting tile t's k-blocks in halves
   float* partial;      // [grid][2][128 * BN] partial tiles
   int* tickets;        // [tiles], zero between launches
   int* status;
@@ -240,7 +241,8 @@ __device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, 
 template <int BN, int EC>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int g,
                                               int tile, int first, int last, uint32_t tb, int r, EpiShared& sh,
-                                              float* stg, uint32_t pre, const float (&rpre)[16]) {
+                                              float* stg, uint32_t pre, const float (&rpre)[16], int cbeg,
+                                              int cend, const float* speer) {
   const int kind = class_kind<EC>(e.kind);
   const int q = r >> 5, lane = r & 31;
   const int tn = tile / a.m_tiles, tm = tile - tn * a.m_tiles;
@@ -304,19 +306,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         rb[c] = 0.f;
       }
     } else {
-      load_resid(a, e, m0, 0, n, ra);
-      load_resid(a, e, m0, 16, n, rb);
+      load_resid(a, e, m0, cbeg, n, ra);
+      load_resid(a, e, m0, cbeg + 16, n, rb);
     }
   }
   if (rope) rot = e.rope[half + fi];
   float pc0[16];
-  if constexpr (BN > 16) partial_load(0, pc0);
+  if constexpr (BN > 16) partial_load(cbeg, pc0);
 #pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += 16) {
+  for (int c0 = cbeg; c0 < cend; c0 += 16) {
     const int buf = (c0 >> 4) & 1;
     float* sb = stg + buf * (128 * 17);
     float rc[16];
-    if (resid && !pre && c0 + 32 < BN) load_resid(a, e, m0, c0 + 32, n, rc);
+    if (resid && !pre && c0 + 32 < cend) load_resid(a, e, m0, c0 + 32, n, rc);
     float rx[16];
     if (resid) {
       if (pre) {
@@ -328,10 +330,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
     }
     float pn0[16];
     if constexpr (BN > 16) {
-      if (c0 + 16 < BN) partial_load(c0 + 16, pn0);
+      if (c0 + 16 < cend) partial_load(c0 + 16, pn0);
     }
     float v[16];
     tmem_ld16(tb + c0, v);
+    if (speer) {   // the cluster peer's half-K sum of these columns, [column - cbeg][row]
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] += speer[(c0 - cbeg + c) * 128 + r];
+    }
     constexpr int kRound = 7;
     if (BN == 16 && first != last && last - first <= kRound) {
       // the other pieces in CTA order: k-th other CTA is first + k, skipping g
@@ -618,6 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t empty[C::kStages];
   __shared__ __align__(8) uint64_t acc_full[2];
   __shared__ __align__(8) uint64_t acc_empty[2];
+  __shared__ __align__(8) uint64_t pair_rdy;   // cluster peer's ring is idle (count 1)
+  __shared__ __align__(8) uint64_t pair_dat;   // cluster peer's half sums have landed here (count 128)
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ EpiShared esh;
@@ -638,6 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);
     }
+    mbar_init(&pair_rdy, 1);
+    mbar_init(&pair_dat, 128);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -649,6 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the cluster peer arrives on this CTA's barriers only after they exist
+  if (a.csplit) cluster_sync_all();
   const uint32_t tmem = tmem_slot;
   grid_dep_launch();
 
@@ -774,6 +786,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // they are fetched while the MMAs run, whether or not this CTA ends up
       // finishing the tile.
       const int tn0 = t / a.m_tiles, m0 = (t - tn0 * a.m_tiles) * BN;
+      // columns (tokens) this CTA finishes: all, or its half of a cluster-split tile
+      const int cbeg = a.csplit ? (g & 1) * (BN / 2) : 0;
+      const int cend = a.csplit ? cbeg + BN / 2 : BN;
       tile_cols_prepare<BN, EC>(a, e, m0, r, esh);
       float rpre[16];
 #pragma unroll
@@ -783,11 +798,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the MMAs run, so the epilogue reads it from TMEM.
       uint32_t pre = 0;
       if constexpr (EC == kEcNorm) {
-        if (e.kind == EPI_RESID && whole && u0 == u && u1 == seg_end) {
+        if (e.kind == EPI_RESID && (whole || a.csplit) && u0 == u && u1 == seg_end) {
           const int n = tn0 * kTileN + r;
           pre = trow + (buf ^ 1) * BN;
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32) {
+          for (int c0 = cbeg; c0 < cend; c0 += 32) {
             float xv[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -813,7 +828,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tb = trow + buf * BN;
       bool finish = whole;
       int first = g, last = g;
-      if (!whole) {
+      const float* speer = nullptr;
+      if (a.csplit) {
+        // Cluster pair: each CTA sends the peer the half-K sums of the
+        // peer's columns, straight into the peer's (idle) operand ring, and
+        // finishes its own columns with the peer's sums added.
+        const uint32_t peer = static_cast<uint32_t>(g & 1) ^ 1u;
+        const int pbeg = static_cast<int>(peer) * (BN / 2);
+        // all of this CTA's MMAs have completed, so its ring is idle
+        if (r == 0) mbar_arrive_remote(mapa_shared(smem_u32(&pair_rdy), peer));
+        bool ok = mbar_wait_cluster(&pair_rdy, 0, &abort_flag);
+        if (ok) {
+          const uint32_t dst = mapa_shared(smem_u32(smem), peer) + static_cast<uint32_t>(r) * 4u;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+            float v[16];
+            tmem_ld16(tb + pbeg + c0, v);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) st_cluster_f32(dst + static_cast<uint32_t>((c0 + c) * 128) * 4u, v[c]);
+          }
+          mbar_arrive_remote(mapa_shared(smem_u32(&pair_dat), peer));
+          ok = mbar_wait_cluster(&pair_dat, 0, &abort_flag);
+        }
+        if (!ok) {
+          abort_flag = 1;
+          latch_status(a.status, kDevTimeout);
+        }
+        epi_bar();
+        if (r == 0) esh.flag = abort_flag;
+        epi_bar();
+        if (esh.flag) break;
+        speer = reinterpret_cast<const float*>(smem);
+        finish = true;
+      } else if (!whole) {
         // park this segment's partial sum in the CTA's slot, then take a ticket
         const int side = (u == u0) ? 0 : 1;
         float* dst = a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems + r;
@@ -837,14 +884,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (finish) __threadfence();
       }
       if (finish) {
-        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre, rpre);
+        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre, rpre, cbeg, cend, speer);
         if constexpr (EC == kEcArgmax) {
           // the CTA that finishes the last tile decodes the winning keys and resets them
           __threadfence();
           epi_bar();
           if (r == 0) {
             const int dn = atomicAdd(e.done, 1);
-            esh.flag = (dn == a.n_tiles * a.m_tiles - 1);
+            esh.flag = (dn == (a.csplit ? 2 : 1) * a.n_tiles * a.m_tiles - 1);
           }
           epi_bar();
           if (esh.flag) {
@@ -878,6 +925,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  // no CTA leaves while its cluster peer may still write into its shared memory
+  if (a.csplit) cluster_sync_all();
 }
 
 template <int BN, int EC>
@@ -890,6 +939,9 @@ cudaError_t launch_bn(const AMaps& amaps, const ARegions& rg, const CUtensorMap&
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
+  if (a.csplit)
+    return launch_pdl_cluster(gemm_kernel<BN, EC>, dim3(a.grid), dim3(kThreads), C::kSmem, 2, stream, amaps, xmap, a,
+                              rg, e);
   return launch_pdl(gemm_kernel<BN, EC>, dim3(a.grid), dim3(kThreads), C::kSmem, stream, amaps, xmap, a, rg, e);
 }
 

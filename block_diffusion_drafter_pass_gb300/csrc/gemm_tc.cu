@@ -12,9 +12,14 @@ int gemm_token_tile(int M, int N, int num_sms) {
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128) return 128;
+  const long long nt = (N + kTileN - 1) / kTileN;
+  // 256-token tiles split over K between the two CTAs of a cluster whenever
+  // two CTAs per tile fit in one wave: an MMA instruction of a 256-token tile
+  // does twice the work of a 128-token one at the same issue cost, and the
+  // split keeps the CTA count of 128-token tiles.
+  if (2 * nt * ((M + 255) / 256) <= num_sms) return 256;
   // 256-token tiles, unless 128-token tiles keep clearly more SMs busy (a
   // tile count well under one wave)
-  const long long nt = (N + kTileN - 1) / kTileN;
   auto busy = [&](int bn) {
     const long long t = nt * ((M + bn - 1) / bn);
     const long long waves = (t + num_sms - 1) / num_sms;
@@ -23,10 +28,19 @@ int gemm_token_tile(int M, int N, int num_sms) {
   return busy(128) > busy(256) + 0.05 ? 128 : 256;
 }
 
+bool gemm_cluster_split(int M, int N, int K, int splits, int num_sms) {
+  if (splits != 0 || gemm_token_tile(M, N, num_sms) != 256) return false;
+  const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + 255) / 256);
+  return 2 * tiles <= num_sms && (K + kTileK - 1) / kTileK >= 2;
+}
+
 int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms) {
   const int BN = gemm_token_tile(M, N, num_sms);
   const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + BN - 1) / BN);
   const int kb = (K + kTileK - 1) / kTileK;
+  // one cluster of two CTAs per tile, each with half of the k-blocks: the
+  // stream-K partition of 2 x tiles CTAs is exactly that split
+  if (gemm_cluster_split(M, N, K, splits, num_sms)) return static_cast<int>(2 * tiles);
   const long long units = tiles * kb;
   long long G = splits > 0 ? tiles * std::min(splits, kb) : num_sms;
   // Tensor-bound tiles (BN >= 128) that fit in one wave: one whole tile per
@@ -60,6 +74,10 @@ cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUten
   a.m_tiles = (M + BN - 1) / BN;
   a.units = static_cast<long long>(a.n_tiles) * a.m_tiles * a.k_blocks;
   a.grid = gemm_grid(M, N, K, splits, work.partial_elems, num_sms);
+  a.csplit = gemm_cluster_split(M, N, K, splits, num_sms) ? 1 : 0;
+  // the pair exchange addresses a 128 x 128 float block of the peer's ring
+  // (BN = 256) and pairs CTAs 2t, 2t + 1
+  if (a.csplit && (BN != 256 || a.grid != 2 * a.n_tiles * a.m_tiles)) return cudaErrorInvalidValue;
   a.status = epi.status;
   a.partial = work.partial;
   a.tickets = work.tickets;

@@ -27,6 +27,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// The same, as clusters of `cluster_x` CTAs along x (the grid a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, unsigned cluster_x,
+                               cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 constexpr int kPage = 64;          // tokens per KV page
 constexpr int kMaxBatch = 64;      // sequences per call
 constexpr int kMaxBlock = 32;      // block size B
@@ -145,6 +166,8 @@ int gemm_token_tile(int M, int N, int num_sms);
 // CTAs the GEMM runs with: num_sms stream-K workers (splits = 0) or
 // tiles * splits, reduced until 2 partial tiles per CTA fit partial_elems.
 int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms);
+// True when each 256-token tile is split over K between the two CTAs of a cluster.
+bool gemm_cluster_split(int M, int N, int K, int splits, int num_sms);
 
 // Row-major [rows, cols] bf16 TMA descriptor (box 64 x box_rows, 128B swizzle).
 bool encode_matrix_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);

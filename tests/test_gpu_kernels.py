@@ -32,6 +32,10 @@ DEV = "cuda:0"
     (1024, 300, 512, 1),      # two 256-token tiles with a ragged tail
     (640, 64, 2048, 3),       # explicit split-K
     (256, 128, 128, 2),
+    (2048, 512, 1024, 0),     # 256-token tiles split over K by 2-CTA clusters
+    (1024, 300, 512, 0),      # the same with a ragged token tail
+    (512, 272, 960, 0),       # odd k-block count (15 = 7 + 8)
+    (384, 200, 64, 0),        # one k-block: 256-token tile, no split
 ])
 def test_gemm_matches_fp32_matmul(dfl, N, M, K, splits):
     g = torch.Generator(device="cpu").manual_seed(N * 7 + M * 3 + K)

@@ -226,6 +226,71 @@ def test_gqa_group_layouts(dfl, n_heads, n_kv, blocks):
         assert total > 0
 
 
+def test_tiny_batch16_cluster_split(dfl):
+    """16 sequences x B = 16 (256 block tokens) and a 256-row fuse: every
+    projection (fuse, QKV with RoPE, O and down with the residual, gate/up
+    with SwiGLU, LM head with argmax) runs 256-token tiles split over K by
+    two-CTA clusters that exchange half sums through distributed shared
+    memory."""
+    sh = TINY
+    wn = make_weights_np(sh, seed=81, gamma="jitter", std=0.05)
+    orc = oracle.OracleDrafter(sh, wn)
+    width = sh.n_feat_layers * sh.hidden
+    n = 16
+    with dfl.Drafter(sh, np_weights_to_device(wn, DEV), max_seqs=n, max_batch=n, max_block=16, max_ctx=1024,
+                     max_fuse_tokens=512) as d:
+        rng = np.random.default_rng(82)
+        lens = rng.integers(1, 300, size=n)
+        for s in range(n):
+            f = make_features_np(int(lens[s]), width, seed=83 + s)
+            d.fuse_ctx([s], [int(lens[s])], bf16_dev(f, DEV), pending=False)
+            orc.fuse_ctx([s], [int(lens[s])], f, pending=False)
+        # one fuse call of 16 rows per sequence: M = 256
+        f = make_features_np(16 * n, width, seed=99)
+        d.fuse_ctx(list(range(n)), [16] * n, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(list(range(n)), [16] * n, f, pending=False)
+        d.sync()
+        _check_kv(d, orc, range(n), range(sh.n_layers), "tiny 256-row fuse", ROW_REL_HIGH_GAIN)
+        anchors = make_anchor_ids_np(n, sh.vocab, seed=100)
+        total = 0
+        for B in (16, 8):
+            _, _, c = _draft_and_compare(d, orc, list(range(n)), anchors, B, f"tiny batch {n} B={B}",
+                                         ROW_REL_HIGH_GAIN)
+            total += c
+        assert total > 0
+
+
+def test_qwen3_8b_batch16_two_layers(dfl):
+    """8B width, 2 layers, 16 sequences x B = 16 = 256 block tokens: QKV, O
+    and down run 256-token tiles split over K by two-CTA clusters at full
+    width (fuse of 256 rows too); gate/up and the LM head stay stream-K."""
+    shape, wt, wn = _big_setup(2, seed=91)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    width = shape.n_feat_layers * shape.hidden
+    n = 16
+    with dfl.Drafter(shape, wt, max_seqs=n, max_batch=n, max_block=16, max_ctx=512,
+                     max_fuse_tokens=4096) as d:
+        rng = np.random.default_rng(92)
+        lens = [int(x) for x in rng.integers(16, 240, size=n)]
+        f = make_features_np(sum(lens), width, seed=93)
+        d.fuse_ctx(list(range(n)), lens, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(list(range(n)), lens, f, pending=False)
+        f = make_features_np(16 * n, width, seed=94)
+        d.fuse_ctx(list(range(n)), [16] * n, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(list(range(n)), [16] * n, f, pending=False)
+        d.sync()
+        for s in (0, 7, 15):
+            m = orc.seq_len(s)[0]
+            for l in range(2):
+                k, v = d.read_kv(l, s, 0, m)
+                kr, vr = orc.context(s, l)
+                assert_close(k, kr, f"8B batch {n} K layer {l} seq {s}")
+                assert_close(v, vr, f"8B batch {n} V layer {l} seq {s}")
+        anchors = make_anchor_ids_np(n, shape.vocab, seed=95)
+        _, _, checked = _draft_and_compare(d, orc, list(range(n)), anchors, 16, f"8B 2-layer batch {n}")
+        assert checked > 0
+
+
 def test_mqa_long_context_many_chunks(dfl):
     """One key/value head (d = 128, two query heads) over a 6000-token
     context: the attention work is split into 2-unit chunks (94 pages plus the
