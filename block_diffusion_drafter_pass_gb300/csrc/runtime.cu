@@ -125,6 +125,7 @@ struct dflash_ctx {
   std::vector<std::vector<int>> pages;
   std::vector<int> len_ub, pend, added_since;
   int* h_snap = nullptr;      // pinned copy of d_len
+  std::vector<double> deal_load;   // scratch of the attention work split
   std::unique_ptr<PageUpdates> page_upd{new PageUpdates()};   // staging of one append's new pages
   cudaEvent_t snap_event = nullptr;
   bool snap_pending = false;
@@ -703,18 +704,52 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   // attention work split from the host's length bounds
   long long tiles_ub = 0;
   for (int i = 0; i < n_seq; ++i) tiles_ub += 1LL * nkv * (ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1);
-  // one wave of resident attention CTAs, each with about one chunk of tiles
+  // One wave of resident attention CTAs; item i goes to CTA i mod grid. The
+  // chunk size (even: the kernel consumes units in pairs) is the candidate,
+  // from about one to eight chunks per CTA, whose deal has the smallest
+  // estimated makespan under the host's length bounds, an item costing its
+  // units plus kItemOverhead (query load, pipeline fill and drain, partial
+  // write). Equal-length rows (batch 1) keep one chunk per CTA; rows of mixed
+  // lengths get several smaller chunks, so no CTA draws two long rows.
   int& per_sm = ctx->attn_ctas_per_sm;
   if (per_sm == 0) per_sm = attention_ctas_per_sm(d);
   const int grid_full = per_sm * ctx->num_sms;
-  int chunk = std::max(2, ceil_div(tiles_ub, grid_full));
   auto items_for = [&](int ch) {
     long long it = 0;
     for (int i = 0; i < n_seq; ++i) it += 1LL * nkv * ceil_div(ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1, ch);
     return it;
   };
-  chunk += chunk & 1;   // items start at even units: the kernel consumes units in pairs
-  while (items_for(chunk) > ctx->items_cap) chunk *= 2;
+  constexpr double kItemOverhead = 3.0;
+  auto makespan = [&](int ch) {
+    const long long items = items_for(ch);
+    const int grid = static_cast<int>(std::min<long long>(items, grid_full));
+    std::vector<double>& load = ctx->deal_load;
+    load.assign(grid, 0.0);
+    long long k = 0;
+    for (int i = 0; i < n_seq; ++i) {
+      const int units = ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1;
+      for (int h = 0; h < nkv; ++h)
+        for (int tb = 0; tb < units; tb += ch, ++k) load[k % grid] += std::min(ch, units - tb) + kItemOverhead;
+    }
+    return *std::max_element(load.begin(), load.end());
+  };
+  int chunk = 0;
+  double best = 0.0;
+  for (int per_cta = 1; per_cta <= 8; ++per_cta) {
+    int ch = std::max(2, ceil_div(tiles_ub, static_cast<long long>(per_cta) * grid_full));
+    ch += ch & 1;
+    if (ch == chunk || items_for(ch) > ctx->items_cap) continue;
+    const double ms = makespan(ch);
+    if (chunk == 0 || ms < best) {
+      chunk = ch;
+      best = ms;
+    }
+  }
+  if (chunk == 0) {   // even one chunk per CTA exceeds the partial buffers: longer chunks
+    chunk = std::max(2, ceil_div(tiles_ub, grid_full));
+    chunk += chunk & 1;
+    while (items_for(chunk) > ctx->items_cap) chunk *= 2;
+  }
   const int attn_grid = static_cast<int>(std::min<long long>(items_for(chunk), grid_full));
 
   const int Bb = attention_block_rows(B);
