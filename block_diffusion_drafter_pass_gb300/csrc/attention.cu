@@ -768,12 +768,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // sum, then read each chunk's partial row as one coalesced 16-byte-per-lane
 // load (D = 128) and accumulate it with its weight exp2(m_c - M).
 constexpr int kCombineWarps = 4;
-constexpr int kCombineMaxChunks = 2048;
 
-template <int D>
+// NC: chunk count up to which a row's partials are all loaded at once (the
+// host's bound on the chunks per row picks the instantiation, so short rows
+// do not pay registers, and occupancy, for 32 chunks); rows with more chunks
+// take the general path.
+template <int D, int NC>
 __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int kPer = D / 32;                 // dims per lane: 4 (D = 128) or 2 (D = 64)
-  __shared__ float wsm[kCombineWarps][kCombineMaxChunks];
+  static_assert(NC >= 1 && NC <= 32, "one chunk per lane at most");
   grid_dep_wait();
   grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -786,22 +789,22 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
   for (int s = 0; s < i; ++s) base += nkv * seq_split(a, s).n_chunks;
   const int nch = seq_split(a, i).n_chunks;
   base += kvh * nch;
-  if (j >= B || base + nch > a.items_cap || nch > kCombineMaxChunks) {
+  if (j >= B || base + nch > a.items_cap) {
     if (j < B && lane == 0) latch_status(a.status, kDevBounds);
     return;
   }
   const int r = j * G + gh;
   const size_t rp = static_cast<size_t>(a.rows_pad);
   uint16_t* out = a.out + static_cast<size_t>(i * B + j) * a.n_q_heads * D + static_cast<size_t>(hq) * D + lane * kPer;
-  if (nch <= 32) {
+  if (nch <= NC) {
     // Every chunk in flight at once: lane c holds chunk c's (max, sum), and
     // every lane loads its dims of all partial rows before the weights are
     // known, so the merge costs about one memory latency.
     const float2 ml = lane < nch ? __ldcg(a.part_ml + (base + lane) * rp + r) : make_float2(-INFINITY, 0.f);
     const float* po = a.part_o + (static_cast<size_t>(base) * rp + r) * D + lane * kPer;
-    float v[32][kPer];
+    float v[NC][kPer];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
+    for (int c = 0; c < NC; ++c) {
       if (c < nch) {
         if constexpr (kPer == 4) {
           const float4 t = __ldcg(reinterpret_cast<const float4*>(po + c * rp * D));
@@ -826,7 +829,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
+    for (int c = 0; c < NC; ++c) {
       const float wc = __shfl_sync(0xffffffffu, w, c);
 #pragma unroll
       for (int e = 0; e < kPer; ++e) acc[e] += wc * v[c][e];
@@ -843,13 +846,13 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
   float L = 0.f;
   for (int c = lane; c < nch; c += 32) {
     const float2 ml = a.part_ml[(base + c) * rp + r];
-    const float w = exp2f(ml.x - M);
-    wsm[warp][c] = w;
-    L += w * ml.y;
+    L += exp2f(ml.x - M) * ml.y;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  __syncwarp();
+  // chunk weights are recomputed from (max, sum) where they are used: one
+  // broadcast load each
+  const float* pm = &a.part_ml[static_cast<size_t>(base) * rp + r].x;
   float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
@@ -857,7 +860,9 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
   const size_t stride = rp * D;
   int c = 0;
   for (; c + 4 <= nch; c += 4) {
-    float v[4][kPer];
+    float v[4][kPer], wv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) wv[u] = exp2f(pm[(c + u) * 2 * rp] - M);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if constexpr (kPer == 4) {
@@ -871,11 +876,13 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
 #pragma unroll
     for (int u = 0; u < 4; ++u)
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) acc[e] += wsm[warp][c + u] * v[u][e];
+      for (int e = 0; e < kPer; ++e) acc[e] += wv[u] * v[u][e];
   }
-  for (; c < nch; ++c)
+  for (; c < nch; ++c) {
+    const float wc = exp2f(pm[c * 2 * rp] - M);
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] += wsm[warp][c] * __ldcg(po + c * stride + e);
+    for (int e = 0; e < kPer; ++e) acc[e] += wc * __ldcg(po + c * stride + e);
+  }
   const float inv = 1.f / L;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) out[e] = f32_to_bf16(acc[e] * inv);
@@ -898,9 +905,11 @@ template <int D>
 cudaError_t launch_d(const AttnMaps& maps, const AttnArgs& a, int grid, int part, cudaStream_t stream) {
   if (part == 0)
     return a.spread ? launch_main<D, true>(maps, a, grid, stream) : launch_main<D, false>(maps, a, grid, stream);
-  return launch_pdl(attn_combine_kernel<D>,
-                    dim3(a.n_q_heads, a.meta.n_seq, (a.meta.B + kCombineWarps - 1) / kCombineWarps),
-                    dim3(32 * kCombineWarps), 0, stream, a);
+  const dim3 grid_c(a.n_q_heads, a.meta.n_seq, (a.meta.B + kCombineWarps - 1) / kCombineWarps);
+  const dim3 block_c(32 * kCombineWarps);
+  if (a.max_chunks <= 8) return launch_pdl(attn_combine_kernel<D, 8>, grid_c, block_c, 0, stream, a);
+  if (a.max_chunks <= 16) return launch_pdl(attn_combine_kernel<D, 16>, grid_c, block_c, 0, stream, a);
+  return launch_pdl(attn_combine_kernel<D, 32>, grid_c, block_c, 0, stream, a);
 }
 
 }  // namespace

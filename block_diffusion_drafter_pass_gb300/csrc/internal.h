@@ -185,6 +185,7 @@ struct AttnArgs {
   int pool_pages;
   int chunk_tiles;           // context chunk in 64-key tiles
   int items_cap;             // partial-buffer capacity in work items
+  int max_chunks;            // host bound on the chunks of one (sequence, kv head) row
   int rows_pad;              // row stride of the partial buffers (>= G*B)
   int spread;                // 1: G*B <= 64, query rows spread 16 per TMEM lane quarter
   const uint16_t* q;         // [n_seq*B][n_q*d] bf16 (RoPE applied)

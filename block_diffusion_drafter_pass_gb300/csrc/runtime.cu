@@ -751,6 +751,9 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
     while (items_for(chunk) > ctx->items_cap) chunk *= 2;
   }
   const int attn_grid = static_cast<int>(std::min<long long>(items_for(chunk), grid_full));
+  int max_chunks = 1;
+  for (int i = 0; i < n_seq; ++i)
+    max_chunks = std::max(max_chunks, ceil_div(ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1, chunk));
 
   const int Bb = attention_block_rows(B);
   const CUtensorMap* km = blk_map(ctx, ctx->kb, M, Bb);
@@ -815,6 +818,7 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       a.head_dim = d;
       a.pool_pages = c.max_pages;
       a.chunk_tiles = chunk;
+      a.max_chunks = max_chunks;
       a.items_cap = ctx->items_cap;
       a.rows_pad = 16 * ceil_div((nq / nkv) * B, 16);
       a.spread = (nq / nkv) * B <= 64;
