@@ -132,92 +132,172 @@ __global__ void page_table_update_kernel(const __grid_constant__ PageUpdates u, 
 
 // Row argmax of bf16 logits, lowest index on ties: the per-thread best is kept
 // as a 64-bit key (ordered value << 32 | ~index) so one max picks both.
-// Each row is split over a cluster of kArgCluster CTAs; their partial keys
-// meet in the first CTA's shared memory (distributed shared memory), so no
-// global scratch is needed.
-constexpr int kArgCluster = 8;
-constexpr int kArgThreads = 512;
+//
+// Each CTA reduces one segment of one row. A row is split over a cluster of
+// KC CTAs (KC = 1 when there are enough rows to fill the GPU); their partial
+// keys meet in the first CTA's shared memory (distributed shared memory), so
+// no global scratch is needed. When rows are 16-byte aligned (cols % 8 == 0)
+// the segment streams through a ring of kAmStages bulk copies of kAmChunk
+// columns, so a CTA keeps 64 KB in flight with few registers and the GPU's
+// CTA scheduler balances whole rows over the SMs; otherwise threads read the
+// segment directly.
+constexpr int kAmThreads = 512;
+constexpr int kAmWarps = kAmThreads / 32;
+constexpr int kAmChunk = 8192;   // columns per ring stage (16 KB)
+constexpr int kAmStages = 4;
 
 __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
   return (static_cast<unsigned long long>(ordered_key(v)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx));
 }
 
-__global__ void __cluster_dims__(1, kArgCluster, 1) __launch_bounds__(kArgThreads)
-    rows_argmax_bf16_kernel(const uint16_t* __restrict__ logits, int cols, int32_t* __restrict__ out, int vec_ok) {
-  __shared__ unsigned long long red[kArgThreads / 32];
+__device__ __forceinline__ unsigned long long max_key(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+// Key of a (value, column) candidate: larger values first, then lower
+// columns; -0 and +0 are one value (as a float comparison sees them).
+__device__ __forceinline__ unsigned long long cand_key(float v, int idx) {
+  return idx < 0 ? 0ull : argmax_key(v == 0.f ? 0.f : v, idx);
+}
+
+template <int KC>
+__global__ void __launch_bounds__(kAmThreads)
+    rows_argmax_bf16_kernel(const uint16_t* __restrict__ logits, int cols, int32_t* __restrict__ out, int* status,
+                            int ring) {
+  extern __shared__ __align__(128) uint8_t am_ring[];   // kAmStages x kAmChunk bf16 (ring mode)
+  __shared__ __align__(8) uint64_t full[kAmStages], empty[kAmStages];
+  __shared__ unsigned long long red[kAmWarps];
   __shared__ unsigned long long cta_best;
-  cg::cluster_group cluster = cg::this_cluster();
-  grid_dep_wait();
-  grid_dep_launch();
-  const int row = blockIdx.x;
-  const int seg = static_cast<int>(cluster.block_rank());
-  const int per = ((cols + kArgCluster * 8 - 1) / (kArgCluster * 8)) * 8;   // multiple of 8 columns
+  __shared__ volatile int abort_flag;
+  const int seg = static_cast<int>(blockIdx.x % KC), row = static_cast<int>(blockIdx.x / KC);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = ((cols + KC * 8 - 1) / (KC * 8)) * 8;   // multiple of 8 columns
   const int c_lo = min(cols, seg * per), c_hi = min(cols, c_lo + per);
   const uint16_t* p = logits + static_cast<size_t>(row) * cols;
-  unsigned long long best = 0ull;
-  if (vec_ok) {
-    const uint4* pv = reinterpret_cast<const uint4*>(p + c_lo);
-    const int nvec = (c_hi - c_lo) >> 3;
-    int vi = threadIdx.x;
-    for (; vi + 3 * kArgThreads < nvec; vi += 4 * kArgThreads) {
-      uint4 w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) w[u] = __ldcs(pv + vi + u * kArgThreads);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-        const int base = c_lo + (vi + u * kArgThreads) * 8;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const unsigned long long k0 = argmax_key(__uint_as_float(ws[q] << 16), base + 2 * q);
-          const unsigned long long k1 = argmax_key(__uint_as_float(ws[q] & 0xFFFF0000u), base + 2 * q + 1);
-          best = k0 > best ? k0 : best;
-          best = k1 > best ? k1 : best;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAmStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kAmWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  grid_dep_launch();   // dependents read the result only after their own wait
+  grid_dep_wait();
+  unsigned long long b = 0ull;
+  if (ring) {
+    // This thread's running (value, first column): a vector's maximum comes
+    // from packed bf16 pairs, and only a vector that beats the running value
+    // is searched for the first column holding its maximum.
+    float bv = -INFINITY;
+    int bi = -1;
+    const int n = (c_hi - c_lo + kAmChunk - 1) / kAmChunk;   // chunks of this segment
+    auto issue = [&](int k) {
+      const int s = k % kAmStages;
+      const int c0 = c_lo + k * kAmChunk, len = min(kAmChunk, c_hi - c0);
+      mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(len) * 2u);
+      bulk_load(am_ring + static_cast<size_t>(s) * kAmChunk * 2, p + c0, static_cast<uint32_t>(len) * 2u, &full[s]);
+    };
+    int issued = 0;   // thread 0's count of copies issued
+    if (threadIdx.x == 0)
+      for (; issued < n && issued < kAmStages; ++issued) issue(issued);
+    for (int k = 0; k < n; ++k) {
+      const int s = k % kAmStages;
+      if (!mbar_wait(&full[s], (k / kAmStages) & 1, &abort_flag)) {
+        abort_flag = 1;
+        latch_status(status, kDevTimeout);
+        break;
+      }
+      const int c0 = c_lo + k * kAmChunk, len = min(kAmChunk, c_hi - c0);
+      const uint4* sv = reinterpret_cast<const uint4*>(am_ring + static_cast<size_t>(s) * kAmChunk * 2);
+      for (int v = threadIdx.x; v < (len >> 3); v += kAmThreads) {
+        const uint4 w = sv[v];
+        const __nv_bfloat162 m2 =
+            __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.x), *reinterpret_cast<const __nv_bfloat162*>(&w.y)),
+                    __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.z), *reinterpret_cast<const __nv_bfloat162*>(&w.w)));
+        const float m = fmaxf(__low2float(m2), __high2float(m2));
+        if (m > bv || bi < 0) {
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          int q = 0;
+          for (; q < 8; ++q) {
+            const uint32_t h = (q & 1) ? (ws[q >> 1] & 0xFFFF0000u) : (ws[q >> 1] << 16);
+            if (__uint_as_float(h) == m) break;
+          }
+          bi = c0 + v * 8 + (q < 8 ? q : 0);
+          bv = m;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (threadIdx.x == 0 && k + kAmStages < n) {
+        // every warp has read this stage: refill it
+        if (!mbar_wait(&empty[s], (k / kAmStages) & 1, &abort_flag)) {
+          abort_flag = 1;
+          latch_status(status, kDevTimeout);
+        } else {
+          issue(k + kAmStages);
+          ++issued;
         }
       }
     }
-    for (; vi < nvec; vi += kArgThreads) {
-      const uint4 w = __ldcs(pv + vi);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const unsigned long long k0 = argmax_key(__uint_as_float(ws[q] << 16), c_lo + vi * 8 + 2 * q);
-        const unsigned long long k1 = argmax_key(__uint_as_float(ws[q] & 0xFFFF0000u), c_lo + vi * 8 + 2 * q + 1);
-        best = k0 > best ? k0 : best;
-        best = k1 > best ? k1 : best;
-      }
-    }
-    for (int c = c_lo + (nvec << 3) + threadIdx.x; c < c_hi; c += kArgThreads) {
-      const unsigned long long k = argmax_key(bf16_to_f32(p[c]), c);
-      best = k > best ? k : best;
+    b = cand_key(bv, bi);
+    if (threadIdx.x == 0 && abort_flag) {
+      // copies still in flight land before shared memory is released
+      for (int k = max(0, issued - kAmStages); k < issued; ++k) mbar_wait(&full[k % kAmStages], (k / kAmStages) & 1);
     }
   } else {
-    for (int c = c_lo + threadIdx.x; c < c_hi; c += kArgThreads) {
-      const unsigned long long k = argmax_key(bf16_to_f32(p[c]), c);
-      best = k > best ? k : best;
+    float bv = -INFINITY;
+    int bi = -1;
+    for (int c = c_lo + threadIdx.x; c < c_hi; c += kAmThreads) {
+      const float v = bf16_to_f32(p[c]);
+      if (v > bv || bi < 0) {
+        bv = v;
+        bi = c;
+      }
     }
+    b = cand_key(bv, bi);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
-    best = t > best ? t : best;
-  }
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+  for (int o = 16; o > 0; o >>= 1) b = max_key(b, __shfl_xor_sync(0xffffffffu, b, o));
+  if (lane == 0) red[warp] = b;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kArgThreads / 32; ++w) best = red[w] > best ? red[w] : best;
-    cta_best = best;
+    for (int w = 1; w < kAmWarps; ++w) b = max_key(b, red[w]);
+    cta_best = abort_flag ? 0xFFFFFFFF00000000ull : b;   // a segment that gave up marks the row: id -1
   }
-  cluster.sync();
-  if (seg == 0 && threadIdx.x == 0) {
-    unsigned long long b = 0ull;
-    for (int r = 0; r < kArgCluster; ++r) {
-      const unsigned long long k = *cluster.map_shared_rank(&cta_best, r);
-      b = k > b ? k : b;
+  if constexpr (KC == 1) {
+    if (threadIdx.x == 0)
+      out[row] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(cta_best & 0xFFFFFFFFull));
+  } else {
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (seg == 0 && threadIdx.x == 0) {
+      unsigned long long k = 0ull;
+      for (int r = 0; r < KC; ++r) k = max_key(k, *cluster.map_shared_rank(&cta_best, r));
+      out[row] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
     }
-    out[row] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(b & 0xFFFFFFFFull));
+    cluster.sync();   // keep every CTA's shared memory alive until the first one has read it
   }
-  cluster.sync();   // keep every CTA's shared memory alive until the first one has read it
+}
+
+template <int KC>
+cudaError_t launch_argmax_kc(const uint16_t* logits, int rows, int cols, int32_t* out, int* status, int ring,
+                             cudaStream_t s) {
+  const size_t smem = ring ? static_cast<size_t>(kAmStages) * kAmChunk * 2 : 0;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(rows_argmax_bf16_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kAmStages * kAmChunk * 2));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if constexpr (KC == 1)
+    return launch_pdl(rows_argmax_bf16_kernel<KC>, dim3(rows), dim3(kAmThreads), smem, s, logits, cols, out, status,
+                      ring);
+  else
+    return launch_pdl_cluster(rows_argmax_bf16_kernel<KC>, dim3(rows * KC), dim3(kAmThreads), smem, KC, s, logits,
+                              cols, out, status, ring);
 }
 
 }  // namespace
@@ -249,10 +329,14 @@ cudaError_t launch_page_updates(const PageUpdates& u, int* table, cudaStream_t s
 }
 
 cudaError_t launch_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, int32_t* out, cudaStream_t s) {
+  int* status = nullptr;   // no context: a row whose wait gave up reads -1 instead
   if (rows == 0) return cudaSuccess;
-  const int vec_ok = (cols % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
-  return launch_pdl(rows_argmax_bf16_kernel, dim3(rows, kArgCluster), dim3(kArgThreads), 0, s, logits, cols, out,
-                    vec_ok);
+  const int ring = (cols % 8 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
+  // CTAs per row: enough CTAs to cover the SMs a few times over
+  if (rows >= 256) return launch_argmax_kc<1>(logits, rows, cols, out, status, ring, s);
+  if (rows >= 128) return launch_argmax_kc<2>(logits, rows, cols, out, status, ring, s);
+  if (rows >= 64) return launch_argmax_kc<4>(logits, rows, cols, out, status, ring, s);
+  return launch_argmax_kc<8>(logits, rows, cols, out, status, ring, s);
 }
 
 }  // namespace dfl

@@ -69,6 +69,40 @@ def test_rows_argmax_ties_and_ragged(dfl, cols):
     np.testing.assert_array_equal(got, ref)
 
 
+@pytest.mark.parametrize("rows", [100, 131, 300, 1029])
+@pytest.mark.parametrize("cols", [4096, 4099, 20008])
+def test_rows_argmax_split_and_ring(dfl, rows, cols):
+    """Row counts that split a row over clusters of 4 and 2 CTAs or give each
+    row one CTA, on the bulk-copy ring (cols % 8 == 0, several 8192-column
+    stages and a short last one) and the direct path (cols % 8 != 0)."""
+    rng = np.random.Generator(np.random.PCG64(rows * 10 + cols))
+    vals = np.round(rng.standard_normal((rows, cols)) * 3).astype(np.float32)
+    from synth import bf16_bits
+    bits = bf16_bits(vals)
+    ref = oracle.rows_argmax(bits_to_f32(bits))
+    logits = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    got = dfl.dflash_rows_argmax_bf16(logits).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_rows_argmax_signed_zero_is_one_value(dfl):
+    """-0 and +0 compare equal: a row whose maximum is zero takes the first
+    zero, whichever sign it has (a float comparison, as the oracle's)."""
+    cols = 20008   # three ring stages
+    from synth import bf16_bits
+    vals = -np.ones((4, cols), dtype=np.float32)
+    vals[0, 100], vals[0, 9000] = 0.0, -0.0
+    vals[1, 100], vals[1, 9000] = -0.0, 0.0
+    vals[2, 9000], vals[2, 9001] = -0.0, 0.0
+    vals[3, 5], vals[3, 20007] = 0.0, 1.0
+    bits = bf16_bits(vals)
+    ref = oracle.rows_argmax(bits_to_f32(bits))
+    np.testing.assert_array_equal(ref, [100, 100, 9000, 20007])
+    logits = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    got = dfl.dflash_rows_argmax_bf16(logits).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
 def _tiny_drafter(dfl, max_batch=64, max_block=16, max_ctx=256, max_pages=None):
     wn = make_weights_np(TINY, seed=3)
     d = dfl.Drafter(TINY, np_weights_to_device(wn, DEV), max_seqs=max_batch, max_batch=max_batch,
