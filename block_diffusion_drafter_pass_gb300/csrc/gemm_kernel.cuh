@@ -83,6 +83,7 @@ struct GemmArgs {
   long long units;     // tiles * k_blocks
   int grid;            // CTAs (stream-K workers)
   int csplit;          // 1: CTAs 2t and 2t+1 form a cluster splitting tile t's k-blocks in halves
+  int pair;            // 1: CTA pairs run cta_group::2 MMAs over whole 256 x 256 pair tiles
   float* partial;      // [grid][2][128 * BN] partial tiles
   int* tickets;        // [tiles], zero between launches
   int* status;
@@ -209,6 +210,36 @@ __device__ __forceinline__ void tmem_wait_st_gk() { asm volatile("tcgen05.wait::
 
 // Residual inputs of one 16-column chunk (EPI_RESID); the chunk loop keeps
 // them two chunks ahead of use.
+// LM head: after a tile's epilogue, the CTA that finishes the last of
+// `total` tile epilogues decodes the winning keys into ids (and logits) and
+// resets them for the next call.
+__device__ __forceinline__ void argmax_tile_done(const GemmArgs& a, const GemmEpi& e, EpiShared& esh, int r,
+                                                 int total) {
+  __threadfence();
+  epi_bar();
+  if (r == 0) {
+    const int dn = atomicAdd(e.done, 1);
+    esh.flag = (dn == total - 1);
+  }
+  epi_bar();
+  if (esh.flag) {
+    __threadfence();
+    const int sb = e.argmax_skip_B;
+    for (int m = r; m < a.M; m += 128) {
+      if (sb > 0 && m % sb == 0) continue;
+      const int o = sb > 0 ? (m / sb) * (sb - 1) + (m % sb) - 1 : m;
+      const unsigned long long k = atomicExch(e.keys + m, 0ull);
+      e.out_ids[o] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+      if (e.out_logit) {
+        const float raw = ordered_key_inv(static_cast<uint32_t>(k >> 32));
+        e.out_logit[o] = e.in_ss ? raw * norm_scale(e, m) : raw;
+      }
+    }
+    if (r == 0) *e.done = 0;
+  }
+  epi_bar();
+}
+
 // Stream-K partition: CTA g owns the contiguous range of (tile, k-block)
 // units [unit_begin(g), unit_begin(g + 1)); tiles are ordered so that the m
 // tiles of one weight tile are consecutive (weights reused from L2).
@@ -479,8 +510,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         for (int i = 0; i < 16; ++i) {
           const int row = gq * 16 + i;
           const uint32_t idx = static_cast<uint32_t>(tn * kTileN + row);
-          const unsigned long long cand =
-              (static_cast<unsigned long long>(ordered_key(sb[row * 17 + cc])) << 32) | (0xFFFFFFFFu - idx);
+          const float lv = sb[row * 17 + cc];
+          const unsigned long long cand =   // -0 and +0 are one value, as in a float argmax
+              (static_cast<unsigned long long>(ordered_key(lv == 0.f ? 0.f : lv)) << 32) | (0xFFFFFFFFu - idx);
           best = (static_cast<int>(idx) < a.N && cand > best) ? cand : best;
         }
       }
@@ -885,32 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (finish) {
         epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre, rpre, cbeg, cend, speer);
-        if constexpr (EC == kEcArgmax) {
-          // the CTA that finishes the last tile decodes the winning keys and resets them
-          __threadfence();
-          epi_bar();
-          if (r == 0) {
-            const int dn = atomicAdd(e.done, 1);
-            esh.flag = (dn == (a.csplit ? 2 : 1) * a.n_tiles * a.m_tiles - 1);
-          }
-          epi_bar();
-          if (esh.flag) {
-            __threadfence();
-            const int sb = e.argmax_skip_B;
-            for (int m = r; m < a.M; m += 128) {
-              if (sb > 0 && m % sb == 0) continue;
-              const int o = sb > 0 ? (m / sb) * (sb - 1) + (m % sb) - 1 : m;
-              const unsigned long long k = atomicExch(e.keys + m, 0ull);
-              e.out_ids[o] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
-              if (e.out_logit) {
-                const float raw = ordered_key_inv(static_cast<uint32_t>(k >> 32));
-                e.out_logit[o] = e.in_ss ? raw * norm_scale(e, m) : raw;
-              }
-            }
-            if (r == 0) *e.done = 0;
-          }
-          epi_bar();
-        }
+        if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, (a.csplit ? 2 : 1) * a.n_tiles * a.m_tiles);
       }
       // hand the TMEM buffer back to the MMA warp
       tc_fence_before();
@@ -927,6 +934,238 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // no CTA leaves while its cluster peer may still write into its shared memory
   if (a.csplit) cluster_sync_all();
+}
+
+// ---------------------------------------------------------------------------
+// CTA-pair GEMM (cta_group::2). A cluster of two CTAs computes a tile of two
+// weight tiles (256 rows) by 256 tokens: each CTA stages its own weight tile
+// and half of the tokens (128 rows), and one thread of the first CTA issues
+// M = 256, N = 256 MMAs that read both CTAs' shared memory. Each CTA's TMEM
+// receives its weight tile's rows over all 256 tokens, so the epilogue is the
+// single-CTA one. One MMA instruction does twice the work of a single-CTA
+// 256-token one at the same issue cost (the issuing thread's fixed cost per
+// k-block is what limits single-CTA tensor-bound tiles), and a stage is 32 KB,
+// so six fit. Pairs take whole pair tiles round-robin; a pair's second weight
+// tile past N (odd tile count) loads zeros and stores nothing.
+struct PairCfg {
+  static constexpr int BN = 256;
+  static constexpr int kBHalfBytes = (BN / 2) * kTileK * 2;   // 16 KB
+  static constexpr int kStageBytes = kABytes + kBHalfBytes;     // 32 KB per CTA
+  static constexpr int kStages = 6;
+  static constexpr int kTmemCols = 2 * BN;                      // two accumulators
+  static constexpr int kStgBytes = 2 * 128 * 17 * 4;
+  static constexpr int kSmem = kStages * kStageBytes + kStgBytes + 1024;
+};
+
+template <int EC>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ AMaps amaps, const __grid_constant__ CUtensorMap xmap,
+                     const __grid_constant__ GemmArgs a, const __grid_constant__ ARegions rg,
+                     const __grid_constant__ GemmEpi e) {
+  using P = PairCfg;
+  constexpr int BN = P::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* stg = reinterpret_cast<float*>(smem + P::kStages * P::kStageBytes);
+  __shared__ __align__(8) uint64_t full[P::kStages];    // the first CTA's count both CTAs' bytes
+  __shared__ __align__(8) uint64_t empty[P::kStages];
+  __shared__ __align__(8) uint64_t acc_full[2];
+  __shared__ __align__(8) uint64_t acc_empty[2];        // the first CTA's: 4 epilogue warps of each CTA
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ EpiShared esh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = blockIdx.x;
+  const uint32_t rank = static_cast<uint32_t>(g & 1);
+  const int pair = g >> 1, n_pairs = static_cast<int>(gridDim.x >> 1);
+  const int kb = a.k_blocks;
+  const int pair_tiles = ((a.n_tiles + 1) >> 1) * a.m_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&xmap);
+    for (int i = 0; i < rg.n_regions && i < kMaxAMaps; ++i) tma_prefetch_desc(&amaps.m[i]);
+  }
+  if (warp == 1) tmem_alloc_pair(&tmem_slot, P::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // the peer signals this CTA's barriers only after they exist
+  cluster_sync_all();
+  const uint32_t tmem = tmem_slot;
+  grid_dep_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      const uint64_t wpol = policy_evict_first();
+      const uint32_t lead_full = mapa_shared(smem_u32(&full[0]), 0);   // the first CTA's full barriers
+      struct Cur {
+        int pt, k, ml, rl, mh, rh, brow;
+      };
+      auto at_tile = [&](Cur& c) {
+        const int pr = c.pt / a.m_tiles, tm = c.pt - pr * a.m_tiles;
+        weight_rows(rg, 2 * pr + static_cast<int>(rank), c.ml, c.rl, c.mh, c.rh);
+        c.brow = tm * BN + static_cast<int>(rank) * (BN / 2);
+      };
+      auto advance = [&](Cur& c) {
+        if (++c.k == kb) {
+          c.k = 0;
+          c.pt += n_pairs;
+          if (c.pt < pair_tiles) at_tile(c);
+        }
+      };
+      const int n_units = pair < pair_tiles ? ((pair_tiles - 1 - pair) / n_pairs + 1) * kb : 0;
+      Cur ca{pair, 0, 0, 0, 0, 0, 0};
+      if (n_units > 0) at_tile(ca);
+      Cur cb = ca;
+      auto load_a = [&](int i, const Cur& c) {
+        const int s = i % P::kStages;
+        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * P::kStageBytes);
+        uint8_t* sa = smem + s * P::kStageBytes;
+        tma_load_2d_pair(sa, &amaps.m[c.ml], lead_full + 8u * s, c.k * kTileK, c.rl, wpol);
+        tma_load_2d_pair(sa + kABytes / 2, &amaps.m[c.mh], lead_full + 8u * s, c.k * kTileK, c.rh, wpol);
+      };
+      auto load_b = [&](int i, const Cur& c) {
+        const int s = i % P::kStages;
+        tma_load_2d_pair_nohint(smem + s * P::kStageBytes + kABytes, &xmap, lead_full + 8u * s, c.k * kTileK,
+                                c.brow);
+      };
+      // weights do not depend on the previous kernel: the first stages' are
+      // requested before waiting for it
+      const int pre = min(n_units, P::kStages);
+      for (int i = 0; i < pre; ++i) {
+        load_a(i, ca);
+        advance(ca);
+      }
+      grid_dep_wait();
+      for (int i = 0; i < pre; ++i) {
+        load_b(i, cb);
+        advance(cb);
+      }
+      for (int i = pre; i < n_units; ++i) {
+        const int s = i % P::kStages;
+        if (!mbar_wait(&empty[s], ((i / P::kStages) & 1) ^ 1, &abort_flag)) {
+          abort_flag = 1;
+          latch_status(a.status, kDevTimeout);
+          break;
+        }
+        load_a(i, ca);
+        load_b(i, ca);
+        advance(ca);
+      }
+      if (abort_flag) {
+        // copies in flight complete on the first CTA's barriers: give them
+        // time to land before shared memory is released
+        const unsigned long long t0 = global_ns();
+        while (global_ns() - t0 < 50000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (first CTA) ----------------
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kTileN, BN);
+      grid_dep_wait();
+      int i = 0, j = 0;
+      for (int pt = pair; pt < pair_tiles && !abort_flag; pt += n_pairs, ++j) {
+        const int buf = j & 1;
+        if (!mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, &abort_flag)) {
+          abort_flag = 1;
+          latch_status(a.status, kDevTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * BN;
+        for (int k = 0; k < kb; ++k, ++i) {
+          const int s = i % P::kStages;
+          if (!mbar_wait(&full[s], (i / P::kStages) & 1, &abort_flag)) {
+            abort_flag = 1;
+            latch_status(a.status, kDevTimeout);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * P::kStageBytes);
+          const uint64_t ad = sdesc_kmajor_sw128(sa);
+          const uint64_t bd = sdesc_kmajor_sw128(sa + kABytes);
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 16; ++kk)
+            tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (k != 0 || kk != 0) ? 1u : 0u);
+          tc_commit_pair(&empty[s]);
+        }
+        tc_commit_pair(&acc_full[buf]);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps (both CTAs) ----------------
+    grid_dep_wait();
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t lead_acc_empty = mapa_shared(smem_u32(&acc_empty[0]), 0);
+    int j = 0;
+    for (int pt = pair; pt < pair_tiles; pt += n_pairs, ++j) {
+      const int pr = pt / a.m_tiles, tm = pt - pr * a.m_tiles;
+      const int t = (2 * pr + static_cast<int>(rank)) * a.m_tiles + tm;   // this CTA's tile
+      const int buf = j & 1;
+      tile_cols_prepare<BN, EC>(a, e, tm * BN, r, esh);
+      float rpre[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) rpre[c] = 0.f;
+      if (!mbar_wait(&acc_full[buf], (j >> 1) & 1, &abort_flag)) {
+        abort_flag = 1;
+        latch_status(a.status, kDevTimeout);
+      }
+      epi_bar();
+      if (r == 0) esh.flag = abort_flag;
+      epi_bar();
+      if (esh.flag) break;
+      tc_fence_after();
+      // a pair's second weight tile past N (odd tile count) has no rows to store
+      if (2 * pr + static_cast<int>(rank) < a.n_tiles)
+        epilogue_tile<BN, EC>(a, rg, e, g, t, g, g, trow + buf * BN, r, esh, stg, 0u, rpre, 0, BN, nullptr);
+      if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, 2 * pair_tiles);
+      // hand the accumulator back to the first CTA's MMA thread
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(lead_acc_empty + 8u * buf);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, P::kTmemCols);
+  }
+  // no CTA leaves while its peer may still read or signal its shared memory
+  cluster_sync_all();
+}
+
+template <int EC>
+cudaError_t launch_pair(const AMaps& amaps, const ARegions& rg, const CUtensorMap& xmap, const GemmArgs& a,
+                        const GemmEpi& e, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t err = cudaFuncSetAttribute(gemm_pair_kernel<EC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           PairCfg::kSmem);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  return launch_pdl_cluster(gemm_pair_kernel<EC>, dim3(a.grid), dim3(kThreads), PairCfg::kSmem, 2, stream, amaps,
+                            xmap, a, rg, e);
 }
 
 template <int BN, int EC>
@@ -948,6 +1187,7 @@ cudaError_t launch_bn(const AMaps& amaps, const ARegions& rg, const CUtensorMap&
 template <int EC>
 cudaError_t launch_class_bn(const AMaps& amaps, const ARegions& rg, const CUtensorMap& xmap, const GemmArgs& a,
                             const GemmEpi& e, int BN, cudaStream_t stream) {
+  if (a.pair) return launch_pair<EC>(amaps, rg, xmap, a, e, stream);
   switch (BN) {
     case 16: return launch_bn<16, EC>(amaps, rg, xmap, a, e, stream);
     case 32: return launch_bn<32, EC>(amaps, rg, xmap, a, e, stream);

@@ -7,6 +7,19 @@
 namespace dfl {
 using namespace gk;
 
+namespace {
+// CTA pairs over 256 x 256 pair tiles pay when every pair has one tile (the
+// tile count fits one round) or the round-robin deal stays balanced.
+bool pair_tiles_ok(int M, int N, int num_sms) {
+  const long long nt = (N + kTileN - 1) / kTileN;
+  if (nt < 2) return false;
+  const long long pt = ((nt + 1) / 2) * ((M + 255) / 256), pairs = num_sms / 2;
+  if (pt <= pairs) return true;
+  const long long rounds = (pt + pairs - 1) / pairs;
+  return static_cast<double>(pt) / static_cast<double>(rounds * pairs) >= 0.75;
+}
+}  // namespace
+
 int gemm_token_tile(int M, int N, int num_sms) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
@@ -18,6 +31,8 @@ int gemm_token_tile(int M, int N, int num_sms) {
   // does twice the work of a 128-token one at the same issue cost, and the
   // split keeps the CTA count of 128-token tiles.
   if (2 * nt * ((M + 255) / 256) <= num_sms) return 256;
+  // otherwise CTA pairs over 256-token tiles (two weight tiles per pair)
+  if (pair_tiles_ok(M, N, num_sms)) return 256;
   // 256-token tiles, unless 128-token tiles keep clearly more SMs busy (a
   // tile count well under one wave)
   auto busy = [&](int bn) {
@@ -34,6 +49,16 @@ bool gemm_cluster_split(int M, int N, int K, int splits, int num_sms) {
   return 2 * tiles <= num_sms && (K + kTileK - 1) / kTileK >= 2;
 }
 
+bool gemm_pair_mode(int M, int N, int K, int splits, int num_sms) {
+  if (splits != 0 || M <= 128 || K < 1 || gemm_cluster_split(M, N, K, splits, num_sms)) return false;
+  return pair_tiles_ok(M, N, num_sms);
+}
+
+int gemm_act_rows(int M, int N, int K, int num_sms) {
+  const int BN = gemm_token_tile(M, N, num_sms);
+  return gemm_pair_mode(M, N, K, 0, num_sms) ? BN / 2 : BN;
+}
+
 int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms) {
   const int BN = gemm_token_tile(M, N, num_sms);
   const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + BN - 1) / BN);
@@ -41,6 +66,11 @@ int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms
   // one cluster of two CTAs per tile, each with half of the k-blocks: the
   // stream-K partition of 2 x tiles CTAs is exactly that split
   if (gemm_cluster_split(M, N, K, splits, num_sms)) return static_cast<int>(2 * tiles);
+  // CTA pairs take whole pair tiles round-robin
+  if (gemm_pair_mode(M, N, K, splits, num_sms)) {
+    const long long pair_tiles = static_cast<long long>(((N + kTileN - 1) / kTileN + 1) / 2) * ((M + BN - 1) / BN);
+    return static_cast<int>(2 * std::min<long long>(pair_tiles, num_sms / 2));
+  }
   const long long units = tiles * kb;
   long long G = splits > 0 ? tiles * std::min(splits, kb) : num_sms;
   // Tensor-bound tiles (BN >= 128) that fit in one wave: one whole tile per
@@ -75,13 +105,15 @@ cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUten
   a.units = static_cast<long long>(a.n_tiles) * a.m_tiles * a.k_blocks;
   a.grid = gemm_grid(M, N, K, splits, work.partial_elems, num_sms);
   a.csplit = gemm_cluster_split(M, N, K, splits, num_sms) ? 1 : 0;
+  a.pair = gemm_pair_mode(M, N, K, splits, num_sms) ? 1 : 0;
   // the pair exchange addresses a 128 x 128 float block of the peer's ring
   // (BN = 256) and pairs CTAs 2t, 2t + 1
   if (a.csplit && (BN != 256 || a.grid != 2 * a.n_tiles * a.m_tiles)) return cudaErrorInvalidValue;
   a.status = epi.status;
   a.partial = work.partial;
   a.tickets = work.tickets;
-  if (static_cast<long long>(a.n_tiles) * a.m_tiles > work.n_tickets && a.grid % (a.n_tiles * a.m_tiles) != 0)
+  if (!a.pair && static_cast<long long>(a.n_tiles) * a.m_tiles > work.n_tickets &&
+      a.grid % (a.n_tiles * a.m_tiles) != 0)
     return cudaErrorInvalidValue;
   switch (epilogue_class(epi.kind)) {
     case kEcNorm: return launch_ec_norm(amaps, regions, xmap, a, epi, BN, stream);

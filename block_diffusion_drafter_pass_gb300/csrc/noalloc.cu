@@ -98,7 +98,8 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
   }
   AMaps am;
   CUtensorMap xm;
-  if (!encode_matrix_map(&am.m[0], W, N, K, kWeightBoxRows) || !encode_matrix_map(&xm, X, M, K, BN)) {
+  const int xbox = splits == 0 ? gemm_act_rows(M, N, K, sms) : BN;   // CTA pairs each load half the tokens
+  if (!encode_matrix_map(&am.m[0], W, N, K, kWeightBoxRows) || !encode_matrix_map(&xm, X, M, K, xbox)) {
     set_unattached_error("dflash_gemm_noalloc: cannot describe W or X for TMA");
     return DFLASH_EINVAL;
   }

@@ -623,7 +623,7 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
     AMaps am;
     am.m[0] = ctx->m_wc;
     ARegions rg = stacked({H});
-    const CUtensorMap* xm = act_map(ctx, feats, M, c.n_feat_layers * H, gemm_token_tile(M, H, ctx->num_sms));
+    const CUtensorMap* xm = act_map(ctx, feats, M, c.n_feat_layers * H, gemm_act_rows(M, H, c.n_feat_layers * H, ctx->num_sms));
     if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe feats for TMA");
     GemmEpi e = base_epi(ctx, EPI_NORMSRC);
     e.out_hg = ctx->htg;
@@ -641,7 +641,7 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
     for (int l0 = 0; l0 < c.n_layers; l0 += per_launch) {
       const int nl = std::min(per_launch, c.n_layers - l0);
       const CUtensorMap* xm =
-          act_map(ctx, ctx->htg, M, H, gemm_token_tile(M, 2 * nl * ceil_div(nkv * d, 128) * 128, ctx->num_sms));
+          act_map(ctx, ctx->htg, M, H, gemm_act_rows(M, 2 * nl * ceil_div(nkv * d, 128) * 128, H, ctx->num_sms));
       if (!xm) return fail(ctx, DFLASH_EINVAL, "cannot describe H_t for TMA");
       AMaps am;
       ARegions rg;
@@ -760,13 +760,13 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   // activation descriptors: the box height is the token tile each GEMM uses
   const int sms = ctx->num_sms;
   const int n_qkv = (nq + 2 * nkv) * d, n_gu = ceil_div(F, 64) * 128;
-  const CUtensorMap* hmap_qkv = act_map(ctx, ctx->hg, M, H, gemm_token_tile(M, n_qkv, sms));
-  const CUtensorMap* hmap_gu = act_map(ctx, ctx->hg, M, H, gemm_token_tile(M, n_gu, sms));
-  const CUtensorMap* hmap_lm = act_map(ctx, ctx->hg, M, H, gemm_token_tile(M, c.vocab, sms));
+  const CUtensorMap* hmap_qkv = act_map(ctx, ctx->hg, M, H, gemm_act_rows(M, n_qkv, H, sms));
+  const CUtensorMap* hmap_gu = act_map(ctx, ctx->hg, M, H, gemm_act_rows(M, n_gu, H, sms));
+  const CUtensorMap* hmap_lm = act_map(ctx, ctx->hg, M, H, gemm_act_rows(M, c.vocab, H, sms));
   const int parts = ceil_div(H, 128);
   const int rows_ld = ctx->max_rows();
-  const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, gemm_token_tile(M, H, sms));
-  const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, gemm_token_tile(M, H, sms));
+  const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, gemm_act_rows(M, H, nq * d, sms));
+  const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, gemm_act_rows(M, H, F, sms));
   if (!km || !hmap_qkv || !hmap_gu || !hmap_lm || !amap || !fmap)
     return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
   AttnMaps attn_maps;
@@ -1011,7 +1011,8 @@ dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y, 
   const int BN = gemm_token_tile(M, N, sms);
   AMaps am;
   CUtensorMap xm;
-  if (!encode_2d(&am.m[0], W, N, K, kWeightBoxRows) || !encode_2d(&xm, X, M, K, BN)) return DFLASH_EINVAL;
+  const int xbox = splits == 0 ? gemm_act_rows(M, N, K, sms) : BN;   // CTA pairs each load half the tokens
+  if (!encode_2d(&am.m[0], W, N, K, kWeightBoxRows) || !encode_2d(&xm, X, M, K, xbox)) return DFLASH_EINVAL;
   GemmWork work;
   const int G = gemm_grid(M, N, K, splits, static_cast<size_t>(1) << 40, sms);
   work.partial_elems = static_cast<size_t>(2) * G * 128 * BN;

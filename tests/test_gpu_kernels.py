@@ -36,6 +36,10 @@ DEV = "cuda:0"
     (1024, 300, 512, 0),      # the same with a ragged token tail
     (512, 272, 960, 0),       # odd k-block count (15 = 7 + 8)
     (384, 200, 64, 0),        # one k-block: 256-token tile, no split
+    (6144, 512, 1024, 0),     # CTA pairs (cta_group::2), one pair tile per pair
+    (24576, 512, 512, 0),     # CTA pairs, pair tiles dealt round-robin (3 rounds)
+    (4992, 512, 256, 0),      # CTA pairs, odd weight-tile count (last pair half empty)
+    (5120, 300, 320, 0),      # CTA pairs, ragged token tail in the second CTA's half
 ])
 def test_gemm_matches_fp32_matmul(dfl, N, M, K, splits):
     g = torch.Generator(device="cpu").manual_seed(N * 7 + M * 3 + K)

@@ -291,6 +291,38 @@ def test_qwen3_8b_batch16_two_layers(dfl):
         assert checked > 0
 
 
+def test_qwen3_8b_batch32_two_layers(dfl):
+    """8B width, 2 layers, 32 sequences x B = 16 = 512 block tokens: QKV
+    (RoPE), gate/up (SwiGLU) and the LM head (argmax over 1187 weight tiles,
+    an odd count) run as CTA pairs issuing cta_group::2 MMAs; O, down and the
+    fuse run 256-token tiles split over K by clusters."""
+    shape, wt, wn = _big_setup(2, seed=101)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    width = shape.n_feat_layers * shape.hidden
+    n = 32
+    with dfl.Drafter(shape, wt, max_seqs=n, max_batch=n, max_block=16, max_ctx=256,
+                     max_fuse_tokens=4096) as d:
+        rng = np.random.default_rng(102)
+        lens = [int(x) for x in rng.integers(16, 96, size=n)]
+        f = make_features_np(sum(lens), width, seed=103)
+        d.fuse_ctx(list(range(n)), lens, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(list(range(n)), lens, f, pending=False)
+        f = make_features_np(16 * n, width, seed=104)
+        d.fuse_ctx(list(range(n)), [16] * n, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(list(range(n)), [16] * n, f, pending=False)
+        d.sync()
+        for s in (0, 31):
+            m = orc.seq_len(s)[0]
+            for l in range(2):
+                k, v = d.read_kv(l, s, 0, m)
+                kr, vr = orc.context(s, l)
+                assert_close(k, kr, f"8B batch {n} K layer {l} seq {s}")
+                assert_close(v, vr, f"8B batch {n} V layer {l} seq {s}")
+        anchors = make_anchor_ids_np(n, shape.vocab, seed=105)
+        _, _, checked = _draft_and_compare(d, orc, list(range(n)), anchors, 16, f"8B 2-layer batch {n}")
+        assert checked > 0
+
+
 def test_mqa_long_context_many_chunks(dfl):
     """One key/value head (d = 128, two query heads) over a 6000-token
     context: the attention work is split into 2-unit chunks (94 pages plus the
