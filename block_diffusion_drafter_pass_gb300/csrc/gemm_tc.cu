@@ -9,14 +9,16 @@ using namespace gk;
 
 namespace {
 // CTA pairs over 256 x 256 pair tiles pay when every pair has one tile (the
-// tile count fits one round) or the round-robin deal stays balanced.
+// tile count fits one round) or the round-robin deal keeps at least half of
+// the pairs' time busy: a pair MMA does twice the work per instruction, so
+// even two uneven rounds beat a balanced single-CTA schedule.
 bool pair_tiles_ok(int M, int N, int num_sms) {
   const long long nt = (N + kTileN - 1) / kTileN;
   if (nt < 2) return false;
   const long long pt = ((nt + 1) / 2) * ((M + 255) / 256), pairs = num_sms / 2;
   if (pt <= pairs) return true;
   const long long rounds = (pt + pairs - 1) / pairs;
-  return static_cast<double>(pt) / static_cast<double>(rounds * pairs) >= 0.75;
+  return static_cast<double>(pt) / static_cast<double>(rounds * pairs) >= 0.5;
 }
 }  // namespace
 
