@@ -6,23 +6,25 @@
 // with no mask (the drafter's attention is non-causal).
 //
 // The keys are split into chunks of whole 64-key tiles (flash-decoding). A
-// persistent grid, one CTA per SM, walks the (sequence, kv head, chunk) work
-// items. Per CTA:
-//   warp 0     TMA producer: the item's queries once (two buffers, so the
-//              next item's copies start while this one finishes), then per tile the key
-//              rows [64][d] and the transposed value rows [d][64] of one page
-//              (values are stored transposed in the pool so that both
-//              products read K-major, 128-byte-swizzled operands);
+// persistent grid, one CTA per SM, runs the (sequence, kv head, chunk) work
+// items the host dealt to each CTA (largest first, to the least loaded CTA).
+// Per CTA:
+//   warp 0     TMA producer: the item's queries once, then per step of two
+//              64-key units the key rows [64][d] and the transposed value
+//              rows [d][64] of two pages (values are stored transposed in the
+//              pool so that both products read K-major, 128-byte-swizzled
+//              operands);
 //   warp 1     allocates tensor memory and issues tcgen05.mma from one
-//              thread: S = Q K^T (M = 128 query rows, N = 64 keys) into one of
-//              two TMEM S buffers, then O += P V (N = d) into the item's TMEM
-//              O buffer, with P read from shared memory;
+//              thread: S = Q K^T (M = 128 query rows, N = 128 keys) into one
+//              of two TMEM S buffers, then O += P V (N = d) into the item's
+//              TMEM O buffer; Q and P are the A operand read from TMEM, so
+//              shared memory feeds only K and V;
 //   warp 6     L2 prefetch of the context pages a few steps ahead of warp 0;
-//   warps 2-5  one query row per thread (the TMEM lane quarter of the warp):
-//              online softmax in the log2 domain on S read from TMEM, P
-//              written to shared memory as bf16, O rescaled in TMEM only when
-//              the row maximum grows by more than 2^8 (the stale maximum is a
-//              valid reference point: P and O stay bounded by 256x).
+//   warps 2-5  the softmax: online softmax in the log2 domain on S read from
+//              TMEM, P written over its own S as packed bf16, O rescaled in
+//              TMEM only when the row maximum grows by more than 2^8 (the
+//              stale maximum is a valid reference point: P and O stay
+//              bounded by 256x).
 // S_{t+1} is issued before P_t is ready, so the softmax of one tile overlaps
 // the products of the next. Each item leaves an unnormalised partial (O,
 // running max, running sum); attn_combine_kernel merges the chunks of a row.
@@ -264,6 +266,7 @@ __device__ __forceinline__ SeqSplit seq_split(const AttnArgs& a, int i) {
 
 struct Item {
   int i, kvh, tb, te;   // sequence index, kv head, units [tb, te)
+  int slot;             // partial-buffer slot: (sequence, kv head, chunk) in row-major order
 };
 
 // SPREAD (G*B <= 64): query row r sits in TMEM lane 32*(r/16) + r%16, so all
@@ -276,7 +279,8 @@ struct Item {
 // (tb + 2j, tb + 2j + 1), the second possibly absent.
 template <int D, bool SPREAD>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ AttnArgs a) {
+    attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ AttnArgs a,
+                const __grid_constant__ AttnSched sched) {
   using C = ACfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -346,18 +350,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   grid_dep_launch();
   const uint32_t tmem = tmem_slot;
-  const int total = s_prefix[n_seq];
 
-  auto decode = [&](int item) {
+  // This CTA's records: every role walks the same list and skips the same
+  // records (chunks the device's lengths do not reach).
+  const int rec_end = sched.off[blockIdx.x + 1];
+  auto rec_ok = [&](int k) {
+    const uint32_t w = sched.item[k];
+    const int i = static_cast<int>(w >> 24), h = static_cast<int>((w >> 16) & 0xFFu);
+    return i < n_seq && h < nkv && static_cast<int>(w & 0xFFFFu) < s_nch[i];
+  };
+  auto next_rec = [&](int k) {
+    while (k < rec_end && !rec_ok(k)) ++k;
+    return k;
+  };
+  const int rec_begin = next_rec(sched.off[blockIdx.x]);
+  auto decode = [&](int k) {
+    const uint32_t w = sched.item[k];
     Item it;
-    int i = 0;
-    while (i + 1 < n_seq && item >= s_prefix[i + 1]) ++i;
-    const int local = item - s_prefix[i];
-    it.i = i;
-    it.kvh = local / s_nch[i];
-    const int chunk = local - it.kvh * s_nch[i];
+    it.i = static_cast<int>(w >> 24);
+    it.kvh = static_cast<int>((w >> 16) & 0xFFu);
+    const int chunk = static_cast<int>(w & 0xFFFFu);
     it.tb = chunk * a.chunk_tiles;
-    it.te = min(s_nctx[i] + 1, it.tb + a.chunk_tiles);
+    it.te = min(s_nctx[it.i] + 1, it.tb + a.chunk_tiles);
+    it.slot = s_prefix[it.i] + it.kvh * s_nch[it.i] + chunk;
     return it;
   };
   auto give_up = [&]() {
@@ -371,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int Bb = block_rows(B);
       int q = 0;
       bool dead = false, waited = false;
-      for (int item = blockIdx.x; item < total && !dead; item += gridDim.x) {
-        const Item it = decode(item);
+      for (int rk = rec_begin; rk < rec_end && !dead; rk = next_rec(rk + 1)) {
+        const Item it = decode(rk);
         const int slot = a.meta.slot[it.i], nctx = s_nctx[it.i];
         const int* ptab = a.seqs.page_table + static_cast<size_t>(slot) * a.seqs.pages_per_seq;
         auto page_of = [&](int t) {   // -1 (latched below) if the table is too short
@@ -462,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int q = 0, k = 0;
       bool dead = false;
-      for (int item = blockIdx.x; item < total && !dead; item += gridDim.x, ++k) {
-        const Item it = decode(item);
+      for (int rk = rec_begin; rk < rec_end && !dead; rk = next_rec(rk + 1), ++k) {
+        const Item it = decode(rk);
         const int ns = (it.te - it.tb + 1) >> 1;
         if (!mbar_wait(&q_ready, k & 1, &abort_flag)) {
           give_up();
@@ -513,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128-byte line per lane), so the producer's copies hit L2.
     int q = 0;
     bool stop = false;
-    for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
-      const Item it = decode(item);
+    for (int rk = rec_begin; rk < rec_end && !stop; rk = next_rec(rk + 1)) {
+      const Item it = decode(rk);
       const int slot = a.meta.slot[it.i], nctx = s_nctx[it.i];
       const int* ptab = a.seqs.page_table + static_cast<size_t>(slot) * a.seqs.pages_per_seq;
       for (int t0 = it.tb; t0 < it.te && !stop; t0 += 2, ++q) {
@@ -644,9 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int q = 0, k = 0;
     bool dead = false;
     grid_dep_wait();   // q comes from the projection kernel
-    if (blockIdx.x < total) load_q(decode(blockIdx.x));
-    for (int item = blockIdx.x; item < total && !dead; item += gridDim.x, ++k) {
-      const Item it = decode(item);
+    if (rec_begin < rec_end) load_q(decode(rec_begin));
+    for (int rk = rec_begin; rk < rec_end && !dead; rk = next_rec(rk + 1), ++k) {
+      const Item it = decode(rk);
       const int ns = (it.te - it.tb + 1) >> 1;
       const int len = s_len[it.i], nctx = s_nctx[it.i];
       auto unit_valid = [&](int t) {   // valid keys of unit t (0 if absent)
@@ -725,7 +740,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (dead) break;
       // every S of this item has completed: Q's TMEM columns are free for the next item
-      if (item + static_cast<int>(gridDim.x) < total) load_q(decode(item + gridDim.x));
+      {
+        const int rn = next_rec(rk + 1);
+        if (rn < rec_end) load_q(decode(rn));
+      }
       if (!warp_wait(&o_full, k & 1)) {
         give_up();
         break;
@@ -733,8 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (active) {
         if constexpr (SPREAD) l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
-        const bool keep = row < R && item < a.items_cap;
-        float* po = a.part_o + (static_cast<size_t>(item) * a.rows_pad + row) * D + half * (D / 2);
+        const bool keep = row < R && it.slot < a.items_cap;
+        float* po = a.part_o + (static_cast<size_t>(it.slot) * a.rows_pad + row) * D + half * (D / 2);
 #pragma unroll
         for (int c0 = 0; c0 < (SPREAD ? D / 2 : D); c0 += 32) {
           float ov[32];
@@ -746,8 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<float4*>(po + c0 + c) = make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
           }
         }
-        if (keep && half == 0) a.part_ml[static_cast<size_t>(item) * a.rows_pad + row] = make_float2(m_run, l_run);
-        if (row == 0 && half == 0 && item >= a.items_cap) latch_status(a.status, kDevBounds);   // host sizing prevents this
+        if (keep && half == 0) a.part_ml[static_cast<size_t>(it.slot) * a.rows_pad + row] = make_float2(m_run, l_run);
+        if (row == 0 && half == 0 && it.slot >= a.items_cap) latch_status(a.status, kDevBounds);   // host sizing prevents this
       }
       tc_fence_before();
       __syncwarp();
@@ -889,7 +907,8 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
 }
 
 template <int D, bool SPREAD>
-cudaError_t launch_main(const AttnMaps& maps, const AttnArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch_main(const AttnMaps& maps, const AttnArgs& a, const AttnSched& sched, int grid,
+                        cudaStream_t stream) {
   using C = ACfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -898,13 +917,15 @@ cudaError_t launch_main(const AttnMaps& maps, const AttnArgs& a, int grid, cudaS
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(attn_kernel<D, SPREAD>, dim3(grid), dim3(kThreads), C::kSmem, stream, maps, a);
+  return launch_pdl(attn_kernel<D, SPREAD>, dim3(grid), dim3(kThreads), C::kSmem, stream, maps, a, sched);
 }
 
 template <int D>
-cudaError_t launch_d(const AttnMaps& maps, const AttnArgs& a, int grid, int part, cudaStream_t stream) {
+cudaError_t launch_d(const AttnMaps& maps, const AttnArgs& a, const AttnSched& sched, int grid, int part,
+                     cudaStream_t stream) {
   if (part == 0)
-    return a.spread ? launch_main<D, true>(maps, a, grid, stream) : launch_main<D, false>(maps, a, grid, stream);
+    return a.spread ? launch_main<D, true>(maps, a, sched, grid, stream)
+                    : launch_main<D, false>(maps, a, sched, grid, stream);
   const dim3 grid_c(a.n_q_heads, a.meta.n_seq, (a.meta.B + kCombineWarps - 1) / kCombineWarps);
   const dim3 block_c(32 * kCombineWarps);
   if (a.max_chunks <= 8) return launch_pdl(attn_combine_kernel<D, 8>, grid_c, block_c, 0, stream, a);
@@ -927,12 +948,14 @@ int attention_ctas_per_sm(int head_dim) {
   return n < 1 ? 1 : n;
 }
 
-cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& a, int grid, int part, cudaStream_t stream) {
+cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& a, const AttnSched& sched, int grid, int part,
+                             cudaStream_t stream) {
   const int G = a.n_q_heads / a.n_kv_heads, R = G * a.meta.B;
   if (R > 128 || a.rows_pad < R) return cudaErrorInvalidValue;
   if (a.spread && R > 64) return cudaErrorInvalidValue;
-  if (a.head_dim == 128) return launch_d<128>(maps, a, grid, part, stream);
-  if (a.head_dim == 64) return launch_d<64>(maps, a, grid, part, stream);
+  if (grid < 1 || grid > kSchedCtas || sched.off[grid] > kSchedItems) return cudaErrorInvalidValue;
+  if (a.head_dim == 128) return launch_d<128>(maps, a, sched, grid, part, stream);
+  if (a.head_dim == 64) return launch_d<64>(maps, a, sched, grid, part, stream);
   return cudaErrorInvalidValue;
 }
 

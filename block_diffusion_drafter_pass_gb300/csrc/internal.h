@@ -201,6 +201,17 @@ struct AttnArgs {
   int* status;
 };
 
+// The attention work items each CTA runs, in order: CTA c runs records
+// item[off[c]] .. item[off[c+1]-1], each (sequence << 24) | (kv head << 16) |
+// chunk. The host deals them from its length bounds; a record whose chunk the
+// device's lengths do not reach is skipped.
+constexpr int kSchedCtas = 320;
+constexpr int kSchedItems = 1536;
+struct AttnSched {
+  uint16_t off[kSchedCtas + 1];
+  uint32_t item[kSchedItems];
+};
+
 // Tensor maps the attention kernel reads through (all bf16, 128-byte swizzle):
 //   pool_k  the pool as rows of d elements: key rows of (layer, page, head)
 //   pool_vt the pool as rows of 64 elements: transposed value rows [dim][slot]
@@ -211,7 +222,8 @@ struct AttnMaps {
 };
 
 // part 0: the chunked attention kernel; part 1: the combine kernel.
-cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& a, int grid, int part, cudaStream_t stream);
+cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& a, const AttnSched& sched, int grid, int part,
+                             cudaStream_t stream);
 int attention_block_rows(int B);   // key-box height used for the block's own keys
 int attention_ctas_per_sm(int head_dim);   // resident attention CTAs per SM
 

@@ -18,6 +18,7 @@
 #include <cstring>
 #include <map>
 #include <memory>
+#include <queue>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -126,6 +127,9 @@ struct dflash_ctx {
   std::vector<int> len_ub, pend, added_since;
   int* h_snap = nullptr;      // pinned copy of d_len
   std::vector<double> deal_load;   // scratch of the attention work split
+  std::vector<std::pair<int, uint32_t>> deal_items;
+  std::vector<int> deal_owner, deal_count;
+  std::unique_ptr<AttnSched> attn_sched{new AttnSched()};
   std::unique_ptr<PageUpdates> page_upd{new PageUpdates()};   // staging of one append's new pages
   cudaEvent_t snap_event = nullptr;
   bool snap_pending = false;
@@ -704,32 +708,61 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   // attention work split from the host's length bounds
   long long tiles_ub = 0;
   for (int i = 0; i < n_seq; ++i) tiles_ub += 1LL * nkv * (ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1);
-  // One wave of resident attention CTAs; item i goes to CTA i mod grid. The
-  // chunk size (even: the kernel consumes units in pairs) is the candidate,
-  // from about one to eight chunks per CTA, whose deal has the smallest
-  // estimated makespan under the host's length bounds, an item costing its
-  // units plus kItemOverhead (query load, pipeline fill and drain, partial
-  // write). Equal-length rows (batch 1) keep one chunk per CTA; rows of mixed
-  // lengths get several smaller chunks, so no CTA draws two long rows.
+  // One wave of resident attention CTAs. Items (sequence, kv head, chunk of
+  // `ch` units) are dealt largest first to the least loaded CTA, an item
+  // costing its units plus kItemOverhead (query load, pipeline fill and
+  // drain, partial write). The chunk size (even: the kernel consumes units in
+  // pairs) is the candidate, from about one to eight chunks per CTA, whose
+  // deal has the smallest makespan under the host's length bounds: equal rows
+  // (batch 1) keep one chunk per CTA; rows of mixed lengths get several
+  // shorter chunks, and the short row tails fill the gaps.
   int& per_sm = ctx->attn_ctas_per_sm;
   if (per_sm == 0) per_sm = attention_ctas_per_sm(d);
-  const int grid_full = per_sm * ctx->num_sms;
+  const int grid_full = std::min(per_sm * ctx->num_sms, kSchedCtas);
+  const long long item_cap = std::min<long long>(ctx->items_cap, kSchedItems);
   auto items_for = [&](int ch) {
     long long it = 0;
     for (int i = 0; i < n_seq; ++i) it += 1LL * nkv * ceil_div(ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1, ch);
     return it;
   };
   constexpr double kItemOverhead = 3.0;
-  auto makespan = [&](int ch) {
-    const long long items = items_for(ch);
-    const int grid = static_cast<int>(std::min<long long>(items, grid_full));
-    std::vector<double>& load = ctx->deal_load;
-    load.assign(grid, 0.0);
-    long long k = 0;
+  // deal chunk size ch; returns the makespan and, with `out`, the schedule
+  auto deal = [&](int ch, AttnSched* out, int* grid_out) {
+    std::vector<std::pair<int, uint32_t>>& items = ctx->deal_items;   // (units, record)
+    items.clear();
     for (int i = 0; i < n_seq; ++i) {
       const int units = ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1;
       for (int h = 0; h < nkv; ++h)
-        for (int tb = 0; tb < units; tb += ch, ++k) load[k % grid] += std::min(ch, units - tb) + kItemOverhead;
+        for (int c = 0; c * ch < units; ++c)
+          items.emplace_back(std::min(ch, units - c * ch),
+                             (static_cast<uint32_t>(i) << 24) | (static_cast<uint32_t>(h) << 16) | static_cast<uint32_t>(c));
+    }
+    std::stable_sort(items.begin(), items.end(),
+                     [](const std::pair<int, uint32_t>& x, const std::pair<int, uint32_t>& y) { return x.first > y.first; });
+    const int grid = static_cast<int>(std::min<long long>(static_cast<long long>(items.size()), grid_full));
+    std::vector<double>& load = ctx->deal_load;
+    load.assign(grid, 0.0);
+    std::vector<int>& owner = ctx->deal_owner;
+    owner.resize(items.size());
+    using Slot = std::pair<double, int>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int c = 0; c < grid; ++c) heap.push(Slot(0.0, c));
+    for (size_t k = 0; k < items.size(); ++k) {
+      Slot sl = heap.top();
+      heap.pop();
+      owner[k] = sl.second;
+      sl.first += items[k].first + kItemOverhead;
+      load[sl.second] = sl.first;
+      heap.push(sl);
+    }
+    if (out) {   // per-CTA lists in dealing order
+      std::vector<int>& cnt = ctx->deal_count;
+      cnt.assign(grid + 1, 0);
+      for (size_t k = 0; k < items.size(); ++k) ++cnt[owner[k] + 1];
+      for (int c = 0; c < grid; ++c) cnt[c + 1] += cnt[c];
+      for (int c = 0; c <= grid; ++c) out->off[c] = static_cast<uint16_t>(cnt[c]);
+      for (size_t k = 0; k < items.size(); ++k) out->item[cnt[owner[k]]++] = items[k].second;
+      *grid_out = grid;
     }
     return *std::max_element(load.begin(), load.end());
   };
@@ -738,8 +771,8 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   for (int per_cta = 1; per_cta <= 8; ++per_cta) {
     int ch = std::max(2, ceil_div(tiles_ub, static_cast<long long>(per_cta) * grid_full));
     ch += ch & 1;
-    if (ch == chunk || items_for(ch) > ctx->items_cap) continue;
-    const double ms = makespan(ch);
+    if (ch == chunk || items_for(ch) > item_cap) continue;
+    const double ms = deal(ch, nullptr, nullptr);
     if (chunk == 0 || ms < best) {
       chunk = ch;
       best = ms;
@@ -748,9 +781,11 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   if (chunk == 0) {   // even one chunk per CTA exceeds the partial buffers: longer chunks
     chunk = std::max(2, ceil_div(tiles_ub, grid_full));
     chunk += chunk & 1;
-    while (items_for(chunk) > ctx->items_cap) chunk *= 2;
+    while (items_for(chunk) > item_cap) chunk *= 2;
   }
-  const int attn_grid = static_cast<int>(std::min<long long>(items_for(chunk), grid_full));
+  AttnSched& sched = *ctx->attn_sched;
+  int attn_grid = 1;
+  deal(chunk, &sched, &attn_grid);
   int max_chunks = 1;
   for (int i = 0; i < n_seq; ++i)
     max_chunks = std::max(max_chunks, ceil_div(ceil_div(ctx->len_ub[meta.slot[i]], kPage) + 1, chunk));
@@ -830,11 +865,11 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
       a.status = ctx->d_status;
       {
         ProfScope ps(ctx, DFLASH_K_ATTN, stream, attn_bytes, attn_flops);
-        CK(launch_attention(attn_maps, a, attn_grid, 0, stream));
+        CK(launch_attention(attn_maps, a, sched, attn_grid, 0, stream));
       }
       {
         ProfScope ps(ctx, DFLASH_K_ATTN_COMBINE, stream, 2.0 * M * nq * d, 0);
-        CK(launch_attention(attn_maps, a, attn_grid, 1, stream));
+        CK(launch_attention(attn_maps, a, sched, attn_grid, 1, stream));
       }
     }
     {  // x += attn W_o^T; the FFN's RMSNorm input is folded into the epilogue
