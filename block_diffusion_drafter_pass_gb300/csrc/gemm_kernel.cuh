@@ -83,7 +83,8 @@ struct GemmArgs {
   long long units;     // tiles * k_blocks
   int grid;            // CTAs (stream-K workers)
   int csplit;          // 1: CTAs 2t and 2t+1 form a cluster splitting tile t's k-blocks in halves
-  int pair;            // 1: CTA pairs run cta_group::2 MMAs over whole 256 x 256 pair tiles
+  int pair;            // 1: CTA pairs run cta_group::2 MMAs over whole 256 x 256 pair tiles;
+                       // 2: clusters of two such pairs, each over half of the k-blocks of one pair tile
   float* partial;      // [grid][2][128 * BN] partial tiles
   int* tickets;        // [tiles], zero between launches
   int* status;
@@ -957,20 +958,29 @@ struct PairCfg {
   static constexpr int kSmem = kStages * kStageBytes + kStgBytes + 1024;
 };
 
-template <int EC>
+// KS = 2: a cluster of four CTAs, two pairs over the two halves of the
+// k-blocks of one pair tile; the CTAs holding the same weight tile in the two
+// pairs exchange the half sums of each other's 128 token columns through
+// distributed shared memory (as the single-CTA cluster split does) and each
+// finishes its own 128 columns. Used when four CTAs per pair tile fit one
+// wave, which single pairs would leave half idle.
+template <int EC, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ AMaps amaps, const __grid_constant__ CUtensorMap xmap,
                      const __grid_constant__ GemmArgs a, const __grid_constant__ ARegions rg,
                      const __grid_constant__ GemmEpi e) {
   using P = PairCfg;
   constexpr int BN = P::BN;
+  constexpr int CL = 2 * KS;   // CTAs per cluster
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* stg = reinterpret_cast<float*>(smem + P::kStages * P::kStageBytes);
-  __shared__ __align__(8) uint64_t full[P::kStages];    // the first CTA's count both CTAs' bytes
+  __shared__ __align__(8) uint64_t full[P::kStages];    // the pair's first CTA's count both CTAs' bytes
   __shared__ __align__(8) uint64_t empty[P::kStages];
   __shared__ __align__(8) uint64_t acc_full[2];
-  __shared__ __align__(8) uint64_t acc_empty[2];        // the first CTA's: 4 epilogue warps of each CTA
+  __shared__ __align__(8) uint64_t acc_empty[2];        // the pair's first CTA's: 4 epilogue warps of each CTA
+  __shared__ __align__(8) uint64_t split_rdy;           // KS = 2: the other pair's CTA's ring is idle (count 1)
+  __shared__ __align__(8) uint64_t split_dat;           // KS = 2: its half sums have landed here (count 128)
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ EpiShared esh;
@@ -978,10 +988,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = blockIdx.x;
-  const uint32_t rank = static_cast<uint32_t>(g & 1);
-  const int pair = g >> 1, n_pairs = static_cast<int>(gridDim.x >> 1);
+  const uint32_t crank = static_cast<uint32_t>(g % CL);   // rank in the cluster
+  const uint32_t member = crank & 1u;                      // weight tile of the pair tile this CTA stages
+  const uint32_t half = crank >> 1;                        // KS = 2: which half of the k-blocks
+  const uint32_t lead = crank & ~1u;                       // the pair's first CTA
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
+  const int pair = g / CL, n_pairs = static_cast<int>(gridDim.x) / CL;
   const int kb = a.k_blocks;
+  const int kbeg = KS == 2 ? static_cast<int>(half) * (kb >> 1) : 0;
+  const int kend = KS == 2 && half == 0 ? (kb >> 1) : kb;
+  const int nk = kend - kbeg;
   const int pair_tiles = ((a.n_tiles + 1) >> 1) * a.m_tiles;
+  // columns (tokens) this CTA finishes
+  const int cbeg = KS == 2 ? static_cast<int>(half) * (BN / 2) : 0;
+  const int cend = KS == 2 ? cbeg + BN / 2 : BN;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P::kStages; ++s) {
@@ -992,6 +1012,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 8);
     }
+    mbar_init(&split_rdy, 1);
+    mbar_init(&split_dat, 128);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -1003,38 +1025,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // the peer signals this CTA's barriers only after they exist
+  // the other CTAs signal this CTA's barriers only after they exist
   cluster_sync_all();
   const uint32_t tmem = tmem_slot;
   grid_dep_launch();
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer (both CTAs) ----------------
+      // ---------------- TMA producer (every CTA) ----------------
       const uint64_t wpol = policy_evict_first();
-      const uint32_t lead_full = mapa_shared(smem_u32(&full[0]), 0);   // the first CTA's full barriers
+      const uint32_t lead_full = mapa_shared(smem_u32(&full[0]), lead);   // the pair's first CTA's full barriers
       struct Cur {
         int pt, k, ml, rl, mh, rh, brow;
       };
       auto at_tile = [&](Cur& c) {
         const int pr = c.pt / a.m_tiles, tm = c.pt - pr * a.m_tiles;
-        weight_rows(rg, 2 * pr + static_cast<int>(rank), c.ml, c.rl, c.mh, c.rh);
-        c.brow = tm * BN + static_cast<int>(rank) * (BN / 2);
+        weight_rows(rg, 2 * pr + static_cast<int>(member), c.ml, c.rl, c.mh, c.rh);
+        c.brow = tm * BN + static_cast<int>(member) * (BN / 2);
       };
       auto advance = [&](Cur& c) {
-        if (++c.k == kb) {
-          c.k = 0;
+        if (++c.k == kend) {
+          c.k = kbeg;
           c.pt += n_pairs;
           if (c.pt < pair_tiles) at_tile(c);
         }
       };
-      const int n_units = pair < pair_tiles ? ((pair_tiles - 1 - pair) / n_pairs + 1) * kb : 0;
-      Cur ca{pair, 0, 0, 0, 0, 0, 0};
+      const int n_units = pair < pair_tiles ? ((pair_tiles - 1 - pair) / n_pairs + 1) * nk : 0;
+      Cur ca{pair, kbeg, 0, 0, 0, 0, 0};
       if (n_units > 0) at_tile(ca);
       Cur cb = ca;
       auto load_a = [&](int i, const Cur& c) {
         const int s = i % P::kStages;
-        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * P::kStageBytes);
+        if (member == 0) mbar_arrive_expect_tx(&full[s], 2 * P::kStageBytes);
         uint8_t* sa = smem + s * P::kStageBytes;
         tma_load_2d_pair(sa, &amaps.m[c.ml], lead_full + 8u * s, c.k * kTileK, c.rl, wpol);
         tma_load_2d_pair(sa + kABytes / 2, &amaps.m[c.mh], lead_full + 8u * s, c.k * kTileK, c.rh, wpol);
@@ -1068,16 +1090,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         advance(ca);
       }
       if (abort_flag) {
-        // copies in flight complete on the first CTA's barriers: give them
-        // time to land before shared memory is released
+        // copies in flight complete on the pair's first CTA's barriers: give
+        // them time to land before shared memory is released
         const unsigned long long t0 = global_ns();
         while (global_ns() - t0 < 50000ull) {
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // ---------------- MMA issuer (first CTA) ----------------
+    if (lane == 0 && member == 0) {
+      // ---------------- MMA issuer (the pair's first CTA) ----------------
       constexpr uint32_t idesc = idesc_bf16_f32(2 * kTileN, BN);
       grid_dep_wait();
       int i = 0, j = 0;
@@ -1090,7 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * BN;
-        for (int k = 0; k < kb; ++k, ++i) {
+        for (int k = 0; k < nk; ++k, ++i) {
           const int s = i % P::kStages;
           if (!mbar_wait(&full[s], (i / P::kStages) & 1, &abort_flag)) {
             abort_flag = 1;
@@ -1104,27 +1126,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk)
             tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (k != 0 || kk != 0) ? 1u : 0u);
-          tc_commit_pair(&empty[s]);
+          tc_commit_pair(&empty[s], pair_mask);
         }
-        tc_commit_pair(&acc_full[buf]);
+        tc_commit_pair(&acc_full[buf], pair_mask);
       }
     }
   } else {
-    // ---------------- epilogue warps (both CTAs) ----------------
+    // ---------------- epilogue warps (every CTA) ----------------
     grid_dep_wait();
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t lead_acc_empty = mapa_shared(smem_u32(&acc_empty[0]), 0);
+    const uint32_t lead_acc_empty = mapa_shared(smem_u32(&acc_empty[0]), lead);
     int j = 0;
     for (int pt = pair; pt < pair_tiles; pt += n_pairs, ++j) {
       const int pr = pt / a.m_tiles, tm = pt - pr * a.m_tiles;
-      const int t = (2 * pr + static_cast<int>(rank)) * a.m_tiles + tm;   // this CTA's tile
+      const int tn = 2 * pr + static_cast<int>(member);
+      const int t = tn * a.m_tiles + tm;   // this CTA's tile
       const int buf = j & 1;
       tile_cols_prepare<BN, EC>(a, e, tm * BN, r, esh);
       float rpre[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) rpre[c] = 0.f;
+      // KS = 2 (one pair tile per cluster): the residual input of this CTA's
+      // columns goes into the spare accumulator while the MMAs run
+      uint32_t pre = 0;
+      if constexpr (KS == 2 && EC == kEcNorm) {
+        if (e.kind == EPI_RESID && tn < a.n_tiles) {
+          const int n = tn * kTileN + r, m0 = tm * BN;
+          pre = trow + (buf ^ 1) * BN;
+#pragma unroll 1
+          for (int c0 = cbeg; c0 < cend; c0 += 32) {
+            float xv[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int m = m0 + c0 + c;
+              xv[c] = (n < a.N && m < a.M) ? __ldcg(e.out_f32 + static_cast<size_t>(m) * e.ld_out + n) : 0.f;
+            }
+            tmem_store32(pre + c0, xv);
+          }
+          tmem_wait_st_gk();
+        }
+      }
       if (!mbar_wait(&acc_full[buf], (j >> 1) & 1, &abort_flag)) {
         abort_flag = 1;
         latch_status(a.status, kDevTimeout);
@@ -1134,11 +1177,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       epi_bar();
       if (esh.flag) break;
       tc_fence_after();
+      const uint32_t tb = trow + buf * BN;
+      const float* speer = nullptr;
+      if constexpr (KS == 2) {
+        // send the other half's CTA (same weight tile) the sums of its
+        // columns, straight into its idle ring, and take the sums of ours
+        const uint32_t other = crank ^ 2u;
+        const int obeg = static_cast<int>(half ^ 1u) * (BN / 2);
+        if (r == 0) mbar_arrive_remote(mapa_shared(smem_u32(&split_rdy), other));
+        bool ok = mbar_wait_cluster(&split_rdy, 0, &abort_flag);
+        if (ok) {
+          const uint32_t dst = mapa_shared(smem_u32(smem), other) + static_cast<uint32_t>(r) * 4u;
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+            float v[16];
+            tmem_ld16(tb + obeg + c0, v);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) st_cluster_f32(dst + static_cast<uint32_t>((c0 + c) * 128) * 4u, v[c]);
+          }
+          mbar_arrive_remote(mapa_shared(smem_u32(&split_dat), other));
+          ok = mbar_wait_cluster(&split_dat, 0, &abort_flag);
+        }
+        if (!ok) {
+          abort_flag = 1;
+          latch_status(a.status, kDevTimeout);
+        }
+        epi_bar();
+        if (r == 0) esh.flag = abort_flag;
+        epi_bar();
+        if (esh.flag) break;
+        speer = reinterpret_cast<const float*>(smem);
+      }
       // a pair's second weight tile past N (odd tile count) has no rows to store
-      if (2 * pr + static_cast<int>(rank) < a.n_tiles)
-        epilogue_tile<BN, EC>(a, rg, e, g, t, g, g, trow + buf * BN, r, esh, stg, 0u, rpre, 0, BN, nullptr);
-      if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, 2 * pair_tiles);
-      // hand the accumulator back to the first CTA's MMA thread
+      if (tn < a.n_tiles)
+        epilogue_tile<BN, EC>(a, rg, e, g, t, g, g, tb, r, esh, stg, pre, rpre, cbeg, cend, speer);
+      if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, KS * 2 * pair_tiles);
+      // hand the accumulator back to the pair's first CTA's MMA thread
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(lead_acc_empty + 8u * buf);
@@ -1150,21 +1224,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem, P::kTmemCols);
   }
-  // no CTA leaves while its peer may still read or signal its shared memory
+  // no CTA leaves while another may still read or signal its shared memory
   cluster_sync_all();
 }
 
 template <int EC>
 cudaError_t launch_pair(const AMaps& amaps, const ARegions& rg, const CUtensorMap& xmap, const GemmArgs& a,
                         const GemmEpi& e, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(gemm_pair_kernel<EC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           PairCfg::kSmem);
+  static bool attr_set[2] = {false, false};
+  const int ks = a.pair == 2 ? 1 : 0;
+  if (!attr_set[ks]) {
+    cudaError_t err = ks ? cudaFuncSetAttribute(gemm_pair_kernel<EC, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                PairCfg::kSmem)
+                         : cudaFuncSetAttribute(gemm_pair_kernel<EC, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                PairCfg::kSmem);
     if (err != cudaSuccess) return err;
-    attr_set = true;
+    attr_set[ks] = true;
   }
-  return launch_pdl_cluster(gemm_pair_kernel<EC>, dim3(a.grid), dim3(kThreads), PairCfg::kSmem, 2, stream, amaps,
+  if (ks)
+    return launch_pdl_cluster(gemm_pair_kernel<EC, 2>, dim3(a.grid), dim3(kThreads), PairCfg::kSmem, 4, stream, amaps,
+                              xmap, a, rg, e);
+  return launch_pdl_cluster(gemm_pair_kernel<EC, 1>, dim3(a.grid), dim3(kThreads), PairCfg::kSmem, 2, stream, amaps,
                             xmap, a, rg, e);
 }
 

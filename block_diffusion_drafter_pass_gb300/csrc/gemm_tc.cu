@@ -45,15 +45,28 @@ int gemm_token_tile(int M, int N, int num_sms) {
   return busy(128) > busy(256) + 0.05 ? 128 : 256;
 }
 
-bool gemm_cluster_split(int M, int N, int K, int splits, int num_sms) {
-  if (splits != 0 || gemm_token_tile(M, N, num_sms) != 256) return false;
+namespace {
+// Clusters of two CTA pairs, each over half of the k-blocks of one pair tile,
+// when four CTAs per pair tile fit one wave (256-token tiles).
+bool pair_split_ok(int M, int N, int K, int num_sms) {
+  const long long nt = (N + kTileN - 1) / kTileN;
+  if (M <= 128 || nt < 2 || (K + kTileK - 1) / kTileK < 2) return false;
+  return 4 * ((nt + 1) / 2) * ((M + 255) / 256) <= num_sms;
+}
+}  // namespace
+
+int gemm_pair_mode(int M, int N, int K, int splits, int num_sms) {
+  if (splits != 0 || M <= 128 || K < 1) return 0;
+  if (pair_split_ok(M, N, K, num_sms)) return 2;
   const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + 255) / 256);
-  return 2 * tiles <= num_sms && (K + kTileK - 1) / kTileK >= 2;
+  if (2 * tiles <= num_sms && (K + kTileK - 1) / kTileK >= 2) return 0;   // single-CTA cluster split
+  return pair_tiles_ok(M, N, num_sms) ? 1 : 0;
 }
 
-bool gemm_pair_mode(int M, int N, int K, int splits, int num_sms) {
-  if (splits != 0 || M <= 128 || K < 1 || gemm_cluster_split(M, N, K, splits, num_sms)) return false;
-  return pair_tiles_ok(M, N, num_sms);
+bool gemm_cluster_split(int M, int N, int K, int splits, int num_sms) {
+  if (splits != 0 || gemm_token_tile(M, N, num_sms) != 256 || pair_split_ok(M, N, K, num_sms)) return false;
+  const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + 255) / 256);
+  return 2 * tiles <= num_sms && (K + kTileK - 1) / kTileK >= 2;
 }
 
 int gemm_act_rows(int M, int N, int K, int num_sms) {
@@ -68,9 +81,11 @@ int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms
   // one cluster of two CTAs per tile, each with half of the k-blocks: the
   // stream-K partition of 2 x tiles CTAs is exactly that split
   if (gemm_cluster_split(M, N, K, splits, num_sms)) return static_cast<int>(2 * tiles);
-  // CTA pairs take whole pair tiles round-robin
-  if (gemm_pair_mode(M, N, K, splits, num_sms)) {
+  // CTA pairs take whole pair tiles round-robin; split pairs one pair tile
+  // per cluster of four
+  if (const int pm = gemm_pair_mode(M, N, K, splits, num_sms)) {
     const long long pair_tiles = static_cast<long long>(((N + kTileN - 1) / kTileN + 1) / 2) * ((M + BN - 1) / BN);
+    if (pm == 2) return static_cast<int>(4 * pair_tiles);
     return static_cast<int>(2 * std::min<long long>(pair_tiles, num_sms / 2));
   }
   const long long units = tiles * kb;
@@ -107,7 +122,7 @@ cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUten
   a.units = static_cast<long long>(a.n_tiles) * a.m_tiles * a.k_blocks;
   a.grid = gemm_grid(M, N, K, splits, work.partial_elems, num_sms);
   a.csplit = gemm_cluster_split(M, N, K, splits, num_sms) ? 1 : 0;
-  a.pair = gemm_pair_mode(M, N, K, splits, num_sms) ? 1 : 0;
+  a.pair = gemm_pair_mode(M, N, K, splits, num_sms);
   // the pair exchange addresses a 128 x 128 float block of the peer's ring
   // (BN = 256) and pairs CTAs 2t, 2t + 1
   if (a.csplit && (BN != 256 || a.grid != 2 * a.n_tiles * a.m_tiles)) return cudaErrorInvalidValue;

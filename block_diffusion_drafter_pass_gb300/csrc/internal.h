@@ -168,8 +168,10 @@ int gemm_token_tile(int M, int N, int num_sms);
 int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms);
 // True when each 256-token tile is split over K between the two CTAs of a cluster.
 bool gemm_cluster_split(int M, int N, int K, int splits, int num_sms);
-// True when CTA pairs run cta_group::2 MMAs over 256 x 256 pair tiles.
-bool gemm_pair_mode(int M, int N, int K, int splits, int num_sms);
+// CTA pairs running cta_group::2 MMAs over 256 x 256 pair tiles: 1 = pairs
+// take whole pair tiles, 2 = clusters of two pairs split one pair tile's
+// k-blocks; 0 = single-CTA tiles.
+int gemm_pair_mode(int M, int N, int K, int splits, int num_sms);
 // Box height of the activation tensor map the GEMM reads (its token tile, or
 // half of it when CTA pairs split the tokens).
 int gemm_act_rows(int M, int N, int K, int num_sms);

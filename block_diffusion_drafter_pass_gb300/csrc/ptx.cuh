@@ -290,13 +290,14 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc
       : "memory");
 }
 
-// Arrive once on the mbarrier at `bar`'s offset in both CTAs of the pair when
-// the pair MMAs issued so far have completed.
-__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+// Arrive once on the mbarrier at `bar`'s offset in the CTAs of `cta_mask`
+// (the pair: 0x3 << first rank) when the pair MMAs issued so far have
+// completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
-      "h"(static_cast<uint16_t>(0x3))
+      "h"(cta_mask)
       : "memory");
 }
 

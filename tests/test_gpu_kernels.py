@@ -32,10 +32,11 @@ DEV = "cuda:0"
     (1024, 300, 512, 1),      # two 256-token tiles with a ragged tail
     (640, 64, 2048, 3),       # explicit split-K
     (256, 128, 128, 2),
-    (2048, 512, 1024, 0),     # 256-token tiles split over K by 2-CTA clusters
+    (2048, 512, 1024, 0),     # clusters of two CTA pairs splitting each pair tile's k-blocks
     (1024, 300, 512, 0),      # the same with a ragged token tail
-    (512, 272, 960, 0),       # odd k-block count (15 = 7 + 8)
-    (384, 200, 64, 0),        # one k-block: 256-token tile, no split
+    (512, 272, 960, 0),       # the same with an odd k-block count (15 = 7 + 8)
+    (128, 512, 512, 0),       # one weight tile: 256-token tiles split over K by 2-CTA clusters
+    (384, 200, 64, 0),        # one k-block: CTA pairs, odd weight-tile count
     (6144, 512, 1024, 0),     # CTA pairs (cta_group::2), one pair tile per pair
     (24576, 512, 512, 0),     # CTA pairs, pair tiles dealt round-robin (3 rounds)
     (4992, 512, 256, 0),      # CTA pairs, odd weight-tile count (last pair half empty)

@@ -229,9 +229,9 @@ def test_gqa_group_layouts(dfl, n_heads, n_kv, blocks):
 def test_tiny_batch16_cluster_split(dfl):
     """16 sequences x B = 16 (256 block tokens) and a 256-row fuse: every
     projection (fuse, QKV with RoPE, O and down with the residual, gate/up
-    with SwiGLU, LM head with argmax) runs 256-token tiles split over K by
-    two-CTA clusters that exchange half sums through distributed shared
-    memory."""
+    with SwiGLU and an odd weight-tile count, LM head with argmax) runs as
+    clusters of two CTA pairs (cta_group::2 MMAs), each pair over half of the
+    k-blocks, exchanging half sums through distributed shared memory."""
     sh = TINY
     wn = make_weights_np(sh, seed=81, gamma="jitter", std=0.05)
     orc = oracle.OracleDrafter(sh, wn)
@@ -261,9 +261,10 @@ def test_tiny_batch16_cluster_split(dfl):
 
 
 def test_qwen3_8b_batch16_two_layers(dfl):
-    """8B width, 2 layers, 16 sequences x B = 16 = 256 block tokens: QKV, O
-    and down run 256-token tiles split over K by two-CTA clusters at full
-    width (fuse of 256 rows too); gate/up and the LM head stay stream-K."""
+    """8B width, 2 layers, 16 sequences x B = 16 = 256 block tokens: QKV, O,
+    down and the 256-row fuse run as clusters of two CTA pairs splitting the
+    k-blocks at full width; gate/up and the LM head run as CTA pairs over
+    whole pair tiles."""
     shape, wt, wn = _big_setup(2, seed=91)
     orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
     width = shape.n_feat_layers * shape.hidden
@@ -294,8 +295,9 @@ def test_qwen3_8b_batch16_two_layers(dfl):
 def test_qwen3_8b_batch32_two_layers(dfl):
     """8B width, 2 layers, 32 sequences x B = 16 = 512 block tokens: QKV
     (RoPE), gate/up (SwiGLU) and the LM head (argmax over 1187 weight tiles,
-    an odd count) run as CTA pairs issuing cta_group::2 MMAs; O, down and the
-    fuse run 256-token tiles split over K by clusters."""
+    an odd count) run as CTA pairs issuing cta_group::2 MMAs over whole pair
+    tiles; O, down and the fuse run as clusters of two pairs splitting the
+    k-blocks."""
     shape, wt, wn = _big_setup(2, seed=101)
     orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
     width = shape.n_feat_layers * shape.hidden
