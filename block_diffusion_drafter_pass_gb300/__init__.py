@@ -26,12 +26,12 @@ EXPORTED = (
     "dflash_create", "dflash_destroy", "dflash_last_error", "dflash_seq_reset", "dflash_seq_len",
     "dflash_fuse_ctx", "dflash_draft", "dflash_verify", "dflash_rows_argmax_bf16", "dflash_sync",
     "dflash_debug_read_kv", "dflash_debug_last_draft", "dflash_debug_gemm", "dflash_debug_profile",
-    "dflash_debug_profile_read", "dflash_gemm_noalloc",
+    "dflash_debug_profile_read", "dflash_gemm_noalloc", "dflash_set_path_selector", "dflash_debug_last_selection",
 )
 
 # Kernel classes of the per-kernel accounting (DFLASH_K_* in include/dflash.h).
 KERNEL_CLASSES = ("qkv", "attn", "attn_combine", "o", "gateup", "down", "lmhead", "fuse_wc", "fuse_kv", "norm",
-                  "verify", "other")
+                  "verify", "other", "select")
 
 
 class DFlashError(RuntimeError):
@@ -93,6 +93,8 @@ def load_library() -> ctypes.CDLL:
         "dflash_debug_profile": ([VP, I], I),
         "dflash_debug_profile_read": ([VP, P(dflash_kernel_stat), I], I),
         "dflash_gemm_noalloc": ([VP, VP, VP, I, I, I, I, VP], I),
+        "dflash_set_path_selector": ([VP, VP, VP, VP, I, VP], I),
+        "dflash_debug_last_selection": ([VP, VP, VP, VP], I),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -243,6 +245,23 @@ class Drafter:
                                             _ptr(bonus), _stream(stream)), self.ctx)
         return tau, bonus
 
+    def set_path_selector(self, w_a=None, w_b=None, w_h=None, stream=None) -> None:
+        """Install the DFlash 2 path selector (W_A, W_B, W_H: contiguous bf16
+        CUDA tensors [256, H]); no arguments removes it. While installed,
+        draft() returns the selector's walk over the top-16 candidates."""
+        import torch
+        ws = (w_a, w_b, w_h)
+        if all(w is None for w in ws):
+            _check(load_library().dflash_set_path_selector(self.ctx, 0, 0, 0, 256, _stream(stream)), self.ctx)
+            self._sel = None
+            return
+        for w in ws:
+            if w is None or w.dtype != torch.bfloat16 or not w.is_cuda or not w.is_contiguous() or w.dim() != 2:
+                raise DFlashError(DFLASH_EINVAL, "selector weights must be contiguous bf16 CUDA matrices")
+        _check(load_library().dflash_set_path_selector(self.ctx, _ptr(w_a), _ptr(w_b), _ptr(w_h), w_a.shape[0],
+                                                       _stream(stream)), self.ctx)
+        self._sel = ws   # W_H is read by every draft
+
     # state and inspection ------------------------------------------------------
     def seq_reset(self, seq: int) -> None:
         _check(load_library().dflash_seq_reset(self.ctx, seq), self.ctx)
@@ -286,3 +305,16 @@ class Drafter:
         top = np.empty(max(1, n_seq * (B - 1)), dtype=np.float32)
         _check(load_library().dflash_debug_last_draft(self.ctx, hid.ctypes.data, top.ctypes.data), self.ctx)
         return hid, top[: n_seq * (B - 1)]
+
+    def last_selection(self, n_seq: int, B: int):
+        """(candidate ids [rows, 16], their logits [rows, 16], pair scores
+        [rows, 16, 16]) of the last draft that ran the path selector, rows =
+        n_seq * (B - 1) in sequence-major order."""
+        import numpy as np
+        rows = n_seq * (B - 1)
+        cand = np.empty((max(1, rows), 16), dtype=np.int32)
+        u = np.empty((max(1, rows), 16), dtype=np.float32)
+        sc = np.empty((max(1, rows), 16, 16), dtype=np.float32)
+        _check(load_library().dflash_debug_last_selection(self.ctx, cand.ctypes.data, u.ctypes.data,
+                                                          sc.ctypes.data), self.ctx)
+        return cand[:rows], u[:rows], sc[:rows]

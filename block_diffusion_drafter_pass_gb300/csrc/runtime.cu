@@ -116,6 +116,18 @@ struct dflash_ctx {
   int* done = nullptr;
   float* top_logit = nullptr;
 
+  // path selector (installed by dflash_set_path_selector)
+  bool sel_on = false;
+  CUtensorMap m_wh{};
+  float* sel_table = nullptr;              // [V][512] W_A E | W_B E
+  float* sel_logits = nullptr;             // [max_rows][sel_ld] logits | H
+  int sel_ld = 0, sel_hcol = 0;
+  unsigned long long* sel_part = nullptr;  // [max_rows][32][16] slice keys
+  float* sel_scores = nullptr;             // [max_rows][16][16]
+  int32_t* sel_cand = nullptr;             // [max_rows][16]
+  float* sel_cand_u = nullptr;             // [max_rows][16]
+  int* sel_tickets = nullptr;              // [max_batch]
+
   // weight descriptors
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
   CUtensorMap m_lm{}, m_wc{}, m_pool{}, m_pool_vt{}, m_vblk{};
@@ -134,7 +146,7 @@ struct dflash_ctx {
   cudaEvent_t snap_event = nullptr;
   bool snap_pending = false;
 
-  int last_rows = 0, last_draft_rows = 0;
+  int last_rows = 0, last_draft_rows = 0, last_sel_rows = 0;
   int attn_ctas_per_sm = 0;
   std::string err = "no error";
 
@@ -327,7 +339,9 @@ dflash_status dflash_destroy(dflash_ctx* ctx) {
   cudaDeviceSynchronize();
   void* ptrs[] = {ctx->pool, ctx->rope, ctx->d_len, ctx->d_pend, ctx->d_page_table, ctx->d_status, ctx->x,
                   ctx->hg, ctx->ssA, ctx->ssB, ctx->q, ctx->kb, ctx->vb, ctx->attn, ctx->act, ctx->htg, ctx->ssF,
-                  ctx->part_o, ctx->part_ml, ctx->split_ws, ctx->tickets, ctx->keys, ctx->done, ctx->top_logit};
+                  ctx->part_o, ctx->part_ml, ctx->split_ws, ctx->tickets, ctx->keys, ctx->done, ctx->top_logit,
+                  ctx->sel_table, ctx->sel_logits, ctx->sel_part, ctx->sel_scores, ctx->sel_cand, ctx->sel_cand_u,
+                  ctx->sel_tickets};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (ctx->h_snap) cudaFreeHost(ctx->h_snap);
@@ -919,7 +933,56 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   }
   ctx->last_rows = M;
   ctx->last_draft_rows = n_seq * (B - 1);
-  if (B > 1) {
+  ctx->last_sel_rows = ctx->sel_on ? n_seq * (B - 1) : 0;
+  if (B > 1 && ctx->sel_on) {
+    // LM head and the selector's context gate H = W_H h~ in one GEMM over all
+    // block rows, final RMSNorm scale applied: logits in columns [0, V), H in
+    // [sel_hcol, sel_hcol + 256). Then top-16, pair scores and the walk.
+    const int Md = n_seq * (B - 1);
+    const int n_out = ctx->sel_hcol + kSelDim;
+    const CUtensorMap* hmap_sel = act_map(ctx, ctx->hg, M, H, gemm_act_rows(M, n_out, H, sms));
+    if (!hmap_sel) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+    AMaps am;
+    am.m[0] = ctx->m_lm;
+    am.m[1] = ctx->m_wh;
+    GemmEpi e = base_epi(ctx, EPI_F32_STORE);
+    e.out_f32 = ctx->sel_logits;
+    e.ld_out = ctx->sel_ld;
+    e.in_ss = ctx->ssA;
+    e.in_ss_parts = parts;
+    e.in_ss_ld = rows_ld;
+    {
+      ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(M, n_out, H, n_out, 4), 2.0 * M * n_out * H);
+      CK(launch_gemm(am, stacked({c.vocab, kSelDim}), *hmap_sel, M, n_out, H, 0, e, work, ctx->num_sms, stream));
+    }
+    SelectArgs sa;
+    sa.n_seq = n_seq;
+    sa.B = B;
+    sa.V = c.vocab;
+    sa.logits = ctx->sel_logits;
+    sa.ld = ctx->sel_ld;
+    sa.h_col = ctx->sel_hcol;
+    // about two CTAs per SM over the draft rows, at most 32 slices per row
+    int slices = std::min(kSelMaxSlices, std::max(1, ceil_div(2 * sms, Md)));
+    sa.slice_cols = 4 * ceil_div(ceil_div(c.vocab, slices), 4);
+    sa.slices = ceil_div(c.vocab, sa.slice_cols);
+    sa.part = ctx->sel_part;
+    sa.table = ctx->sel_table;
+    sa.anchors = anchor_ids;
+    sa.scores = ctx->sel_scores;
+    sa.cand = ctx->sel_cand;
+    sa.cand_u = ctx->sel_cand_u;
+    sa.top_logit = ctx->top_logit;
+    sa.tickets = ctx->sel_tickets;
+    sa.draft_ids = draft_ids;
+    sa.status = ctx->d_status;
+    // logits read once, the 16-key lists, candidate rows of the A|B table,
+    // H rows, the scores and ids
+    const double sel_bytes = 4.0 * Md * (c.vocab + kSelDim) + 2.0 * 8 * Md * sa.slices * kSelK +
+                             4.0 * Md * kSelK * 2 * kSelDim + 4.0 * Md * kSelK * kSelK + 4.0 * Md;
+    ProfScope ps(ctx, DFLASH_K_SELECT, stream, sel_bytes, 2.0 * Md * kSelK * kSelK * kSelDim, 2);
+    CK(launch_path_select(sa, stream));
+  } else if (B > 1) {
     // LM head over all block rows (the anchor rows are skipped in the epilogue),
     // final RMSNorm folded in: the argmax is taken on the unscaled logits (a
     // positive per-row scale does not move it) and the winning logit is scaled.
@@ -1018,6 +1081,88 @@ dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0
         for (int di = 0; di < d; ++di) v_out[(static_cast<size_t>(t) * nkv + h) * d + di] = vs[static_cast<size_t>(di) * kPage];
     }
   }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, const uint16_t* w_b,
+                                       const uint16_t* w_h, int dim, void* stream_v) {
+  if (!ctx) return DFLASH_EINVAL;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const dflash_config& c = ctx->cfg;
+  const int H = c.hidden;
+  if (!w_a && !w_b && !w_h) {
+    ctx->sel_on = false;
+    return DFLASH_OK;
+  }
+  if (!w_a || !w_b || !w_h) return fail(ctx, DFLASH_EINVAL, "w_a, w_b, w_h must be all set or all NULL");
+  if (dim != kSelDim) return fail(ctx, DFLASH_EINVAL, "selector width must be 256");
+  if (c.vocab < kSelK) return fail(ctx, DFLASH_EINVAL, "vocab below the 16 candidates");
+  if (!aligned16(w_a) || !aligned16(w_b) || !aligned16(w_h)) return fail(ctx, DFLASH_EINVAL, "weights not 16-byte aligned");
+  const size_t rows = ctx->max_rows();
+  if (!ctx->sel_table) {
+    ctx->sel_hcol = 128 * ceil_div(c.vocab, 128);   // H starts at the first tile after the vocabulary
+    ctx->sel_ld = ctx->sel_hcol + kSelDim;
+    cudaError_t e = dalloc(&ctx->sel_table, static_cast<size_t>(c.vocab) * 2 * kSelDim);
+    if (e == cudaSuccess) e = dalloc(&ctx->sel_logits, rows * ctx->sel_ld);
+    if (e == cudaSuccess) e = dalloc(&ctx->sel_part, rows * kSelMaxSlices * kSelK);
+    if (e == cudaSuccess) e = dalloc(&ctx->sel_scores, rows * kSelK * kSelK);
+    if (e == cudaSuccess) e = dalloc(&ctx->sel_cand, rows * kSelK);
+    if (e == cudaSuccess) e = dalloc(&ctx->sel_cand_u, rows * kSelK);
+    if (e == cudaSuccess) e = dalloc(&ctx->sel_tickets, c.max_batch);
+    if (e == cudaSuccess) e = cudaMemset(ctx->sel_tickets, 0, c.max_batch * sizeof(int));
+    if (e != cudaSuccess) {
+      void* ps[] = {ctx->sel_table, ctx->sel_logits, ctx->sel_part, ctx->sel_scores, ctx->sel_cand, ctx->sel_cand_u,
+                    ctx->sel_tickets};
+      for (void* p : ps)
+        if (p) cudaFree(p);
+      ctx->sel_table = nullptr;
+      ctx->sel_logits = nullptr;
+      ctx->sel_part = nullptr;
+      ctx->sel_scores = nullptr;
+      ctx->sel_cand = nullptr;
+      ctx->sel_cand_u = nullptr;
+      ctx->sel_tickets = nullptr;
+      return fail(ctx, e == cudaErrorMemoryAllocation ? DFLASH_ENOMEM : DFLASH_ECUDA,
+                  std::string("selector buffers: ") + cudaGetErrorString(e));
+    }
+  }
+  ctx->sel_on = false;
+  CUtensorMap m_wa, m_wb;
+  if (!encode_2d(&m_wa, w_a, kSelDim, H, kWeightBoxRows) || !encode_2d(&m_wb, w_b, kSelDim, H, kWeightBoxRows) ||
+      !encode_2d(&ctx->m_wh, w_h, kSelDim, H, kWeightBoxRows))
+    return fail(ctx, DFLASH_ECUDA, "selector weight descriptor encode failed");
+  // table[v] = (W_A E[v] | W_B E[v]): the embedding rows are the tokens of a
+  // GEMM against the stacked [W_A; W_B], in chunks of at most 1024 rows
+  constexpr int kChunk = 1024;
+  GemmWork work = gemm_work(ctx);
+  AMaps am;
+  am.m[0] = m_wa;
+  am.m[1] = m_wb;
+  for (int r0 = 0; r0 < c.vocab; r0 += kChunk) {
+    const int M = std::min(kChunk, c.vocab - r0);
+    CUtensorMap xm;
+    if (!encode_2d(&xm, ctx->w.embed + static_cast<size_t>(r0) * H, M, H,
+                   gemm_act_rows(M, 2 * kSelDim, H, ctx->num_sms)))
+      return fail(ctx, DFLASH_ECUDA, "embedding descriptor encode failed");
+    GemmEpi e = base_epi(ctx, EPI_F32_STORE);
+    e.out_f32 = ctx->sel_table + static_cast<size_t>(r0) * 2 * kSelDim;
+    e.ld_out = 2 * kSelDim;
+    CK(launch_gemm(am, stacked({kSelDim, kSelDim}), xm, M, 2 * kSelDim, H, 0, e, work, ctx->num_sms, stream));
+  }
+  CK(cudaStreamSynchronize(stream));
+  ctx->sel_on = true;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_debug_last_selection(dflash_ctx* ctx, int32_t* cand_out, float* u_out, float* scores_out) {
+  if (!ctx) return DFLASH_EINVAL;
+  if (!ctx->last_sel_rows) return fail(ctx, DFLASH_EINVAL, "the last draft did not run the path selector");
+  CK(cudaDeviceSynchronize());
+  const size_t n = ctx->last_sel_rows;
+  if (cand_out) CK(cudaMemcpy(cand_out, ctx->sel_cand, n * kSelK * sizeof(int32_t), cudaMemcpyDeviceToHost));
+  if (u_out) CK(cudaMemcpy(u_out, ctx->sel_cand_u, n * kSelK * sizeof(float), cudaMemcpyDeviceToHost));
+  if (scores_out)
+    CK(cudaMemcpy(scores_out, ctx->sel_scores, n * kSelK * kSelK * sizeof(float), cudaMemcpyDeviceToHost));
   return DFLASH_OK;
 }
 

@@ -186,6 +186,32 @@ dflash_status dflash_rows_argmax_bf16(const uint16_t* logits, int rows, int cols
  * device status word: OK, ETIMEOUT or EDEVICE. */
 dflash_status dflash_sync(dflash_ctx* ctx);
 
+/* Install (or remove) the DFlash 2 path selector ("DFlash 2" notes,
+ * "Solution - Lightweight Path Selector"). While installed, dflash_draft
+ * keeps the 16 largest logits of every masked position t as its candidates
+ * C_t (largest first, lower id first among equal logits), scores every
+ * adjacent pair a in C_{t-1}, b in C_t as
+ *     S_t(a, b) = U_t(b) + < A(a) * H(h_t), B(b) >
+ * (U_t the drafter's logit, * elementwise, C_0's predecessor the anchor) and
+ * returns the greedy walk: at each position the candidate with the largest
+ * score after the previous pick (the higher-ranked one among equal scores),
+ * instead of the plain argmax ids. The maps are linear:
+ *     A(a) = W_A E[a],  B(b) = W_B E[b],  H(h_t) = W_H h~_t,
+ * E the drafter's token embedding and h~_t the final-normalised hidden state
+ * that the LM head reads.
+ *
+ *  w_a, w_b, w_h  device [dim, H] bf16, 16-byte aligned; all three NULL
+ *                 removes the selector. W_A and W_B are read only here (the
+ *                 library keeps A and B of every token, V x 512 fp32); W_H is
+ *                 borrowed like the other weights.
+ *  dim            256
+ * Enqueued on `stream`, then waits for it. The first install allocates the
+ * tables and buffers (V*2 KB plus max_batch*max_block rows of (V+256) fp32
+ * logits). Errors: EINVAL (dim != 256, vocab < 16, some but not all pointers
+ * NULL, misaligned pointer), ENOMEM, ECUDA. */
+dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, const uint16_t* w_b,
+                                       const uint16_t* w_h, int dim, void* stream);
+
 /* ---- inspection hooks (used by the parity tests; they synchronise) ---- */
 
 /* Copy `n` cached tokens of layer `layer` of `seq`, starting at position
@@ -198,6 +224,15 @@ dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0
  * [n_seq*B, H] fp32 (before the final RMSNorm), and the winning logit of each
  * draft row [n_seq*(B-1)] fp32. Host outputs; either may be NULL. */
 dflash_status dflash_debug_last_draft(dflash_ctx* ctx, float* hidden_out, float* top_logit_out);
+
+/* Selector state of the last dflash_draft call made with the selector
+ * installed, per draft row r = i*(B-1) + t (host outputs, any may be NULL):
+ *  cand_out    [rows, 16] int32  candidate ids C_t, largest logit first
+ *  u_out       [rows, 16] fp32   their logits U_t
+ *  scores_out  [rows, 16, 16] fp32  S_t(a, b), a the rank in C_{t-1}, b the
+ *              rank in C_t; at t = 0 only a = 0 (the anchor) is defined.
+ * EINVAL when the last draft did not run the selector. */
+dflash_status dflash_debug_last_selection(dflash_ctx* ctx, int32_t* cand_out, float* u_out, float* scores_out);
 
 /* Y[M, N] (fp32) = X[M, K] * W[N, K]^T with the library's tensor-core GEMM,
  * all device pointers (W, X bf16; K multiple of 8). splits = split-K factor
@@ -248,6 +283,7 @@ enum {
   DFLASH_K_NORM,          /* embedding and RMSNorm rows                 */
   DFLASH_K_VERIFY,        /* verify + commit                            */
   DFLASH_K_OTHER,         /* bookkeeping kernels                        */
+  DFLASH_K_SELECT,        /* path selector: top-16, pair scores, walk   */
   DFLASH_K_COUNT
 };
 

@@ -103,7 +103,7 @@ def select_block(weights, shape, sel: Dict[str, np.ndarray], anchor: int, k_ctx,
     h_gates = hf @ sel["w_h"].T
     ids, gaps, picks = greedy_walk(anchor, cands, u, weights["embed"], sel["w_a"], sel["w_b"], h_gates)
     return {"draft": ids, "gap": gaps, "pick": picks, "cand": cands, "u": u, "gap16": gap16,
-            "plain_draft": base["draft"], "hidden": base["hidden"]}
+            "h_gate": h_gates, "logits": logits, "plain_draft": base["draft"], "hidden": base["hidden"]}
 
 
 def drafter_select(orc, seq_ids, anchors, B: int, sel: Dict[str, np.ndarray]):

@@ -12,6 +12,7 @@ from .generators import (  # noqa: F401
     bf16_bits,
     bits_to_f32,
     make_weights_np,
+    make_selector_weights_np,
     make_weights_torch,
     torch_weights_to_np,
     make_features_np,

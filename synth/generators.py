@@ -180,6 +180,24 @@ def torch_weights_to_np(w) -> Dict[str, object]:
 # Activations, ids, lengths
 # ----------------------------------------------------------------------------
 
+def make_selector_weights_np(shape: DrafterShape, seed: int = 0, dim: int = 256,
+                             std: float = None, embed_std: float = 0.02,
+                             lm_std: float = 0.02) -> Dict[str, np.ndarray]:
+    """Path-selector maps W_A, W_B, W_H [dim, H] as float32 arrays of bf16 values.
+
+    The default std makes the pair term's spread comparable to the logits'
+    spread, so the selector's walk both follows and leaves the plain greedy
+    path: with E ~ N(0, embed_std^2), normalised hidden rows of unit RMS and
+    W ~ N(0, std^2), the pair term has std sqrt(dim) std^3 embed_std^2 H^1.5
+    and a logit std lm_std sqrt(H); std solves their equality.
+    """
+    H = shape.hidden
+    if std is None:
+        std = float((lm_std / (np.sqrt(dim) * embed_std ** 2 * H)) ** (1.0 / 3.0))
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return {k: _normal(rng, (dim, H), std) for k in ("w_a", "w_b", "w_h")}
+
+
 def make_features_np(n_tokens: int, width: int, seed: int) -> np.ndarray:
     """Concatenated target features [n, L_f*H], N(0, 1) per element, bf16 values."""
     rng = np.random.Generator(np.random.PCG64(seed))

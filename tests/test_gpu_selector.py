@@ -1,0 +1,200 @@
+"""The path selector's CUDA path against the CPU oracle through the C ABI.
+
+What must agree with oracle.path_selector ("DFlash 2" notes, "Solution -
+Lightweight Path Selector"): each row's 16 candidates form a top-16 of the
+oracle's logits within the logit tolerance (the oracle's exact set where its
+16th and 17th logits are more than GAP apart), carry the oracle's logits, and
+every pair score S_t(a, b) over those lists matches the oracle's; the walk's
+pick at each position, given its own previous pick, is the oracle's argmax
+wherever the oracle's best and second-best scores are more than GAP apart.
+Cases: the tiny drafter with ragged contexts at B = 2, 8, 16 and 32 (one to
+32 column slices per row, up to 31 positions in the walk), 32 sequences of
+the tiny drafter (512 block rows: CTA-pair LM head with the H rows stacked),
+and the Qwen3-8B shape (vocabulary 151936, 11 column slices) at 2 layers.
+With W_H = 0 the walk must return the plain greedy draft.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import path_selector as ops
+from synth import (TINY, QWEN3_8B, make_weights_np, make_selector_weights_np, make_features_np,
+                   make_anchor_ids_np, make_weights_torch, torch_weights_to_np)
+from tests.gpu_util import np_weights_to_device, bf16_dev, i32_dev, assert_close, GAP, ATOL, RTOL
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def dfl():
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_diffusion_drafter_pass_gb300 as m
+    return m
+
+
+def _sel_dev(sel):
+    return {k: bf16_dev(v, DEV) for k, v in sel.items()}
+
+
+def _compare_selection(d, orc, sel_np, seqs, anchors, B, got_ids, what):
+    """Check one selector draft; returns (walk decisions checked, oracle results).
+
+    Candidate lists: distinct ids in non-increasing logit order, logits within
+    the logit tolerance of the oracle's, and a valid top-16 of the oracle's
+    logits (no excluded id beats an included one by more than twice the
+    tolerance); where the oracle's 16th and 17th logits are more than GAP
+    apart, the oracle's own set. Pair scores: the oracle's S_t(a, b) over the
+    library's candidate lists. Walk: at every position, given the library's
+    own previous pick, the pick must be the oracle's argmax wherever the
+    oracle's best and second-best scores are more than GAP apart.
+    """
+    ref = ops.drafter_select(orc, seqs, anchors, B, sel_np)
+    cand, u, sc = d.last_selection(len(seqs), B)
+    T = B - 1
+    E = orc.w["embed"]
+    s_w = {k: np.asarray(v, dtype=E.dtype) for k, v in sel_np.items()}
+    checked = 0
+    for i, r in enumerate(ref):
+        for t in range(T):
+            row = i * T + t
+            c = cand[row]
+            L = r["logits"][t]
+            tag = f"{what} seq {i} t {t}"
+            assert len(set(c.tolist())) == ops.K_SEL and c.min() >= 0 and c.max() < L.shape[0], f"{tag}: ids"
+            assert np.all(np.diff(u[row]) <= 0), f"{tag}: candidates not in logit order"
+            assert_close(u[row], L[c], f"{tag}: candidate logits")
+            out = np.ones(L.shape[0], dtype=bool)
+            out[c] = False
+            tol = ATOL + RTOL * np.abs(L)
+            worst_in = np.min(L[c] + tol[c])
+            assert np.max(L[out] - tol[out]) <= worst_in, f"{tag}: not a top-16 of the oracle's logits"
+            if r["gap16"][t] > GAP:
+                assert sorted(c.tolist()) == sorted(r["cand"][t].tolist()), f"{tag}: candidate set"
+            prev = [int(anchors[i])] if t == 0 else cand[row - 1].tolist()
+            s_ref = ops.pair_scores(L[c], c, prev, E, s_w["w_a"], s_w["w_b"], r["h_gate"][t])
+            assert_close(sc[row][: len(prev)], s_ref, f"{tag}: pair scores")
+            p = 0 if t == 0 else int(np.flatnonzero(cand[row - 1] == got_ids[i, t - 1])[0])
+            srt = np.sort(s_ref[p])[::-1]
+            if srt[0] - srt[1] > GAP:
+                assert got_ids[i, t] == c[int(np.argmax(s_ref[p]))], f"{tag}: walk id"
+                checked += 1
+    return checked, ref
+
+
+def _tiny(dfl, max_batch, max_block, seed=3):
+    wn = make_weights_np(TINY, seed=seed)
+    d = dfl.Drafter(TINY, np_weights_to_device(wn, DEV), max_seqs=max_batch, max_batch=max_batch,
+                    max_block=max_block, max_ctx=512, max_fuse_tokens=10000)
+    return d, wn, oracle.OracleDrafter(TINY, wn)
+
+
+def test_tiny_selector_ragged_block_sizes(dfl):
+    d, wn, orc = _tiny(dfl, max_batch=6, max_block=32)
+    with d:
+        sel = make_selector_weights_np(TINY, seed=21)
+        d.set_path_selector(**_sel_dev(sel))
+        width = TINY.n_feat_layers * TINY.hidden
+        lens = [0, 1, 63, 64, 130, 257]
+        f = make_features_np(sum(lens), width, seed=22)
+        seqs = list(range(6))
+        d.fuse_ctx(seqs, lens, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(seqs, lens, f, pending=False)
+        anchors = make_anchor_ids_np(6, TINY.vocab, seed=23)
+        total, differs = 0, 0
+        for B, idx in ((16, seqs), (8, seqs), (2, seqs), (32, [5]), (16, [2])):
+            a = anchors[idx]
+            ids = d.draft(idx, i32_dev(a, DEV), B)
+            d.sync()
+            walked, ref = _compare_selection(d, orc, sel, idx, a, B, ids.cpu().numpy(), f"tiny B={B}")
+            total += walked
+            differs += sum(int((r["draft"] != r["plain_draft"]).any()) for r in ref)
+        assert total >= 40, total
+        assert differs > 0, "the walk never left the greedy path: the case does not exercise the pair term"
+
+
+def test_tiny_selector_batch32_pair_tiles(dfl):
+    d, wn, orc = _tiny(dfl, max_batch=32, max_block=16, seed=5)
+    with d:
+        sel = make_selector_weights_np(TINY, seed=31)
+        d.set_path_selector(**_sel_dev(sel))
+        width = TINY.n_feat_layers * TINY.hidden
+        rng = np.random.default_rng(32)
+        lens = [int(x) for x in rng.integers(0, 300, size=32)]
+        f = make_features_np(sum(lens), width, seed=33)
+        seqs = list(range(32))
+        d.fuse_ctx(seqs, lens, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(seqs, lens, f, pending=False)
+        anchors = make_anchor_ids_np(32, TINY.vocab, seed=34)
+        ids = d.draft(seqs, i32_dev(anchors, DEV), 16)
+        d.sync()
+        walked, _ = _compare_selection(d, orc, sel, seqs, anchors, 16, ids.cpu().numpy(), "tiny batch 32")
+        assert walked >= 100, walked
+
+
+def test_selector_with_zero_gate_is_greedy(dfl):
+    """W_H = 0 leaves S_t(a, b) = U_t(b): the walk is the plain argmax draft."""
+    d, wn, orc = _tiny(dfl, max_batch=4, max_block=16, seed=7)
+    with d:
+        width = TINY.n_feat_layers * TINY.hidden
+        lens = [40, 0, 200, 77]
+        f = make_features_np(sum(lens), width, seed=41)
+        seqs = [0, 1, 2, 3]
+        d.fuse_ctx(seqs, lens, bf16_dev(f, DEV), pending=False)
+        anchors = i32_dev(make_anchor_ids_np(4, TINY.vocab, seed=42), DEV)
+        plain = d.draft(seqs, anchors, 16).cpu().numpy()
+        _, top = d.last_draft(4, 16)
+        sel = make_selector_weights_np(TINY, seed=43)
+        sel["w_h"] = np.zeros_like(sel["w_h"])
+        d.set_path_selector(**_sel_dev(sel))
+        walk = d.draft(seqs, anchors, 16).cpu().numpy()
+        cand, u, _ = d.last_selection(4, 16)
+        d.sync()
+        gap = u[:, 0] - u[:, 1]
+        sure = (gap > 1e-3).reshape(4, 15)
+        np.testing.assert_array_equal(walk[sure], plain[sure])
+        np.testing.assert_array_equal(cand[:, 0].reshape(4, 15)[sure], plain[sure])
+        assert_close(u[:, 0], top, "top logits with and without the selector")
+        # removing the selector restores the plain draft
+        d.set_path_selector()
+        again = d.draft(seqs, anchors, 16).cpu().numpy()
+        d.sync()
+        np.testing.assert_array_equal(again, plain)
+
+
+def test_qwen3_8b_shape_selector_two_layers(dfl):
+    shape = QWEN3_8B.with_layers(2)
+    wt = make_weights_torch(shape, seed=51, device=DEV, gamma="jitter")
+    wn = torch_weights_to_np(wt)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    width = shape.n_feat_layers * shape.hidden
+    with dfl.Drafter(shape, wt, max_seqs=2, max_batch=2, max_block=16, max_ctx=1024,
+                     max_fuse_tokens=1024) as d:
+        sel = make_selector_weights_np(shape, seed=52)
+        d.set_path_selector(**_sel_dev(sel))
+        f = make_features_np(900, width, seed=53)
+        d.fuse_ctx([0, 1], [200, 700], bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx([0, 1], [200, 700], f, pending=False)
+        anchors = make_anchor_ids_np(2, shape.vocab, seed=54)
+        ids = d.draft([0, 1], i32_dev(anchors, DEV), 16)
+        d.sync()
+        walked, _ = _compare_selection(d, orc, sel, [0, 1], anchors, 16, ids.cpu().numpy(), "8B 2-layer")
+        assert walked >= 4, walked
+
+
+def test_selector_argument_errors(dfl):
+    d, wn, _ = _tiny(dfl, max_batch=2, max_block=8)
+    with d:
+        sel = _sel_dev(make_selector_weights_np(TINY, seed=1))
+        with pytest.raises(dfl.DFlashError) as e:
+            d.set_path_selector(sel["w_a"], sel["w_b"], None)
+        assert e.value.status == dfl.DFLASH_EINVAL
+        lib = dfl.load_library()
+        st = lib.dflash_set_path_selector(d.ctx, sel["w_a"].data_ptr(), sel["w_b"].data_ptr(),
+                                          sel["w_h"].data_ptr(), 128, None)
+        assert st == dfl.DFLASH_EINVAL
+        # no selection to read before a selector draft
+        with pytest.raises(dfl.DFlashError):
+            d.last_selection(1, 8)
