@@ -344,6 +344,9 @@ def run_ours(args):
     start_lens = [max(0, c - W - K // 2) for c in lens]
     shape = QWEN3_8B.with_layers(args.layers)
     cyc = Cycle(dfl, shape, batch, start_lens, B, total_steps, seed=1000 * rank, dev=dev)
+    sel = selector_weights(shape, dev, seed=7 + rank)
+    if args.path_selector:
+        cyc.d.set_path_selector(**sel)
 
     # NVTX range names let a profiler select the warm-up steps
     # (ncu --nvtx --nvtx-include "warmup/")
@@ -386,6 +389,20 @@ def run_ours(args):
     kd = min(K, 200)
     ms_draft = timed(lambda k: cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts), kd, world, dev)
     len_end = cyc.d.seq_len(0)[0]
+    # the drafter pass with the other selector setting (plain argmax <-> path selector)
+    cyc.d.set_path_selector(**({} if args.path_selector else sel))
+    for _ in range(3):
+        cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts)
+    ms_other = timed(lambda k: cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts), kd, world, dev)
+    cyc.d.profile_read()
+    cyc.d.profile(True)
+    timed(lambda k: cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts), kd, world, dev)
+    cyc.d.profile(False)
+    st_other = cyc.d.profile_read()
+    cyc.d.set_path_selector(**(sel if args.path_selector else {}))
+    ms_sel, ms_plain = (ms_draft, ms_other) if args.path_selector else (ms_other, ms_draft)
+    st_sel = stats if args.path_selector else st_other
+    n_sel = K if args.path_selector else kd
 
     if rank != 0:
         return None
@@ -417,7 +434,9 @@ def run_ours(args):
                    "context": ctx if ctx else f"U[{spread[0]}, {spread[1]}]",
                    "context_at_timed_start": start_lens[0] + W, "context_at_end": len_end,
                    "global_batch": batch * world, "parallelism": f"replicas x{world}",
-                   "step": "rows_argmax(target logits) + fuse_ctx(B, pending) + verify + draft",
+                   "step": "rows_argmax(target logits) + fuse_ctx(B, pending) + verify + draft"
+                           + (" (path selector installed: draft returns its walk)" if args.path_selector else ""),
+                   "path_selector": bool(args.path_selector),
                    "l2": "no flush: each step streams 3.4 GB of weights (> 129 MB L2)"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -436,9 +455,37 @@ def run_ours(args):
                        "ms_per_pass": ms_draft / kd},
         "latency_model": latency_model(ms_draft / kd, max_ms / K, peaks["hbm_gbs"], B),
         "kernels": kernels,
+        "path_selector": selector_summary(st_sel, n_sel, ms_sel / kd, ms_plain / kd, peaks, peak_kind, batch, world),
     }
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(shape, cyc.weights, lens[0], B)
+    return out
+
+
+def selector_weights(shape, dev, seed: int):
+    """Seeded W_A, W_B, W_H [256, H] of the DFlash 2 path selector on the device."""
+    import torch
+    from synth import make_selector_weights_np
+    return {k: torch.from_numpy(v).to(torch.bfloat16).to(dev)
+            for k, v in make_selector_weights_np(shape, seed=seed).items()}
+
+
+def selector_summary(st, n, ms_sel: float, ms_plain: float, peaks, peak_kind: str, batch: int, world: int):
+    """The drafter pass with the path selector against the plain pass, and the
+    selector kernels (top-16 over the fp32 logits, pair scores and walk)
+    against the HBM roofline."""
+    sel = st.get("select", {})
+    lm = st.get("lmhead", {})
+    out = {"passes_per_s": whole_job_rate(1, world, ms_sel) if ms_sel else None, "ms_per_pass": ms_sel,
+           "plain_ms_per_pass": ms_plain, "overhead_ms": ms_sel - ms_plain, "overhead_frac": ms_sel / ms_plain - 1.0,
+           "batch": batch}
+    if sel.get("launches") and sel.get("ms"):
+        gbs = sel["bytes"] / (sel["ms"] / 1e3) / 1e9
+        out.update({"select_us_per_pass": 1e3 * sel["ms"] / n, "select_launches_per_pass": sel["launches"] / n,
+                    "select_GB_per_pass": sel["bytes"] / n / 1e9,
+                    "select_roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_kind} hbm_gbs"},
+                    "lmhead_us_per_pass": 1e3 * lm["ms"] / n if lm.get("ms") else None})
     return out
 
 
@@ -683,6 +730,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=5,
                     help="drafter depth (5 = the benchmarked drafter; fewer only for small profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path-selector", action="store_true",
+                    help="install the DFlash 2 path selector for the timed cycle (draft returns its walk)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

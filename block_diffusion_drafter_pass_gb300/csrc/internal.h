@@ -258,18 +258,20 @@ cudaError_t launch_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, 
 // ----------------------------------------------------------------------------
 constexpr int kSelK = 16;          // candidates per masked position
 constexpr int kSelDim = 256;       // width of A, B and H
-constexpr int kSelMaxSlices = 32;  // column slices of a row (one per lane in the merge)
+constexpr int kSelMaxSlices = 64;  // column slices of a row
+constexpr int kSelSliceCols = 8192;  // columns of one slice (256 threads x 8 float4)
 struct SelectArgs {
   int n_seq, B, V;
   const float* logits;            // [n_seq*B][ld] fp32, scaled logits in [0, V), H(h_t) at [h_col, h_col+256)
   int ld, h_col;
-  int slices, slice_cols;         // row split of the top-16 pass (slice_cols a multiple of 4)
+  int slices;                     // ceil(V / kSelSliceCols) <= kSelMaxSlices
   unsigned long long* part;       // [n_seq*(B-1)][slices][16] keys
   const float* table;             // [V][512] fp32: W_A E[v] | W_B E[v]
   const int32_t* anchors;         // [n_seq]
   float* scores;                  // [n_seq][B-1][16][16]
   int32_t* cand;                  // [n_seq][B-1][16]
   float* cand_u;                  // [n_seq][B-1][16]
+  int32_t* next;                  // [n_seq][B-1][16] the walk's pick after each predecessor rank
   float* top_logit;               // [n_seq][B-1]
   int* tickets;                   // [n_seq], zero between launches
   int32_t* draft_ids;             // [n_seq][B-1]

@@ -36,8 +36,15 @@ namespace dfl {
 namespace {
 
 constexpr int kTopThreads = 256;
+constexpr int kTopQ = 8;                                  // float4 per thread
+constexpr int kSliceCols = kTopThreads * 4 * kTopQ;       // 8192 columns per CTA
+constexpr int kTopCandCap = 8 * 16 * 4 * kTopQ;           // 8 warps x 16 lanes x 32 keys
 constexpr int kPairThreads = 512;
 constexpr int kPadRow = kSelDim + 1;   // shared-memory row pitch (bank spread)
+static_assert(kSliceCols == kSelSliceCols, "slice width");
+static_assert(kSelDim == 256, "H(h_t) is loaded by one thread per dimension of the first 256");
+static_assert(2 * 2 * kSelMaxSlices * kSelK * 8 <= 2 * kSelK * kPadRow * 4, "merge lists fit the staging buffer");
+static_assert(kMaxBlock * kSelK * kSelK <= 2 * kSelK * kPadRow, "the walk's scores fit the staging buffer");
 
 // Order-preserving 64-bit key of (logit, column): larger logit first, lower
 // column first among equal logits. 0 never arises from a number and marks an
@@ -58,104 +65,123 @@ __device__ __forceinline__ int key_col(unsigned long long k) {
   return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k));
 }
 
-// t[] sorted in decreasing order; keeps the kSelK largest of t and k.
-__device__ __forceinline__ void top_insert(unsigned long long (&t)[kSelK], unsigned long long k) {
-  if (k <= t[kSelK - 1]) return;
-  t[kSelK - 1] = k;
-#pragma unroll
-  for (int i = kSelK - 1; i > 0; --i) {
-    const unsigned long long hi = t[i] > t[i - 1] ? t[i] : t[i - 1];
-    const unsigned long long lo = t[i] > t[i - 1] ? t[i - 1] : t[i];
-    t[i - 1] = hi;
-    t[i] = lo;
-  }
-}
-
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
-}
-
-// Every lane holds a decreasing list t[]; returns, in lane k < kSelK, the
-// k-th largest key of the warp's union (0 where fewer exist). Keys are
-// distinct, so each round's maximum leaves exactly one lane's list.
-__device__ __forceinline__ unsigned long long warp_top(unsigned long long (&t)[kSelK]) {
-  const int lane = threadIdx.x & 31;
-  unsigned long long mine = 0;
-  for (int k = 0; k < kSelK; ++k) {
-    const unsigned long long m = warp_max_u64(t[0]);
-    if (lane == k) mine = m;
-    if (m != 0 && t[0] == m) {
-#pragma unroll
-      for (int i = 0; i + 1 < kSelK; ++i) t[i] = t[i + 1];
-      t[kSelK - 1] = 0;
-    }
-  }
-  return mine;
-}
-
 // Logits row of draft row r (block row j = 1 + r % T of sequence r / T).
 __device__ __forceinline__ size_t draft_logit_row(int r, int B) {
   const int T = B - 1;
   return static_cast<size_t>(r / T) * B + 1 + r % T;
 }
 
-__global__ void __launch_bounds__(kTopThreads) sel_topk_kernel(const float* __restrict__ logits, int ld, int V,
-                                                               int B, int slice_cols,
-                                                               unsigned long long* __restrict__ part) {
-  __shared__ unsigned long long wtop[kTopThreads / 32][kSelK];
+// Exact top-16 of m distinct nonzero keys in shared memory by counting: a
+// key's rank is the number of larger keys. Threads tid, tid + nthr, ... take
+// one key each; out[rank] for ranks below 16, zeros past m.
+__device__ __forceinline__ void top_by_rank(const unsigned long long* keys, int m, int tid, int nthr,
+                                            unsigned long long* out) {
+  for (int j = tid; j < m; j += nthr) {
+    const unsigned long long k = keys[j];
+    int rank = 0;
+    for (int q = 0; q < m; ++q) rank += keys[q] > k;
+    if (rank < kSelK) out[rank] = k;
+  }
+  if (tid >= m && tid < kSelK) out[tid] = 0;
+}
+
+// Order-preserving unsigned image of a float (for integer max on floats).
+__device__ __forceinline__ uint32_t ordered_bits(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// CTA (slice, row): the 16 largest keys of columns [s * kSliceCols, +kSliceCols)
+// of draft row r. Every thread holds kTopQ float4 of the slice.
+// Threshold: in every warp two lanes reach the warp's second largest lane
+// maximum, so 16 values of the CTA reach the smallest of the 8 warps' second
+// largest lane maxima and every value below it is out. Values at or above it
+// (about 30 per CTA for unordered data; ties can add more) are appended as
+// keys and ranked exactly. If ties overflow the buffer, the slice is redone
+// with exact keys: the warp's 16th largest lane-maximum key bounds it, and at
+// most 16 lanes x 32 keys per warp reach that.
+__global__ void __launch_bounds__(kTopThreads, 4) sel_topk_kernel(const float* __restrict__ logits, int ld, int V,
+                                                                  int B, unsigned long long* __restrict__ part) {
+  __shared__ unsigned long long s_cand[kTopCandCap];
+  __shared__ unsigned long long s_tau_key;
+  __shared__ uint32_t s_r2[kTopThreads / 32];
+  __shared__ int s_m;
   grid_dep_wait();
   grid_dep_launch();
   const int s = blockIdx.x, r = blockIdx.y, slices = gridDim.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) {
+    s_tau_key = 0;
+    s_m = 0;
+  }
   const float* row = logits + draft_logit_row(r, B) * ld;
-  const int c0 = s * slice_cols, c1 = min(V, c0 + slice_cols);
-  unsigned long long t[kSelK];
+  const int c0 = s * kSliceCols, c1 = min(V, c0 + kSliceCols);
+  // columns c0 + 4 (tid + 256 u) + e; whole float4 below c1 lie below the
+  // row's padded width (a multiple of 128); columns past c1 read as -inf and
+  // are masked where keys are formed
+  float4 v[kTopQ];
 #pragma unroll
-  for (int i = 0; i < kSelK; ++i) t[i] = 0;
-  // float4 body (c0 and the row pitch are multiples of 4 floats), four loads
-  // in flight per thread, then the ragged tail
-  const int n4 = c1 > c0 ? (c1 - c0) >> 2 : 0;
-  const float4* p4 = reinterpret_cast<const float4*>(row + c0);
-  int i = threadIdx.x;
-  for (; i + 3 * kTopThreads < n4; i += 4 * kTopThreads) {
-    float4 v[4];
+  for (int u = 0; u < kTopQ; ++u) {
+    const int c = c0 + 4 * (tid + kTopThreads * u);
+    v[u] = c < c1 ? __ldcs(reinterpret_cast<const float4*>(row + c)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  }
+  // lane maximum (fmaxf skips NaN; an all-NaN lane counts as -inf, which
+  // only loosens the bound)
+  float bv = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = __ldcs(p4 + i + u * kTopThreads);
+  for (int u = 0; u < kTopQ; ++u) bv = fmaxf(bv, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+  if (bv != bv) bv = -INFINITY;
+  const uint32_t ob = ordered_bits(bv == 0.f ? 0.f : bv);
+  const uint32_t m1 = __reduce_max_sync(0xffffffffu, ob);
+  const int l1 = __ffs(__ballot_sync(0xffffffffu, ob == m1)) - 1;
+  const uint32_t m2 = __reduce_max_sync(0xffffffffu, lane == l1 ? 0u : ob);
+  if (lane == 0) s_r2[tid >> 5] = m2;
+  __syncthreads();   // s_r2, s_tau_key, s_m
+  uint32_t tb = s_r2[0];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = c0 + 4 * (i + u * kTopThreads);
-      top_insert(t, logit_key(v[u].x, c));
-      top_insert(t, logit_key(v[u].y, c + 1));
-      top_insert(t, logit_key(v[u].z, c + 2));
-      top_insert(t, logit_key(v[u].w, c + 3));
+  for (int w = 1; w < kTopThreads / 32; ++w) tb = min(tb, s_r2[w]);
+  const float tau = __uint_as_float((tb & 0x80000000u) ? (tb & 0x7FFFFFFFu) : ~tb);
+  auto key_at = [&](float x, int c) -> unsigned long long {
+    return (c < c1 && x == x) ? logit_key(x, c) : 0ull;
+  };
+#pragma unroll
+  for (int u = 0; u < kTopQ; ++u) {
+    const int c = c0 + 4 * (tid + kTopThreads * u);
+    const float x4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (x4[e] >= tau) {   // -0 and +0 compare equal; NaN never passes
+        const unsigned long long k = key_at(x4[e], c + e);
+        if (k != 0) {
+          const int at = atomicAdd(&s_m, 1);
+          if (at < kTopCandCap) s_cand[at] = k;
+        }
+      }
     }
   }
-  for (; i < n4; i += kTopThreads) {
-    const float4 v = __ldcs(p4 + i);
-    const int c = c0 + 4 * i;
-    top_insert(t, logit_key(v.x, c));
-    top_insert(t, logit_key(v.y, c + 1));
-    top_insert(t, logit_key(v.z, c + 2));
-    top_insert(t, logit_key(v.w, c + 3));
-  }
-  for (int c = c0 + 4 * n4 + threadIdx.x; c < c1; c += kTopThreads) top_insert(t, logit_key(row[c], c));
-  const unsigned long long w = warp_top(t);
-  if (lane < kSelK) wtop[warp][lane] = w;
   __syncthreads();
-  if (warp == 0) {
-    // lane l takes entries 4l .. 4l+3 of the warps' lists (consecutive
-    // entries of one warp's decreasing list)
-    const unsigned long long* flat = &wtop[0][0];
-#pragma unroll
-    for (int q = 0; q < kSelK; ++q) t[q] = q < 4 ? flat[4 * lane + q] : 0ull;
-    const unsigned long long k = warp_top(t);
-    if (lane < kSelK) part[(static_cast<size_t>(r) * slices + s) * kSelK + lane] = k;
+  if (s_m > kTopCandCap) {   // ties at the threshold: exact keys (the slice is read again)
+    const int n_local = kTopQ * 4;
+    unsigned long long best = 0;
+    for (int q = 0; q < n_local; ++q) {
+      const int c = c0 + 4 * (tid + kTopThreads * (q >> 2)) + (q & 3);
+      if (c < c1) best = max(best, key_at(row[c], c));
+    }
+    int kr = 0;
+    for (int o = 1; o < 32; ++o) kr += __shfl_sync(0xffffffffu, best, (lane + o) & 31) > best;
+    __syncthreads();   // every thread has read s_m
+    if (tid == 0) s_m = 0;
+    if (kr == kSelK - 1) atomicMax(&s_tau_key, best);
+    __syncthreads();
+    const unsigned long long tk = s_tau_key;   // 0 when no warp has 16 lanes with keys: all keys kept
+    for (int q = 0; q < n_local; ++q) {
+      const int c = c0 + 4 * (tid + kTopThreads * (q >> 2)) + (q & 3);
+      const unsigned long long k = c < c1 ? key_at(row[c], c) : 0ull;
+      if (k != 0 && k >= tk) s_cand[atomicAdd(&s_m, 1)] = k;
+    }
+    __syncthreads();
   }
+  top_by_rank(s_cand, s_m, tid, kTopThreads, part + (static_cast<size_t>(r) * slices + s) * kSelK);
 }
 
 struct PairsArgs {
@@ -168,40 +194,24 @@ struct PairsArgs {
   float* scores;                    // [n_seq][T][kSelK][kSelK]
   int32_t* cand;                    // [n_seq][T][kSelK]
   float* cand_u;                    // [n_seq][T][kSelK]
+  int32_t* next;                    // [n_seq][T][kSelK] pick at t after predecessor rank a
   float* top_logit;                 // [n_seq][T] the largest logit of each row
   int* tickets;                     // [n_seq], zero between launches
   int32_t* draft_ids;               // [n_seq][T]
   int* status;
 };
 
-// Merge the slice lists of draft row r into its kSelK candidates (one warp).
-__device__ __forceinline__ unsigned long long merge_row(const PairsArgs& a, int r) {
-  const int lane = threadIdx.x & 31;
-  unsigned long long t[kSelK];
-  const unsigned long long* src = a.part + (static_cast<size_t>(r) * a.slices + lane) * kSelK;
-  if (lane < a.slices) {
-    const ulonglong2* s2 = reinterpret_cast<const ulonglong2*>(src);
-#pragma unroll
-    for (int q = 0; q < kSelK / 2; ++q) {
-      const ulonglong2 v = __ldcg(s2 + q);
-      t[2 * q] = v.x;
-      t[2 * q + 1] = v.y;
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < kSelK; ++q) t[q] = 0;
-  }
-  return warp_top(t);
-}
-
 __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_constant__ PairsArgs a) {
   // [0]: A(a) * H(h_t) of the predecessors, [1]: B(b) of the candidates;
-  // the walk reuses the whole array for a sequence's T score matrices
-  __shared__ float s_buf[2][kSelK][kPadRow];
+  // before that the merge's key lists, after it the walk's score matrices
+  __shared__ __align__(16) float s_buf[2][kSelK][kPadRow];
   __shared__ int s_cd[kMaxBlock * kSelK];
   __shared__ float s_h[kSelDim];
   __shared__ int s_pred[kSelK], s_cand[kSelK];
   __shared__ float s_u[kSelK];
+  __shared__ unsigned long long s_top[2][kSelK];
+  __shared__ unsigned long long s_tau[2];
+  __shared__ int s_m[2];
   __shared__ int s_last;
   float(&s_ah)[kSelK][kPadRow] = s_buf[0];
   float(&s_b)[kSelK][kPadRow] = s_buf[1];
@@ -211,26 +221,58 @@ __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_pred = t == 0 ? 1 : kSelK;
   const size_t row = static_cast<size_t>(i) * a.B + 1 + t;
-  if (warp == 0) {
-    const unsigned long long k = merge_row(a, i * T + t);
-    if (lane < kSelK) {
-      int c = key_col(k);
-      if (k == 0 || c < 0 || c >= a.V) {
-        latch_status(a.status, kDevBounds);
-        c = 0;
-      }
-      s_cand[lane] = c;
-      s_u[lane] = k ? key_value(k) : -INFINITY;
+  // Merge the slice lists: threads [0, 256) take draft row t, [256, 512) row
+  // t-1. A slice list's 16th key bounds the row's 16th largest from below, so
+  // only keys at or above the largest such bound are ranked.
+  const int half = threadIdx.x >> 8, ht = threadIdx.x & 255;
+  const int n_keys = a.slices * kSelK;   // <= kSelMaxSlices * 16 = 1024
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(&s_buf[0][0][0]) + half * 2 * kSelMaxSlices * kSelK;
+  unsigned long long* kept = keys + kSelMaxSlices * kSelK;
+  const bool merging = half == 0 || t > 0;
+  if (threadIdx.x < 2) {
+    s_tau[threadIdx.x] = 0;
+    s_m[threadIdx.x] = 0;
+  }
+  if (merging) {   // all loads in flight before the stores
+    const unsigned long long* src = a.part + static_cast<size_t>(i * T + t - half) * n_keys;
+    unsigned long long kv[kSelMaxSlices * kSelK / 256];
+#pragma unroll
+    for (int u = 0; u < kSelMaxSlices * kSelK / 256; ++u) kv[u] = ht + 256 * u < n_keys ? __ldcg(src + ht + 256 * u) : 0ull;
+#pragma unroll
+    for (int u = 0; u < kSelMaxSlices * kSelK / 256; ++u)
+      if (ht + 256 * u < n_keys) keys[ht + 256 * u] = kv[u];
+  }
+  if (half == 0) s_h[ht] = a.logits[row * a.ld + a.h_col + ht];
+  __syncthreads();
+  if (merging && ht < a.slices) atomicMax(&s_tau[half], keys[ht * kSelK + kSelK - 1]);
+  __syncthreads();
+  if (merging) {
+    const unsigned long long tau = s_tau[half];
+    for (int q = ht; q < n_keys; q += 256) {
+      const unsigned long long k = keys[q];
+      if (k != 0 && k >= tau) kept[atomicAdd(&s_m[half], 1)] = k;
     }
-  } else if (warp == 1) {
+  }
+  __syncthreads();
+  if (merging) top_by_rank(kept, s_m[half], ht, 256, s_top[half]);
+  __syncthreads();
+  if (threadIdx.x < kSelK) {
+    const unsigned long long k = s_top[0][threadIdx.x];
+    int c = key_col(k);
+    if (k == 0 || c < 0 || c >= a.V) {
+      latch_status(a.status, kDevBounds);
+      c = 0;
+    }
+    s_cand[threadIdx.x] = c;
+    s_u[threadIdx.x] = k ? key_value(k) : -INFINITY;
+  } else if (threadIdx.x < 2 * kSelK) {
+    const int q = threadIdx.x - kSelK;
     if (t > 0) {
-      const unsigned long long k = merge_row(a, i * T + t - 1);
-      if (lane < kSelK) {
-        int c = key_col(k);
-        if (k == 0 || c < 0 || c >= a.V) c = 0;   // reported by the CTA that owns row t-1
-        s_pred[lane] = c;
-      }
-    } else if (lane == 0) {
+      const unsigned long long k = s_top[1][q];
+      int c = key_col(k);
+      if (k == 0 || c < 0 || c >= a.V) c = 0;   // reported by the CTA that owns row t-1
+      s_pred[q] = c;
+    } else if (q == 0) {
       int c = a.anchors[i];
       if (c < 0 || c >= a.V) {
         latch_status(a.status, kDevBounds);
@@ -238,31 +280,37 @@ __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_co
       }
       s_pred[0] = c;
     }
-  } else if (warp >= 8) {
-    const int d = threadIdx.x - 256;
-    s_h[d] = a.logits[row * a.ld + a.h_col + d];
   }
   __syncthreads();
-  // stage A(pred) * H and B(cand): 16 rows of 256 each, float4 loads
+  // stage A(pred) * H and B(cand): 16 rows of 256 each, float4 loads, all
+  // four of a thread in flight before the stores
   {
     constexpr int kQuads = kSelK * kSelDim / 4;   // 1024 float4 per matrix
+    constexpr int kPer = 2 * kQuads / kPairThreads;
+    float4 tv[kPer];
 #pragma unroll
-    for (int q = threadIdx.x; q < 2 * kQuads; q += kPairThreads) {
+    for (int u = 0; u < kPer; ++u) {
+      const int q = threadIdx.x + kPairThreads * u;
       const int which = q / kQuads, rr = (q % kQuads) / (kSelDim / 4), d4 = (q % (kSelDim / 4)) * 4;
-      if (which == 0 && rr >= n_pred) continue;
-      const int tok = which == 0 ? s_pred[rr] : s_cand[rr];
-      const float4 v = __ldg(reinterpret_cast<const float4*>(a.table + static_cast<size_t>(tok) * (2 * kSelDim) +
-                                                            which * kSelDim + d4));
+      const int tok = which == 0 ? (rr < n_pred ? s_pred[rr] : -1) : s_cand[rr];
+      tv[u] = tok >= 0 ? __ldg(reinterpret_cast<const float4*>(a.table + static_cast<size_t>(tok) * (2 * kSelDim) +
+                                                               which * kSelDim + d4))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int q = threadIdx.x + kPairThreads * u;
+      const int which = q / kQuads, rr = (q % kQuads) / (kSelDim / 4), d4 = (q % (kSelDim / 4)) * 4;
       if (which == 0) {
-        s_ah[rr][d4 + 0] = v.x * s_h[d4 + 0];
-        s_ah[rr][d4 + 1] = v.y * s_h[d4 + 1];
-        s_ah[rr][d4 + 2] = v.z * s_h[d4 + 2];
-        s_ah[rr][d4 + 3] = v.w * s_h[d4 + 3];
+        s_ah[rr][d4 + 0] = tv[u].x * s_h[d4 + 0];
+        s_ah[rr][d4 + 1] = tv[u].y * s_h[d4 + 1];
+        s_ah[rr][d4 + 2] = tv[u].z * s_h[d4 + 2];
+        s_ah[rr][d4 + 3] = tv[u].w * s_h[d4 + 3];
       } else {
-        s_b[rr][d4 + 0] = v.x;
-        s_b[rr][d4 + 1] = v.y;
-        s_b[rr][d4 + 2] = v.z;
-        s_b[rr][d4 + 3] = v.w;
+        s_b[rr][d4 + 0] = tv[u].x;
+        s_b[rr][d4 + 1] = tv[u].y;
+        s_b[rr][d4 + 2] = tv[u].z;
+        s_b[rr][d4 + 3] = tv[u].w;
       }
     }
   }
@@ -283,7 +331,15 @@ __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_co
       }
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 16);
-    if (lane < kSelK) a.scores[(sbase + warp) * kSelK + lane] = s_u[lane] + acc;
+    // lanes l and l ^ 16 hold the same score; the walk's step from
+    // predecessor a is the first maximum over b
+    float sv = s_u[b] + acc;
+    if (sv != sv) sv = -INFINITY;
+    const uint32_t ob = ordered_bits(sv == 0.f ? 0.f : sv);
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, ob);
+    const int best = __ffs(__ballot_sync(0xffffffffu, ob == mx)) - 1;
+    if (lane < kSelK) a.scores[(sbase + warp) * kSelK + lane] = sv;
+    if (lane == 0) a.next[sbase + warp] = best;
   }
   if (threadIdx.x < kSelK) {
     a.cand[sbase + threadIdx.x] = s_cand[threadIdx.x];
@@ -297,34 +353,28 @@ __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_co
   }
   __syncthreads();
   if (!s_last) return;
-  // The last CTA of sequence i: gather its T score matrices (T * 256 <=
-  // 31 * 256 floats, within s_buf) and candidate lists, then walk.
+  // The last CTA of sequence i: gather the T steps (the pick after each
+  // predecessor) and candidate lists, then follow the picks from the anchor.
   __threadfence();
-  float* sc = &s_buf[0][0][0];
-  int* cd = s_cd;
-  const size_t s0 = static_cast<size_t>(i) * T * kSelK * kSelK;
-  for (int q = threadIdx.x; q < T * kSelK * kSelK; q += kPairThreads) sc[q] = __ldcg(a.scores + s0 + q);
-  for (int q = threadIdx.x; q < T * kSelK; q += kPairThreads)
-    cd[q] = __ldcg(a.cand + static_cast<size_t>(i) * T * kSelK + q);
+  const size_t c0 = static_cast<size_t>(i) * T * kSelK;
+  {
+    const int q = threadIdx.x;
+    const int nx = q < T * kSelK ? __ldcg(a.next + c0 + q) : 0;
+    const int id = q < T * kSelK ? __ldcg(a.cand + c0 + q) : 0;
+    if (q < T * kSelK) {
+      s_cd[q] = id;
+      reinterpret_cast<int*>(&s_buf[0][0][0])[q] = nx;
+    }
+  }
   __syncthreads();
-  if (warp == 0) {
+  if (threadIdx.x == 0) {
+    const int* nx = reinterpret_cast<const int*>(&s_buf[0][0][0]);
     int p = 0;   // rank of the predecessor (the anchor at t = 0)
     for (int tt = 0; tt < T; ++tt) {
-      int b = lane & 15;
-      float v = sc[(tt * kSelK + p) * kSelK + b];
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int ob = __shfl_xor_sync(0xffffffffu, b, o);
-        if (ov > v || (ov == v && ob < b)) {
-          v = ov;
-          b = ob;
-        }
-      }
-      p = b;
-      if (lane == 0) a.draft_ids[static_cast<size_t>(i) * T + tt] = cd[tt * kSelK + p];
+      p = nx[tt * kSelK + p] & (kSelK - 1);
+      a.draft_ids[static_cast<size_t>(i) * T + tt] = s_cd[tt * kSelK + p];
     }
-    if (lane == 0) a.tickets[i] = 0;
+    a.tickets[i] = 0;
   }
 }
 
@@ -334,7 +384,7 @@ cudaError_t launch_path_select(const SelectArgs& s, cudaStream_t stream) {
   if (s.n_seq <= 0 || s.B < 2) return cudaSuccess;
   const int T = s.B - 1, rows = s.n_seq * T;
   cudaError_t e = launch_pdl(sel_topk_kernel, dim3(s.slices, rows), dim3(kTopThreads), 0, stream, s.logits, s.ld,
-                             s.V, s.B, s.slice_cols, s.part);
+                             s.V, s.B, s.part);
   if (e != cudaSuccess) return e;
   PairsArgs a;
   a.part = s.part;
@@ -349,6 +399,7 @@ cudaError_t launch_path_select(const SelectArgs& s, cudaStream_t stream) {
   a.scores = s.scores;
   a.cand = s.cand;
   a.cand_u = s.cand_u;
+  a.next = s.next;
   a.top_logit = s.top_logit;
   a.tickets = s.tickets;
   a.draft_ids = s.draft_ids;

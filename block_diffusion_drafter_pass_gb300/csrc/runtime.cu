@@ -126,6 +126,7 @@ struct dflash_ctx {
   float* sel_scores = nullptr;             // [max_rows][16][16]
   int32_t* sel_cand = nullptr;             // [max_rows][16]
   float* sel_cand_u = nullptr;             // [max_rows][16]
+  int32_t* sel_next = nullptr;             // [max_rows][16]
   int* sel_tickets = nullptr;              // [max_batch]
 
   // weight descriptors
@@ -341,7 +342,7 @@ dflash_status dflash_destroy(dflash_ctx* ctx) {
                   ctx->hg, ctx->ssA, ctx->ssB, ctx->q, ctx->kb, ctx->vb, ctx->attn, ctx->act, ctx->htg, ctx->ssF,
                   ctx->part_o, ctx->part_ml, ctx->split_ws, ctx->tickets, ctx->keys, ctx->done, ctx->top_logit,
                   ctx->sel_table, ctx->sel_logits, ctx->sel_part, ctx->sel_scores, ctx->sel_cand, ctx->sel_cand_u,
-                  ctx->sel_tickets};
+                  ctx->sel_tickets, ctx->sel_next};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (ctx->h_snap) cudaFreeHost(ctx->h_snap);
@@ -962,16 +963,14 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
     sa.logits = ctx->sel_logits;
     sa.ld = ctx->sel_ld;
     sa.h_col = ctx->sel_hcol;
-    // about two CTAs per SM over the draft rows, at most 32 slices per row
-    int slices = std::min(kSelMaxSlices, std::max(1, ceil_div(2 * sms, Md)));
-    sa.slice_cols = 4 * ceil_div(ceil_div(c.vocab, slices), 4);
-    sa.slices = ceil_div(c.vocab, sa.slice_cols);
+    sa.slices = ceil_div(c.vocab, kSelSliceCols);
     sa.part = ctx->sel_part;
     sa.table = ctx->sel_table;
     sa.anchors = anchor_ids;
     sa.scores = ctx->sel_scores;
     sa.cand = ctx->sel_cand;
     sa.cand_u = ctx->sel_cand_u;
+    sa.next = ctx->sel_next;
     sa.top_logit = ctx->top_logit;
     sa.tickets = ctx->sel_tickets;
     sa.draft_ids = draft_ids;
@@ -1096,7 +1095,8 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
   }
   if (!w_a || !w_b || !w_h) return fail(ctx, DFLASH_EINVAL, "w_a, w_b, w_h must be all set or all NULL");
   if (dim != kSelDim) return fail(ctx, DFLASH_EINVAL, "selector width must be 256");
-  if (c.vocab < kSelK) return fail(ctx, DFLASH_EINVAL, "vocab below the 16 candidates");
+  if (c.vocab < kSelK || c.vocab > kSelMaxSlices * kSelSliceCols)
+    return fail(ctx, DFLASH_EINVAL, "vocab outside [16, 524288] for the path selector");
   if (!aligned16(w_a) || !aligned16(w_b) || !aligned16(w_h)) return fail(ctx, DFLASH_EINVAL, "weights not 16-byte aligned");
   const size_t rows = ctx->max_rows();
   if (!ctx->sel_table) {
@@ -1108,11 +1108,12 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
     if (e == cudaSuccess) e = dalloc(&ctx->sel_scores, rows * kSelK * kSelK);
     if (e == cudaSuccess) e = dalloc(&ctx->sel_cand, rows * kSelK);
     if (e == cudaSuccess) e = dalloc(&ctx->sel_cand_u, rows * kSelK);
+    if (e == cudaSuccess) e = dalloc(&ctx->sel_next, rows * kSelK);
     if (e == cudaSuccess) e = dalloc(&ctx->sel_tickets, c.max_batch);
     if (e == cudaSuccess) e = cudaMemset(ctx->sel_tickets, 0, c.max_batch * sizeof(int));
     if (e != cudaSuccess) {
       void* ps[] = {ctx->sel_table, ctx->sel_logits, ctx->sel_part, ctx->sel_scores, ctx->sel_cand, ctx->sel_cand_u,
-                    ctx->sel_tickets};
+                    ctx->sel_tickets, ctx->sel_next};
       for (void* p : ps)
         if (p) cudaFree(p);
       ctx->sel_table = nullptr;
@@ -1122,6 +1123,7 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
       ctx->sel_cand = nullptr;
       ctx->sel_cand_u = nullptr;
       ctx->sel_tickets = nullptr;
+      ctx->sel_next = nullptr;
       return fail(ctx, e == cudaErrorMemoryAllocation ? DFLASH_ENOMEM : DFLASH_ECUDA,
                   std::string("selector buffers: ") + cudaGetErrorString(e));
     }

@@ -208,7 +208,7 @@ dflash_status dflash_sync(dflash_ctx* ctx);
  * Enqueued on `stream`, then waits for it. The first install allocates the
  * tables and buffers (V*2 KB plus max_batch*max_block rows of (V+256) fp32
  * logits). Errors: EINVAL (dim != 256, vocab < 16, some but not all pointers
- * NULL, misaligned pointer), ENOMEM, ECUDA. */
+ * NULL, misaligned pointer, vocab above 524288), ENOMEM, ECUDA. */
 dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, const uint16_t* w_b,
                                        const uint16_t* w_h, int dim, void* stream);
 

@@ -13,6 +13,8 @@ the tiny drafter (512 block rows: CTA-pair LM head with the H rows stacked),
 and the Qwen3-8B shape (vocabulary 151936, 11 column slices) at 2 layers.
 With W_H = 0 the walk must return the plain greedy draft.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -70,7 +72,8 @@ def _compare_selection(d, orc, sel_np, seqs, anchors, B, got_ids, what):
             out[c] = False
             tol = ATOL + RTOL * np.abs(L)
             worst_in = np.min(L[c] + tol[c])
-            assert np.max(L[out] - tol[out]) <= worst_in, f"{tag}: not a top-16 of the oracle's logits"
+            if out.any():
+                assert np.max(L[out] - tol[out]) <= worst_in, f"{tag}: not a top-16 of the oracle's logits"
             if r["gap16"][t] > GAP:
                 assert sorted(c.tolist()) == sorted(r["cand"][t].tolist()), f"{tag}: candidate set"
             prev = [int(anchors[i])] if t == 0 else cand[row - 1].tolist()
@@ -84,11 +87,27 @@ def _compare_selection(d, orc, sel_np, seqs, anchors, B, got_ids, what):
     return checked, ref
 
 
-def _tiny(dfl, max_batch, max_block, seed=3):
-    wn = make_weights_np(TINY, seed=seed)
-    d = dfl.Drafter(TINY, np_weights_to_device(wn, DEV), max_seqs=max_batch, max_batch=max_batch,
+def _tiny(dfl, max_batch, max_block, seed=3, shape=TINY, edit=None):
+    wn = make_weights_np(shape, seed=seed)
+    if edit:
+        edit(wn)
+    d = dfl.Drafter(shape, np_weights_to_device(wn, DEV), max_seqs=max_batch, max_batch=max_batch,
                     max_block=max_block, max_ctx=512, max_fuse_tokens=10000)
-    return d, wn, oracle.OracleDrafter(TINY, wn)
+    return d, wn, oracle.OracleDrafter(shape, wn)
+
+
+def _run_case(dfl, d, orc, shape, sel_seed, lens, B, what, feat_seed=61):
+    sel = make_selector_weights_np(shape, seed=sel_seed)
+    d.set_path_selector(**_sel_dev(sel))
+    width = shape.n_feat_layers * shape.hidden
+    seqs = list(range(len(lens)))
+    f = make_features_np(sum(lens), width, seed=feat_seed)
+    d.fuse_ctx(seqs, lens, bf16_dev(f, DEV), pending=False)
+    orc.fuse_ctx(seqs, lens, f, pending=False)
+    anchors = make_anchor_ids_np(len(lens), shape.vocab, seed=feat_seed + 1)
+    ids = d.draft(seqs, i32_dev(anchors, DEV), B)
+    d.sync()
+    return _compare_selection(d, orc, sel, seqs, anchors, B, ids.cpu().numpy(), what)
 
 
 def test_tiny_selector_ragged_block_sizes(dfl):
@@ -198,3 +217,35 @@ def test_selector_argument_errors(dfl):
         # no selection to read before a selector draft
         with pytest.raises(dfl.DFlashError):
             d.last_selection(1, 8)
+
+
+def test_selector_all_equal_logits(dfl):
+    """A zero LM head makes every logit 0: the candidates are the 16 lowest
+    ids in order (the tie rule). Vocabulary 10000: the first 8192-column
+    slice holds more tied keys than the threshold filter's buffer and takes
+    the exact-key path, the second (1808 columns) does not."""
+    def zero_head(wn):
+        wn["lm_head"] = np.zeros_like(wn["lm_head"])
+    shape = dataclasses.replace(TINY, vocab=10000, mask_id=9999)
+    d, wn, orc = _tiny(dfl, max_batch=2, max_block=16, seed=9, shape=shape, edit=zero_head)
+    with d:
+        checked, _ = _run_case(dfl, d, orc, shape, 71, [30, 100], 16, "zero LM head")
+        cand, u, _ = d.last_selection(2, 16)
+        np.testing.assert_array_equal(cand, np.tile(np.arange(16), (30, 1)))
+        assert np.all(u == 0)
+
+
+def test_selector_vocab_16_and_wide_vocab(dfl):
+    """Vocabulary 16 (every token a candidate) and vocabulary 300000 (37
+    column slices of 8192: the merge ranks more than 512 keys)."""
+    small = dataclasses.replace(TINY, vocab=16, mask_id=15)
+    d, wn, orc = _tiny(dfl, max_batch=2, max_block=8, seed=11, shape=small)
+    with d:
+        _run_case(dfl, d, orc, small, 81, [5, 70], 8, "vocab 16")
+        cand, _, _ = d.last_selection(2, 8)
+        assert all(sorted(r.tolist()) == list(range(16)) for r in cand)
+    wide = dataclasses.replace(TINY, vocab=300000, mask_id=299999)
+    d, wn, orc = _tiny(dfl, max_batch=2, max_block=8, seed=12, shape=wide)
+    with d:
+        checked, _ = _run_case(dfl, d, orc, wide, 82, [64, 9], 8, "vocab 300000")
+        assert checked >= 2, checked
