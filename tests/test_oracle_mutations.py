@@ -168,3 +168,64 @@ def test_mean_len_without_bonus_is_caught(monkeypatch):
         return accepted / generated, accepted / cycles
     _patch(monkeypatch, "acceptance_stats", bad)
     _expect_failure(pins.test_worked_numbers_from_the_pages)
+
+
+# ----------------------------------------------------------------------------
+# Sampling oracle (oracle/sampling.py)
+# ----------------------------------------------------------------------------
+
+def test_sampling_residual_sign_error_is_caught(monkeypatch):
+    """Resampling from max(0, q - p) instead of max(0, p - q)."""
+    from oracle import sampling as osm
+    from tests import test_sampling_pins as spins
+
+    def bad(drafts, q, p, u_accept, u_resample):
+        B = len(p)
+        for j in range(B - 1):
+            x = int(drafts[j])
+            px, qx = osm.prob_of(*p[j], x), osm.prob_of(*q[j], x)
+            if qx > 0 and u_accept[j] < min(1.0, px / qx):
+                continue
+            ids = q[j][0]
+            r = np.array([max(0.0, qv - osm.prob_of(*p[j], int(y))) for y, qv in zip(ids, q[j][1])])
+            return j + 1, osm.draw(ids, r, u_resample[j])
+        return B, osm.draw(*p[B - 1], u_resample[B - 1])
+    monkeypatch.setattr(osm, "verify_sample", bad)
+    _expect_failure(lambda: spins.test_speculative_sampling_is_lossless(1))
+
+
+def test_sampling_inverted_ratio_is_caught(monkeypatch):
+    """Accepting with min(1, q/p) instead of min(1, p/q)."""
+    from oracle import sampling as osm
+    from tests import test_sampling_pins as spins
+
+    def bad(drafts, q, p, u_accept, u_resample):
+        B = len(p)
+        for j in range(B - 1):
+            x = int(drafts[j])
+            px, qx = osm.prob_of(*p[j], x), osm.prob_of(*q[j], x)
+            if px > 0 and u_accept[j] < min(1.0, qx / px):
+                continue
+            ids = p[j][0]
+            r = np.array([max(0.0, pv - osm.prob_of(*q[j], int(y))) for y, pv in zip(ids, p[j][1])])
+            if r.sum() == 0:
+                r = np.asarray(p[j][1], dtype=float)
+            return j + 1, osm.draw(ids, r, u_resample[j])
+        return B, osm.draw(*p[B - 1], u_resample[B - 1])
+    monkeypatch.setattr(osm, "verify_sample", bad)
+    _expect_failure(lambda: spins.test_speculative_sampling_is_lossless(2))
+
+
+def test_sampling_top_p_off_by_one_is_caught(monkeypatch):
+    """Keeping the tokens strictly below top_p (dropping the one that reaches it)."""
+    from oracle import sampling as osm
+    from tests import test_sampling_pins as spins
+    orig = osm.filtered_probs
+
+    def bad(logits, temperature, top_k, top_p):
+        ids, p = orig(logits, temperature, top_k, 1.0)
+        c = np.cumsum(p)
+        n = max(1, int(np.searchsorted(c, top_p, side="left")))
+        return ids[:n], p[:n] / p[:n].sum()
+    monkeypatch.setattr(osm, "filtered_probs", bad)
+    _expect_failure(spins.test_top_p_worked_case)
