@@ -27,11 +27,13 @@ EXPORTED = (
     "dflash_fuse_ctx", "dflash_draft", "dflash_verify", "dflash_rows_argmax_bf16", "dflash_sync",
     "dflash_debug_read_kv", "dflash_debug_last_draft", "dflash_debug_gemm", "dflash_debug_profile",
     "dflash_debug_profile_read", "dflash_gemm_noalloc", "dflash_set_path_selector", "dflash_debug_last_selection",
+    "dflash_draft_sample", "dflash_sample_filter", "dflash_verify_sample",
 )
+SAMPLE_WIDTH = 32   # DFLASH_SAMPLE_WIDTH
 
 # Kernel classes of the per-kernel accounting (DFLASH_K_* in include/dflash.h).
 KERNEL_CLASSES = ("qkv", "attn", "attn_combine", "o", "gateup", "down", "lmhead", "fuse_wc", "fuse_kv", "norm",
-                  "verify", "other", "select")
+                  "verify", "other", "select", "sample")
 
 
 class DFlashError(RuntimeError):
@@ -95,6 +97,9 @@ def load_library() -> ctypes.CDLL:
         "dflash_gemm_noalloc": ([VP, VP, VP, I, I, I, I, VP], I),
         "dflash_set_path_selector": ([VP, VP, VP, VP, I, VP], I),
         "dflash_debug_last_selection": ([VP, VP, VP, VP], I),
+        "dflash_draft_sample": ([VP, i32p, I, VP, I, ctypes.c_float, I, ctypes.c_float, VP, VP, VP, VP, VP], I),
+        "dflash_sample_filter": ([VP, VP, I, I, ctypes.c_float, I, ctypes.c_float, VP, VP, VP, VP, VP], I),
+        "dflash_verify_sample": ([VP, i32p, I, I, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -261,6 +266,58 @@ class Drafter:
         _check(load_library().dflash_set_path_selector(self.ctx, _ptr(w_a), _ptr(w_b), _ptr(w_h), w_a.shape[0],
                                                        _stream(stream)), self.ctx)
         self._sel = ws   # W_H is read by every draft
+
+    # temperature sampling ------------------------------------------------------
+    def draft_sample(self, seq_ids, anchor_ids, B: int, temperature: float, top_k: int, top_p: float, uniforms,
+                     out=None, q_ids=None, q_probs=None, stream=None):
+        """Drafter pass with a sampling head: (draft ids [n, B-1], q ids
+        [n, B-1, 32], q probs [n, B-1, 32]); uniforms fp32 [n, B-1] on the device."""
+        import torch
+        n = len(seq_ids)
+        T = max(B - 1, 0)
+        if out is None:
+            out = torch.empty(n, T, dtype=torch.int32, device=self.device)
+        if q_ids is None:
+            q_ids = torch.empty(n, T, SAMPLE_WIDTH, dtype=torch.int32, device=self.device)
+        if q_probs is None:
+            q_probs = torch.empty(n, T, SAMPLE_WIDTH, dtype=torch.float32, device=self.device)
+        assert anchor_ids.dtype == torch.int32 and anchor_ids.is_cuda
+        assert uniforms is None or (uniforms.dtype == torch.float32 and uniforms.is_contiguous())
+        _check(load_library().dflash_draft_sample(self.ctx, _i32(seq_ids), n, _ptr(anchor_ids), B, float(temperature),
+                                                  int(top_k), float(top_p), _ptr(uniforms),
+                                                  _ptr(out) if out.numel() else 0, _ptr(q_ids) if q_ids.numel() else 0,
+                                                  _ptr(q_probs) if q_probs.numel() else 0, _stream(stream)), self.ctx)
+        return out, q_ids, q_probs
+
+    def sample_filter(self, logits, temperature: float, top_k: int, top_p: float, uniforms=None, stream=None):
+        """Filtered distributions of bf16 logit rows [rows, V]: (ids [rows, 32],
+        probs [rows, 32], draws [rows] or None when no uniforms are given)."""
+        import torch
+        assert logits.dtype == torch.bfloat16 and logits.is_cuda and logits.is_contiguous()
+        rows, cols = logits.shape
+        ids = torch.empty(rows, SAMPLE_WIDTH, dtype=torch.int32, device=logits.device)
+        probs = torch.empty(rows, SAMPLE_WIDTH, dtype=torch.float32, device=logits.device)
+        drawn = torch.empty(rows, dtype=torch.int32, device=logits.device) if uniforms is not None else None
+        _check(load_library().dflash_sample_filter(self.ctx, _ptr(logits), rows, cols, float(temperature), int(top_k),
+                                                   float(top_p), _ptr(uniforms), _ptr(ids), _ptr(probs),
+                                                   _ptr(drawn), _stream(stream)), self.ctx)
+        return ids, probs, drawn
+
+    def verify_sample(self, seq_ids, B: int, draft_ids, q_ids, q_probs, p_ids, p_probs, u_accept, u_resample,
+                      tau=None, bonus=None, stream=None):
+        """Lossless speculative-sampling verify + commit -> (tau, token)."""
+        import torch
+        n = len(seq_ids)
+        if tau is None:
+            tau = torch.empty(n, dtype=torch.int32, device=self.device)
+        if bonus is None:
+            bonus = torch.empty(n, dtype=torch.int32, device=self.device)
+        nz = lambda t: _ptr(t) if t is not None and t.numel() else 0
+        _check(load_library().dflash_verify_sample(self.ctx, _i32(seq_ids), n, B, nz(draft_ids), nz(q_ids),
+                                                   nz(q_probs), _ptr(p_ids), _ptr(p_probs), nz(u_accept),
+                                                   _ptr(u_resample), _ptr(tau), _ptr(bonus), _stream(stream)),
+               self.ctx)
+        return tau, bonus
 
     # state and inspection ------------------------------------------------------
     def seq_reset(self, seq: int) -> None:

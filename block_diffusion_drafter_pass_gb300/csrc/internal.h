@@ -279,4 +279,40 @@ struct SelectArgs {
 };
 cudaError_t launch_path_select(const SelectArgs& s, cudaStream_t stream);
 
+// ----------------------------------------------------------------------------
+// Temperature sampling (top-k <= 32, top-p) and the speculative-sampling verify
+// ----------------------------------------------------------------------------
+constexpr int kSampleWidth = 32;     // list width: ids / probabilities per row
+constexpr int kSampleMaxSlices = 64; // column slices of a row
+struct FilterArgs {
+  const unsigned long long* part;  // [rows][slices][32] slice lists
+  int slices;
+  float inv_temperature;
+  int top_k;                       // 1..32
+  float top_p;                     // (0, 1]
+  const float* uniforms;           // [rows] (with drawn)
+  int32_t* out_ids;                // [rows][32], -1 past the kept entries
+  float* out_probs;                // [rows][32]
+  int32_t* drawn;                  // [rows] or null
+};
+struct VerifySampleArgs {
+  const int32_t* drafts;           // [n][B-1]
+  const int32_t* q_ids;            // [n][B-1][32] the drafter's filtered lists
+  const float* q_probs;
+  const int32_t* p_ids;            // [n][B][32] the target's filtered lists
+  const float* p_probs;
+  const float* u_accept;           // [n][B-1]
+  const float* u_resample;         // [n][B]
+  int32_t* tau;                    // [n]
+  int32_t* bonus;                  // [n]
+  int* status;
+};
+// Slice lists (topk_slices_kernel, 32 wide) then the filter / draw of every
+// row. bf16: rows of a [rows][ld] bf16 matrix; otherwise fp32 rows of the
+// drafter's logits with the block's anchor rows skipped (draft_B = B).
+cudaError_t launch_sample_filter(const void* logits, bool bf16, int ld, int V, int rows, int draft_B,
+                                 unsigned long long* part, const FilterArgs& fa, cudaStream_t s);
+int sample_slice_cols(bool bf16);
+cudaError_t launch_verify_sample(const SeqMeta& meta, SeqState st, const VerifySampleArgs& a, cudaStream_t s);
+
 }  // namespace dfl

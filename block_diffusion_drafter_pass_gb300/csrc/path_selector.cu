@@ -14,8 +14,8 @@
 // final-normalised row.
 //
 // Per draft pass (after the LM-head GEMM stored logits and H as fp32):
-//   sel_topk_kernel   CTA (slice, row): the 16 largest (logit, column) keys
-//                     of one column slice of one draft row;
+//   topk_slices_kernel (topk.cuh) CTA (slice, row): the 16 largest (logit,
+//                     column) keys of one 8192-column slice of one draft row;
 //   sel_pairs_kernel  CTA (position t, sequence): merges the slice lists of
 //                     rows t and t-1 into C_t and C_{t-1}, stages A of the
 //                     predecessors and B of the candidates in shared memory
@@ -31,158 +31,20 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace dfl {
 namespace {
 
-constexpr int kTopThreads = 256;
-constexpr int kTopQ = 8;                                  // float4 per thread
-constexpr int kSliceCols = kTopThreads * 4 * kTopQ;       // 8192 columns per CTA
-constexpr int kTopCandCap = 8 * 16 * 4 * kTopQ;           // 8 warps x 16 lanes x 32 keys
 constexpr int kPairThreads = 512;
 constexpr int kPadRow = kSelDim + 1;   // shared-memory row pitch (bank spread)
-static_assert(kSliceCols == kSelSliceCols, "slice width");
+using topk::key_col;
+using topk::key_value;
+using topk::ordered_bits;
+static_assert(topk::In<float>::kSliceCols == kSelSliceCols, "slice width");
 static_assert(kSelDim == 256, "H(h_t) is loaded by one thread per dimension of the first 256");
 static_assert(2 * 2 * kSelMaxSlices * kSelK * 8 <= 2 * kSelK * kPadRow * 4, "merge lists fit the staging buffer");
 static_assert(kMaxBlock * kSelK * kSelK <= 2 * kSelK * kPadRow, "the walk's scores fit the staging buffer");
-
-// Order-preserving 64-bit key of (logit, column): larger logit first, lower
-// column first among equal logits. 0 never arises from a number and marks an
-// empty entry.
-__device__ __forceinline__ unsigned long long logit_key(float v, int col) {
-  uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
-  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return (static_cast<unsigned long long>(b) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(col));
-}
-
-__device__ __forceinline__ float key_value(unsigned long long k) {
-  uint32_t b = static_cast<uint32_t>(k >> 32);
-  b = (b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b;
-  return __uint_as_float(b);
-}
-
-__device__ __forceinline__ int key_col(unsigned long long k) {
-  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k));
-}
-
-// Logits row of draft row r (block row j = 1 + r % T of sequence r / T).
-__device__ __forceinline__ size_t draft_logit_row(int r, int B) {
-  const int T = B - 1;
-  return static_cast<size_t>(r / T) * B + 1 + r % T;
-}
-
-// Exact top-16 of m distinct nonzero keys in shared memory by counting: a
-// key's rank is the number of larger keys. Threads tid, tid + nthr, ... take
-// one key each; out[rank] for ranks below 16, zeros past m.
-__device__ __forceinline__ void top_by_rank(const unsigned long long* keys, int m, int tid, int nthr,
-                                            unsigned long long* out) {
-  for (int j = tid; j < m; j += nthr) {
-    const unsigned long long k = keys[j];
-    int rank = 0;
-    for (int q = 0; q < m; ++q) rank += keys[q] > k;
-    if (rank < kSelK) out[rank] = k;
-  }
-  if (tid >= m && tid < kSelK) out[tid] = 0;
-}
-
-// Order-preserving unsigned image of a float (for integer max on floats).
-__device__ __forceinline__ uint32_t ordered_bits(float v) {
-  const uint32_t b = __float_as_uint(v);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// CTA (slice, row): the 16 largest keys of columns [s * kSliceCols, +kSliceCols)
-// of draft row r. Every thread holds kTopQ float4 of the slice.
-// Threshold: in every warp two lanes reach the warp's second largest lane
-// maximum, so 16 values of the CTA reach the smallest of the 8 warps' second
-// largest lane maxima and every value below it is out. Values at or above it
-// (about 30 per CTA for unordered data; ties can add more) are appended as
-// keys and ranked exactly. If ties overflow the buffer, the slice is redone
-// with exact keys: the warp's 16th largest lane-maximum key bounds it, and at
-// most 16 lanes x 32 keys per warp reach that.
-__global__ void __launch_bounds__(kTopThreads, 4) sel_topk_kernel(const float* __restrict__ logits, int ld, int V,
-                                                                  int B, unsigned long long* __restrict__ part) {
-  __shared__ unsigned long long s_cand[kTopCandCap];
-  __shared__ unsigned long long s_tau_key;
-  __shared__ uint32_t s_r2[kTopThreads / 32];
-  __shared__ int s_m;
-  grid_dep_wait();
-  grid_dep_launch();
-  const int s = blockIdx.x, r = blockIdx.y, slices = gridDim.x;
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (tid == 0) {
-    s_tau_key = 0;
-    s_m = 0;
-  }
-  const float* row = logits + draft_logit_row(r, B) * ld;
-  const int c0 = s * kSliceCols, c1 = min(V, c0 + kSliceCols);
-  // columns c0 + 4 (tid + 256 u) + e; whole float4 below c1 lie below the
-  // row's padded width (a multiple of 128); columns past c1 read as -inf and
-  // are masked where keys are formed
-  float4 v[kTopQ];
-#pragma unroll
-  for (int u = 0; u < kTopQ; ++u) {
-    const int c = c0 + 4 * (tid + kTopThreads * u);
-    v[u] = c < c1 ? __ldcs(reinterpret_cast<const float4*>(row + c)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  }
-  // lane maximum (fmaxf skips NaN; an all-NaN lane counts as -inf, which
-  // only loosens the bound)
-  float bv = -INFINITY;
-#pragma unroll
-  for (int u = 0; u < kTopQ; ++u) bv = fmaxf(bv, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
-  if (bv != bv) bv = -INFINITY;
-  const uint32_t ob = ordered_bits(bv == 0.f ? 0.f : bv);
-  const uint32_t m1 = __reduce_max_sync(0xffffffffu, ob);
-  const int l1 = __ffs(__ballot_sync(0xffffffffu, ob == m1)) - 1;
-  const uint32_t m2 = __reduce_max_sync(0xffffffffu, lane == l1 ? 0u : ob);
-  if (lane == 0) s_r2[tid >> 5] = m2;
-  __syncthreads();   // s_r2, s_tau_key, s_m
-  uint32_t tb = s_r2[0];
-#pragma unroll
-  for (int w = 1; w < kTopThreads / 32; ++w) tb = min(tb, s_r2[w]);
-  const float tau = __uint_as_float((tb & 0x80000000u) ? (tb & 0x7FFFFFFFu) : ~tb);
-  auto key_at = [&](float x, int c) -> unsigned long long {
-    return (c < c1 && x == x) ? logit_key(x, c) : 0ull;
-  };
-#pragma unroll
-  for (int u = 0; u < kTopQ; ++u) {
-    const int c = c0 + 4 * (tid + kTopThreads * u);
-    const float x4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (x4[e] >= tau) {   // -0 and +0 compare equal; NaN never passes
-        const unsigned long long k = key_at(x4[e], c + e);
-        if (k != 0) {
-          const int at = atomicAdd(&s_m, 1);
-          if (at < kTopCandCap) s_cand[at] = k;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (s_m > kTopCandCap) {   // ties at the threshold: exact keys (the slice is read again)
-    const int n_local = kTopQ * 4;
-    unsigned long long best = 0;
-    for (int q = 0; q < n_local; ++q) {
-      const int c = c0 + 4 * (tid + kTopThreads * (q >> 2)) + (q & 3);
-      if (c < c1) best = max(best, key_at(row[c], c));
-    }
-    int kr = 0;
-    for (int o = 1; o < 32; ++o) kr += __shfl_sync(0xffffffffu, best, (lane + o) & 31) > best;
-    __syncthreads();   // every thread has read s_m
-    if (tid == 0) s_m = 0;
-    if (kr == kSelK - 1) atomicMax(&s_tau_key, best);
-    __syncthreads();
-    const unsigned long long tk = s_tau_key;   // 0 when no warp has 16 lanes with keys: all keys kept
-    for (int q = 0; q < n_local; ++q) {
-      const int c = c0 + 4 * (tid + kTopThreads * (q >> 2)) + (q & 3);
-      const unsigned long long k = c < c1 ? key_at(row[c], c) : 0ull;
-      if (k != 0 && k >= tk) s_cand[atomicAdd(&s_m, 1)] = k;
-    }
-    __syncthreads();
-  }
-  top_by_rank(s_cand, s_m, tid, kTopThreads, part + (static_cast<size_t>(r) * slices + s) * kSelK);
-}
 
 struct PairsArgs {
   const unsigned long long* part;   // [rows][slices][kSelK] slice lists
@@ -222,40 +84,15 @@ __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_co
   const int n_pred = t == 0 ? 1 : kSelK;
   const size_t row = static_cast<size_t>(i) * a.B + 1 + t;
   // Merge the slice lists: threads [0, 256) take draft row t, [256, 512) row
-  // t-1. A slice list's 16th key bounds the row's 16th largest from below, so
-  // only keys at or above the largest such bound are ranked.
+  // t-1 (nothing at t = 0, though they join the barriers).
   const int half = threadIdx.x >> 8, ht = threadIdx.x & 255;
-  const int n_keys = a.slices * kSelK;   // <= kSelMaxSlices * 16 = 1024
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(&s_buf[0][0][0]) + half * 2 * kSelMaxSlices * kSelK;
   unsigned long long* kept = keys + kSelMaxSlices * kSelK;
   const bool merging = half == 0 || t > 0;
-  if (threadIdx.x < 2) {
-    s_tau[threadIdx.x] = 0;
-    s_m[threadIdx.x] = 0;
-  }
-  if (merging) {   // all loads in flight before the stores
-    const unsigned long long* src = a.part + static_cast<size_t>(i * T + t - half) * n_keys;
-    unsigned long long kv[kSelMaxSlices * kSelK / 256];
-#pragma unroll
-    for (int u = 0; u < kSelMaxSlices * kSelK / 256; ++u) kv[u] = ht + 256 * u < n_keys ? __ldcg(src + ht + 256 * u) : 0ull;
-#pragma unroll
-    for (int u = 0; u < kSelMaxSlices * kSelK / 256; ++u)
-      if (ht + 256 * u < n_keys) keys[ht + 256 * u] = kv[u];
-  }
   if (half == 0) s_h[ht] = a.logits[row * a.ld + a.h_col + ht];
-  __syncthreads();
-  if (merging && ht < a.slices) atomicMax(&s_tau[half], keys[ht * kSelK + kSelK - 1]);
-  __syncthreads();
-  if (merging) {
-    const unsigned long long tau = s_tau[half];
-    for (int q = ht; q < n_keys; q += 256) {
-      const unsigned long long k = keys[q];
-      if (k != 0 && k >= tau) kept[atomicAdd(&s_m[half], 1)] = k;
-    }
-  }
-  __syncthreads();
-  if (merging) top_by_rank(kept, s_m[half], ht, 256, s_top[half]);
-  __syncthreads();
+  topk::merge_lists<kSelK>(a.part + static_cast<size_t>(i * T + t - (merging ? half : 0)) * a.slices * kSelK,
+                           merging ? a.slices : 0, ht, 256, keys, kept, &s_tau[half], &s_m[half], s_top[half],
+                           [] { __syncthreads(); });
   if (threadIdx.x < kSelK) {
     const unsigned long long k = s_top[0][threadIdx.x];
     int c = key_col(k);
@@ -383,7 +220,8 @@ __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_co
 cudaError_t launch_path_select(const SelectArgs& s, cudaStream_t stream) {
   if (s.n_seq <= 0 || s.B < 2) return cudaSuccess;
   const int T = s.B - 1, rows = s.n_seq * T;
-  cudaError_t e = launch_pdl(sel_topk_kernel, dim3(s.slices, rows), dim3(kTopThreads), 0, stream, s.logits, s.ld,
+  cudaError_t e = launch_pdl(topk::topk_slices_kernel<float, kSelK, true>, dim3(s.slices, rows), dim3(topk::kThreads), 0,
+                             stream, s.logits, s.ld,
                              s.V, s.B, s.part);
   if (e != cudaSuccess) return e;
   PairsArgs a;

@@ -127,6 +127,7 @@ struct dflash_ctx {
   int32_t* sel_cand = nullptr;             // [max_rows][16]
   float* sel_cand_u = nullptr;             // [max_rows][16]
   int32_t* sel_next = nullptr;             // [max_rows][16]
+  unsigned long long* samp_part = nullptr; // [max_rows][64][32] sampling slice lists
   int* sel_tickets = nullptr;              // [max_batch]
 
   // weight descriptors
@@ -342,7 +343,8 @@ dflash_status dflash_destroy(dflash_ctx* ctx) {
                   ctx->hg, ctx->ssA, ctx->ssB, ctx->q, ctx->kb, ctx->vb, ctx->attn, ctx->act, ctx->htg, ctx->ssF,
                   ctx->part_o, ctx->part_ml, ctx->split_ws, ctx->tickets, ctx->keys, ctx->done, ctx->top_logit,
                   ctx->sel_table, ctx->sel_logits, ctx->sel_part, ctx->sel_scores, ctx->sel_cand, ctx->sel_cand_u,
-                  ctx->sel_tickets, ctx->sel_next};
+                  ctx->sel_tickets, ctx->sel_next,
+                  ctx->samp_part};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (ctx->h_snap) cudaFreeHost(ctx->h_snap);
@@ -701,8 +703,82 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
   return DFLASH_OK;
 }
 
+namespace {
+
+// Temperature-sampling head of a draft (dflash_draft_sample).
+struct SampleReq {
+  float temperature, top_p;
+  int top_k;
+  const float* uniforms;
+  int32_t* q_ids;
+  float* q_probs;
+};
+
+// The selector's and the sampling head's fp32 logits rows [max_rows][V_pad + 256]
+// and the sampling slice lists, allocated at first use.
+dflash_status ensure_logits32(dflash_ctx* ctx) {
+  if (ctx->sel_logits) return DFLASH_OK;
+  const dflash_config& c = ctx->cfg;
+  const size_t rows = ctx->max_rows();
+  ctx->sel_hcol = 128 * ceil_div(c.vocab, 128);   // H starts at the first tile after the vocabulary
+  ctx->sel_ld = ctx->sel_hcol + kSelDim;
+  cudaError_t e = dalloc(&ctx->sel_logits, rows * ctx->sel_ld);
+  if (e == cudaSuccess) e = cudaMemset(ctx->sel_logits, 0, rows * ctx->sel_ld * sizeof(float));
+  if (e != cudaSuccess) {
+    if (ctx->sel_logits) cudaFree(ctx->sel_logits);
+    ctx->sel_logits = nullptr;
+    return fail(ctx, e == cudaErrorMemoryAllocation ? DFLASH_ENOMEM : DFLASH_ECUDA,
+                std::string("logits buffer: ") + cudaGetErrorString(e));
+  }
+  return DFLASH_OK;
+}
+
+dflash_status ensure_sample_part(dflash_ctx* ctx) {
+  if (ctx->samp_part) return DFLASH_OK;
+  const cudaError_t e = dalloc(&ctx->samp_part, static_cast<size_t>(ctx->max_rows()) * kSampleMaxSlices * kSampleWidth);
+  if (e != cudaSuccess) {
+    ctx->samp_part = nullptr;
+    return fail(ctx, e == cudaErrorMemoryAllocation ? DFLASH_ENOMEM : DFLASH_ECUDA,
+                std::string("sampling lists: ") + cudaGetErrorString(e));
+  }
+  return DFLASH_OK;
+}
+
+dflash_status check_sampling(dflash_ctx* ctx, float temperature, int top_k, float top_p) {
+  if (!(temperature > 0.f) || !(temperature < 1e30f)) return fail(ctx, DFLASH_EINVAL, "temperature must be positive");
+  if (top_k < 1 || top_k > kSampleWidth) return fail(ctx, DFLASH_EINVAL, "top_k must be in [1, 32]");
+  if (!(top_p > 0.f) || top_p > 1.f) return fail(ctx, DFLASH_EINVAL, "top_p must be in (0, 1]");
+  return DFLASH_OK;
+}
+
+dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids, int B,
+                         int32_t* draft_ids, void* stream_v, const SampleReq* samp);
+
+}  // namespace
+
 dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids, int B,
                            int32_t* draft_ids, void* stream_v) {
+  return draft_impl(ctx, seq_ids, n_seq, anchor_ids, B, draft_ids, stream_v, nullptr);
+}
+
+dflash_status dflash_draft_sample(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids,
+                                  int B, float temperature, int top_k, float top_p, const float* uniforms,
+                                  int32_t* draft_ids, int32_t* q_ids, float* q_probs, void* stream_v) {
+  if (!ctx) return DFLASH_EINVAL;
+  dflash_status st = check_sampling(ctx, temperature, top_k, top_p);
+  if (st != DFLASH_OK) return st;
+  if (ctx->sel_on) return fail(ctx, DFLASH_EINVAL, "the path selector is installed (its walk is greedy)");
+  if (ctx->cfg.vocab > kSampleMaxSlices * sample_slice_cols(false))
+    return fail(ctx, DFLASH_EINVAL, "vocab above 524288 for sampling");
+  if (B > 1 && (!uniforms || !q_ids || !q_probs)) return fail(ctx, DFLASH_EINVAL, "null uniforms or q lists");
+  SampleReq r{temperature, top_p, top_k, uniforms, q_ids, q_probs};
+  return draft_impl(ctx, seq_ids, n_seq, anchor_ids, B, draft_ids, stream_v, &r);
+}
+
+namespace {
+
+dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids, int B,
+                         int32_t* draft_ids, void* stream_v, const SampleReq* samp) {
   if (!ctx) return DFLASH_EINVAL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const dflash_config& c = ctx->cfg;
@@ -713,6 +789,11 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   meta.B = B;
   if (n_seq == 0) return DFLASH_OK;
   if (!anchor_ids || (B > 1 && !draft_ids)) return fail(ctx, DFLASH_EINVAL, "null anchor_ids or draft_ids");
+  if (samp && B > 1) {
+    st = ensure_logits32(ctx);
+    if (st == DFLASH_OK) st = ensure_sample_part(ctx);
+    if (st != DFLASH_OK) return st;
+  }
   consume_snapshot(ctx, false);
 
   const int H = c.hidden, d = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, F = c.ffn;
@@ -934,8 +1015,39 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   }
   ctx->last_rows = M;
   ctx->last_draft_rows = n_seq * (B - 1);
-  ctx->last_sel_rows = ctx->sel_on ? n_seq * (B - 1) : 0;
-  if (B > 1 && ctx->sel_on) {
+  ctx->last_sel_rows = ctx->sel_on && !samp ? n_seq * (B - 1) : 0;
+  if (B > 1 && samp) {
+    // LM head into fp32 rows (final RMSNorm scale applied), then the 32
+    // largest logits of every masked row, the filter and the draw
+    const int Md = n_seq * (B - 1);
+    const CUtensorMap* hmap_s = act_map(ctx, ctx->hg, M, H, gemm_act_rows(M, c.vocab, H, sms));
+    if (!hmap_s) return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+    AMaps am;
+    am.m[0] = ctx->m_lm;
+    GemmEpi e = base_epi(ctx, EPI_F32_STORE);
+    e.out_f32 = ctx->sel_logits;
+    e.ld_out = ctx->sel_ld;
+    e.in_ss = ctx->ssA;
+    e.in_ss_parts = parts;
+    e.in_ss_ld = rows_ld;
+    {
+      ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(M, c.vocab, H, c.vocab, 4), 2.0 * M * c.vocab * H);
+      CK(launch_gemm(am, stacked({c.vocab}), *hmap_s, M, c.vocab, H, 0, e, work, ctx->num_sms, stream));
+    }
+    FilterArgs fa;
+    fa.slices = ceil_div(c.vocab, sample_slice_cols(false));
+    fa.part = ctx->samp_part;
+    fa.inv_temperature = 1.f / samp->temperature;
+    fa.top_k = samp->top_k;
+    fa.top_p = samp->top_p;
+    fa.uniforms = samp->uniforms;
+    fa.out_ids = samp->q_ids;
+    fa.out_probs = samp->q_probs;
+    fa.drawn = draft_ids;
+    ProfScope ps(ctx, DFLASH_K_SAMPLE, stream, 4.0 * Md * c.vocab + 8.0 * Md * fa.slices * kSampleWidth * 2 +
+                 8.0 * Md * kSampleWidth + 8.0 * Md, 0, 2);
+    CK(launch_sample_filter(ctx->sel_logits, false, ctx->sel_ld, c.vocab, Md, B, ctx->samp_part, fa, stream));
+  } else if (B > 1 && ctx->sel_on) {
     // LM head and the selector's context gate H = W_H h~ in one GEMM over all
     // block rows, final RMSNorm scale applied: logits in columns [0, V), H in
     // [sel_hcol, sel_hcol + 256). Then top-16, pair scores and the walk.
@@ -1003,21 +1115,10 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
   return DFLASH_OK;
 }
 
-dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, int B, const int32_t* draft_ids,
-                            const int32_t* target_ids, int32_t* tau, int32_t* bonus, void* stream_v) {
-  if (!ctx) return DFLASH_EINVAL;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-  SeqMeta meta;
-  dflash_status st = check_seqs(ctx, seq_ids, n_seq, &meta);
-  if (st != DFLASH_OK) return st;
-  if (B < 1 || B > ctx->cfg.max_block) return fail(ctx, DFLASH_EINVAL, "B out of range");
-  meta.B = B;
-  if (n_seq == 0) return DFLASH_OK;
-  if ((B > 1 && !draft_ids) || !target_ids || !tau || !bonus) return fail(ctx, DFLASH_EINVAL, "null pointer");
-  {
-    ProfScope ps(ctx, DFLASH_K_VERIFY, stream, 4.0 * n_seq * (2 * B + 2), 0);
-    CK(launch_verify(meta, seq_state(ctx), draft_ids, target_ids, tau, bonus, stream));
-  }
+// After a verify launch: the host's length bounds take every pending token
+// (the device commits tau of them), and a snapshot of the exact lengths is
+// requested to tighten the bounds later.
+dflash_status commit_host_side(dflash_ctx* ctx, const SeqMeta& meta, int n_seq, cudaStream_t stream) {
   bool had_pending = false;
   for (int i = 0; i < n_seq; ++i) {
     const int s = meta.slot[i];
@@ -1035,6 +1136,26 @@ dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, 
     }
   }
   return DFLASH_OK;
+}
+
+}  // namespace
+
+dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, int B, const int32_t* draft_ids,
+                            const int32_t* target_ids, int32_t* tau, int32_t* bonus, void* stream_v) {
+  if (!ctx) return DFLASH_EINVAL;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  SeqMeta meta;
+  dflash_status st = check_seqs(ctx, seq_ids, n_seq, &meta);
+  if (st != DFLASH_OK) return st;
+  if (B < 1 || B > ctx->cfg.max_block) return fail(ctx, DFLASH_EINVAL, "B out of range");
+  meta.B = B;
+  if (n_seq == 0) return DFLASH_OK;
+  if ((B > 1 && !draft_ids) || !target_ids || !tau || !bonus) return fail(ctx, DFLASH_EINVAL, "null pointer");
+  {
+    ProfScope ps(ctx, DFLASH_K_VERIFY, stream, 4.0 * n_seq * (2 * B + 2), 0);
+    CK(launch_verify(meta, seq_state(ctx), draft_ids, target_ids, tau, bonus, stream));
+  }
+  return commit_host_side(ctx, meta, n_seq, stream);
 }
 
 dflash_status dflash_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, int32_t* out, void* stream) {
@@ -1083,6 +1204,71 @@ dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0
   return DFLASH_OK;
 }
 
+dflash_status dflash_sample_filter(dflash_ctx* ctx, const uint16_t* logits, int rows, int cols, float temperature,
+                                   int top_k, float top_p, const float* uniforms, int32_t* out_ids, float* out_probs,
+                                   int32_t* drawn, void* stream_v) {
+  if (!ctx) return DFLASH_EINVAL;
+  dflash_status st = check_sampling(ctx, temperature, top_k, top_p);
+  if (st != DFLASH_OK) return st;
+  if (rows < 0 || rows > ctx->max_rows()) return fail(ctx, DFLASH_EINVAL, "rows outside [0, max_batch * max_block]");
+  if (rows == 0) return DFLASH_OK;
+  if (cols < kSampleWidth || cols % 8 || cols > kSampleMaxSlices * sample_slice_cols(true))
+    return fail(ctx, DFLASH_EINVAL, "cols must be a multiple of 8 in [32, 1048576]");
+  if (!logits || !out_ids || !out_probs || (drawn && !uniforms)) return fail(ctx, DFLASH_EINVAL, "null pointer");
+  if (!aligned16(logits)) return fail(ctx, DFLASH_EINVAL, "logits not 16-byte aligned");
+  st = ensure_sample_part(ctx);
+  if (st != DFLASH_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  FilterArgs fa;
+  fa.slices = ceil_div(cols, sample_slice_cols(true));
+  fa.part = ctx->samp_part;
+  fa.inv_temperature = 1.f / temperature;
+  fa.top_k = top_k;
+  fa.top_p = top_p;
+  fa.uniforms = uniforms;
+  fa.out_ids = out_ids;
+  fa.out_probs = out_probs;
+  fa.drawn = drawn;
+  ProfScope ps(ctx, DFLASH_K_SAMPLE, stream, 2.0 * rows * cols + 16.0 * rows * fa.slices * kSampleWidth +
+               8.0 * rows * kSampleWidth, 0, 2);
+  CK(launch_sample_filter(logits, true, cols, cols, rows, 0, ctx->samp_part, fa, stream));
+  return DFLASH_OK;
+}
+
+dflash_status dflash_verify_sample(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, int B, const int32_t* draft_ids,
+                                   const int32_t* q_ids, const float* q_probs, const int32_t* p_ids,
+                                   const float* p_probs, const float* u_accept, const float* u_resample,
+                                   int32_t* tau, int32_t* bonus, void* stream_v) {
+  if (!ctx) return DFLASH_EINVAL;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  SeqMeta meta;
+  dflash_status st = check_seqs(ctx, seq_ids, n_seq, &meta);
+  if (st != DFLASH_OK) return st;
+  if (B < 1 || B > ctx->cfg.max_block) return fail(ctx, DFLASH_EINVAL, "B out of range");
+  meta.B = B;
+  if (n_seq == 0) return DFLASH_OK;
+  if ((B > 1 && (!draft_ids || !q_ids || !q_probs || !u_accept)) || !p_ids || !p_probs || !u_resample || !tau ||
+      !bonus)
+    return fail(ctx, DFLASH_EINVAL, "null pointer");
+  VerifySampleArgs a;
+  a.drafts = draft_ids;
+  a.q_ids = q_ids;
+  a.q_probs = q_probs;
+  a.p_ids = p_ids;
+  a.p_probs = p_probs;
+  a.u_accept = u_accept;
+  a.u_resample = u_resample;
+  a.tau = tau;
+  a.bonus = bonus;
+  a.status = ctx->d_status;
+  {
+    ProfScope ps(ctx, DFLASH_K_VERIFY, stream, 4.0 * n_seq * (2 * B + 2) + 8.0 * n_seq * (2 * B - 1) * kSampleWidth,
+                 0);
+    CK(launch_verify_sample(meta, seq_state(ctx), a, stream));
+  }
+  return commit_host_side(ctx, meta, n_seq, stream);
+}
+
 dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, const uint16_t* w_b,
                                        const uint16_t* w_h, int dim, void* stream_v) {
   if (!ctx) return DFLASH_EINVAL;
@@ -1099,11 +1285,10 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
     return fail(ctx, DFLASH_EINVAL, "vocab outside [16, 524288] for the path selector");
   if (!aligned16(w_a) || !aligned16(w_b) || !aligned16(w_h)) return fail(ctx, DFLASH_EINVAL, "weights not 16-byte aligned");
   const size_t rows = ctx->max_rows();
+  dflash_status lst = ensure_logits32(ctx);
+  if (lst != DFLASH_OK) return lst;
   if (!ctx->sel_table) {
-    ctx->sel_hcol = 128 * ceil_div(c.vocab, 128);   // H starts at the first tile after the vocabulary
-    ctx->sel_ld = ctx->sel_hcol + kSelDim;
     cudaError_t e = dalloc(&ctx->sel_table, static_cast<size_t>(c.vocab) * 2 * kSelDim);
-    if (e == cudaSuccess) e = dalloc(&ctx->sel_logits, rows * ctx->sel_ld);
     if (e == cudaSuccess) e = dalloc(&ctx->sel_part, rows * kSelMaxSlices * kSelK);
     if (e == cudaSuccess) e = dalloc(&ctx->sel_scores, rows * kSelK * kSelK);
     if (e == cudaSuccess) e = dalloc(&ctx->sel_cand, rows * kSelK);
@@ -1112,12 +1297,11 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
     if (e == cudaSuccess) e = dalloc(&ctx->sel_tickets, c.max_batch);
     if (e == cudaSuccess) e = cudaMemset(ctx->sel_tickets, 0, c.max_batch * sizeof(int));
     if (e != cudaSuccess) {
-      void* ps[] = {ctx->sel_table, ctx->sel_logits, ctx->sel_part, ctx->sel_scores, ctx->sel_cand, ctx->sel_cand_u,
+      void* ps[] = {ctx->sel_table, ctx->sel_part, ctx->sel_scores, ctx->sel_cand, ctx->sel_cand_u,
                     ctx->sel_tickets, ctx->sel_next};
       for (void* p : ps)
         if (p) cudaFree(p);
       ctx->sel_table = nullptr;
-      ctx->sel_logits = nullptr;
       ctx->sel_part = nullptr;
       ctx->sel_scores = nullptr;
       ctx->sel_cand = nullptr;

@@ -186,6 +186,62 @@ dflash_status dflash_rows_argmax_bf16(const uint16_t* logits, int rows, int cols
  * device status word: OK, ETIMEOUT or EDEVICE. */
 dflash_status dflash_sync(dflash_ctx* ctx);
 
+/* ---- temperature sampling and lossless rejection-sampling verify ----
+ * The DFlash notes evaluate at temperature 1 ("DFlash - Block Diffusion for
+ * Flash Speculative Decoding", 6.2 "Sampling (Temperature = 1)", with the
+ * "Lossless Guarantee"; the "DFlash 2" notes at temperature 1, top-p 0.95,
+ * top-k 20, lossless rejection sampling). A filtered distribution keeps the
+ * top_k largest logits (lower id first among equal logits), takes their
+ * softmax at the temperature, keeps the shortest prefix (in that order) whose
+ * mass reaches top_p, and renormalises. Lists are DFLASH_SAMPLE_WIDTH wide:
+ * ids in decreasing probability, then -1 with probability 0. Draws are
+ * inverse-CDF draws with caller-supplied uniforms in [0, 1): the first list
+ * entry whose cumulative probability exceeds u. Arguments: temperature > 0,
+ * top_k in [1, 32], top_p in (0, 1]; EINVAL otherwise. */
+#define DFLASH_SAMPLE_WIDTH 32
+
+/* The drafter pass of dflash_draft with a sampling head: every masked
+ * position j is drawn from the drafter's filtered distribution q_j.
+ *  uniforms   device [n_seq, B-1] fp32, one per masked position
+ *  draft_ids  device [n_seq, B-1] int32 output (the draws)
+ *  q_ids      device [n_seq, B-1, 32] int32 output, q_probs fp32 output:
+ *             the lists q_j the draws came from (dflash_verify_sample's input)
+ * The first call allocates the fp32 logits rows (max_batch*max_block rows of
+ * V+256 floats) and the list scratch. Errors: EINVAL (also while a path
+ * selector is installed, or vocab above 524288), ENOMEM. */
+dflash_status dflash_draft_sample(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq,
+                                  const int32_t* anchor_ids, int B, float temperature, int top_k,
+                                  float top_p, const float* uniforms, int32_t* draft_ids,
+                                  int32_t* q_ids, float* q_probs, void* stream);
+
+/* Filtered distributions of bf16 logit rows (the target's block logits):
+ *  logits     device [rows, cols] bf16, row pitch cols, 16-byte aligned;
+ *             cols a multiple of 8, 32 <= cols <= 1048576; rows <= max_batch*max_block
+ *  out_ids    device [rows, 32] int32, out_probs device [rows, 32] fp32
+ *  uniforms, drawn  device [rows] fp32 / int32, or both NULL: one draw per row
+ * Uses the context's list scratch only (no sequence state). Errors: EINVAL, ENOMEM. */
+dflash_status dflash_sample_filter(dflash_ctx* ctx, const uint16_t* logits, int rows, int cols,
+                                   float temperature, int top_k, float top_p, const float* uniforms,
+                                   int32_t* out_ids, float* out_probs, int32_t* drawn, void* stream);
+
+/* Lossless speculative-sampling verify and commit. Per sequence, walking
+ * j = 0..B-2: draft x_j (drawn from q_j) is accepted when
+ * u_accept[j] < min(1, p_j(x_j) / q_j(x_j)); at the first rejection the
+ * emitted token is drawn from max(0, p_j - q_j) (over p_j's list, in its
+ * order) with u_resample[j], tau = j + 1; when every draft is accepted,
+ * tau = B and the bonus is drawn from p_{B-1} with u_resample[B-1]. Then the
+ * first min(tau, pending) pending tokens are committed, as dflash_verify.
+ *  draft_ids, q_ids, q_probs   device, as dflash_draft_sample wrote them
+ *  p_ids, p_probs    device [n_seq, B, 32]: the target's filtered lists after
+ *                    each block position (dflash_sample_filter of its logits)
+ *  u_accept [n_seq, B-1], u_resample [n_seq, B]  device fp32 uniforms
+ *  tau, bonus        device [n_seq] int32 outputs
+ * Errors: EINVAL. An empty target list latches EDEVICE (reported by sync). */
+dflash_status dflash_verify_sample(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, int B,
+                                   const int32_t* draft_ids, const int32_t* q_ids, const float* q_probs,
+                                   const int32_t* p_ids, const float* p_probs, const float* u_accept,
+                                   const float* u_resample, int32_t* tau, int32_t* bonus, void* stream);
+
 /* Install (or remove) the DFlash 2 path selector ("DFlash 2" notes,
  * "Solution - Lightweight Path Selector"). While installed, dflash_draft
  * keeps the 16 largest logits of every masked position t as its candidates
@@ -284,6 +340,7 @@ enum {
   DFLASH_K_VERIFY,        /* verify + commit                            */
   DFLASH_K_OTHER,         /* bookkeeping kernels                        */
   DFLASH_K_SELECT,        /* path selector: top-16, pair scores, walk   */
+  DFLASH_K_SAMPLE,        /* top-32 lists, filter and draw              */
   DFLASH_K_COUNT
 };
 

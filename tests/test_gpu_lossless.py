@@ -75,7 +75,7 @@ def test_speculative_loop_matches_greedy_target(dfl, selector):
             outs[s].append(targets[s].next(outs[s], 0))
             anchors.append(outs[s][-1])
         taus = []
-        while min(len(o) for o in outs) < target_len:
+        while max(len(o) for o in outs) < target_len:
             drafts = d.draft(seqs, i32_dev(anchors, DEV), B).cpu().numpy()
             t_ids = np.zeros((n, B), dtype=np.int32)
             fb = []
