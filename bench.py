@@ -218,6 +218,7 @@ class Cycle:
         self.logits = logits.to(torch.bfloat16)
         del logits
         self.targets = torch.empty(batch, B, dtype=torch.int32, device=dev)
+        self.sampling = None
         self.drafts = torch.empty(batch, B - 1, dtype=torch.int32, device=dev)
         self.tau = torch.empty(batch, dtype=torch.int32, device=dev)
         self.bonus = torch.randint(0, shape.vocab - 1, (batch,), generator=g, device=dev, dtype=torch.int32)
@@ -226,12 +227,53 @@ class Cycle:
         self.d.draft(self.seqs, self.bonus, B, out=self.drafts)
         torch.cuda.synchronize()
 
+    def enable_sampling(self, temperature: float, top_k: int, top_p: float, seed: int) -> None:
+        """Switch the cycle to temperature sampling: the target's filtered lists
+        replace its argmax, the speculative-sampling verify replaces the greedy
+        one and the drafter draws its block. Uniform draws are seeded inputs,
+        one ring slot per step."""
+        torch = self.torch
+        b, B, W = len(self.seqs), self.B, self.dfl.SAMPLE_WIDTH
+        g = torch.Generator(device=self.dev)
+        g.manual_seed(seed)
+        sp = {"t": temperature, "k": top_k, "p": top_p,
+              "u_acc": torch.rand(self.ring, b, B - 1, generator=g, device=self.dev),
+              "u_res": torch.rand(self.ring, b, B, generator=g, device=self.dev),
+              "u_draft": torch.rand(self.ring, b, B - 1, generator=g, device=self.dev),
+              "p_ids": torch.empty(b * B, W, dtype=torch.int32, device=self.dev),
+              "p_probs": torch.empty(b * B, W, dtype=torch.float32, device=self.dev),
+              "q_ids": torch.empty(b, B - 1, W, dtype=torch.int32, device=self.dev),
+              "q_probs": torch.empty(b, B - 1, W, dtype=torch.float32, device=self.dev)}
+        self.sampling = sp
+        self.d.draft_sample(self.seqs, self.bonus, B, temperature, top_k, top_p, sp["u_draft"][0], out=self.drafts,
+                            q_ids=sp["q_ids"], q_probs=sp["q_probs"])
+        torch.cuda.synchronize()
+
+    def _verify_and_draft(self, r: int) -> None:
+        sp = self.sampling
+        if sp is None:
+            self.d.verify(self.seqs, self.B, self.drafts, self.targets, tau=self.tau, bonus=self.bonus)
+            self.d.draft(self.seqs, self.bonus, self.B, out=self.drafts)
+            return
+        b, B = len(self.seqs), self.B
+        self.d.verify_sample(self.seqs, B, self.drafts, sp["q_ids"], sp["q_probs"], sp["p_ids"].view(b, B, -1),
+                             sp["p_probs"].view(b, B, -1), sp["u_acc"][r], sp["u_res"][r], tau=self.tau,
+                             bonus=self.bonus)
+        self.d.draft_sample(self.seqs, self.bonus, B, sp["t"], sp["k"], sp["p"], sp["u_draft"][r], out=self.drafts,
+                            q_ids=sp["q_ids"], q_probs=sp["q_probs"])
+
+    def _target_side(self, logits) -> None:
+        sp = self.sampling
+        if sp is None:
+            self.dfl.dflash_rows_argmax_bf16(logits, out=self.targets.view(-1))
+        else:
+            self.d.sample_filter(logits, sp["t"], sp["k"], sp["p"], ids=sp["p_ids"], probs=sp["p_probs"])
+
     def step(self, k: int) -> None:
         r = k % self.ring
-        self.dfl.dflash_rows_argmax_bf16(self.logits[r], out=self.targets.view(-1))
+        self._target_side(self.logits[r])
         self.d.fuse_ctx(self.seqs, [self.B] * len(self.seqs), self.feats[r], pending=True)
-        self.d.verify(self.seqs, self.B, self.drafts, self.targets, tau=self.tau, bonus=self.bonus)
-        self.d.draft(self.seqs, self.bonus, self.B, out=self.drafts)
+        self._verify_and_draft(r)
 
     def step_e2e(self, k: int, host) -> None:
         """The same cycle through the public API with host buffers: every
@@ -244,13 +286,12 @@ class Cycle:
             self._copy_inputs(0, host)
         slot = k % 2
         cur.wait_event(host["copied"][slot])
-        self.dfl.dflash_rows_argmax_bf16(self.logits[slot], out=self.targets.view(-1))
+        self._target_side(self.logits[slot])
         self.d.fuse_ctx(self.seqs, [self.B] * len(self.seqs), self.feats[slot], pending=True)
         host["consumed"][slot].record(cur)
         if k + 1 < host["steps"]:
             self._copy_inputs(k + 1, host)
-        self.d.verify(self.seqs, self.B, self.drafts, self.targets, tau=self.tau, bonus=self.bonus)
-        self.d.draft(self.seqs, self.bonus, self.B, out=self.drafts)
+        self._verify_and_draft(k % self.ring)
         host["drafts"].copy_(self.drafts, non_blocking=True)
         host["tau"].copy_(self.tau, non_blocking=True)
         host["bonus"].copy_(self.bonus, non_blocking=True)
@@ -347,6 +388,8 @@ def run_ours(args):
     sel = selector_weights(shape, dev, seed=7 + rank)
     if args.path_selector:
         cyc.d.set_path_selector(**sel)
+    if args.sampling:
+        cyc.enable_sampling(1.0, 20, 0.95, seed=11 + rank)
 
     # NVTX range names let a profiler select the warm-up steps
     # (ncu --nvtx --nvtx-include "warmup/")
@@ -389,7 +432,11 @@ def run_ours(args):
     kd = min(K, 200)
     ms_draft = timed(lambda k: cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts), kd, world, dev)
     len_end = cyc.d.seq_len(0)[0]
-    # the drafter pass with the other selector setting (plain argmax <-> path selector)
+    # the drafter pass with the other head: plain argmax <-> path selector, and
+    # the sampling head (top-k 20, top-p 0.95, temperature 1) with the target's
+    # filter and the speculative-sampling verify
+    samp_out = (None if args.path_selector
+                else sampling_summary(cyc, kd, world, dev, None if args.sampling else ms_draft))
     cyc.d.set_path_selector(**({} if args.path_selector else sel))
     for _ in range(3):
         cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts)
@@ -422,8 +469,11 @@ def run_ours(args):
                          "GB_per_step": s["bytes"] / K / 1e9,
                          "GBps": s["bytes"] / t / 1e9 if t else None,
                          "TFLOPs": s["flops"] / t / 1e12 if t else None}
-    launches_per_step = sum(s["launches"] for s in stats.values()) / K + 1   # + rows_argmax
-    step_bytes = sum(s["bytes"] for s in stats.values()) / K + batch * B * (QWEN3_8B.vocab * 2 + 4)
+    # the target's argmax runs outside the context's accounting; the sampling
+    # filter inside it
+    launches_per_step = sum(s["launches"] for s in stats.values()) / K + (0 if args.sampling else 1)
+    step_bytes = sum(s["bytes"] for s in stats.values()) / K + (0 if args.sampling else
+                                                                  batch * B * (QWEN3_8B.vocab * 2 + 4))
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -435,7 +485,10 @@ def run_ours(args):
                    "context_at_timed_start": start_lens[0] + W, "context_at_end": len_end,
                    "global_batch": batch * world, "parallelism": f"replicas x{world}",
                    "step": "rows_argmax(target logits) + fuse_ctx(B, pending) + verify + draft"
-                           + (" (path selector installed: draft returns its walk)" if args.path_selector else ""),
+                           + (" (path selector installed: draft returns its walk)" if args.path_selector else "")
+                           + (" at temperature 1, top-k 20, top-p 0.95: sample_filter(target logits) + fuse_ctx + "
+                              "verify_sample + draft_sample" if args.sampling else ""),
+                   "sampling": bool(args.sampling),
                    "path_selector": bool(args.path_selector),
                    "l2": "no flush: each step streams 3.4 GB of weights (> 129 MB L2)"},
         "clocks": clocks,
@@ -456,9 +509,50 @@ def run_ours(args):
         "latency_model": latency_model(ms_draft / kd, max_ms / K, peaks["hbm_gbs"], B),
         "kernels": kernels,
         "path_selector": selector_summary(st_sel, n_sel, ms_sel / kd, ms_plain / kd, peaks, peak_kind, batch, world),
+        "sampling": samp_out,
     }
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(shape, cyc.weights, lens[0], B)
+    return out
+
+
+def sampling_summary(cyc, kd: int, world: int, dev, ms_plain_total):
+    """Temperature-1 pieces timed on their own (top-k 20, top-p 0.95): the
+    drafter pass with its sampling head, the target-side filter of the
+    block's bf16 logits, and the speculative-sampling verify (no pending
+    tokens, so it commits nothing)."""
+    import torch
+    if cyc.sampling is None:
+        saved = None
+        cyc.enable_sampling(1.0, 20, 0.95, seed=99)
+    else:
+        saved = cyc.sampling
+    sp = cyc.sampling
+    b, B = len(cyc.seqs), cyc.B
+    ms_ds = timed(lambda k: cyc.d.draft_sample(cyc.seqs, cyc.bonus, B, 1.0, 20, 0.95, sp["u_draft"][k % cyc.ring],
+                                               out=cyc.drafts, q_ids=sp["q_ids"], q_probs=sp["q_probs"]),
+                  kd, world, dev)
+    ms_f = timed(lambda k: cyc.d.sample_filter(cyc.logits[k % cyc.ring], 1.0, 20, 0.95, ids=sp["p_ids"],
+                                               probs=sp["p_probs"]), kd, world, dev)
+    ms_am = timed(lambda k: cyc.dfl.dflash_rows_argmax_bf16(cyc.logits[k % cyc.ring], out=cyc.targets.view(-1)),
+                  kd, world, dev)
+    ms_v = timed(lambda k: cyc.d.verify_sample(cyc.seqs, B, cyc.drafts, sp["q_ids"], sp["q_probs"],
+                                               sp["p_ids"].view(b, B, -1), sp["p_probs"].view(b, B, -1),
+                                               sp["u_acc"][k % cyc.ring], sp["u_res"][k % cyc.ring],
+                                               tau=cyc.tau, bonus=cyc.bonus), kd, world, dev)
+    if saved is None:
+        cyc.sampling = None
+        cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts)
+        torch.cuda.synchronize()
+    V = cyc.shape.vocab
+    out = {"temperature": 1.0, "top_k": 20, "top_p": 0.95,
+           "draft_sample_ms_per_pass": ms_ds / kd,
+           "target_filter_us": 1e3 * ms_f / kd, "target_argmax_us": 1e3 * ms_am / kd,
+           "verify_sample_us": 1e3 * ms_v / kd,
+           "target_filter_GBps": b * B * V * 2 / (ms_f / kd / 1e3) / 1e9}
+    if ms_plain_total:
+        out["draft_plain_ms_per_pass"] = ms_plain_total / kd
+        out["draft_sample_overhead_ms"] = (ms_ds - ms_plain_total) / kd
     return out
 
 
@@ -732,7 +826,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path-selector", action="store_true",
                     help="install the DFlash 2 path selector for the timed cycle (draft returns its walk)")
+    ap.add_argument("--sampling", action="store_true",
+                    help="time the temperature-1 cycle (top-k 20, top-p 0.95, lossless rejection sampling)")
     args = ap.parse_args(argv)
+    if args.sampling and args.path_selector:
+        ap.error("--sampling and --path-selector exclude each other (the selector's walk is greedy)")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

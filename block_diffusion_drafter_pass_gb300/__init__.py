@@ -289,15 +289,19 @@ class Drafter:
                                                   _ptr(q_probs) if q_probs.numel() else 0, _stream(stream)), self.ctx)
         return out, q_ids, q_probs
 
-    def sample_filter(self, logits, temperature: float, top_k: int, top_p: float, uniforms=None, stream=None):
+    def sample_filter(self, logits, temperature: float, top_k: int, top_p: float, uniforms=None, ids=None,
+                      probs=None, drawn=None, stream=None):
         """Filtered distributions of bf16 logit rows [rows, V]: (ids [rows, 32],
         probs [rows, 32], draws [rows] or None when no uniforms are given)."""
         import torch
         assert logits.dtype == torch.bfloat16 and logits.is_cuda and logits.is_contiguous()
         rows, cols = logits.shape
-        ids = torch.empty(rows, SAMPLE_WIDTH, dtype=torch.int32, device=logits.device)
-        probs = torch.empty(rows, SAMPLE_WIDTH, dtype=torch.float32, device=logits.device)
-        drawn = torch.empty(rows, dtype=torch.int32, device=logits.device) if uniforms is not None else None
+        if ids is None:
+            ids = torch.empty(rows, SAMPLE_WIDTH, dtype=torch.int32, device=logits.device)
+        if probs is None:
+            probs = torch.empty(rows, SAMPLE_WIDTH, dtype=torch.float32, device=logits.device)
+        if uniforms is not None and drawn is None:
+            drawn = torch.empty(rows, dtype=torch.int32, device=logits.device)
         _check(load_library().dflash_sample_filter(self.ctx, _ptr(logits), rows, cols, float(temperature), int(top_k),
                                                    float(top_p), _ptr(uniforms), _ptr(ids), _ptr(probs),
                                                    _ptr(drawn), _stream(stream)), self.ctx)
