@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_co
   __shared__ int s_pred[kSelK], s_cand[kSelK];
   __shared__ float s_u[kSelK];
   __shared__ unsigned long long s_top[2][kSelK];
-  __shared__ unsigned long long s_tau[2];
+  __shared__ unsigned long long s_tau[2], s_lo[2];
   __shared__ int s_m[2];
   __shared__ int s_last;
   float(&s_ah)[kSelK][kPadRow] = s_buf[0];
@@ -91,7 +91,8 @@ __global__ void __launch_bounds__(kPairThreads) sel_pairs_kernel(const __grid_co
   const bool merging = half == 0 || t > 0;
   if (half == 0) s_h[ht] = a.logits[row * a.ld + a.h_col + ht];
   topk::merge_lists<kSelK>(a.part + static_cast<size_t>(i * T + t - (merging ? half : 0)) * a.slices * kSelK,
-                           merging ? a.slices : 0, ht, 256, keys, kept, &s_tau[half], &s_m[half], s_top[half],
+                           merging ? a.slices : 0, ht, 256, keys, kept, &s_tau[half], &s_lo[half], &s_m[half],
+                           s_top[half],
                            [] { __syncthreads(); });
   if (threadIdx.x < kSelK) {
     const unsigned long long k = s_top[0][threadIdx.x];

@@ -1213,7 +1213,7 @@ dflash_status dflash_sample_filter(dflash_ctx* ctx, const uint16_t* logits, int 
   if (rows < 0 || rows > ctx->max_rows()) return fail(ctx, DFLASH_EINVAL, "rows outside [0, max_batch * max_block]");
   if (rows == 0) return DFLASH_OK;
   if (cols < kSampleWidth || cols % 8 || cols > kSampleMaxSlices * sample_slice_cols(true))
-    return fail(ctx, DFLASH_EINVAL, "cols must be a multiple of 8 in [32, 1048576]");
+    return fail(ctx, DFLASH_EINVAL, "cols must be a multiple of 8 in [32, 524288]");
   if (!logits || !out_ids || !out_probs || (drawn && !uniforms)) return fail(ctx, DFLASH_EINVAL, "null pointer");
   if (!aligned16(logits)) return fail(ctx, DFLASH_EINVAL, "logits not 16-byte aligned");
   st = ensure_sample_part(ctx);

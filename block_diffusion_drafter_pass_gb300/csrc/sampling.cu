@@ -53,13 +53,13 @@ __device__ __forceinline__ int draw_lane(float c, float total, float u, bool rea
 __global__ void __launch_bounds__(kFilterThreads) sample_filter_kernel(const __grid_constant__ FilterArgs a) {
   __shared__ unsigned long long s_keys[kSampleMaxSlices * kW], s_kept[kSampleMaxSlices * kW];
   __shared__ unsigned long long s_top[kW];
-  __shared__ unsigned long long s_thr;
+  __shared__ unsigned long long s_thr, s_lo;
   __shared__ int s_m;
   grid_dep_wait();
   grid_dep_launch();
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   topk::merge_lists<kW>(a.part + static_cast<size_t>(r) * a.slices * kW, a.slices, tid, kFilterThreads, s_keys,
-                        s_kept, &s_thr, &s_m, s_top, [] { __syncthreads(); });
+                        s_kept, &s_thr, &s_lo, &s_m, s_top, [] { __syncthreads(); });
   if (tid >= 32) return;
   const unsigned long long k = s_top[lane];
   const bool valid = k != 0 && lane < a.top_k;

@@ -6,8 +6,8 @@
 // order-preserving image of the float above the complemented column; 0 never
 // arises from a number and marks an empty entry. NaN is never a candidate.
 //
-// Pass 1, topk_slices_kernel: one CTA of 256 threads per (column slice, row),
-// each thread holding 32 fp32 or 64 bf16 values of the slice in registers.
+// Pass 1, topk_slices_kernel: one CTA of 256 threads per 8192-column slice of
+// a row, each thread holding 32 fp32 or bf16 values of the slice in registers.
 // Threshold: in every warp, R = K / 8 lanes reach the warp's R-th largest lane
 // maximum, so K values of the CTA reach the smallest of the 8 warps' R-th
 // largest lane maxima and every value below it is out. The values at or above
@@ -17,9 +17,10 @@
 // the current bound since the buffer holds more than K distinct keys at or
 // above it, becomes the bound and the slice is scanned again, until the keys
 // at or above the bound fit.
-// Pass 2 (merge_lists, called by the consuming kernel): a slice list's K-th
-// key bounds the row's K-th largest from below; the keys at or above the
-// largest such bound are ranked by counting.
+// Pass 2 (merge_lists, called by the consuming kernel): the keys at or above
+// a lower bound of the row's K-th largest key are ranked by counting; the
+// bound is the larger of the slices' largest K-th key and the smallest c-th
+// key, c = ceil(K / slices).
 #pragma once
 #include <cuda_runtime.h>
 
@@ -32,7 +33,6 @@ namespace dfl {
 namespace topk {
 
 constexpr int kThreads = 256;
-constexpr int kQuads = 8;                               // 16-byte loads per thread
 constexpr int kCandCap = 4096;                          // shared key buffer
 
 template <typename InT>
@@ -40,14 +40,16 @@ struct In;
 template <>
 struct In<float> {
   static constexpr int kPerLoad = 4;
+  static constexpr int kQuads = 8;                                 // 16-byte loads per thread: 32 values
   static constexpr int kMinBlocks = 4;                             // CTAs per SM (64 registers)
   static constexpr int kSliceCols = kThreads * kQuads * kPerLoad;   // 8192
 };
 template <>
 struct In<uint16_t> {
   static constexpr int kPerLoad = 8;
-  static constexpr int kMinBlocks = 3;                             // 64 values per thread need more registers
-  static constexpr int kSliceCols = kThreads * kQuads * kPerLoad;   // 16384
+  static constexpr int kQuads = 4;                                 // 32 values per thread
+  static constexpr int kMinBlocks = 4;
+  static constexpr int kSliceCols = kThreads * kQuads * kPerLoad;   // 8192
 };
 
 __device__ __forceinline__ uint32_t ordered_bits(float v) {
@@ -79,6 +81,7 @@ __device__ __forceinline__ void top_by_rank(const unsigned long long* keys, int 
   for (int j = tid; j < m; j += nthr) {
     const unsigned long long k = keys[j];
     int rank = 0;
+#pragma unroll 8
     for (int q = 0; q < m; ++q) rank += keys[q] > k;
     if (rank < K) out[rank] = k;
   }
@@ -97,13 +100,28 @@ __device__ __forceinline__ size_t logit_row(int r, int B) {
 }
 
 template <typename InT>
-__device__ __forceinline__ float elem(const uint4 (&v)[kQuads], int q) {
+__device__ __forceinline__ float elem(const uint4 (&v)[In<InT>::kQuads], int q) {
   if constexpr (In<InT>::kPerLoad == 4) {
     const uint32_t w = (&v[q >> 2].x)[q & 3];
     return __uint_as_float(w);
   } else {
     const uint32_t w = (&v[q >> 3].x)[(q & 7) >> 1];
     return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+}
+
+// Largest value of one 16-byte load (NaN skipped): fp32 maxima, or packed
+// bf16x2 maxima for bf16 (exact, -0 and +0 equal).
+template <typename InT>
+__device__ __forceinline__ float load_max(const uint4& w) {
+  if constexpr (In<InT>::kPerLoad == 4) {
+    return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+  } else {
+    const __nv_bfloat162 m = __hmax2(__hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.x),
+                                             *reinterpret_cast<const __nv_bfloat162*>(&w.y)),
+                                     __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&w.z),
+                                             *reinterpret_cast<const __nv_bfloat162*>(&w.w)));
+    return fmaxf(__bfloat162float(m.x), __bfloat162float(m.y));
   }
 }
 
@@ -114,7 +132,8 @@ __device__ __forceinline__ float elem(const uint4 (&v)[kQuads], int q) {
 template <typename InT, int K, bool kDraftRows>
 __global__ void __launch_bounds__(kThreads, In<InT>::kMinBlocks) topk_slices_kernel(const InT* __restrict__ logits, int ld, int V,
                                                                   int B, unsigned long long* __restrict__ part) {
-  constexpr int kPer = In<InT>::kPerLoad, kSlice = In<InT>::kSliceCols, kVals = kQuads * kPer;
+  constexpr int kQuads = In<InT>::kQuads, kPer = In<InT>::kPerLoad, kSlice = In<InT>::kSliceCols;
+  constexpr int kVals = kQuads * kPer;
   constexpr int R = K / 8;
   static_assert(K % 8 == 0 && R >= 1 && R <= 4, "K of 8, 16, 24 or 32");
   __shared__ unsigned long long s_cand[kCandCap];
@@ -133,13 +152,27 @@ __global__ void __launch_bounds__(kThreads, In<InT>::kMinBlocks) topk_slices_ker
 #pragma unroll
   for (int u = 0; u < kQuads; ++u) {
     const int c = c0 + kPer * (tid + kThreads * u);
-    v[u] = c < c1 ? __ldcs(reinterpret_cast<const uint4*>(row + c)) : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+    v[u] = c < c1 ? __ldcs(reinterpret_cast<const uint4*>(row + c)) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
   }
-  // lane maximum over valid columns (fmaxf skips NaN)
+  // maximum of every 16-byte load (NaN skipped) and of the lane; a full
+  // slice needs no column checks, a ragged one masks columns past c1
+  const bool full = c1 - c0 == kSlice;
+  float lm[kQuads];
+#pragma unroll
+  for (int u = 0; u < kQuads; ++u) lm[u] = load_max<InT>(v[u]);
+  if (!full) {
+#pragma unroll
+    for (int u = 0; u < kQuads; ++u) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e)
+        if (col_of(u * kPer + e) < c1) m = fmaxf(m, elem<InT>(v, u * kPer + e));
+      lm[u] = m;
+    }
+  }
   float bv = -INFINITY;
 #pragma unroll
-  for (int q = 0; q < kVals; ++q)
-    if (col_of(q) < c1) bv = fmaxf(bv, elem<InT>(v, q));
+  for (int u = 0; u < kQuads; ++u) bv = fmaxf(bv, lm[u]);
   uint32_t ob = ordered_bits(bv == 0.f ? 0.f : bv);
   // the warp's R-th largest lane maximum: remove the largest R - 1 times
   uint32_t rth = 0;
@@ -166,8 +199,14 @@ __global__ void __launch_bounds__(kThreads, In<InT>::kMinBlocks) topk_slices_ker
       }
     }
   };
+  const float tf0 = key_value(thr);
 #pragma unroll
-  for (int q = 0; q < kVals; ++q) offer(elem<InT>(v, q), col_of(q));
+  for (int u = 0; u < kQuads; ++u) {
+    if (lm[u] >= tf0) {   // rare: this load holds a value at or above the bound
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) offer(elem<InT>(v, u * kPer + e), col_of(u * kPer + e));
+    }
+  }
   __syncthreads();
   while (s_m > kCandCap) {
     // ties overflowed the buffer: its K-th largest key is the next bound, and
@@ -203,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, In<InT>::kMinBlocks) topk_slices_ker
 template <int K, typename Bar>
 __device__ __forceinline__ void merge_lists(const unsigned long long* __restrict__ src, int slices, int tid, int nthr,
                                             unsigned long long* keys, unsigned long long* kept,
-                                            unsigned long long* s_thr, int* s_m, unsigned long long* out,
-                                            Bar bar) {
+                                            unsigned long long* s_thr, unsigned long long* s_lo, int* s_m,
+                                            unsigned long long* out, Bar bar) {
   const int n = slices * K;
   constexpr int kMaxPer = 8;   // slices * K <= 8 * nthr
   unsigned long long kv[kMaxPer];
@@ -215,12 +254,20 @@ __device__ __forceinline__ void merge_lists(const unsigned long long* __restrict
     if (tid + nthr * u < n) keys[tid + nthr * u] = kv[u];
   if (tid == 0) {
     *s_thr = 0;
+    s_lo[0] = ~0ull;
     *s_m = 0;
   }
   bar();
-  if (tid < slices) atomicMax(s_thr, keys[tid * K + K - 1]);
+  // two lower bounds of the row's K-th largest key: the largest of the
+  // slices' K-th keys, and, with c = ceil(K / slices) keys taken from every
+  // slice (at least K in all), the smallest of the slices' c-th keys
+  if (tid < slices) {
+    const int c = (K + slices - 1) / slices;
+    atomicMax(s_thr, keys[tid * K + K - 1]);
+    atomicMin(s_lo, keys[tid * K + c - 1]);
+  }
   bar();
-  const unsigned long long t = *s_thr;
+  const unsigned long long t = max(*s_thr, s_lo[0]);
   for (int q = tid; q < n; q += nthr) {
     const unsigned long long k = keys[q];
     if (k != 0 && k >= t) kept[atomicAdd(s_m, 1)] = k;

@@ -216,7 +216,7 @@ dflash_status dflash_draft_sample(dflash_ctx* ctx, const int32_t* seq_ids, int n
 
 /* Filtered distributions of bf16 logit rows (the target's block logits):
  *  logits     device [rows, cols] bf16, row pitch cols, 16-byte aligned;
- *             cols a multiple of 8, 32 <= cols <= 1048576; rows <= max_batch*max_block
+ *             cols a multiple of 8, 32 <= cols <= 524288; rows <= max_batch*max_block
  *  out_ids    device [rows, 32] int32, out_probs device [rows, 32] fp32
  *  uniforms, drawn  device [rows] fp32 / int32, or both NULL: one draw per row
  * Uses the context's list scratch only (no sequence state). Errors: EINVAL, ENOMEM. */

@@ -76,7 +76,7 @@ def _check_filter_rows(ids, probs, drawn, vals, us, temperature, top_k, top_p, w
 
 @pytest.mark.parametrize("temperature,top_k,top_p", [(1.0, 20, 0.95), (0.7, 32, 0.8), (1.3, 5, 1.0), (1.0, 1, 0.95)])
 def test_filter_target_logits_matches_oracle(dfl, temperature, top_k, top_p):
-    """1024 rows of bf16 N(0, 3) logits over vocabulary 151936 (ten column
+    """1024 rows of bf16 N(0, 3) logits over vocabulary 151936 (19 column
     slices, the last ragged)."""
     d, _ = _drafter(dfl)
     with d:
