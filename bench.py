@@ -664,6 +664,50 @@ def run_verify(args):
                          "frac": bytes_am / (am_us * 1e3) / peaks["hbm_gbs"], "peak_source": f"{kind} hbm_gbs"}}
 
 
+def run_filter(args):
+    """Target-side temperature filter: dflash_sample_filter over 512 rows (32
+    sequences x B = 16) of bf16 N(0, 3) logits, vocabulary 151936, top-k 20,
+    top-p 0.95, temperature 1 (the DFlash 2 notes' sampling setting), with a
+    draw per row. 8 logit buffers (1.2 GB) rotate so every call reads from HBM."""
+    import torch
+    import block_diffusion_drafter_pass_gb300 as dfl
+    from synth import TINY, make_weights_torch
+    from block_diffusion_drafter_pass_gb300 import _build
+    _build.build()
+    dfl.load_library()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    rows, V, ring = 512, 151936, 8
+    K, W = args.steps, args.warmup
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    logits = torch.empty(ring, rows, V, device=dev, dtype=torch.bfloat16)
+    for r in range(ring):
+        logits[r] = torch.empty(rows, V, device=dev).normal_(0.0, 3.0, generator=g).to(torch.bfloat16)
+    us = torch.rand(ring, rows, generator=g, device=dev)
+    d = dfl.Drafter(TINY, make_weights_torch(TINY, seed=1, device=dev), max_seqs=32, max_batch=32, max_block=16,
+                    max_ctx=256, max_fuse_tokens=1024)
+    ids = torch.empty(rows, dfl.SAMPLE_WIDTH, dtype=torch.int32, device=dev)
+    probs = torch.empty(rows, dfl.SAMPLE_WIDTH, dtype=torch.float32, device=dev)
+    drawn = torch.empty(rows, dtype=torch.int32, device=dev)
+    step = lambda k: d.sample_filter(logits[k % ring], 1.0, 20, 0.95, uniforms=us[k % ring], ids=ids, probs=probs,
+                                     drawn=drawn)
+    for k in range(W):
+        step(k)
+    with ClockSampler(0) as clk:
+        ms = timed(step, K, 1, dev)
+    peaks, kind = measured_peaks()
+    gbs = rows * V * 2 / (ms / K / 1e3) / 1e9
+    return {"metric": "target temperature filter latency (512 rows x 151936 bf16, top-k 20, top-p 0.95)",
+            "value": 1e3 * ms / K, "unit": "us", "higher_is_better": False, "n_gpus": 1, "steps": K, "warmup": W,
+            "dtype": "bf16 -> fp32", "data": "synthetic (N(0,3) bf16 logits, uniform draws)",
+            "config": {"workload": "filter_512", "rows": rows, "vocab": V, "l2": "8 rotating 155 MB buffers"},
+            "clocks": clk.summary(),
+            "roofline": {"bound": "hbm", "kernel": "topk_slices_kernel + sample_filter_kernel", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "peak_source": f"{kind} hbm_gbs"}}
+
+
 def run_fill(args):
     """Context fill: dflash_fuse_ctx of 4096 committed target-feature rows per
     call (fusion projection + every layer's K/V + RoPE + paged append)."""
@@ -818,7 +862,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["verify_b64", "fill_4096"],
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["verify_b64", "fill_4096", "filter_512"],
                     default="qwen3_8b_b1_ctx4096")
     ap.add_argument("--block", type=int, default=16)
     ap.add_argument("--layers", type=int, default=5,
@@ -839,6 +883,8 @@ def main(argv=None):
         out = run_verify(args)
     elif args.workload == "fill_4096":
         out = run_fill(args)
+    elif args.workload == "filter_512":
+        out = run_filter(args)
     else:
         out = run_ours(args)
     if out is not None:

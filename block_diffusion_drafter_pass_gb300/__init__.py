@@ -28,6 +28,8 @@ EXPORTED = (
     "dflash_debug_read_kv", "dflash_debug_last_draft", "dflash_debug_gemm", "dflash_debug_profile",
     "dflash_debug_profile_read", "dflash_gemm_noalloc", "dflash_set_path_selector", "dflash_debug_last_selection",
     "dflash_draft_sample", "dflash_sample_filter", "dflash_verify_sample",
+    "dflash_block_sched_create", "dflash_block_sched_destroy", "dflash_block_sched_observe",
+    "dflash_block_sched_set_cost", "dflash_block_sched_expected_tau", "dflash_block_sched_choose",
 )
 SAMPLE_WIDTH = 32   # DFLASH_SAMPLE_WIDTH
 
@@ -100,6 +102,12 @@ def load_library() -> ctypes.CDLL:
         "dflash_draft_sample": ([VP, i32p, I, VP, I, ctypes.c_float, I, ctypes.c_float, VP, VP, VP, VP, VP], I),
         "dflash_sample_filter": ([VP, VP, I, I, ctypes.c_float, I, ctypes.c_float, VP, VP, VP, VP, VP], I),
         "dflash_verify_sample": ([VP, i32p, I, I, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I),
+        "dflash_block_sched_create": ([i32p, I, ctypes.c_float, ctypes.c_float, ctypes.c_float, P(VP)], I),
+        "dflash_block_sched_destroy": ([VP], I),
+        "dflash_block_sched_observe": ([VP, I, i32p, I], I),
+        "dflash_block_sched_set_cost": ([VP, I, ctypes.c_float], I),
+        "dflash_block_sched_expected_tau": ([VP, I, P(ctypes.c_double)], I),
+        "dflash_block_sched_choose": ([VP, P(I)], I),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -165,6 +173,46 @@ def dflash_gemm_noalloc(W, X, Y=None, splits: int = 0, stream=None):
         Y = torch.empty(M, N, dtype=torch.float32, device=W.device)
     _check(load_library().dflash_gemm_noalloc(_ptr(W), _ptr(X), _ptr(Y), N, M, K, splits, _stream(stream)))
     return Y
+
+
+class BlockScheduler:
+    """Dynamic block-size scheduling (host logic in the library, no GPU needed):
+    observe acceptance lengths, set per-size cycle costs, choose the next B."""
+
+    def __init__(self, sizes, decay: float = 0.99, prior_accept: float = 1.0, prior_reject: float = 1.0):
+        lib = load_library()
+        h = ctypes.c_void_p()
+        _check(lib.dflash_block_sched_create(_i32(sizes), len(sizes), float(decay), float(prior_accept),
+                                             float(prior_reject), ctypes.byref(h)))
+        self.h = h
+
+    def observe(self, B: int, taus) -> None:
+        taus = [int(t) for t in taus]
+        _check(load_library().dflash_block_sched_observe(self.h, int(B), _i32(taus), len(taus)))
+
+    def set_cost(self, B: int, cycle_ms: float) -> None:
+        _check(load_library().dflash_block_sched_set_cost(self.h, int(B), float(cycle_ms)))
+
+    def expected_tau(self, B: int) -> float:
+        v = ctypes.c_double()
+        _check(load_library().dflash_block_sched_expected_tau(self.h, int(B), ctypes.byref(v)))
+        return v.value
+
+    def choose(self) -> int:
+        b = ctypes.c_int()
+        _check(load_library().dflash_block_sched_choose(self.h, ctypes.byref(b)))
+        return b.value
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            load_library().dflash_block_sched_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Drafter:

@@ -242,6 +242,37 @@ dflash_status dflash_verify_sample(dflash_ctx* ctx, const int32_t* seq_ids, int 
                                    const int32_t* p_ids, const float* p_probs, const float* u_accept,
                                    const float* u_resample, int32_t* tau, int32_t* bonus, void* stream);
 
+/* ---- dynamic block-size scheduling (host logic) ----
+ * The DFlash notes (6.5, block size) find that a drafter trained at block 16
+ * also serves block 8, which allows choosing B per cycle. The scheduler keeps,
+ * per draft position j, exponentially decayed counts of cycles that reached
+ * j and that accepted it, read from acceptance lengths tau (tau - 1 leading
+ * drafts accepted). With a_j = (accepted_j + prior_accept) /
+ * (reached_j + prior_accept + prior_reject),
+ *     E[tau | B] = 1 + sum_{j=1}^{B-1} prod_{i<=j} a_i,
+ * and dflash_block_sched_choose returns, among the sizes whose cycle cost is
+ * set, the one with the largest E[tau | B] / cost(B) (the smaller on ties; the
+ * smallest size when no cost is set). Host memory only; no CUDA call. */
+typedef struct dflash_block_sched dflash_block_sched;
+
+/* sizes: host [n_sizes] distinct block sizes in [1, 32]; decay in (0, 1]
+ * (1 = plain counts); priors > 0. Errors: EINVAL, ENOMEM. */
+dflash_status dflash_block_sched_create(const int32_t* sizes, int n_sizes, float decay, float prior_accept,
+                                        float prior_reject, dflash_block_sched** out);
+dflash_status dflash_block_sched_destroy(dflash_block_sched* s);
+
+/* Record n cycles run with block B: taus host [n], each in [1, B]. Errors: EINVAL. */
+dflash_status dflash_block_sched_observe(dflash_block_sched* s, int B, const int32_t* taus, int n);
+
+/* Cycle cost of size B (one of the sizes), any positive unit (ms). Errors: EINVAL. */
+dflash_status dflash_block_sched_set_cost(dflash_block_sched* s, int B, float cycle_ms);
+
+/* E[tau | B] under the current counts, B in [1, largest size]. Errors: EINVAL. */
+dflash_status dflash_block_sched_expected_tau(const dflash_block_sched* s, int B, double* out);
+
+/* The size to run next. Errors: EINVAL. */
+dflash_status dflash_block_sched_choose(const dflash_block_sched* s, int* B_out);
+
 /* Install (or remove) the DFlash 2 path selector ("DFlash 2" notes,
  * "Solution - Lightweight Path Selector"). While installed, dflash_draft
  * keeps the 16 largest logits of every masked position t as its candidates
