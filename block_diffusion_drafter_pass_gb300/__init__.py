@@ -30,6 +30,7 @@ EXPORTED = (
     "dflash_draft_sample", "dflash_sample_filter", "dflash_verify_sample",
     "dflash_block_sched_create", "dflash_block_sched_destroy", "dflash_block_sched_observe",
     "dflash_block_sched_set_cost", "dflash_block_sched_expected_tau", "dflash_block_sched_choose",
+    "dflash_debug_wait_timeout",
 )
 SAMPLE_WIDTH = 32   # DFLASH_SAMPLE_WIDTH
 
@@ -108,6 +109,7 @@ def load_library() -> ctypes.CDLL:
         "dflash_block_sched_set_cost": ([VP, I, ctypes.c_float], I),
         "dflash_block_sched_expected_tau": ([VP, I, P(ctypes.c_double)], I),
         "dflash_block_sched_choose": ([VP, P(I)], I),
+        "dflash_debug_wait_timeout": ([VP, I, VP], I),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -382,6 +384,10 @@ class Drafter:
 
     def sync(self) -> None:
         _check(load_library().dflash_sync(self.ctx), self.ctx)
+
+    def debug_wait_timeout(self, limit_us: int, stream=None) -> None:
+        """Launch one bounded wait that runs out after limit_us (failure-path check)."""
+        _check(load_library().dflash_debug_wait_timeout(self.ctx, int(limit_us), _stream(stream)), self.ctx)
 
     def read_kv(self, layer: int, seq: int, pos0: int, n: int):
         """Cached K, V of `n` positions as float32 arrays [n, n_kv, d]."""

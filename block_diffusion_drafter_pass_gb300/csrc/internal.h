@@ -250,6 +250,8 @@ struct PageUpdates {
   int page[kPageUpdMax];
 };
 cudaError_t launch_page_updates(const PageUpdates& u, int* table, cudaStream_t s);
+// One bounded mbarrier wait that nothing satisfies (failure-path check).
+cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, int32_t* out, cudaStream_t s);
 
 // ----------------------------------------------------------------------------

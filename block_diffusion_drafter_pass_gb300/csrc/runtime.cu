@@ -25,6 +25,7 @@
 
 #include "dflash.h"
 #include "internal.h"
+#include <nvtx3/nvToolsExt.h>
 
 using namespace dfl;
 
@@ -163,6 +164,13 @@ struct dflash_ctx {
 };
 
 namespace {
+
+// One NVTX range per API call (header-only NVTX 3: a no-op unless a profiler
+// is attached).
+struct ApiRange {
+  explicit ApiRange(const char* name) { nvtxRangePushA(name); }
+  ~ApiRange() { nvtxRangePop(); }
+};
 
 dflash_status fail(dflash_ctx* c, dflash_status s, const std::string& msg) {
   if (c) c->err = msg;
@@ -567,6 +575,7 @@ dflash_status dflash_seq_len(dflash_ctx* ctx, int seq, int* committed, int* pend
 
 dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* n_new,
                               const uint16_t* feats, int pending, void* stream_v) {
+  ApiRange nvtx_range("dflash_fuse_ctx");
   if (!ctx) return DFLASH_EINVAL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const dflash_config& c = ctx->cfg;
@@ -758,12 +767,14 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
 
 dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids, int B,
                            int32_t* draft_ids, void* stream_v) {
+  ApiRange nvtx_range("dflash_draft");
   return draft_impl(ctx, seq_ids, n_seq, anchor_ids, B, draft_ids, stream_v, nullptr);
 }
 
 dflash_status dflash_draft_sample(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids,
                                   int B, float temperature, int top_k, float top_p, const float* uniforms,
                                   int32_t* draft_ids, int32_t* q_ids, float* q_probs, void* stream_v) {
+  ApiRange nvtx_range("dflash_draft_sample");
   if (!ctx) return DFLASH_EINVAL;
   dflash_status st = check_sampling(ctx, temperature, top_k, top_p);
   if (st != DFLASH_OK) return st;
@@ -1142,6 +1153,7 @@ dflash_status commit_host_side(dflash_ctx* ctx, const SeqMeta& meta, int n_seq, 
 
 dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, int B, const int32_t* draft_ids,
                             const int32_t* target_ids, int32_t* tau, int32_t* bonus, void* stream_v) {
+  ApiRange nvtx_range("dflash_verify");
   if (!ctx) return DFLASH_EINVAL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   SeqMeta meta;
@@ -1159,6 +1171,7 @@ dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, 
 }
 
 dflash_status dflash_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, int32_t* out, void* stream) {
+  ApiRange nvtx_range("dflash_rows_argmax_bf16");
   if (rows < 0 || cols < 1) return DFLASH_EINVAL;
   if (rows > 0 && (!logits || !out)) return DFLASH_EINVAL;
   return launch_rows_argmax_bf16(logits, rows, cols, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -1207,6 +1220,7 @@ dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0
 dflash_status dflash_sample_filter(dflash_ctx* ctx, const uint16_t* logits, int rows, int cols, float temperature,
                                    int top_k, float top_p, const float* uniforms, int32_t* out_ids, float* out_probs,
                                    int32_t* drawn, void* stream_v) {
+  ApiRange nvtx_range("dflash_sample_filter");
   if (!ctx) return DFLASH_EINVAL;
   dflash_status st = check_sampling(ctx, temperature, top_k, top_p);
   if (st != DFLASH_OK) return st;
@@ -1239,6 +1253,7 @@ dflash_status dflash_verify_sample(dflash_ctx* ctx, const int32_t* seq_ids, int 
                                    const int32_t* q_ids, const float* q_probs, const int32_t* p_ids,
                                    const float* p_probs, const float* u_accept, const float* u_resample,
                                    int32_t* tau, int32_t* bonus, void* stream_v) {
+  ApiRange nvtx_range("dflash_verify_sample");
   if (!ctx) return DFLASH_EINVAL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   SeqMeta meta;
@@ -1271,6 +1286,7 @@ dflash_status dflash_verify_sample(dflash_ctx* ctx, const int32_t* seq_ids, int 
 
 dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, const uint16_t* w_b,
                                        const uint16_t* w_h, int dim, void* stream_v) {
+  ApiRange nvtx_range("dflash_set_path_selector");
   if (!ctx) return DFLASH_EINVAL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const dflash_config& c = ctx->cfg;
@@ -1337,6 +1353,13 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
   }
   CK(cudaStreamSynchronize(stream));
   ctx->sel_on = true;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_debug_wait_timeout(dflash_ctx* ctx, int limit_us, void* stream) {
+  if (!ctx || limit_us < 1 || limit_us > 2000000) return ctx ? fail(ctx, DFLASH_EINVAL, "limit_us out of range") : DFLASH_EINVAL;
+  CK(launch_wait_probe(1000ull * static_cast<unsigned long long>(limit_us), ctx->d_status,
+                       static_cast<cudaStream_t>(stream)));
   return DFLASH_OK;
 }
 

@@ -109,6 +109,17 @@ __global__ void verify_kernel(const __grid_constant__ SeqMeta meta, SeqState st,
   }
 }
 
+// A wait that nothing satisfies: one thread waits on an mbarrier no thread
+// arrives on, gives up after limit_ns and latches the timeout bit, the path
+// every bounded wait of the library takes when it runs out.
+__global__ void wait_probe_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait_for(&bar, 0, limit_ns)) latch_status(status, kDevTimeout);
+}
+
 __global__ void fuse_advance_kernel(const __grid_constant__ SeqMeta meta, SeqState st, int pending) {
   grid_dep_wait();
   grid_dep_launch();
@@ -321,6 +332,11 @@ cudaError_t launch_verify(const SeqMeta& meta, SeqState st, const int32_t* draft
 cudaError_t launch_fuse_advance(const SeqMeta& meta, SeqState st, int pending, cudaStream_t s) {
   if (meta.n_seq == 0) return cudaSuccess;
   return launch_pdl(fuse_advance_kernel, dim3(1), dim3(kMaxBatch), 0, s, meta, st, pending);
+}
+
+cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_page_updates(const PageUpdates& u, int* table, cudaStream_t s) {

@@ -312,6 +312,12 @@ dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0
  * draft row [n_seq*(B-1)] fp32. Host outputs; either may be NULL. */
 dflash_status dflash_debug_last_draft(dflash_ctx* ctx, float* hidden_out, float* top_logit_out);
 
+/* Failure-path check: launches one kernel whose bounded mbarrier wait nothing
+ * satisfies; it gives up after limit_us microseconds (1 .. 2e6) and latches the
+ * timeout bit, so the next dflash_sync returns DFLASH_ETIMEOUT (and clears it).
+ * No fault, no trap; the context stays usable. Errors: EINVAL, ECUDA. */
+dflash_status dflash_debug_wait_timeout(dflash_ctx* ctx, int limit_us, void* stream);
+
 /* Selector state of the last dflash_draft call made with the selector
  * installed, per draft row r = i*(B-1) + t (host outputs, any may be NULL):
  *  cand_out    [rows, 16] int32  candidate ids C_t, largest logit first
