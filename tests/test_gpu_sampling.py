@@ -94,14 +94,20 @@ def test_filter_target_logits_matches_oracle(dfl, temperature, top_k, top_p):
 
 def test_filter_ties_small_and_ragged_rows(dfl):
     """All-equal rows (ties overflow the threshold buffer: the exact-key
-    rounds), a 40-column row, a row with a few large values, and rows whose
-    width is not a multiple of the slice."""
+    rounds), rows of three distinct values, ascending rows, a 40-column row,
+    a row with a few large values, and rows whose width is not a multiple of
+    the slice."""
     d, _ = _drafter(dfl)
     with d:
-        for V, fill in ((20000, "zeros"), (40, "normal"), (16392, "spiky"), (32776, "normal")):
+        for V, fill in ((20000, "zeros"), (40, "normal"), (16392, "spiky"), (32776, "normal"), (24576, "ascending"),
+                        (16384, "few_levels")):
             rng = np.random.Generator(np.random.PCG64(V))
             if fill == "zeros":
                 vals = np.zeros((6, V), dtype=np.float32)
+            elif fill == "ascending":   # the largest values in the last columns of the last slice
+                vals = np.tile(np.linspace(-4, 4, V, dtype=np.float32), (6, 1))
+            elif fill == "few_levels":  # three distinct values: long runs of ties at the bound
+                vals = rng.integers(0, 3, size=(6, V)).astype(np.float32)
             elif fill == "spiky":
                 vals = np.full((6, V), -5.0, dtype=np.float32)
                 for r in range(6):
