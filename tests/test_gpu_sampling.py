@@ -274,6 +274,34 @@ def test_verify_sample_greedy_limit(dfl):
             assert (int(tau[i]), int(tok[i])) == oracle.verify_block(drafts[i], t[i])
 
 
+def test_sampling_block_of_one(dfl):
+    """B = 1: no drafts; the verify draws the bonus from p_0 and commits one
+    pending token; the sampling draft runs the layers and returns no ids."""
+    n = 4
+    rng = np.random.Generator(np.random.PCG64(5))
+    d, _ = _drafter(dfl, max_batch=n, max_block=8)
+    with d:
+        seqs = list(range(n))
+        width = TINY.n_feat_layers * TINY.hidden
+        d.fuse_ctx(seqs, [1] * n, bf16_dev(make_features_np(n, width, seed=6), DEV), pending=True)
+        p = [_random_list(rng, 50, int(rng.integers(1, 33))) for _ in seqs]
+        p_ids = np.array([x[0] for x in p], dtype=np.int32).reshape(n, 1, 32)
+        p_pr = np.array([x[1] for x in p], dtype=np.float32).reshape(n, 1, 32)
+        ur = rng.random((n, 1)).astype(np.float32)
+        tau, tok = d.verify_sample(seqs, 1, None, None, None, i32_dev(p_ids, DEV), _f32_dev(p_pr), None, _f32_dev(ur))
+        d.sync()
+        for i in seqs:
+            ids = p_ids[i, 0][p_ids[i, 0] >= 0]
+            pr = p_pr[i, 0][p_ids[i, 0] >= 0].astype(np.float64)
+            c = np.cumsum(pr)
+            if np.all(np.abs(c[:-1] - ur[i, 0] * c[-1]) > EPS):
+                assert (int(tau[i]), int(tok[i])) == (1, osm.draw(ids, pr, ur[i, 0]))
+            assert d.seq_len(i) == (1, 0)
+        out, q_ids, q_probs = d.draft_sample(seqs, i32_dev(np.arange(n), DEV), 1, 1.0, 20, 0.95, None)
+        d.sync()
+        assert out.numel() == 0
+
+
 def test_sampling_argument_errors(dfl):
     d, _ = _drafter(dfl, max_batch=2, max_block=8)
     with d:
