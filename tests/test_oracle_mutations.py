@@ -229,3 +229,44 @@ def test_sampling_top_p_off_by_one_is_caught(monkeypatch):
         return ids[:n], p[:n] / p[:n].sum()
     monkeypatch.setattr(osm, "filtered_probs", bad)
     _expect_failure(spins.test_top_p_worked_case)
+
+
+# ----------------------------------------------------------------------------
+# Path selector oracle (oracle/path_selector.py)
+# ----------------------------------------------------------------------------
+
+def _walk_variant(kind):
+    from oracle import path_selector as ps
+
+    def bad(anchor, cands, u, E, w_a, w_b, h_gates):
+        prev = int(anchor)
+        ids, gaps, picks = [], [], []
+        for t in range(cands.shape[0]):
+            if kind == "swap_maps":
+                s = ps.pair_scores(u[t], cands[t], [prev], E, w_b, w_a, h_gates[t])[0]
+            elif kind == "gate_shift":
+                s = ps.pair_scores(u[t], cands[t], [prev], E, w_a, w_b, h_gates[max(t - 1, 0)])[0]
+            else:
+                s = ps.pair_scores(u[t], cands[t], [prev], E, w_a, w_b, h_gates[t])[0]
+            j = int(np.argmax(s))
+            ids.append(int(cands[t, j]))
+            gaps.append(0.0)
+            picks.append(j)
+            if kind != "anchor_only":
+                prev = int(cands[t, j])
+        return np.array(ids), np.array(gaps), np.array(picks)
+    return bad
+
+
+@pytest.mark.parametrize("kind", ["anchor_only", "swap_maps", "gate_shift"])
+def test_path_selector_walk_mistakes_are_caught(monkeypatch, kind):
+    """The walk keeping the anchor as predecessor, A and B exchanged, or the
+    gate taken from the previous position: a worked pin fails."""
+    from oracle import path_selector as ps
+    from tests import test_path_selector_pins as sp
+    monkeypatch.setattr(ps, "greedy_walk", _walk_variant(kind))
+
+    def both():
+        sp.test_one_hot_walk_worked_by_hand()
+        sp.test_asymmetric_maps_and_position_gates_worked_by_hand()
+    _expect_failure(both)

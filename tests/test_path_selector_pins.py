@@ -94,3 +94,42 @@ def test_one_hot_walk_worked_by_hand():
     assert s[0, 1] == pytest.approx(1.1)
     assert s[0, 0] == pytest.approx(1.0)
     assert s[1, 0] == pytest.approx(1.2)
+
+
+def test_asymmetric_maps_and_position_gates_worked_by_hand():
+    """W_A = I, W_B a permutation P (B(b) = e_{P(b)}), so the pair term is g_t
+    when a == P(b): the maps enter in their roles, not symmetrically. P is the
+    3-cycle 3 -> 5 -> 4 -> 3 (P(4) = 3, P(3) = 5, P(5) = 4) and swaps 8 <-> 9,
+    so a == P(b) and P(a) == b differ. Candidates [[7, 4], [8, 4], [8, 4]], logits
+    [[1, 0.9], [1, 0.95], [1, 0.99]], gates g = (0.2, 0.05, 0.05):
+      t0 after anchor 3: B(4) = e_3 matches A(3): 0.9 + 0.2 = 1.1 > 1 -> 4;
+      t1 after 4: P(8) = 9 != 4, P(4) = 3 != 4: 1 > 0.95           -> 8;
+      t2 after 8: P(8) = 9 != 8, P(4) = 3 != 8: 1 > 0.99           -> 8.
+    With the gates of t0 and t1 exchanged (0.05, 0.2, 0.05): t0 after 3:
+    0.95 < 1 -> 7; t1 after 7: no match -> 8; t2 after 8 -> 8. A third case
+    makes the gate of t1 decide."""
+    V = ps.D_SEL
+    E = np.eye(V)
+    I = np.eye(ps.D_SEL, V)
+    perm = np.arange(V)
+    perm[[3, 4, 5, 8, 9]] = [5, 3, 4, 9, 8]
+    wb = np.eye(ps.D_SEL, V)[perm].T.copy()   # B(b) = W_B e_b = e_{perm[b]}
+    assert np.array_equal(wb @ E[4], E[3][: ps.D_SEL]) and np.array_equal(wb @ E[8], E[9][: ps.D_SEL])
+    pad = [200 + j for j in range(14)]
+    cands = np.array([[7, 4] + pad, [8, 4] + pad, [8, 4] + pad])
+    u = np.array([[1.0, 0.9] + [-100.0] * 14, [1.0, 0.95] + [-100.0] * 14, [1.0, 0.99] + [-100.0] * 14])
+
+    def walk(gs):
+        gates = np.stack([np.full(ps.D_SEL, g) for g in gs])
+        return list(ps.greedy_walk(3, cands, u, E, I, wb, gates)[0])
+
+    assert walk((0.2, 0.05, 0.05)) == [4, 8, 8]
+    assert walk((0.05, 0.2, 0.05)) == [7, 8, 8]
+    # the gate of position t, not t-1: candidates [[7, 4], [8, 5], [8, 4]],
+    # logits [[1, 0.9], [1, 0.97], [1, 0.99]], gates (0.2, 0.01, 0.3):
+    # t0 after 3 -> 4 (1.1); t1 after 4: P(5) = 4 matches, 0.97 + 0.01 < 1
+    # -> 8 (with t0's gate it would be 1.17 -> 5); t2 after 8: no match -> 8
+    cands3 = np.array([[7, 4] + pad, [8, 5] + pad, [8, 4] + pad])
+    u3 = np.array([[1.0, 0.9] + [-100.0] * 14, [1.0, 0.97] + [-100.0] * 14, [1.0, 0.99] + [-100.0] * 14])
+    gates3 = np.stack([np.full(ps.D_SEL, g) for g in (0.2, 0.01, 0.3)])
+    assert list(ps.greedy_walk(3, cands3, u3, E, I, wb, gates3)[0]) == [4, 8, 8]
