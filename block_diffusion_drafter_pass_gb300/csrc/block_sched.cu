@@ -6,8 +6,12 @@
 // scheduler keeps, per draft position j, exponentially decayed counts of
 // cycles that reached j (every earlier draft accepted) and that accepted it,
 // read from each cycle's acceptance length tau (tau - 1 leading drafts
-// accepted, notes 2.2). With a_j = (accepted_j + prior_a) / (reached_j +
-// prior_a + prior_r), a block of B drafts is expected to yield
+// accepted, notes 2.2). Each position's rate is shrunk toward the pooled
+// rate of all positions, so positions a smaller block never reaches inherit
+// it: with w = prior_a + prior_r,
+//     pooled = (sum accepted + prior_a) / (sum reached + w),
+//     a_j = (accepted_j + w * pooled) / (reached_j + w),
+// and a block of B drafts is expected to yield
 //     E[tau | B] = 1 + sum_{j=1}^{B-1} prod_{i<=j} a_i
 // tokens, and among the sizes whose cycle cost T(B) is known the scheduler
 // picks the largest E[tau | B] / T(B) (the smaller size on ties).
@@ -30,9 +34,16 @@ struct dflash_block_sched {
 namespace {
 
 double expected_tau(const dflash_block_sched* s, int B) {
+  const double w = s->prior_a + s->prior_r;
+  double sa = 0.0, sr = 0.0;
+  for (size_t j = 0; j < s->reached.size(); ++j) {
+    sa += s->accepted[j];
+    sr += s->reached[j];
+  }
+  const double pooled = (sa + s->prior_a) / (sr + w);
   double e = 1.0, prod = 1.0;
   for (int j = 1; j < B; ++j) {
-    prod *= (s->accepted[j - 1] + s->prior_a) / (s->reached[j - 1] + s->prior_a + s->prior_r);
+    prod *= (s->accepted[j - 1] + w * pooled) / (s->reached[j - 1] + w);
     e += prod;
   }
   return e;

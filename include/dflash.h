@@ -247,8 +247,11 @@ dflash_status dflash_verify_sample(dflash_ctx* ctx, const int32_t* seq_ids, int 
  * also serves block 8, which allows choosing B per cycle. The scheduler keeps,
  * per draft position j, exponentially decayed counts of cycles that reached
  * j and that accepted it, read from acceptance lengths tau (tau - 1 leading
- * drafts accepted). With a_j = (accepted_j + prior_accept) /
- * (reached_j + prior_accept + prior_reject),
+ * drafts accepted). Each position's rate is shrunk toward the pooled rate of
+ * all positions (positions never reached inherit it): with
+ * w = prior_accept + prior_reject,
+ * pooled = (sum accepted + prior_accept) / (sum reached + w) and
+ * a_j = (accepted_j + w * pooled) / (reached_j + w),
  *     E[tau | B] = 1 + sum_{j=1}^{B-1} prod_{i<=j} a_i,
  * and dflash_block_sched_choose returns, among the sizes whose cycle cost is
  * set, the one with the largest E[tau | B] / cost(B) (the smaller on ties; the

@@ -14,9 +14,14 @@ reading taken, the plainest one the rest supports:
     later positions were not reached;
   - per draft position j the scheduler keeps exponentially decayed counts of
     "reached" and "accepted" (every observation first multiplies the old
-    counts by `decay`), and estimates a_j = (accepted_j + prior_a) /
-    (reached_j + prior_a + prior_r), the acceptance probability of position j
-    given that every earlier draft was accepted;
+    counts by `decay`), and estimates the acceptance probability of position
+    j given that every earlier draft was accepted by shrinking its own rate
+    toward the pooled rate of all positions,
+        pooled = (sum_j accepted_j + prior_a) / (sum_j reached_j + prior_a + prior_r),
+        a_j = (accepted_j + w * pooled) / (reached_j + w),  w = prior_a + prior_r,
+    so positions a smaller block never reaches inherit the pooled rate
+    instead of the bare prior (a scheduler running block 8 at high
+    acceptance can then see that block 16 pays);
   - the expected acceptance length of block B is
     E[tau | B] = 1 + sum_{j=1}^{B-1} prod_{i=1}^{j} a_i;
   - given the cycle cost T(B) of each allowed size (measured by the caller),
@@ -58,7 +63,9 @@ class BlockScheduler:
                     break
 
     def acceptance(self) -> np.ndarray:
-        return (self.accepted + self.prior_a) / (self.reached + self.prior_a + self.prior_r)
+        w = self.prior_a + self.prior_r
+        pooled = (self.accepted.sum() + self.prior_a) / (self.reached.sum() + w)
+        return (self.accepted + w * pooled) / (self.reached + w)
 
     def expected_tau(self, B: int) -> float:
         a = self.acceptance()

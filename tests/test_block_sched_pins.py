@@ -8,7 +8,8 @@ from oracle.block_sched import BlockScheduler as OracleSched
 
 
 def test_constant_acceptance_gives_the_geometric_sum():
-    """With every a_j equal to a, E[tau | B] = sum_{j<B} a^j = (1 - a^B) / (1 - a)."""
+    """With every a_j equal to a, E[tau | B] = sum_{j<B} a^j = (1 - a^B) / (1 - a)
+    (no data: every position takes the pooled prior rate 3/4)."""
     s = OracleSched([4, 8, 16, 32], decay=1.0, prior_a=3.0, prior_r=1.0)   # no data: a = 3/4 everywhere
     for B in (1, 4, 8, 16, 32):
         a = 0.75
@@ -21,8 +22,13 @@ def test_counts_after_worked_observations():
     # tau 3: positions 1, 2 accepted, 3 rejected; tau 1: position 1 rejected; tau 8: 1..7 accepted
     np.testing.assert_array_equal(s.reached[:7], [3, 2, 2, 1, 1, 1, 1])
     np.testing.assert_array_equal(s.accepted[:7], [2, 2, 1, 1, 1, 1, 1])
+    # pooled rate (9 + 1) / (11 + 2) = 10/13, w = 2: a_1 = (2 + 20/13) / 5,
+    # a_3 = (1 + 20/13) / 4, and the never-reached position 8 gets 10/13
     a = s.acceptance()
-    assert abs(a[0] - 3 / 5) < 1e-12 and abs(a[2] - 2 / 4) < 1e-12
+    assert abs(a[0] - 46 / 65) < 1e-12 and abs(a[2] - 33 / 52) < 1e-12
+    s16 = OracleSched([16], decay=1.0, prior_a=1.0, prior_r=1.0)
+    s16.observe(8, [3, 1, 8])
+    assert abs(s16.acceptance()[8] - 10 / 13) < 1e-12
     # decay multiplies the old counts before each observation
     t = OracleSched([4], decay=0.5, prior_a=1.0, prior_r=1.0)
     t.observe(4, [4, 1])
@@ -91,3 +97,26 @@ def test_library_scheduler_rejects_bad_arguments(dfl):
     with pytest.raises(dfl.DFlashError):
         s.set_cost(12, 1.0)    # not one of the sizes
     s.close()
+
+
+def test_scheduler_converges_to_the_best_block():
+    """I.i.d. acceptance p = 0.85 per draft and cycle costs 0.5 + 0.01 B ms:
+    E[tau | B] / T(B) = (1 - p^B) / (1 - p) / T(B) peaks at B = 16 among
+    4, 8, 16, 32. Starting from whatever the empty scheduler picks, choosing
+    and observing 400 cycles must settle on 16 (positions beyond the running
+    block inherit the pooled rate, so growing the block can pay off)."""
+    p, sizes = 0.85, [4, 8, 16, 32]
+    cost = {b: 0.5 + 0.01 * b for b in sizes}
+    rate = {b: (1 - p ** b) / (1 - p) / cost[b] for b in sizes}
+    assert max(rate, key=rate.get) == 16
+    rng = np.random.Generator(np.random.PCG64(9))
+    s = OracleSched(sizes, decay=0.99)
+    for b in sizes:
+        s.set_cost(b, cost[b])
+    picks = []
+    for _ in range(400):
+        b = s.choose()
+        picks.append(b)
+        tau = 1 + int(np.sum(np.cumprod(rng.random(b - 1) < p)))
+        s.observe(b, [tau])
+    assert all(b == 16 for b in picks[-100:])
