@@ -120,3 +120,24 @@ def test_scheduler_converges_to_the_best_block():
         tau = 1 + int(np.sum(np.cumprod(rng.random(b - 1) < p)))
         s.observe(b, [tau])
     assert all(b == 16 for b in picks[-100:])
+
+
+def test_library_scheduler_converges_too(dfl):
+    """The library's host scheduler in the same loop: low acceptance (0.3)
+    settles on the shortest block, high acceptance (0.85) on 16."""
+    sizes = [4, 8, 16, 32]
+    cost = {b: 0.5 + 0.01 * b for b in sizes}
+    for p, want in ((0.3, 4), (0.85, 16)):
+        rate = {b: (1 - p ** b) / (1 - p) / cost[b] for b in sizes}
+        assert max(rate, key=rate.get) == want
+        rng = np.random.Generator(np.random.PCG64(int(p * 100)))
+        s = dfl.BlockScheduler(sizes, decay=0.99)
+        for b in sizes:
+            s.set_cost(b, cost[b])
+        picks = []
+        for _ in range(400):
+            b = s.choose()
+            picks.append(b)
+            s.observe(b, [1 + int(np.sum(np.cumprod(rng.random(b - 1) < p)))])
+        s.close()
+        assert all(b == want for b in picks[-100:]), (p, picks[-20:])

@@ -270,3 +270,26 @@ def test_path_selector_walk_mistakes_are_caught(monkeypatch, kind):
         sp.test_one_hot_walk_worked_by_hand()
         sp.test_asymmetric_maps_and_position_gates_worked_by_hand()
     _expect_failure(both)
+
+
+def test_block_sched_counting_the_rejected_position_is_caught(monkeypatch):
+    """Counting the rejected position as accepted (tau drafts accepted
+    instead of tau - 1)."""
+    from oracle import block_sched as obs
+    from tests import test_block_sched_pins as bp
+
+    def bad_observe(self, B, taus):
+        for tau in taus:
+            self.reached *= self.decay
+            self.accepted *= self.decay
+            a = min(int(tau), B - 1)
+            for j in range(1, B):
+                if j <= a:
+                    self.reached[j - 1] += 1
+                    self.accepted[j - 1] += 1
+                elif j == a + 1:
+                    self.reached[j - 1] += 1
+                else:
+                    break
+    monkeypatch.setattr(obs.BlockScheduler, "observe", bad_observe)
+    _expect_failure(bp.test_counts_after_worked_observations)
