@@ -293,3 +293,61 @@ def test_block_sched_counting_the_rejected_position_is_caught(monkeypatch):
                     break
     monkeypatch.setattr(obs.BlockScheduler, "observe", bad_observe)
     _expect_failure(bp.test_counts_after_worked_observations)
+
+
+# ----------------------------------------------------------------------------
+# Two-tap convolution oracle (oracle/two_tap_conv.py)
+# ----------------------------------------------------------------------------
+
+def _conv_variant(kind):
+    def bad(x, c):
+        nb = np.zeros_like(x)
+        if kind == "successor":
+            nb[:-1] = x[1:]
+        else:
+            nb[1:] = x[:-1]
+        src = nb if kind == "coeff_from_prev" else x
+        out = np.zeros_like(x)
+        for i, xi in ((0, x), (1, nb)):
+            k = c["base"][i][None, :]
+            if kind != "no_correction":
+                k = k + (src @ c["V"][i].T) @ c["U"][i].T
+            out = out + k * xi
+        return out
+    return bad
+
+
+@pytest.mark.parametrize("kind", ["successor", "coeff_from_prev", "no_correction"])
+def test_two_tap_conv_mistakes_are_caught(monkeypatch, kind):
+    from oracle import two_tap_conv as tc
+    from tests import test_two_tap_conv_pins as cp
+    monkeypatch.setattr(tc, "conv2", _conv_variant(kind))
+
+    def pins():
+        cp.test_shift_kernel_moves_rows_down()
+        cp.test_tap0_only_kernel_is_pointwise()
+        cp.test_correction_scales_with_U_and_is_absent_without_it()
+    _expect_failure(pins)
+
+
+def test_two_tap_conv_output_after_the_residual_is_caught(monkeypatch):
+    """The output convolution applied to the residual stream after the add."""
+    import oracle.dflash_oracle as od
+    from oracle import two_tap_conv as tc
+    from tests import test_two_tap_conv_pins as cp
+
+    def bad_layer(x, layer, convs, k_ctx, v_ctx, pos0, shape):
+        B = x.shape[0]
+        nq, nkv, d = shape.n_heads, shape.n_kv_heads, shape.head_dim
+        pos = pos0 + np.arange(B)
+        h = tc.conv2(od.rms_norm(x, layer["g_attn"], shape.rms_eps), convs["ai"])
+        q = od.apply_rope((h @ layer["w_q"].T).reshape(B, nq, d), pos, shape.rope_base)
+        k = od.apply_rope((h @ layer["w_k"].T).reshape(B, nkv, d), pos, shape.rope_base)
+        v = (h @ layer["w_v"].T).reshape(B, nkv, d)
+        a = od.block_attention(q, np.concatenate([k_ctx, k]), np.concatenate([v_ctx, v])).reshape(B, nq * d)
+        x = tc.conv2(x + a @ layer["w_o"].T, convs["ao"])
+        h2 = tc.conv2(od.rms_norm(x, layer["g_ffn"], shape.rms_eps), convs["fi"])
+        f = (od.silu(h2 @ layer["w_gate"].T) * (h2 @ layer["w_up"].T)) @ layer["w_down"].T
+        return tc.conv2(x + f, convs["fo"])
+    monkeypatch.setattr(tc, "decoder_layer_conv", bad_layer)
+    _expect_failure(cp.test_zero_output_kernels_leave_the_embedding)
