@@ -351,3 +351,30 @@ def test_two_tap_conv_output_after_the_residual_is_caught(monkeypatch):
         return tc.conv2(x + f, convs["fo"])
     monkeypatch.setattr(tc, "decoder_layer_conv", bad_layer)
     _expect_failure(cp.test_zero_output_kernels_leave_the_embedding)
+
+
+# ----------------------------------------------------------------------------
+# 8-bit block KV format oracle (oracle/kv_quant.py)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["half_even", "exact_scale", "block16"])
+def test_kv_quant_mistakes_are_caught(monkeypatch, kind):
+    from oracle import kv_quant as kq
+    from tests import test_kv_quant_pins as qp
+    orig_q, orig_d = kq.quantize, kq.dequantize
+    if kind == "half_even":
+        monkeypatch.setattr(kq, "_round_half_away", np.round)
+    elif kind == "exact_scale":
+        def q2(x):
+            q, sc = orig_q(x)
+            blocks = np.asarray(x, dtype=np.float64).reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+            return q, np.abs(blocks).max(axis=-1) / 127      # the scale kept unrounded
+        monkeypatch.setattr(kq, "quantize", q2)
+    else:
+        monkeypatch.setattr(kq, "BLOCK", 16)
+
+    def pins():
+        qp.test_exact_multiples_decode_exactly()
+        qp.test_decode_error_bound()
+        qp.test_zero_blocks_and_symmetry()
+    _expect_failure(pins)
