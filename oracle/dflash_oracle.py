@@ -98,7 +98,8 @@ def rows_argmax(logits: np.ndarray) -> np.ndarray:
 
 
 def top2_gap(logits: np.ndarray) -> np.ndarray:
-    """Largest minus second-largest value per row."""
+    """Largest minus second-largest value per row, counting repeats: a row
+    whose maximum occurs twice has gap 0."""
     part = np.partition(logits, -2, axis=-1)
     return part[..., -1] - part[..., -2]
 
@@ -184,7 +185,8 @@ def draft_block(weights, shape, anchor: int, k_ctx: Sequence[np.ndarray],
 
     k_ctx[l], v_ctx[l] [C, n_kv, d] are layer l's injected context K/V.
     Returns draft ids [B-1] (greedy per masked position), the final residual
-    stream [B, H], the top logit and the top-1/top-2 gap per masked position.
+    stream [B, H], the logits of every masked position [B-1, V], the top logit
+    and the top-1/top-2 gap per masked position.
     """
     C = k_ctx[0].shape[0] if len(k_ctx) else 0
     ids = np.array([anchor] + [shape.mask_id] * (B - 1), dtype=np.int64)
@@ -198,10 +200,11 @@ def draft_block(weights, shape, anchor: int, k_ctx: Sequence[np.ndarray],
         top1 = np.max(logits, axis=-1)
         gap = top2_gap(logits)
     else:
+        logits = np.zeros((0, weights["lm_head"].shape[0]))
         draft = np.zeros(0, dtype=np.int64)
         top1 = np.zeros(0)
         gap = np.zeros(0)
-    return {"draft": draft, "hidden": x, "top1": top1, "gap": gap}
+    return {"draft": draft, "hidden": x, "logits": logits, "top1": top1, "gap": gap}
 
 
 # ----------------------------------------------------------------------------

@@ -93,9 +93,42 @@ def compare_draft(got_ids, got_hidden, got_top, ref, B, what, row_rel=None, emu_
         assert_hidden_like_bf16_storage(got_hidden, ref["hidden"], emu_hidden, f"{what}: final residual stream")
     if B > 1:
         assert_close(got_top, ref["top1"], f"{what}: winning logits", row_rel=row_rel)
+        ids = np.asarray(got_ids, dtype=np.int64)
         sure = ref["gap"] > GAP
-        np.testing.assert_array_equal(np.asarray(got_ids)[sure], ref["draft"][sure],
+        np.testing.assert_array_equal(ids[sure], ref["draft"][sure],
                                       err_msg=f"{what}: draft ids (gap > {GAP})")
-        # where the oracle's choice is ambiguous the GPU's id must still be a near-top logit
+        check_near_top(ids, got_top, ref, what, row_rel)
         return int(sure.sum())
     return 0
+
+
+def logit_tol(top1, row_rel=None):
+    """Per-row logit tolerance of the winning-logit comparison."""
+    top1 = np.asarray(top1, dtype=np.float64)
+    if row_rel is None:
+        return ATOL + RTOL * np.abs(top1)
+    return np.full_like(top1, ATOL + row_rel * np.max(np.abs(top1)))
+
+
+def check_near_top(ids, got_top, ref, what, row_rel=None):
+    """Every draft row, the ambiguous ones included. If each GPU logit is
+    within tol of the oracle's, the GPU's winner g and the oracle's winner o
+    satisfy l[g] >= l'[g] - tol >= l'[o] - tol >= l[o] - 2 tol. So the
+    oracle's logit at the GPU's id is at most two tolerances below the
+    oracle's top logit, and the GPU's reported winning logit is the oracle's
+    logit at that id within one tolerance (the id and its logit belong
+    together)."""
+    logits = np.asarray(ref["logits"], dtype=np.float64)
+    top1 = np.asarray(ref["top1"], dtype=np.float64)
+    assert ids.shape == (logits.shape[0],), f"{what}: {ids.shape} draft ids for {logits.shape[0]} rows"
+    assert ((ids >= 0) & (ids < logits.shape[1])).all(), f"{what}: draft id out of range"
+    at_id = logits[np.arange(len(ids)), ids]
+    tol = logit_tol(top1, row_rel)
+    short = top1 - at_id - 2 * tol
+    assert float(short.max()) <= 0.0, (
+        f"{what}: row {int(short.argmax())} draft id {int(ids[short.argmax()])} has oracle logit "
+        f"{at_id[short.argmax()]:.4g}, more than two tolerances below the top {top1[short.argmax()]:.4g}")
+    off = np.abs(np.asarray(got_top, dtype=np.float64) - at_id) - tol
+    assert float(off.max()) <= 0.0, (
+        f"{what}: row {int(off.argmax())} winning logit {got_top[off.argmax()]:.4g} is not the oracle's "
+        f"logit {at_id[off.argmax()]:.4g} at the GPU's id")

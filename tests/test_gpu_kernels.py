@@ -7,7 +7,7 @@ import pytest
 import oracle
 from synth import (TINY, make_weights_np, make_features_np, make_target_logits_bf16_np, make_verify_case_np,
                    bits_to_f32)
-from tests.gpu_util import np_weights_to_device, bf16_dev, i32_dev
+from tests.gpu_util import np_weights_to_device, bf16_dev, i32_dev, assert_close
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -137,6 +137,8 @@ def test_verify_and_commit_bit_exact_batch64(dfl):
     orc.fuse_ctx(seqs, ctx_len, feats[:sum(ctx_len)], pending=False)
     d.fuse_ctx(seqs, [B] * b, bf16_dev(feats[sum(ctx_len):], DEV), pending=True)
     orc.fuse_ctx(seqs, [B] * b, feats[sum(ctx_len):], pending=True)
+    # every cached byte (committed context and the pending block) before verify
+    before = {s: d.read_kv(0, s, 0, ctx_len[s] + B) for s in seqs}
     tau, bonus = d.verify(seqs, B, i32_dev(drafts, DEV), t_gpu)
     rt, rb = orc.verify(seqs, B, drafts, t_ref)
     d.sync()
@@ -145,12 +147,31 @@ def test_verify_and_commit_bit_exact_batch64(dfl):
     assert (rt == np.minimum(ms, B - 1) + 1).all()
     for s in seqs:
         assert d.seq_len(s) == orc.seq_len(s)
-    # the committed slots keep exactly the bytes appended before verify
+    # the committed slots keep exactly the bytes appended before verify (bf16
+    # bit patterns compared, so -0 and +0 differ), and they are the oracle's
+    # K/V within the tolerance
+    for s in seqs:
+        n = orc.seq_len(s)[0]
+        assert n == ctx_len[s] + int(rt[seqs.index(s)])
+        k, v = d.read_kv(0, s, 0, n)
+        np.testing.assert_array_equal(k.view(np.uint32), before[s][0][:n].view(np.uint32))
+        np.testing.assert_array_equal(v.view(np.uint32), before[s][1][:n].view(np.uint32))
+        kr, vr = orc.context(s, 0)
+        assert_close(k, kr, f"committed K seq {s}")
+        assert_close(v, vr, f"committed V seq {s}")
+    # the next cycle appends at the committed length: the rolled-back slots are
+    # overwritten by the new block and the committed prefix is untouched
+    feats2 = make_features_np(b * B, width, seed=15)
+    d.fuse_ctx(seqs, [B] * b, bf16_dev(feats2, DEV), pending=True)
+    orc.fuse_ctx(seqs, [B] * b, feats2, pending=True)
     for s in (0, 17, 63):
         n = orc.seq_len(s)[0]
-        k, v = d.read_kv(0, s, 0, n)
-        kr, vr = orc.context(s, 0)
-        assert np.abs(k - kr).max() < 5e-2 and np.abs(v - vr).max() < 5e-2
+        k, v = d.read_kv(0, s, 0, n + B)
+        np.testing.assert_array_equal(k[:n].view(np.uint32), before[s][0][:n].view(np.uint32))
+        np.testing.assert_array_equal(v[:n].view(np.uint32), before[s][1][:n].view(np.uint32))
+        st = orc.seqs[s]
+        assert_close(k[n:], st["k"][0][n:n + B], f"re-appended K seq {s}")
+        assert_close(v[n:], st["v"][0][n:n + B], f"re-appended V seq {s}")
     d.close()
 
 

@@ -140,6 +140,26 @@ def test_causal_mask_is_caught(monkeypatch):
     _expect_failure(pins.test_draft_pass_matches_scalar_brute_force)
 
 
+@pytest.mark.parametrize("kind", ["third_value", "distinct_values", "wrong_axis"])
+def test_top2_gap_mistakes_are_caught(monkeypatch, kind):
+    """top2_gap picks the rows whose draft ids must match bit for bit; a
+    mistake would silently grow or shrink that set."""
+    def bad(logits):
+        if kind == "third_value":        # top-1 minus the third-largest value
+            part = np.partition(logits, -3, axis=-1)
+            return part[..., -1] - part[..., -3]
+        if kind == "distinct_values":    # a repeated maximum skipped: ties look certain
+            out = []
+            for row in np.reshape(logits, (-1, logits.shape[-1])):
+                u = np.unique(row)
+                out.append(u[-1] - u[-2] if len(u) > 1 else 0.0)
+            return np.reshape(np.array(out), logits.shape[:-1])
+        part = np.partition(logits, -2, axis=0)   # partitioned over rows, not columns
+        return part[-1] - part[-2]
+    _patch(monkeypatch, "top2_gap", bad)
+    _expect_failure(pins.test_top2_gap_matches_a_scan_and_a_sort)
+
+
 def test_verify_off_by_one_is_caught(monkeypatch):
     def bad(drafts, targets):
         B = len(targets)

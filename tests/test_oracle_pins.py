@@ -279,7 +279,7 @@ def _draft_loops(w, sh, anchor, feats_ctx, B):
             act = [gt[i] / (1 + math.exp(-gt[i])) * up[i] for i in range(len(gt))]
             dn = _matvec(lw["w_down"], act)
             x[b] = [x[b][i] + dn[i] for i in range(H)]
-    drafts = []
+    drafts, all_logits = [], []
     for b in range(1, B):
         hf = _rms_loop(x[b], w["g_final"], sh.rms_eps)
         logits = _matvec(w["lm_head"], hf)
@@ -288,7 +288,8 @@ def _draft_loops(w, sh, anchor, feats_ctx, B):
             if logits[i] > logits[best]:
                 best = i
         drafts.append(best)
-    return drafts, x
+        all_logits.append(logits)
+    return drafts, x, all_logits
 
 
 def test_draft_pass_matches_scalar_brute_force():
@@ -298,9 +299,15 @@ def test_draft_pass_matches_scalar_brute_force():
     od = oracle.OracleDrafter(sh, w)
     od.fuse_ctx([0], [6], feats, pending=False)
     res = od.draft([0], [7], 4)[0]
-    ref_ids, ref_x = _draft_loops(w, sh, 7, feats, 4)
+    ref_ids, ref_x, ref_logits = _draft_loops(w, sh, 7, feats, 4)
     np.testing.assert_allclose(res["hidden"], np.array(ref_x), rtol=1e-11, atol=1e-11)
     np.testing.assert_array_equal(res["draft"], ref_ids)
+    np.testing.assert_allclose(res["logits"], np.array(ref_logits), rtol=1e-11, atol=1e-11)
+    # top logit and top-1/top-2 gap of each row, by a scan of the brute-force logits
+    for r, row in enumerate(ref_logits):
+        first, second = _two_largest_scan(row)
+        assert abs(res["top1"][r] - first) <= 1e-11
+        assert abs(res["gap"][r] - (first - second)) <= 1e-11
 
 
 def test_draft_is_invariant_to_a_global_position_shift():
@@ -361,6 +368,47 @@ def test_rows_argmax_lowest_index_on_ties():
             if x[i, j] > x[i, best]:
                 best = j
         assert got[i] == best
+
+
+def _two_largest_scan(row):
+    """The largest and second-largest entries of a row by one scan that keeps
+    both, a repeat of the maximum counting as the second largest."""
+    first, second = -math.inf, -math.inf
+    for v in row:
+        if v > first:
+            first, second = v, first
+        elif v > second:
+            second = v
+    return first, second
+
+
+def test_top2_gap_matches_a_scan_and_a_sort():
+    """top2_gap decides which draft rows must match bit for bit, so it is
+    pinned on its own: random rows, rows whose maximum repeats (gap 0), rows
+    whose second value repeats, all-equal rows, a two-column row and rows with
+    infinities, against a two-value scan and against Python's sorted()."""
+    r = _rng(19)
+    rows = [r.standard_normal(40) for _ in range(20)]
+    rows += [np.round(r.standard_normal(40) * 2) / 2 for _ in range(20)]   # many exact ties
+    tie_top = r.standard_normal(40)
+    tie_top[[3, 31]] = tie_top.max() + 1.0                               # maximum occurs twice
+    tie_second = r.standard_normal(40)
+    tie_second[[5, 6, 7]] = tie_second.max() + 1.0
+    tie_second[20] = tie_second.max() + 0.25                             # second value occurs three times
+    rows += [tie_top, tie_second, np.full(40, 1.5), np.array([2.0, -1.0])]
+    inf_row = r.standard_normal(40)
+    inf_row[9] = -math.inf
+    rows.append(inf_row)
+    x = np.stack([np.resize(row, 40) for row in rows])
+    got = oracle.top2_gap(x)
+    assert got.shape == (x.shape[0],)
+    for i, row in enumerate(x):
+        first, second = _two_largest_scan(row)
+        srt = sorted(row.tolist(), reverse=True)
+        assert got[i] == first - second == srt[0] - srt[1]
+    assert got[40] == 0.0 and got[42] == 0.0                              # repeated maximum, all equal
+    assert got[41] == 0.25                                               # the repeated second value counts once
+    assert (got >= 0).all()
 
 
 def _tau_bruteforce(d, t):
