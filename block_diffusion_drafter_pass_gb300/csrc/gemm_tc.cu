@@ -96,12 +96,13 @@ int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms
   // the memory system.
   if (splits == 0 && BN >= 128 && tiles <= num_sms) G = tiles;
   if (G > units) G = units;
-  // 2 partial slots of 128 x BN floats per CTA, unless every CTA owns whole tiles
+  // 2 partial slots of 128 x BN floats per CTA, unless every CTA owns whole
+  // tiles: the largest grid up to G that either divides the tile count (no
+  // partials) or fits the partial buffer
   const long long cap = static_cast<long long>(partial_elems / (2ull * kTileN * BN));
   if (G > cap && tiles % G != 0) {
     long long d = std::min<long long>(G, tiles);
-    while (d > 1 && (tiles % d != 0) && d > cap) --d;
-    while (d > 1 && tiles % d != 0) --d;
+    while (d > cap && tiles % d != 0) --d;
     G = d;
   }
   return static_cast<int>(std::max<long long>(G, 1));

@@ -80,12 +80,14 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
     return DFLASH_EINVAL;
   }
   if (splits > 0) {
-    // an explicit split factor runs tiles x splits CTAs with two 128 x BN partial slots each
-    const long long ctas = std::min(tiles * std::min(splits, k_blocks), tiles * k_blocks);
-    const long long need = 2 * ctas * 128 * BN;
-    if (ctas > 1 && tiles % ctas != 0 && need > static_cast<long long>(kPartialFloats)) {
+    // An explicit split factor s runs tiles x min(s, k_blocks) CTAs. With one
+    // split per tile every CTA owns a whole tile and writes no partials; with
+    // more, each CTA has two 128 x BN partial slots.
+    const int per_tile = std::min(splits, k_blocks);
+    const long long need = 2 * tiles * per_tile * 128 * BN;
+    if (per_tile > 1 && need > static_cast<long long>(kPartialFloats)) {
       set_unattached_error("dflash_gemm_noalloc: split-K partials exceed the fixed 8 MiB scratch "
-                           "(2 x splits x roundup(M) x roundup(N,128) floats); use fewer splits");
+                           "(2 x splits x M rounded up to the token tile x roundup(N,128) floats); use fewer splits");
       return DFLASH_EINVAL;
     }
   }
@@ -130,9 +132,12 @@ extern "C" dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* 
     set_unattached_error("dflash_gemm_noalloc: kernel launch failed");
     return DFLASH_ECUDA;
   }
+  // The status word is read on the caller's stream, never on the legacy
+  // default stream: a blocking copy there would wait for every blocking
+  // stream of the device and would break another thread's global-mode capture.
   int st = 0;
-  if (cudaStreamSynchronize(stream) != cudaSuccess ||
-      cudaMemcpy(&st, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+  if (cudaMemcpyAsync(&st, status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
     set_unattached_error("dflash_gemm_noalloc: CUDA error while waiting for the GEMM");
     return DFLASH_ECUDA;
   }

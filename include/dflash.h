@@ -349,12 +349,16 @@ dflash_status dflash_debug_gemm(const uint16_t* W, const uint16_t* X, float* Y,
  * first call before starting any stream capture. Every call shares the
  * array: the tickets and status are cleared at the start of each call, and
  * calls that overlap on the GPU (other threads or streams) race on it.
- * The call waits for its stream before returning.
+ * The call waits for its stream before returning (the status word is read
+ * back on that stream; the legacy default stream is not touched unless it is
+ * the stream passed).
  * W, X, Y: device pointers (W, X bf16, 16-byte aligned; K a multiple of 8).
  * splits: split-K factor, 0 = chosen to fit the array.
  * Errors: EINVAL for bad arguments, more than 4096 output tiles, or an
- * explicit `splits` whose partial tiles exceed the fixed scratch
- * (2 x splits x roundup(M) x roundup(N, 128) floats above 2^21); ECUDA;
+ * explicit `splits` above 1 whose partial tiles exceed the fixed scratch
+ * (2 x splits x roundup(M, T) x roundup(N, 128) floats above 2^21, T the
+ * token tile: 16, 32, 64, 128 or 256, the smallest of these that holds M, and
+ * 256 above 128); ECUDA;
  * ETIMEOUT/EDEVICE as reported by the kernel. Messages via
  * dflash_last_error(NULL). */
 dflash_status dflash_gemm_noalloc(const uint16_t* W, const uint16_t* X, float* Y,
