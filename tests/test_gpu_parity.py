@@ -374,3 +374,104 @@ def test_draft_is_bit_reproducible(dfl):
                 continue
             for a, b in zip(cur, first):
                 np.testing.assert_array_equal(a, b)
+
+
+# ----------------------------------------------------------------------------
+# The long-context, 32K and serving-batch configurations
+# ----------------------------------------------------------------------------
+
+def test_long_positions_262144(dfl):
+    """A context of 262144 injected tokens (the longest configuration): one
+    key/value head of d = 128 at tiny width, so the fp64 oracle holds the whole
+    cache. K/V are compared at positions around 2^17 and up to 2^18 - 1, where
+    RoPE angles reach 2.6e5 rad (the library's fp64-built table), and the
+    draft over the whole context at B = 8, 16 and 32."""
+    from dataclasses import replace
+    sh = replace(TINY, n_heads=2, n_kv_heads=1, head_dim=128)
+    wn = make_weights_np(sh, seed=111, gamma="jitter", std=0.05)
+    orc = oracle.OracleDrafter(sh, wn)
+    width = sh.n_feat_layers * sh.hidden
+    C, chunk = 262144, 32768
+    with dfl.Drafter(sh, np_weights_to_device(wn, DEV), max_seqs=1, max_batch=1, max_block=32,
+                     max_ctx=C + 64, max_fuse_tokens=chunk) as d:
+        for i in range(C // chunk):
+            f = make_features_np(chunk, width, seed=112 + i)
+            d.fuse_ctx([0], [chunk], bf16_dev(f, DEV), pending=False)
+            orc.fuse_ctx([0], [chunk], f, pending=False)
+            del f
+        d.sync()
+        assert d.seq_len(0) == (C, 0)
+        st = orc.seqs[0]
+        for p in (0, 63, 131071, 131072, 131073, 200001, 262080, 262143):
+            k, v = d.read_kv(0, 0, p, 1)
+            assert_close(k, st["k"][0][p:p + 1], f"K pos {p}", row_rel=ROW_REL_HIGH_GAIN)
+            assert_close(v, st["v"][0][p:p + 1], f"V pos {p}", row_rel=ROW_REL_HIGH_GAIN)
+        anchors = make_anchor_ids_np(1, sh.vocab, seed=120)
+        total = 0
+        for B in (8, 16, 32):
+            _, _, c = _draft_and_compare(d, orc, [0], anchors, B, f"C=262144 B={B}", ROW_REL_HIGH_GAIN)
+            total += c
+        assert total > 0
+
+
+def test_qwen3_8b_context_32768_two_layers(dfl):
+    """Batch 1 at context 32768 (the context of the bandwidth target) at the
+    8B width: 5 fused target layers, 2 drafter layers, the context appended in
+    4096-token chunks; K/V at page and chunk boundaries, then the B = 16 draft."""
+    shape, wt, wn = _big_setup(2, seed=131)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    width = shape.n_feat_layers * shape.hidden
+    C, chunk = 32768, 4096
+    with dfl.Drafter(shape, wt, max_seqs=1, max_batch=1, max_block=16, max_ctx=C + 64,
+                     max_fuse_tokens=chunk) as d:
+        for i in range(C // chunk):
+            f = make_features_np(chunk, width, seed=132 + i)
+            d.fuse_ctx([0], [chunk], bf16_dev(f, DEV), pending=False)
+            orc.fuse_ctx([0], [chunk], f, pending=False)
+            del f
+        d.sync()
+        st = orc.seqs[0]
+        for l in (0, 1):
+            for p in (0, 4095, 4096, 16383, 16384, 32767):
+                k, v = d.read_kv(l, 0, p, 1)
+                assert_close(k, st["k"][l][p:p + 1], f"8B C=32768 K layer {l} pos {p}")
+                assert_close(v, st["v"][l][p:p + 1], f"8B C=32768 V layer {l} pos {p}")
+        anchors = make_anchor_ids_np(1, shape.vocab, seed=140)
+        _, _, checked = _draft_and_compare(d, orc, [0], anchors, 16, "8B 2-layer C=32768")
+        assert checked > 0
+
+
+def test_qwen3_8b_batch32_serving_lengths(dfl):
+    """The serving batch: 32 sequences with contexts uniform in [1024, 8192]
+    (the benchmark's seeded lengths), B = 16, at the 8B width with 2 drafter
+    layers (one fused target layer keeps the host oracle's fusion short; the
+    drafter side is the benchmarked one). The attention work is dealt largest
+    first over several chunks per CTA at these lengths."""
+    from dataclasses import replace
+    from synth import make_serving_lengths
+    shape = replace(QWEN3_8B.with_layers(2), n_feat_layers=1)
+    wt = make_weights_torch(shape, seed=151, device=DEV, gamma="jitter")
+    wn = torch_weights_to_np(wt)
+    orc = oracle.OracleDrafter(shape, wn, dtype=np.float32)
+    width = shape.n_feat_layers * shape.hidden
+    n = 32
+    lens = [int(x) for x in make_serving_lengths(n, 1024, 8192, seed=0)]
+    with dfl.Drafter(shape, wt, max_seqs=n, max_batch=n, max_block=16, max_ctx=8192 + 64,
+                     max_fuse_tokens=8192) as d:
+        for s in range(n):
+            f = make_features_np(lens[s], width, seed=152 + s)
+            d.fuse_ctx([s], [lens[s]], bf16_dev(f, DEV), pending=False)
+            orc.fuse_ctx([s], [lens[s]], f, pending=False)
+            del f
+        d.sync()
+        for s in (0, 13, 31):
+            st = orc.seqs[s]
+            m = lens[s]
+            for l in (0, 1):
+                for p in (0, 63, 64, m // 2, m - 1):
+                    k, v = d.read_kv(l, s, p, 1)
+                    assert_close(k, st["k"][l][p:p + 1], f"batch 32 K seq {s} layer {l} pos {p}")
+                    assert_close(v, st["v"][l][p:p + 1], f"batch 32 V seq {s} layer {l} pos {p}")
+        anchors = make_anchor_ids_np(n, shape.vocab, seed=190)
+        _, _, checked = _draft_and_compare(d, orc, list(range(n)), anchors, 16, "8B 2-layer batch 32 U[1024, 8192]")
+        assert checked > 0
