@@ -81,28 +81,36 @@ struct GemmArgs {
   int M, N, K;
   int k_blocks, n_tiles, m_tiles;
   long long units;     // tiles * k_blocks
-  int grid;            // CTAs (stream-K workers)
+  int grid;            // CTAs
+  int workers;         // stream-K workers: CTAs, or CTA pairs (pair = 3)
   int csplit;          // 1: CTAs 2t and 2t+1 form a cluster splitting tile t's k-blocks in halves
   int pair;            // 1: CTA pairs run cta_group::2 MMAs over whole 256 x 256 pair tiles;
-                       // 2: clusters of two such pairs, each over half of the k-blocks of one pair tile
+                       // 2: clusters of two such pairs, each over half of the k-blocks of one pair tile;
+                       // 3: CTA pairs over equal ranges of (pair tile, k-block) units (stream-K)
   float* partial;      // [grid][2][128 * BN] partial tiles
   int* tickets;        // [tiles], zero between launches
   int* status;
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barriers of the epilogue warps: barrier 1 + grp joins the 128 threads
+// of epilogue group grp (one warp per TMEM lane quarter); barrier 3 joins the
+// 256 threads of both groups of the pair kernel.
+__device__ __forceinline__ void epi_bar(int grp = 0) { asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory"); }
+__device__ __forceinline__ void epi_bar_all() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
 // Reductions over the tile's 128 rows go through shared memory: a 16-column
 // chunk is staged as [128 rows][17], thread t reduces rows 16*(t>>4) .. +15
 // of column t&15, and 16 threads combine the 8 row groups.
 struct EpiShared {
-  unsigned long long cand8[2][8][16];  // argmax candidate per (row group, column), per chunk parity
-  float red8[2][8][16];                // sum of squares per (row group, column), per chunk parity
+  union {   // one kernel instantiation uses one of them; slot = epilogue group * 2 + chunk parity
+    unsigned long long cand8[4][8][16];  // argmax candidate per (row group, column)
+    float red8[4][8][16];                // sum of squares per (row group, column)
+  };
   int row_pos[256];                  // QKV_ROPE / KV_APPEND: absolute position of each column
   int row_dst[256];                  // KV_APPEND: (page, slot) part of the pool row index
   float row_scale[256];              // folded RMSNorm scale of each column
   float2 rope_base[16][64];          // RoPE (cos, sin) at each chunk's first position, per frequency
-  int flag;
+  int flag[2];                       // per epilogue group
 };
 
 __device__ __forceinline__ int region_of(const ARegions& rg, int tile) {
@@ -146,11 +154,12 @@ __device__ __forceinline__ float norm_scale(const GemmEpi& e, int m) {
 
 // Per-column metadata of one output tile (columns m0 .. m0+BN-1), computed
 // once by all 128 epilogue threads before the tile is drained.
+// Columns [cb, ce) of the tile, by epilogue group grp.
 template <int BN, int EC>
 __device__ __forceinline__ void tile_cols_prepare(const GemmArgs& a, const GemmEpi& e, int m0, int r,
-                                                  EpiShared& sh) {
+                                                  EpiShared& sh, int cb = 0, int ce = BN, int grp = 0) {
   const int kind = class_kind<EC>(e.kind);
-  for (int col = r; col < BN; col += 128) {
+  for (int col = cb + r; col < ce; col += 128) {
     const int m = m0 + col;
     float sc = 1.f;
     int pos = -1, dst = -1;
@@ -181,16 +190,16 @@ __device__ __forceinline__ void tile_cols_prepare(const GemmArgs& a, const GemmE
     sh.row_pos[col] = pos;
     sh.row_dst[col] = dst;
   }
-  epi_bar();
-  // RoPE bases of every chunk: one round of loads for the whole tile
+  epi_bar(grp);
+  // RoPE bases of every chunk: one round of loads for the whole column range
   if (kind == EPI_QKV_ROPE || kind == EPI_KV_APPEND) {
     const int half = e.head_dim >> 1;
-    for (int k = r; k < (BN / 16) * half; k += 128) {
-      const int ch = k / half, fi = k - ch * half;
+    for (int k = r; k < ((ce - cb) / 16) * half; k += 128) {
+      const int kc = k / half, fi = k - kc * half, ch = cb / 16 + kc;
       const int pos = sh.row_pos[ch * 16];
       sh.rope_base[ch][fi] = pos >= 0 ? e.rope[static_cast<size_t>(pos) * half + fi] : make_float2(1.f, 0.f);
     }
-    epi_bar();
+    epi_bar(grp);
   }
 }
 
@@ -215,15 +224,15 @@ __device__ __forceinline__ void tmem_wait_st_gk() { asm volatile("tcgen05.wait::
 // `total` tile epilogues decodes the winning keys into ids (and logits) and
 // resets them for the next call.
 __device__ __forceinline__ void argmax_tile_done(const GemmArgs& a, const GemmEpi& e, EpiShared& esh, int r,
-                                                 int total) {
+                                                 int total, int grp = 0) {
   __threadfence();
-  epi_bar();
+  epi_bar(grp);
   if (r == 0) {
     const int dn = atomicAdd(e.done, 1);
-    esh.flag = (dn == total - 1);
+    esh.flag[grp] = (dn == total - 1);
   }
-  epi_bar();
-  if (esh.flag) {
+  epi_bar(grp);
+  if (esh.flag[grp]) {
     __threadfence();
     const int sb = e.argmax_skip_B;
     for (int m = r; m < a.M; m += 128) {
@@ -238,12 +247,13 @@ __device__ __forceinline__ void argmax_tile_done(const GemmArgs& a, const GemmEp
     }
     if (r == 0) *e.done = 0;
   }
-  epi_bar();
+  epi_bar(grp);
 }
 
-// Stream-K partition: CTA g owns the contiguous range of (tile, k-block)
-// units [unit_begin(g), unit_begin(g + 1)); tiles are ordered so that the m
-// tiles of one weight tile are consecutive (weights reused from L2).
+// Stream-K partition: worker g (a CTA, or a CTA pair) owns the contiguous
+// range of (tile, k-block) units [unit_begin(g), unit_begin(g + 1)); tiles are
+// ordered so that the m tiles of one weight tile are consecutive (weights
+// reused from L2).
 // floor(x / y) for x >= 0, y > 0; a 32-bit division whenever both fit
 // (a 64-bit division is a long dependent instruction sequence)
 __device__ __forceinline__ long long div_floor(long long x, long long y) {
@@ -251,12 +261,12 @@ __device__ __forceinline__ long long div_floor(long long x, long long y) {
   return x / y;
 }
 __device__ __forceinline__ long long unit_begin(int g, const GemmArgs& a) {
-  return div_floor(static_cast<long long>(g) * a.units, a.grid);
+  return div_floor(static_cast<long long>(g) * a.units, a.workers);
 }
-// The CTA whose range holds unit u: the largest g with floor(g U / G) <= u,
+// The worker whose range holds unit u: the largest g with floor(g U / G) <= u,
 // i.e. g U < (u + 1) G, which is floor(((u + 1) G - 1) / U).
 __device__ __forceinline__ int cta_of(long long u, const GemmArgs& a) {
-  return static_cast<int>(div_floor((u + 1) * a.grid - 1, a.units));
+  return static_cast<int>(div_floor((u + 1) * a.workers - 1, a.units));
 }
 
 __device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, int m0, int c0, int n,
@@ -268,13 +278,45 @@ __device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, 
   }
 }
 
-// Drain one finished tile from TMEM (plus the other CTAs' partial tiles) and
-// run the epilogue. r = TMEM lane of this thread (0..127).
-template <int BN, int EC>
+// Park a tile's partial sum: TMEM columns [0, BN) of this thread's lane to
+// dst[column * 128] (column-major, so each warp store covers 128 bytes), 32
+// columns per TMEM load.
+template <int BN>
+__device__ __forceinline__ void park_partial(uint32_t tb, float* dst, int cb = 0, int ce = BN) {
+  if constexpr (BN < 32) {
+#pragma unroll
+    for (int c0 = cb; c0 < ce; c0 += 16) {
+      float v[16];
+      tmem_ld16(tb + c0, v);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) dst[static_cast<size_t>(c0 + c) * kTileN] = v[c];
+    }
+  } else {
+#pragma unroll 1
+    for (int c0 = cb; c0 < ce; c0 += 32) {
+      float v[32];
+      tmem_ld32(tb + c0, v);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) dst[static_cast<size_t>(c0 + c) * kTileN] = v[c];
+    }
+  }
+}
+
+// Drain one finished tile from TMEM (plus the other workers' partial tiles)
+// and run the epilogue. r = TMEM lane of this thread (0..127). g, first and
+// last are stream-K workers; worker w's partial slots belong to CTA
+// w * cstep + cbase (CTA pairs: the pair's CTA that holds the same weight
+// tile), and tile_u0 is the tile's first unit in the workers' partition.
+// G = 2: two epilogue groups each drain a column range [cbeg, cend) of the
+// tile; group grp has its own named barrier, staging buffer (single-buffered,
+// with one more barrier per chunk where rows are exchanged) and reduction
+// slots.
+template <int BN, int EC, int G = 1>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int g,
                                               int tile, int first, int last, uint32_t tb, int r, EpiShared& sh,
                                               float* stg, uint32_t pre, const float (&rpre)[16], int cbeg,
-                                              int cend, const float* speer) {
+                                              int cend, const float* speer, long long tile_u0, int cstep = 1,
+                                              int cbase = 0, int grp = 0) {
   const int kind = class_kind<EC>(e.kind);
   const int q = r >> 5, lane = r & 31;
   const int tn = tile / a.m_tiles, tm = tile - tn * a.m_tiles;
@@ -307,19 +349,29 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   // same from run to run. Every CTA after the tile's first one starts inside
   // the tile, so its piece is its first segment (slot 0); the first CTA's
   // piece is in slot 1 when that CTA began in an earlier tile.
-  const bool first_in_slot1 = unit_begin(first, a) < static_cast<long long>(tile) * a.k_blocks;
+  const bool first_in_slot1 = unit_begin(first, a) < tile_u0;
   auto partial_src = [&](int o) {
     const int side = (o == first && first_in_slot1) ? 1 : 0;
-    return a.partial + (static_cast<size_t>(o) * 2 + side) * slot_elems + r;
+    return a.partial + (static_cast<size_t>(o * cstep + cbase) * 2 + side) * slot_elems + r;
   };
-  int oth0 = -1;
-  for (int o = first; o <= last; ++o) {
-    if (o != g && oth0 < 0) oth0 = o;
-  }
-  const float* ps0 = oth0 >= 0 ? partial_src(oth0) : nullptr;
-  auto partial_load = [&](int c0, float (&p0)[16]) {
+  // wider tiles: the first kAhead other pieces, in CTA order, are read one
+  // chunk ahead, all in one round of loads (256-token tiles: two, the most a
+  // stream-K pair range splits a tile into when it holds more than one
+  // tile's units; further pieces are read on use)
+  constexpr int kAhead = BN >= 256 ? 2 : 3;
+  const float* psrc[kAhead];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) p0[c] = ps0 ? __ldcg(ps0 + static_cast<size_t>(c0 + c) * kTileN) : 0.f;
+  for (int k = 0; k < kAhead; ++k) {   // the k-th other piece: worker first + k, skipping g
+    const int o = first + k + (first + k >= g ? 1 : 0);
+    psrc[k] = o <= last ? partial_src(o) : nullptr;
+  }
+  const int n_oth = last - first;
+  auto partial_load = [&](int c0, float (&p0)[kAhead][16]) {
+#pragma unroll
+    for (int k = 0; k < kAhead; ++k) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) p0[k][c] = psrc[k] ? __ldcg(psrc[k] + static_cast<size_t>(c0 + c) * kTileN) : 0.f;
+    }
   };
   // RoPE: when a chunk's 16 positions are consecutive (one sequence's block),
   // (cos, sin) is read once at its first position and advanced by the row's
@@ -343,12 +395,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
     }
   }
   if (rope) rot = e.rope[half + fi];
-  float pc0[16];
-  if constexpr (BN > 16) partial_load(cbeg, pc0);
+  float pc0[kAhead][16];
+  if constexpr (BN > 16) {
+    if (n_oth) partial_load(cbeg, pc0);
+  }
 #pragma unroll 1
   for (int c0 = cbeg; c0 < cend; c0 += 16) {
     const int buf = (c0 >> 4) & 1;
-    float* sb = stg + buf * (128 * 17);
+    float* sb = G == 1 ? stg + buf * (128 * 17) : stg + grp * (128 * 17);
+    const int pb = buf + 2 * grp;   // reduction slot of this chunk
     float rc[16];
     if (resid && !pre && c0 + 32 < cend) load_resid(a, e, m0, c0 + 32, n, rc);
     float rx[16];
@@ -360,9 +415,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         for (int c = 0; c < 16; ++c) rx[c] = ra[c];
       }
     }
-    float pn0[16];
+    float pn0[kAhead][16];
     if constexpr (BN > 16) {
-      if (c0 + 16 < cend) partial_load(c0 + 16, pn0);
+      if (n_oth && c0 + 16 < cend) partial_load(c0 + 16, pn0);
     }
     float v[16];
     tmem_ld16(tb + c0, v);
@@ -401,12 +456,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
 #pragma unroll
       for (int c = 0; c < 16; ++c) sum[c] = 0.f;
       for (int o = first; o <= last; ++o) {
+        const int k = (o - first) - (o > g ? 1 : 0);   // rank of o among the other pieces
         if (o == g) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) sum[c] += v[c];
-        } else if (BN > 16 && o == oth0) {
+        } else if (BN > 16 && k < kAhead) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) sum[c] += pc0[c];
+          for (int kk = 0; kk < kAhead; ++kk) {
+            if (kk == k) {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) sum[c] += pc0[kk][c];
+            }
+          }
         } else {
           const float* src = partial_src(o);
 #pragma unroll
@@ -424,10 +485,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
     if (paired_kind) {   // exchange with row r ^ P through the chunk's staging buffer
 #pragma unroll
       for (int c = 0; c < 16; ++c) sb[r * 17 + c] = v[c];
-      epi_bar();
+      epi_bar(grp);
       const int pr = r ^ P;
 #pragma unroll
       for (int c = 0; c < 16; ++c) other[c] = sb[pr * 17 + c];
+      if constexpr (G == 2) epi_bar(grp);   // single buffer: all reads before the next chunk's writes
     }
 
     if (kind == EPI_F32_STORE || kind == EPI_F32_ADD) {
@@ -483,18 +545,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         }
       }
       // column sums of squares over the tile's 128 rows
-      epi_bar();
+      epi_bar(grp);
       const int cc = r & 15, gq = r >> 4;
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 16; ++i) s4[i & 3] += sb[(gq * 16 + i) * 17 + cc];
-      sh.red8[buf][gq][cc] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-      epi_bar();
+      sh.red8[pb][gq][cc] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      epi_bar(grp);
       if (r < 16) {
         const int m = m0 + c0 + r;
         float t = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) t += sh.red8[buf][k][r];
+        for (int k = 0; k < 8; ++k) t += sh.red8[pb][k][r];
         if (m < a.M) e.out_ss[static_cast<size_t>(tn) * e.out_ss_ld + m] = t;
       }
     } else if (kind == EPI_ARGMAX) {
@@ -502,7 +564,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
       // packed as (ordered key << 32) | ~row so one 64-bit max decides
 #pragma unroll
       for (int c = 0; c < 16; ++c) sb[r * 17 + c] = v[c];
-      epi_bar();
+      epi_bar(grp);
       const int cc = r & 15, gq = r >> 4;
       const int m = m0 + c0 + cc;
       unsigned long long best = 0ull;
@@ -517,12 +579,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
           best = (static_cast<int>(idx) < a.N && cand > best) ? cand : best;
         }
       }
-      sh.cand8[buf][gq][cc] = best;
-      epi_bar();
+      sh.cand8[pb][gq][cc] = best;
+      epi_bar(grp);
       if (r < 16) {
-        unsigned long long b8 = sh.cand8[buf][0][r];
+        unsigned long long b8 = sh.cand8[pb][0][r];
 #pragma unroll
-        for (int k = 1; k < 8; ++k) b8 = sh.cand8[buf][k][r] > b8 ? sh.cand8[buf][k][r] : b8;
+        for (int k = 1; k < 8; ++k) b8 = sh.cand8[pb][k][r] > b8 ? sh.cand8[pb][k][r] : b8;
         if (b8) atomicMax(e.keys + (m0 + c0 + r), b8);
       }
     } else if (kind == EPI_SWIGLU) {
@@ -597,7 +659,43 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
           ov[c] = f32_to_bf16(x);
         }
       }
-      if (kind == EPI_QKV_ROPE && reg != 2 && allpos && m0 + c0 + 16 <= a.M) {   // whole chunk of q or k
+      // KV append, value rows: the chunk's 16 tokens at consecutive slots of
+      // one page are 32 contiguous bytes of this row of the transposed value
+      // tile, written with the widest aligned stores (the per-token path
+      // would make 16 two-byte stores to 16 sectors shared with no other lane)
+      bool vrun = kind == EPI_KV_APPEND && (reg & 1) && dstv[0] >= 0 && (dstv[0] & (kPage - 1)) + 16 <= kPage;
+#pragma unroll
+      for (int c = 1; c < 16; ++c) vrun = vrun && dstv[c] == dstv[0] + c;
+      if (vrun) {
+        const int slot0 = dstv[0] & (kPage - 1);
+        const int layer = e.layer0 + (reg >> 1);
+        uint16_t* p = e.pool +
+                      (static_cast<size_t>(layer) * e.pool_pages * 2 * e.n_kv_heads * kPage +
+                       static_cast<size_t>(dstv[0] - slot0)) * d +
+                      static_cast<size_t>(e.n_kv_heads) * kPage * d + (static_cast<size_t>(hd) * d + di) * kPage + slot0;
+        uint32_t w[8];
+        if ((slot0 & 1) == 0) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            w[c] = static_cast<uint32_t>(ov[2 * c]) | (static_cast<uint32_t>(ov[2 * c + 1]) << 16);
+          if ((slot0 & 7) == 0) {
+            uint4* q4 = reinterpret_cast<uint4*>(p);
+            q4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            q4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            uint32_t* q2 = reinterpret_cast<uint32_t*>(p);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) q2[c] = w[c];
+          }
+        } else {   // odd first slot: one value, seven aligned pairs, one value
+          p[0] = ov[0];
+          uint32_t* q2 = reinterpret_cast<uint32_t*>(p + 1);
+#pragma unroll
+          for (int c = 0; c < 7; ++c)
+            q2[c] = static_cast<uint32_t>(ov[2 * c + 1]) | (static_cast<uint32_t>(ov[2 * c + 2]) << 16);
+          p[15] = ov[15];
+        }
+      } else if (kind == EPI_QKV_ROPE && reg != 2 && allpos && m0 + c0 + 16 <= a.M) {   // whole chunk of q or k
         const size_t ld = static_cast<size_t>(reg == 0 ? e.n_q_heads : e.n_kv_heads) * d;
         uint16_t* p = (reg == 0 ? e.out_q : e.out_k) + static_cast<size_t>(m0 + c0) * ld + rf;
 #pragma unroll
@@ -635,12 +733,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
     }
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      pc0[c] = pn0[c];
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k) pc0[k][c] = pn0[k][c];
       ra[c] = rb[c];
       rb[c] = rc[c];
     }
   }
-  epi_bar();
+  epi_bar(grp);
 }
 
 
@@ -854,9 +953,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         latch_status(a.status, kDevTimeout);
       }
       epi_bar();
-      if (r == 0) esh.flag = abort_flag;   // one reader, so all epilogue threads agree
+      if (r == 0) esh.flag[0] = abort_flag;   // one reader, so all epilogue threads agree
       epi_bar();
-      if (esh.flag) break;
+      if (esh.flag[0]) break;
       tc_fence_after();
       const uint32_t tb = trow + buf * BN;
       bool finish = whole;
@@ -888,36 +987,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           latch_status(a.status, kDevTimeout);
         }
         epi_bar();
-        if (r == 0) esh.flag = abort_flag;
+        if (r == 0) esh.flag[0] = abort_flag;
         epi_bar();
-        if (esh.flag) break;
+        if (esh.flag[0]) break;
         speer = reinterpret_cast<const float*>(smem);
         finish = true;
       } else if (!whole) {
         // park this segment's partial sum in the CTA's slot, then take a ticket
         const int side = (u == u0) ? 0 : 1;
-        float* dst = a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems + r;
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          float v[16];
-          tmem_ld16(tb + c0, v);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) dst[static_cast<size_t>(c0 + c) * kTileN] = v[c];
-        }
+        park_partial<BN>(tb, a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems + r);
         first = cta_of(static_cast<long long>(t) * kb, a);
         last = cta_of(static_cast<long long>(t + 1) * kb - 1, a);
         __threadfence();
         epi_bar();
         if (r == 0) {
           const int tk = atomicAdd(a.tickets + t, 1);
-          esh.flag = (tk == last - first);
+          esh.flag[0] = (tk == last - first);
           if (tk == last - first) a.tickets[t] = 0;
         }
         epi_bar();
-        finish = esh.flag != 0;
+        finish = esh.flag[0] != 0;
         if (finish) __threadfence();
       }
       if (finish) {
-        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre, rpre, cbeg, cend, speer);
+        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre, rpre, cbeg, cend, speer,
+                              static_cast<long long>(t) * kb);
         if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, (a.csplit ? 2 : 1) * a.n_tiles * a.m_tiles);
       }
       // hand the TMEM buffer back to the MMA warp
@@ -948,29 +1042,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 // k-block is what limits single-CTA tensor-bound tiles), and a stage is 32 KB,
 // so six fit. Pairs take whole pair tiles round-robin; a pair's second weight
 // tile past N (odd tile count) loads zeros and stores nothing.
+constexpr int kEpiGroups = 2;                     // epilogue groups of the pair kernel
+constexpr int kPairThreads = 64 + kEpiGroups * 128; // TMA warp, MMA warp, epilogue groups
 struct PairCfg {
   static constexpr int BN = 256;
   static constexpr int kBHalfBytes = (BN / 2) * kTileK * 2;   // 16 KB
   static constexpr int kStageBytes = kABytes + kBHalfBytes;     // 32 KB per CTA
   static constexpr int kStages = 6;
   static constexpr int kTmemCols = 2 * BN;                      // two accumulators
-  static constexpr int kStgBytes = 2 * 128 * 17 * 4;
+  static constexpr int kStgBytes = kEpiGroups * 128 * 17 * 4;   // one exchange buffer per epilogue group
   static constexpr int kSmem = kStages * kStageBytes + kStgBytes + 1024;
 };
 
-// KS = 2: a cluster of four CTAs, two pairs over the two halves of the
-// k-blocks of one pair tile; the CTAs holding the same weight tile in the two
-// pairs exchange the half sums of each other's 128 token columns through
+// MODE 1: pairs take whole pair tiles round-robin.
+// MODE 2 (KS = 2): a cluster of four CTAs, two pairs over the two halves of
+// the k-blocks of one pair tile; the CTAs holding the same weight tile in the
+// two pairs exchange the half sums of each other's 128 token columns through
 // distributed shared memory (as the single-CTA cluster split does) and each
 // finishes its own 128 columns. Used when four CTAs per pair tile fit one
 // wave, which single pairs would leave half idle.
-template <int EC, int KS>
-__global__ void __launch_bounds__(kThreads, 1)
+// MODE 3: stream-K over pairs. Pair p owns an equal contiguous range of
+// (pair tile, k-block) units, so every SM pair has the same MMA work whatever
+// the tile count. Each CTA of the pair holds one weight tile's 128 rows of
+// the pair tile, an ordinary 128 x 256 tile: a segment that does not cover a
+// whole tile is parked in the CTA's partial slot and the tile is finished by
+// the last CTA (of those holding the same weight tile) to take its ticket, as
+// in the single-CTA kernel.
+template <int EC, int MODE>
+__global__ void __launch_bounds__(kPairThreads, 1)
     gemm_pair_kernel(const __grid_constant__ AMaps amaps, const __grid_constant__ CUtensorMap xmap,
                      const __grid_constant__ GemmArgs a, const __grid_constant__ ARegions rg,
                      const __grid_constant__ GemmEpi e) {
   using P = PairCfg;
   constexpr int BN = P::BN;
+  constexpr int KS = MODE == 2 ? 2 : 1;
+  constexpr bool SK = MODE == 3;
   constexpr int CL = 2 * KS;   // CTAs per cluster
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -978,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t full[P::kStages];    // the pair's first CTA's count both CTAs' bytes
   __shared__ __align__(8) uint64_t empty[P::kStages];
   __shared__ __align__(8) uint64_t acc_full[2];
-  __shared__ __align__(8) uint64_t acc_empty[2];        // the pair's first CTA's: 4 epilogue warps of each CTA
+  __shared__ __align__(8) uint64_t acc_empty[2];        // the pair's first CTA's: every epilogue warp of each CTA
   __shared__ __align__(8) uint64_t split_rdy;           // KS = 2: the other pair's CTA's ring is idle (count 1)
   __shared__ __align__(8) uint64_t split_dat;           // KS = 2: its half sums have landed here (count 128)
   __shared__ uint32_t tmem_slot;
@@ -1002,6 +1108,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // columns (tokens) this CTA finishes
   const int cbeg = KS == 2 ? static_cast<int>(half) * (BN / 2) : 0;
   const int cend = KS == 2 ? cbeg + BN / 2 : BN;
+  // MODE 3: this pair's range of (pair tile, k-block) units
+  const long long su0 = SK ? unit_begin(pair, a) : 0, su1 = SK ? unit_begin(pair + 1, a) : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P::kStages; ++s) {
@@ -1010,10 +1118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8);
+      mbar_init(&acc_empty[b], 2 * 4 * kEpiGroups);   // every epilogue warp of both CTAs
     }
     mbar_init(&split_rdy, 1);
-    mbar_init(&split_dat, 128);
+    mbar_init(&split_dat, 128 * kEpiGroups);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -1046,12 +1154,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto advance = [&](Cur& c) {
         if (++c.k == kend) {
           c.k = kbeg;
-          c.pt += n_pairs;
+          c.pt += SK ? 1 : n_pairs;
           if (c.pt < pair_tiles) at_tile(c);
         }
       };
-      const int n_units = pair < pair_tiles ? ((pair_tiles - 1 - pair) / n_pairs + 1) * nk : 0;
+      int n_units;
       Cur ca{pair, kbeg, 0, 0, 0, 0, 0};
+      if constexpr (SK) {
+        n_units = static_cast<int>(su1 - su0);
+        ca.pt = static_cast<int>(su0 / kb);
+        ca.k = static_cast<int>(su0 - static_cast<long long>(ca.pt) * kb);
+      } else {
+        n_units = pair < pair_tiles ? ((pair_tiles - 1 - pair) / n_pairs + 1) * nk : 0;
+      }
       if (n_units > 0) at_tile(ca);
       Cur cb = ca;
       auto load_a = [&](int i, const Cur& c) {
@@ -1103,7 +1218,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(2 * kTileN, BN);
       grid_dep_wait();
       int i = 0, j = 0;
-      for (int pt = pair; pt < pair_tiles && !abort_flag; pt += n_pairs, ++j) {
+      // segments: whole pair tiles (MODE 1, 2), or the stretches of this
+      // pair's unit range inside one pair tile (MODE 3)
+      long long su = su0;
+      for (int pt = SK ? 0 : pair; (SK ? su < su1 : pt < pair_tiles) && !abort_flag; pt += n_pairs, ++j) {
+        int seg_k = nk;
+        if constexpr (SK) {
+          const long long tp = su / kb;
+          const long long se = min(su1, (tp + 1) * kb);
+          seg_k = static_cast<int>(se - su);
+          su = se;
+        }
         const int buf = j & 1;
         if (!mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, &abort_flag)) {
           abort_flag = 1;
@@ -1112,7 +1237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * BN;
-        for (int k = 0; k < nk; ++k, ++i) {
+        for (int k = 0; k < seg_k; ++k, ++i) {
           const int s = i % P::kStages;
           if (!mbar_wait(&full[s], (i / P::kStages) & 1, &abort_flag)) {
             abort_flag = 1;
@@ -1133,18 +1258,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue warps (every CTA) ----------------
+    // Two groups of four warps (one per TMEM lane quarter); group grp drains
+    // columns [gcb, gce), half of this CTA's columns. Decisions every thread
+    // must share (give up after a failed wait, finish a tile) are taken once
+    // for both groups behind the 256-thread barrier.
     grid_dep_wait();
+    const int grp = (warp - 2) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int et = threadIdx.x - 64;   // epilogue thread 0 .. 255
     const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t lead_acc_empty = mapa_shared(smem_u32(&acc_empty[0]), lead);
+    const size_t slot_elems = static_cast<size_t>(kTileN) * BN;
+    const int gw = (cend - cbeg) / kEpiGroups;
+    const int gcb = cbeg + grp * gw, gce = gcb + gw;
+    float* gstg = stg;   // epilogue_tile picks the group's buffer
     int j = 0;
-    for (int pt = pair; pt < pair_tiles; pt += n_pairs, ++j) {
+    long long su = su0;
+    for (int pt0 = SK ? 0 : pair; SK ? su < su1 : pt0 < pair_tiles; pt0 += n_pairs, ++j) {
+      int pt = pt0;
+      long long seg_u = 0, seg_end = 0;
+      if constexpr (SK) {
+        pt = static_cast<int>(su / kb);
+        seg_u = su;
+        seg_end = min(su1, static_cast<long long>(pt + 1) * kb);
+        su = seg_end;
+      }
       const int pr = pt / a.m_tiles, tm = pt - pr * a.m_tiles;
       const int tn = 2 * pr + static_cast<int>(member);
       const int t = tn * a.m_tiles + tm;   // this CTA's tile
       const int buf = j & 1;
-      tile_cols_prepare<BN, EC>(a, e, tm * BN, r, esh);
+      tile_cols_prepare<BN, EC>(a, e, tm * BN, r, esh, gcb, gce, grp);
       float rpre[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) rpre[c] = 0.f;
@@ -1156,7 +1300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int n = tn * kTileN + r, m0 = tm * BN;
           pre = trow + (buf ^ 1) * BN;
 #pragma unroll 1
-          for (int c0 = cbeg; c0 < cend; c0 += 32) {
+          for (int c0 = gcb; c0 < gce; c0 += 32) {
             float xv[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -1172,24 +1316,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         abort_flag = 1;
         latch_status(a.status, kDevTimeout);
       }
-      epi_bar();
-      if (r == 0) esh.flag = abort_flag;
-      epi_bar();
-      if (esh.flag) break;
+      epi_bar_all();
+      if (et == 0) esh.flag[0] = abort_flag;
+      epi_bar_all();
+      if (esh.flag[0]) break;
       tc_fence_after();
       const uint32_t tb = trow + buf * BN;
       const float* speer = nullptr;
       if constexpr (KS == 2) {
         // send the other half's CTA (same weight tile) the sums of its
-        // columns, straight into its idle ring, and take the sums of ours
+        // columns, straight into its idle ring, and take the sums of ours;
+        // group grp sends its share of them
         const uint32_t other = crank ^ 2u;
-        const int obeg = static_cast<int>(half ^ 1u) * (BN / 2);
-        if (r == 0) mbar_arrive_remote(mapa_shared(smem_u32(&split_rdy), other));
+        const int obeg = static_cast<int>(half ^ 1u) * (BN / 2) + grp * gw;
+        if (et == 0) mbar_arrive_remote(mapa_shared(smem_u32(&split_rdy), other));
         bool ok = mbar_wait_cluster(&split_rdy, 0, &abort_flag);
         if (ok) {
-          const uint32_t dst = mapa_shared(smem_u32(smem), other) + static_cast<uint32_t>(r) * 4u;
+          const uint32_t dst = mapa_shared(smem_u32(smem), other) + static_cast<uint32_t>(grp * gw * 128 + r) * 4u;
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+          for (int c0 = 0; c0 < gw; c0 += 16) {
             float v[16];
             tmem_ld16(tb + obeg + c0, v);
 #pragma unroll
@@ -1202,16 +1347,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           abort_flag = 1;
           latch_status(a.status, kDevTimeout);
         }
-        epi_bar();
-        if (r == 0) esh.flag = abort_flag;
-        epi_bar();
-        if (esh.flag) break;
-        speer = reinterpret_cast<const float*>(smem);
+        epi_bar_all();
+        if (et == 0) esh.flag[0] = abort_flag;
+        epi_bar_all();
+        if (esh.flag[0]) break;
+        speer = reinterpret_cast<const float*>(smem) + (gcb - cbeg) * 128;
       }
-      // a pair's second weight tile past N (odd tile count) has no rows to store
-      if (tn < a.n_tiles)
-        epilogue_tile<BN, EC>(a, rg, e, g, t, g, g, tb, r, esh, stg, pre, rpre, cbeg, cend, speer);
-      if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, KS * 2 * pair_tiles);
+      if constexpr (SK) {
+        // a pair's second weight tile past N (odd tile count) has no rows: no
+        // partial, no ticket, nothing to finish
+        bool finish = false;
+        int first = pair, last = pair;
+        const long long tu0 = static_cast<long long>(pt) * kb;
+        if (tn < a.n_tiles) {
+          finish = seg_u == tu0 && seg_end == tu0 + kb;
+          if (!finish) {
+            // park this segment's partial sum in the CTA's slot, then take a ticket
+            const int side = (seg_u == su0) ? 0 : 1;
+            park_partial<BN>(tb, a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems + r, gcb, gce);
+            first = cta_of(tu0, a);
+            last = cta_of(tu0 + kb - 1, a);
+            __threadfence();
+            epi_bar_all();
+            if (et == 0) {
+              const int tk = atomicAdd(a.tickets + t, 1);
+              esh.flag[0] = (tk == last - first);
+              if (tk == last - first) a.tickets[t] = 0;
+            }
+            epi_bar_all();
+            finish = esh.flag[0] != 0;
+            if (finish) __threadfence();
+          }
+        }
+        if (finish) {
+          epilogue_tile<BN, EC, kEpiGroups>(a, rg, e, pair, t, first, last, tb, r, esh, gstg, 0u, rpre, gcb, gce,
+                                            nullptr, tu0, 2, static_cast<int>(member), grp);
+          if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, kEpiGroups * a.n_tiles * a.m_tiles, grp);
+        }
+      } else {
+        // a pair's second weight tile past N (odd tile count) has no rows to store
+        if (tn < a.n_tiles)
+          epilogue_tile<BN, EC, kEpiGroups>(a, rg, e, g, t, g, g, tb, r, esh, gstg, pre, rpre, gcb, gce, speer,
+                                            static_cast<long long>(t) * kb, 1, 0, grp);
+        if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, kEpiGroups * KS * 2 * pair_tiles, grp);
+      }
       // hand the accumulator back to the pair's first CTA's MMA thread
       tc_fence_before();
       __syncwarp();
@@ -1228,24 +1407,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
 }
 
+template <int EC, int MODE>
+cudaError_t launch_pair_mode(const AMaps& amaps, const ARegions& rg, const CUtensorMap& xmap, const GemmArgs& a,
+                             const GemmEpi& e, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t err = cudaFuncSetAttribute(gemm_pair_kernel<EC, MODE>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::kSmem);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  return launch_pdl_cluster(gemm_pair_kernel<EC, MODE>, dim3(a.grid), dim3(kPairThreads), PairCfg::kSmem,
+                            MODE == 2 ? 4 : 2, stream, amaps, xmap, a, rg, e);
+}
+
 template <int EC>
 cudaError_t launch_pair(const AMaps& amaps, const ARegions& rg, const CUtensorMap& xmap, const GemmArgs& a,
                         const GemmEpi& e, cudaStream_t stream) {
-  static bool attr_set[2] = {false, false};
-  const int ks = a.pair == 2 ? 1 : 0;
-  if (!attr_set[ks]) {
-    cudaError_t err = ks ? cudaFuncSetAttribute(gemm_pair_kernel<EC, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                PairCfg::kSmem)
-                         : cudaFuncSetAttribute(gemm_pair_kernel<EC, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                PairCfg::kSmem);
-    if (err != cudaSuccess) return err;
-    attr_set[ks] = true;
-  }
-  if (ks)
-    return launch_pdl_cluster(gemm_pair_kernel<EC, 2>, dim3(a.grid), dim3(kThreads), PairCfg::kSmem, 4, stream, amaps,
-                              xmap, a, rg, e);
-  return launch_pdl_cluster(gemm_pair_kernel<EC, 1>, dim3(a.grid), dim3(kThreads), PairCfg::kSmem, 2, stream, amaps,
-                            xmap, a, rg, e);
+  if (a.pair == 2) return launch_pair_mode<EC, 2>(amaps, rg, xmap, a, e, stream);
+  if (a.pair == 3) return launch_pair_mode<EC, 3>(amaps, rg, xmap, a, e, stream);
+  return launch_pair_mode<EC, 1>(amaps, rg, xmap, a, e, stream);
 }
 
 template <int BN, int EC>

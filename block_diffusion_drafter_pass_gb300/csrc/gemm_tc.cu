@@ -58,9 +58,20 @@ bool pair_split_ok(int M, int N, int K, int num_sms) {
 int gemm_pair_mode(int M, int N, int K, int splits, int num_sms) {
   if (splits != 0 || M <= 128 || K < 1) return 0;
   if (pair_split_ok(M, N, K, num_sms)) return 2;
-  const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + 255) / 256);
+  const long long nt = (N + kTileN - 1) / kTileN;
+  const long long tiles = nt * ((M + 255) / 256);
   if (2 * tiles <= num_sms && (K + kTileK - 1) / kTileK >= 2) return 0;   // single-CTA cluster split
-  return pair_tiles_ok(M, N, num_sms) ? 1 : 0;
+  if (!pair_tiles_ok(M, N, num_sms)) return 0;
+  // Round-robin pairs leave (rounds x pairs - pair tiles) pair slots idle.
+  // Stream-K over the pairs gives every pair the same MMA work, but each
+  // split tile costs a partial tile written by one CTA and read back by the
+  // finishing one (about as long as the epilogue itself), so it is taken only
+  // when round-robin would keep under 60% of the pairs busy (one full round
+  // and a short second one: the fused K/V projection of 5 layers at 512
+  // tokens).
+  const long long pt = ((nt + 1) / 2) * ((M + 255) / 256), pairs = num_sms / 2;
+  const long long rounds = (pt + pairs - 1) / pairs;
+  return rounds > 1 && static_cast<double>(pt) / static_cast<double>(rounds * pairs) < 0.6 ? 3 : 1;
 }
 
 bool gemm_cluster_split(int M, int N, int K, int splits, int num_sms) {
@@ -86,6 +97,10 @@ int gemm_grid(int M, int N, int K, int splits, size_t partial_elems, int num_sms
   if (const int pm = gemm_pair_mode(M, N, K, splits, num_sms)) {
     const long long pair_tiles = static_cast<long long>(((N + kTileN - 1) / kTileN + 1) / 2) * ((M + BN - 1) / BN);
     if (pm == 2) return static_cast<int>(4 * pair_tiles);
+    // stream-K pairs need two 128 x 256 partial slots per CTA; without room
+    // for them the pairs take whole tiles round-robin
+    if (pm == 3 && static_cast<long long>(num_sms / 2) * 2 * 2 * kTileN * BN <= static_cast<long long>(partial_elems))
+      return static_cast<int>(2 * std::min<long long>(pair_tiles * kb, num_sms / 2));
     return static_cast<int>(2 * std::min<long long>(pair_tiles, num_sms / 2));
   }
   const long long units = tiles * kb;
@@ -124,6 +139,18 @@ cudaError_t launch_gemm(const AMaps& amaps, const ARegions& regions, const CUten
   a.grid = gemm_grid(M, N, K, splits, work.partial_elems, num_sms);
   a.csplit = gemm_cluster_split(M, N, K, splits, num_sms) ? 1 : 0;
   a.pair = gemm_pair_mode(M, N, K, splits, num_sms);
+  a.workers = a.grid;
+  if (a.pair == 3) {
+    const long long tiles = static_cast<long long>(a.n_tiles) * a.m_tiles;
+    const long long pair_tiles = static_cast<long long>((a.n_tiles + 1) / 2) * a.m_tiles;
+    const bool room = static_cast<size_t>(a.grid) * 2 * kTileN * BN <= work.partial_elems && tiles <= work.n_tickets;
+    if (room) {
+      a.workers = a.grid / 2;
+      a.units = pair_tiles * a.k_blocks;
+    } else {
+      a.pair = 1;   // gemm_grid chose the round-robin grid for this case
+    }
+  }
   // the pair exchange addresses a 128 x 128 float block of the peer's ring
   // (BN = 256) and pairs CTAs 2t, 2t + 1
   if (a.csplit && (BN != 256 || a.grid != 2 * a.n_tiles * a.m_tiles)) return cudaErrorInvalidValue;

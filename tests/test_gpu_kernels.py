@@ -41,6 +41,8 @@ DEV = "cuda:0"
     (24576, 512, 512, 0),     # CTA pairs, pair tiles dealt round-robin (3 rounds)
     (4992, 512, 256, 0),      # CTA pairs, odd weight-tile count (last pair half empty)
     (5120, 300, 320, 0),      # CTA pairs, ragged token tail in the second CTA's half
+    (10240, 512, 512, 0),     # 80 pair tiles on 76 pairs: stream-K over the pairs (split tiles finished by tickets)
+    (10112, 300, 1024, 0),    # stream-K pairs, odd weight-tile count and a ragged token tail
 ])
 def test_gemm_matches_fp32_matmul(dfl, N, M, K, splits):
     g = torch.Generator(device="cpu").manual_seed(N * 7 + M * 3 + K)

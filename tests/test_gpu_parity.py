@@ -475,3 +475,34 @@ def test_qwen3_8b_batch32_serving_lengths(dfl):
         anchors = make_anchor_ids_np(n, shape.vocab, seed=190)
         _, _, checked = _draft_and_compare(d, orc, list(range(n)), anchors, 16, "8B 2-layer batch 32 U[1024, 8192]")
         assert checked > 0
+
+
+def test_kv_append_512_rows_stream_k_pairs(dfl):
+    """A 512-row append into 5 layers of 8 key/value heads of d = 128 (the 8B
+    drafter's K/V width on a narrow hidden size): the fused K/V projection
+    has 80 pair tiles for 76 SM pairs, so the pairs split them stream-K and
+    the split tiles are finished by whichever CTA takes the last ticket. The
+    cached K/V of every layer, at page-aligned and odd slot offsets, and a
+    batch-32 draft over them are compared with the oracle."""
+    from dataclasses import replace
+    sh = replace(TINY, n_heads=8, n_kv_heads=8, head_dim=128, n_layers=5)
+    wn = make_weights_np(sh, seed=201, gamma="jitter", std=0.05)
+    orc = oracle.OracleDrafter(sh, wn, dtype=np.float32)
+    width = sh.n_feat_layers * sh.hidden
+    n = 32
+    with dfl.Drafter(sh, np_weights_to_device(wn, DEV), max_seqs=n, max_batch=n, max_block=16, max_ctx=512,
+                     max_fuse_tokens=8192) as d:
+        rng = np.random.default_rng(202)
+        lens = [int(x) for x in rng.integers(0, 150, size=n)]   # odd and even first slots of the append
+        f = make_features_np(sum(lens), width, seed=203)
+        d.fuse_ctx(list(range(n)), lens, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(list(range(n)), lens, f, pending=False)
+        f = make_features_np(16 * n, width, seed=204)
+        d.fuse_ctx(list(range(n)), [16] * n, bf16_dev(f, DEV), pending=False)
+        orc.fuse_ctx(list(range(n)), [16] * n, f, pending=False)
+        d.sync()
+        _check_kv(d, orc, range(n), range(sh.n_layers), "512-row append", ROW_REL_HIGH_GAIN)
+        anchors = make_anchor_ids_np(n, sh.vocab, seed=205)
+        _, _, c = _draft_and_compare(d, orc, list(range(n)), anchors, 16, "batch 32 after a stream-K append",
+                                     ROW_REL_HIGH_GAIN)
+        assert c > 0
