@@ -398,3 +398,49 @@ def test_kv_quant_mistakes_are_caught(monkeypatch, kind):
         qp.test_decode_error_bound()
         qp.test_zero_blocks_and_symmetry()
     _expect_failure(pins)
+
+
+# ----------------------------------------------------------------------------
+# target pass
+# ----------------------------------------------------------------------------
+from oracle import target_pass as otp
+from tests import test_target_pass_pins as tpins
+
+
+@pytest.mark.parametrize("kind", ["off_by_one", "non_causal"])
+def test_target_causal_mask_mistakes_are_caught(monkeypatch, kind):
+    orig = otp.causal_block_attention
+
+    def bad(q, k, v, n_ctx):
+        if kind == "non_causal":
+            return od.block_attention(q, k, v)
+        # each block position misses its own key (keeps at least one key)
+        B = q.shape[0]
+        out = np.empty_like(q)
+        for j in range(B):
+            lim = max(1, n_ctx + j)
+            out[j:j + 1] = orig(q[j:j + 1], k[:lim], v[:lim], lim - 1)
+        return out
+    monkeypatch.setattr(otp, "causal_block_attention", bad)
+    _expect_failure(tpins.test_causal_attention_matches_explicit_loops)
+    _expect_failure(tpins.test_target_pass_matches_scalar_brute_force)
+
+
+def test_target_feature_layers_zero_based_reading_is_caught(monkeypatch):
+    orig = otp.feature_layers
+    monkeypatch.setattr(otp, "feature_layers", lambda n, f: [l + 1 for l in orig(n, f)])
+    _expect_failure(tpins.test_feature_layers_match_the_setup_table)
+
+
+def test_target_caching_unrotated_keys_is_caught(monkeypatch):
+    orig = otp.target_layer
+
+    def bad(x, layer, k_ctx, v_ctx, pos0, shape):
+        x2, k, v = orig(x, layer, k_ctx, v_ctx, pos0, shape)
+        B = x.shape[0]
+        h = od.rms_norm(x, layer["g_attn"], shape.rms_eps)
+        k_raw = (h @ layer["w_k"].T).reshape(B, shape.n_kv_heads, shape.head_dim)
+        return x2, k_raw, v
+    monkeypatch.setattr(otp, "target_layer", bad)
+    _expect_failure(tpins.test_block_pass_equals_one_token_passes)
+    _expect_failure(tpins.test_target_pass_matches_scalar_brute_force)
