@@ -30,7 +30,7 @@ EXPORTED = (
     "dflash_draft_sample", "dflash_sample_filter", "dflash_verify_sample",
     "dflash_block_sched_create", "dflash_block_sched_destroy", "dflash_block_sched_observe",
     "dflash_block_sched_set_cost", "dflash_block_sched_expected_tau", "dflash_block_sched_choose",
-    "dflash_debug_wait_timeout",
+    "dflash_debug_wait_timeout", "dflash_target_feature_layers", "dflash_target_create", "dflash_target_forward",
 )
 SAMPLE_WIDTH = 32   # DFLASH_SAMPLE_WIDTH
 
@@ -110,6 +110,9 @@ def load_library() -> ctypes.CDLL:
         "dflash_block_sched_expected_tau": ([VP, I, P(ctypes.c_double)], I),
         "dflash_block_sched_choose": ([VP, P(I)], I),
         "dflash_debug_wait_timeout": ([VP, I, VP], I),
+        "dflash_target_feature_layers": ([I, I, i32p], I),
+        "dflash_target_create": ([P(dflash_config), P(dflash_weights), i32p, P(VP)], I),
+        "dflash_target_forward": ([VP, i32p, I, VP, I, I, VP, VP, VP], I),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -226,13 +229,15 @@ class Drafter:
     """
 
     def __init__(self, shape, weights, *, max_seqs: int = 4, max_batch: int = 4, max_block: int = 16,
-                 max_ctx: int = 4096, max_pages: Optional[int] = None, max_fuse_tokens: int = 1024):
+                 max_ctx: int = 4096, max_pages: Optional[int] = None, max_fuse_tokens: int = 1024,
+                 _feat_layers=None):
         import torch
         lib = load_library()
         self.shape = shape
         self._weights = weights  # keep the borrowed tensors alive
-        for t in [weights[k] for k in ("w_c", "g_c", "embed", "lm_head", "g_final")] + \
-                 [v for lw in weights["layers"] for v in lw.values()]:
+        top = ("embed", "lm_head", "g_final") if _feat_layers is not None else ("w_c", "g_c", "embed", "lm_head",
+                                                                                "g_final")
+        for t in [weights[k] for k in top] + [v for lw in weights["layers"] for v in lw.values()]:
             if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
                 raise DFlashError(DFLASH_EINVAL, "weights must be contiguous bf16 CUDA tensors")
         if max_pages is None:
@@ -246,12 +251,16 @@ class Drafter:
             layers[i] = dflash_layer_weights(*[_ptr(lw[k]) for k in ("w_q", "w_k", "w_v", "w_o", "w_gate",
                                                                       "w_up", "w_down", "g_attn", "g_ffn")])
         self._layers = layers
-        w = dflash_weights(_ptr(weights["w_c"]), _ptr(weights["g_c"]), _ptr(weights["embed"]),
+        w = dflash_weights(_ptr(weights.get("w_c")), _ptr(weights.get("g_c")), _ptr(weights["embed"]),
                            _ptr(weights["lm_head"]), _ptr(weights["g_final"]), layers)
         ctx = ctypes.c_void_p()
-        _check(lib.dflash_create(ctypes.byref(self.cfg), ctypes.byref(w), ctypes.byref(ctx)), None)
+        if _feat_layers is None:
+            _check(lib.dflash_create(ctypes.byref(self.cfg), ctypes.byref(w), ctypes.byref(ctx)), None)
+        else:
+            _check(lib.dflash_target_create(ctypes.byref(self.cfg), ctypes.byref(w), _i32(_feat_layers),
+                                            ctypes.byref(ctx)), None)
         self.ctx = ctx
-        self.device = weights["w_c"].device
+        self.device = weights["embed"].device
 
     # lifecycle ---------------------------------------------------------------
     def close(self) -> None:
@@ -433,3 +442,52 @@ class Drafter:
         _check(load_library().dflash_debug_last_selection(self.ctx, cand.ctypes.data, u.ctypes.data,
                                                           sc.ctypes.data), self.ctx)
         return cand[:rows], u[:rows], sc[:rows]
+
+
+def target_feature_layers(n_layers: int, n_feat: int = 5):
+    """The library's default feature layers (0-based) of an n_layers target."""
+    out = (ctypes.c_int32 * n_feat)()
+    _check(load_library().dflash_target_feature_layers(n_layers, n_feat, out), None)
+    return [int(x) for x in out]
+
+
+class Target(Drafter):
+    """A target context (dflash_target_create): the causal verify pass that
+    caches its own K/V and hands its feature layers' outputs to the drafter.
+    `shape.n_feat_layers` is the number of feature layers; `weights` as for
+    Drafter without w_c and g_c. dflash_verify, seq_len, read_kv and the
+    other inspection hooks work as on a Drafter."""
+
+    def __init__(self, shape, weights, feat_layers=None, *, max_seqs: int = 4, max_batch: int = 4,
+                 max_block: int = 16, max_ctx: int = 4096, max_pages: Optional[int] = None):
+        if feat_layers is None:
+            feat_layers = target_feature_layers(shape.n_layers, shape.n_feat_layers)
+        self.feat_layers = list(feat_layers)
+        super().__init__(shape, weights, max_seqs=max_seqs, max_batch=max_batch, max_block=max_block,
+                         max_ctx=max_ctx, max_pages=max_pages, max_fuse_tokens=1, _feat_layers=self.feat_layers)
+
+    def forward(self, seq_ids, block_ids, B: int, pending: bool, out=None, feats=None, want_feats: bool = True,
+                stream=None):
+        """One causal pass over block_ids [n, B] (int32 CUDA). Returns
+        (target ids [n, B], features [n * B, n_feat * H] bf16 or None)."""
+        import torch
+        n = len(seq_ids)
+        assert block_ids.dtype == torch.int32 and block_ids.is_cuda and block_ids.is_contiguous()
+        if out is None:
+            out = torch.empty(n, B, dtype=torch.int32, device=self.device)
+        if feats is None and want_feats and self.feat_layers:
+            feats = torch.empty(n * B, len(self.feat_layers) * self.shape.hidden, dtype=torch.bfloat16,
+                                device=self.device)
+        _check(load_library().dflash_target_forward(self.ctx, _i32(seq_ids), n, _ptr(block_ids), B,
+                                                    1 if pending else 0, _ptr(out), _ptr(feats), _stream(stream)),
+               self.ctx)
+        return out, feats
+
+    def last_pass(self, n_seq: int, B: int):
+        """(final residual stream [n_seq*B, H] fp32, winning logit of every
+        block position [n_seq*B] fp32) of the last forward."""
+        import numpy as np
+        hid = np.empty((n_seq * B, self.shape.hidden), dtype=np.float32)
+        top = np.empty(n_seq * B, dtype=np.float32)
+        _check(load_library().dflash_debug_last_draft(self.ctx, hid.ctypes.data, top.ctypes.data), self.ctx)
+        return hid, top

@@ -1,9 +1,11 @@
-// attention.cu - non-causal block attention over the injected context.
+// attention.cu - block attention over the injected context (non-causal, the
+// drafter) or over the target's own cache (causal within the block).
 //
 // For each sequence and kv head, the G*B query rows of the block (G query
 // heads per kv head, B block positions) attend to every committed context key
-// of that layer (paged, 64 tokens per page) and to the block's own B keys,
-// with no mask (the drafter's attention is non-causal).
+// of that layer (paged, 64 tokens per page) and to the block's own B keys:
+// all of them in the drafter's non-causal pass; keys 0..j of the block for
+// block position j in the target's causal pass (AttnArgs::causal).
 //
 // The keys are split into chunks of whole 64-key tiles (flash-decoding). A
 // persistent grid, one CTA per SM, runs the (sequence, kv head, chunk) work
@@ -566,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = SPREAD ? (lane >> 4) : 0;             // which unit of the step (SPREAD)
     const int row = SPREAD ? quarter * 16 + (lane & 15) : quarter * 32 + lane;   // query row r
     const bool active = (SPREAD ? quarter * 16 : quarter * 32) < R;              // warp-uniform
+    const int jq = row / G;                                                     // block position of row r
     const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t o_tmem = lane_tmem + C::kOCol;
     const float sl2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));   // log2(e)/sqrt(d)
@@ -664,8 +667,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = decode(rk);
       const int ns = (it.te - it.tb + 1) >> 1;
       const int len = s_len[it.i], nctx = s_nctx[it.i];
-      auto unit_valid = [&](int t) {   // valid keys of unit t (0 if absent)
-        return t >= it.te ? 0 : (t < nctx ? min(kKeyTile, len - t * kKeyTile) : B);
+      // valid keys of unit t (0 if absent); causal: block position jq sees
+      // the block's keys 0..jq (at least one, so a unit present is present
+      // for every lane and the TMEM loads below stay warp-uniform)
+      auto unit_valid = [&](int t) {
+        return t >= it.te ? 0 : (t < nctx ? min(kKeyTile, len - t * kKeyTile) : (a.causal ? min(B, jq + 1) : B));
       };
       float m_run = -INFINITY, l_run = 0.f;   // l_run: this thread's share of the row sum
       for (int j = 0; j < ns; ++j) {

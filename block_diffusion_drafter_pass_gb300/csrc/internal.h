@@ -51,6 +51,7 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 constexpr int kPage = 64;          // tokens per KV page
 constexpr int kMaxBatch = 64;      // sequences per call
 constexpr int kMaxBlock = 32;      // block size B
+constexpr int kMaxTargetLayers = 64;   // layers of a target context
 constexpr int kMaxAMaps = 12;      // weight tensor maps per GEMM launch
 
 // device status bits (dflash_sync maps them to ETIMEOUT / EDEVICE)
@@ -195,6 +196,7 @@ struct AttnArgs {
   int max_chunks;            // host bound on the chunks of one (sequence, kv head) row
   int rows_pad;              // row stride of the partial buffers (>= G*B)
   int spread;                // 1: G*B <= 64, query rows spread 16 per TMEM lane quarter
+  int causal;                // 1: block position j sees block keys 0..j only (target pass)
   const uint16_t* q;         // [n_seq*B][n_q*d] bf16 (RoPE applied)
   const uint16_t* pool;      // the KV pool (read directly only for L2 prefetches)
   float* part_o;             // [items][rows_pad][d]
@@ -233,8 +235,14 @@ int attention_ctas_per_sm(int head_dim);   // resident attention CTAs per SM
 // Small kernels
 // ----------------------------------------------------------------------------
 // Block embedding: x (fp32), hg = bf16(x * gain), ss[m] = sum(x^2).
-cudaError_t launch_embed(const uint16_t* embed, const int32_t* anchors, int mask_id, int vocab, const SeqMeta& meta,
-                         int H, const uint16_t* gain, float* x, uint16_t* hg, float* ss, int* status, cudaStream_t s);
+cudaError_t launch_embed(const uint16_t* embed, const int32_t* anchors, int mask_id, const int32_t* ids, int vocab,
+                         const SeqMeta& meta, int H, const uint16_t* gain, float* x, uint16_t* hg, float* ss,
+                         int* status, cudaStream_t s);
+// Target pass: one layer's block keys/values appended to the pool at len + j.
+cudaError_t launch_block_kv_append(const SeqMeta& meta, SeqState st, int layer, const uint16_t* kb, const uint16_t* vb,
+                                   uint16_t* pool, int pool_pages, int n_kv, int d, int* status, cudaStream_t s);
+// Target pass: x [M][H] fp32 -> bf16 columns col0.. of feature rows of pitch ld.
+cudaError_t launch_feat_copy(const float* x, int M, int H, uint16_t* feats, int ld, int col0, cudaStream_t s);
 cudaError_t launch_verify(const SeqMeta& meta, SeqState st, const int32_t* drafts, const int32_t* targets,
                           int32_t* tau, int32_t* bonus, cudaStream_t s);
 cudaError_t launch_fuse_advance(const SeqMeta& meta, SeqState st, int pending, cudaStream_t s);

@@ -149,6 +149,13 @@ struct dflash_ctx {
   cudaEvent_t snap_event = nullptr;
   bool snap_pending = false;
 
+  // target mode (dflash_target_create): a causal pass over caller ids that
+  // caches its own K/V; feat_slot[l] = index of layer l among the feature
+  // layers, or -1
+  bool target = false;
+  std::vector<int> feat_slot;
+  int n_feat = 0;
+
   int last_rows = 0, last_draft_rows = 0, last_sel_rows = 0;
   int attn_ctas_per_sm = 0;
   std::string err = "no error";
@@ -362,12 +369,22 @@ dflash_status dflash_destroy(dflash_ctx* ctx) {
   return DFLASH_OK;
 }
 
-dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w, dflash_ctx** out) {
+}  // extern "C"
+
+namespace {
+
+// feat_layers == nullptr: a drafter context; otherwise a target context whose
+// cfg->n_feat_layers feature layers are feat_layers[0 ..] (0-based, strictly
+// increasing); the fusion weights are not used.
+dflash_status create_impl(const dflash_config* cfg_in, const dflash_weights* w, const int32_t* feat_layers,
+                          dflash_ctx** out) {
   dflash_ctx* ctx = nullptr;
   if (!out) return fail(nullptr, DFLASH_EINVAL, "out is null");
   *out = nullptr;
   if (!cfg_in || !w || !w->layers) return fail(nullptr, DFLASH_EINVAL, "null config or weights");
-  const dflash_config c = *cfg_in;
+  dflash_config c = *cfg_in;
+  const bool target = feat_layers != nullptr;
+  if (target) c.max_fuse_tokens = 1;   // no fusion in a target context
   const int d = c.head_dim;
   if (c.hidden < 64 || c.hidden % 64) return fail(nullptr, DFLASH_EINVAL, "hidden must be a positive multiple of 64");
   if (d != 64 && d != 128) return fail(nullptr, DFLASH_EINVAL, "head_dim must be 64 or 128");
@@ -377,8 +394,15 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
     return fail(nullptr, DFLASH_EINVAL, "n_heads*d and n_kv_heads*d must be multiples of 128");
   if (c.ffn < 8 || c.ffn % 8) return fail(nullptr, DFLASH_EINVAL, "ffn must be a positive multiple of 8");
   if (c.vocab < 2 || c.mask_id < 0 || c.mask_id >= c.vocab) return fail(nullptr, DFLASH_EINVAL, "bad vocab/mask_id");
-  if (c.n_layers < 1 || c.n_layers > 16 || c.n_feat_layers < 1 || c.n_feat_layers > 16)
+  if (!target && (c.n_layers < 1 || c.n_layers > 16 || c.n_feat_layers < 1 || c.n_feat_layers > 16))
     return fail(nullptr, DFLASH_EINVAL, "n_layers and n_feat_layers must be in 1..16");
+  if (target) {
+    if (c.n_layers < 1 || c.n_layers > kMaxTargetLayers || c.n_feat_layers < 0 || c.n_feat_layers > 16)
+      return fail(nullptr, DFLASH_EINVAL, "target: n_layers must be in 1..64 and n_feat_layers in 0..16");
+    for (int k = 0; k < c.n_feat_layers; ++k)
+      if (feat_layers[k] < 0 || feat_layers[k] >= c.n_layers || (k > 0 && feat_layers[k] <= feat_layers[k - 1]))
+        return fail(nullptr, DFLASH_EINVAL, "target: feature layers must be increasing layer indices");
+  }
   if (c.max_batch < 1 || c.max_batch > kMaxBatch) return fail(nullptr, DFLASH_EINVAL, "max_batch must be in 1..64");
   if (c.max_block < 1 || c.max_block > kMaxBlock) return fail(nullptr, DFLASH_EINVAL, "max_block must be in 1..32");
   if ((c.n_heads / c.n_kv_heads) * c.max_block > 128)
@@ -390,7 +414,7 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
   // the pool is also read as rows of 64 elements (transposed values)
   if (pool_rows * (d / 64) >= (1LL << 31))
     return fail(nullptr, DFLASH_EINVAL, "KV pool too large for 32-bit TMA coordinates");
-  const void* ptrs[] = {w->w_c, w->g_c, w->embed, w->lm_head, w->g_final};
+  const void* ptrs[] = {w->embed, w->lm_head, w->g_final, target ? w->embed : w->w_c, target ? w->embed : w->g_c};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return fail(nullptr, DFLASH_EINVAL, "weight pointer null or not 16-byte aligned");
   for (int l = 0; l < c.n_layers; ++l) {
@@ -403,6 +427,12 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
 
   ctx = new dflash_ctx();
   ctx->cfg = c;
+  ctx->target = target;
+  ctx->feat_slot.assign(c.n_layers, -1);
+  if (target) {
+    ctx->n_feat = c.n_feat_layers;
+    for (int k = 0; k < c.n_feat_layers; ++k) ctx->feat_slot[feat_layers[k]] = k;
+  }
   ctx->layers.assign(w->layers, w->layers + c.n_layers);
   ctx->w = *w;
   ctx->w.layers = ctx->layers.data();
@@ -491,7 +521,7 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
   // weight descriptors (box 64 K-elements x 64 rows)
   const int wb = kWeightBoxRows;
   bool ok = encode_2d(&ctx->m_lm, w->lm_head, c.vocab, H, wb) &&
-            encode_2d(&ctx->m_wc, w->w_c, H, static_cast<uint64_t>(c.n_feat_layers) * H, wb) &&
+            (target || encode_2d(&ctx->m_wc, w->w_c, H, static_cast<uint64_t>(c.n_feat_layers) * H, wb)) &&
             encode_2d(&ctx->m_pool, ctx->pool, pool_rows, d, 64) &&
             encode_2d(&ctx->m_pool_vt, ctx->pool, static_cast<uint64_t>(pool_rows) * (d / 64), 64, 64) &&
             encode_2d(&ctx->m_vblk, ctx->vb, static_cast<uint64_t>(c.max_batch) * nkv * d, 64, 64);
@@ -524,6 +554,32 @@ dflash_status dflash_create(const dflash_config* cfg_in, const dflash_weights* w
   ctx->added_since.assign(c.max_seqs, 0);
   *out = ctx;
 #undef CA
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dflash_status dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_ctx** out) {
+  return create_impl(cfg, w, nullptr, out);
+}
+
+dflash_status dflash_target_create(const dflash_config* cfg, const dflash_weights* w, const int32_t* feat_layers,
+                                   dflash_ctx** out) {
+  static const int32_t none = 0;
+  if (cfg && cfg->n_feat_layers > 0 && !feat_layers) return fail(nullptr, DFLASH_EINVAL, "feat_layers is null");
+  return create_impl(cfg, w, feat_layers ? feat_layers : &none, out);
+}
+
+dflash_status dflash_target_feature_layers(int n_layers, int n_feat, int32_t* out) {
+  if (n_layers < 5 || n_feat < 1 || n_feat > 16 || !out || n_feat > n_layers - 3) return DFLASH_EINVAL;
+  // uniformly spaced from layer 2 to the third-to-last (1-based), to the nearest layer
+  const int first = 2, last = n_layers - 2;
+  for (int k = 0; k < n_feat; ++k) {
+    const double pos = n_feat == 1 ? first : first + k * static_cast<double>(last - first) / (n_feat - 1);
+    out[k] = static_cast<int32_t>(std::floor(pos + 0.5)) - 1;
+  }
   return DFLASH_OK;
 }
 
@@ -577,6 +633,7 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
                               const uint16_t* feats, int pending, void* stream_v) {
   ApiRange nvtx_range("dflash_fuse_ctx");
   if (!ctx) return DFLASH_EINVAL;
+  if (ctx->target) return fail(ctx, DFLASH_EINVAL, "a target context has no fusion (its pass caches its own K/V)");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const dflash_config& c = ctx->cfg;
   SeqMeta meta;
@@ -760,8 +817,18 @@ dflash_status check_sampling(dflash_ctx* ctx, float temperature, int top_k, floa
   return DFLASH_OK;
 }
 
+// Target pass (dflash_target_forward): the block is the caller's ids, the
+// attention causal, the block's K/V appended to the context's own pool, the
+// argmax taken at every block position, the feature layers' outputs copied.
+struct TargetReq {
+  const int32_t* block_ids;   // device [n_seq * B]
+  int pending;
+  int32_t* target_ids;        // device [n_seq * B]
+  uint16_t* feats;            // device [n_seq * B][n_feat * H] or null
+};
+
 dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids, int B,
-                         int32_t* draft_ids, void* stream_v, const SampleReq* samp);
+                         int32_t* draft_ids, void* stream_v, const SampleReq* samp, const TargetReq* tgt = nullptr);
 
 }  // namespace
 
@@ -769,6 +836,14 @@ dflash_status dflash_draft(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, c
                            int32_t* draft_ids, void* stream_v) {
   ApiRange nvtx_range("dflash_draft");
   return draft_impl(ctx, seq_ids, n_seq, anchor_ids, B, draft_ids, stream_v, nullptr);
+}
+
+dflash_status dflash_target_forward(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* block_ids, int B,
+                                    int pending, int32_t* target_ids, uint16_t* feats, void* stream_v) {
+  ApiRange nvtx_range("dflash_target_forward");
+  if (!ctx) return DFLASH_EINVAL;
+  TargetReq t{block_ids, pending, target_ids, feats};
+  return draft_impl(ctx, seq_ids, n_seq, nullptr, B, nullptr, stream_v, nullptr, &t);
 }
 
 dflash_status dflash_draft_sample(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids,
@@ -789,7 +864,7 @@ dflash_status dflash_draft_sample(dflash_ctx* ctx, const int32_t* seq_ids, int n
 namespace {
 
 dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, const int32_t* anchor_ids, int B,
-                         int32_t* draft_ids, void* stream_v, const SampleReq* samp) {
+                         int32_t* draft_ids, void* stream_v, const SampleReq* samp, const TargetReq* tgt) {
   if (!ctx) return DFLASH_EINVAL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const dflash_config& c = ctx->cfg;
@@ -797,15 +872,70 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
   dflash_status st = check_seqs(ctx, seq_ids, n_seq, &meta);
   if (st != DFLASH_OK) return st;
   if (B < 1 || B > c.max_block) return fail(ctx, DFLASH_EINVAL, "B out of range");
+  if ((tgt != nullptr) != ctx->target)
+    return fail(ctx, DFLASH_EINVAL, ctx->target ? "a target context runs dflash_target_forward"
+                                                : "dflash_target_forward needs a target context");
   meta.B = B;
   if (n_seq == 0) return DFLASH_OK;
-  if (!anchor_ids || (B > 1 && !draft_ids)) return fail(ctx, DFLASH_EINVAL, "null anchor_ids or draft_ids");
+  if (tgt) {
+    if (!tgt->block_ids || !tgt->target_ids) return fail(ctx, DFLASH_EINVAL, "null block_ids or target_ids");
+    if (tgt->feats && (!aligned16(tgt->feats) || ctx->n_feat == 0))
+      return fail(ctx, DFLASH_EINVAL, "feats not 16-byte aligned, or no feature layers");
+    if (tgt->pending != 0 && tgt->pending != 1) return fail(ctx, DFLASH_EINVAL, "pending must be 0 or 1");
+  } else if (!anchor_ids || (B > 1 && !draft_ids)) {
+    return fail(ctx, DFLASH_EINVAL, "null anchor_ids or draft_ids");
+  }
   if (samp && B > 1) {
     st = ensure_logits32(ctx);
     if (st == DFLASH_OK) st = ensure_sample_part(ctx);
     if (st != DFLASH_OK) return st;
   }
   consume_snapshot(ctx, false);
+  if (tgt) {
+    // the block's K/V go to positions len .. len + B - 1: reserve their pages
+    // (all or nothing), as an append of B tokens does
+    for (int i = 0; i < n_seq; ++i) {
+      const int s = meta.slot[i];
+      if (ctx->pend[s]) return fail(ctx, DFLASH_EINVAL, "target pass over a sequence with pending tokens");
+      if (ctx->len_ub[s] + B > c.max_ctx) {
+        consume_snapshot(ctx, true);
+        if (ctx->len_ub[s] + B > c.max_ctx) return fail(ctx, DFLASH_EINVAL, "block would exceed max_ctx");
+      }
+      meta.row0[i] = i * B;
+    }
+    meta.row0[n_seq] = n_seq * B;
+    auto need_pages = [&]() {
+      int need = 0;
+      for (int i = 0; i < n_seq; ++i) {
+        const int s = meta.slot[i];
+        need += std::max(0, ceil_div(ctx->len_ub[s] + B, kPage) - static_cast<int>(ctx->pages[s].size()));
+      }
+      return need;
+    };
+    if (need_pages() > static_cast<int>(ctx->free_pages.size())) {
+      consume_snapshot(ctx, true);
+      if (need_pages() > static_cast<int>(ctx->free_pages.size()))
+        return fail(ctx, DFLASH_ENOMEM, "KV page pool exhausted");
+    }
+    PageUpdates& upd = *ctx->page_upd;
+    upd.n = 0;
+    for (int i = 0; i < n_seq; ++i) {
+      const int s = meta.slot[i];
+      auto& pg = ctx->pages[s];
+      const int want = ceil_div(ctx->len_ub[s] + B, kPage);
+      for (int k = static_cast<int>(pg.size()); k < want; ++k) {
+        pg.push_back(ctx->free_pages.back());
+        ctx->free_pages.pop_back();
+        upd.idx[upd.n] = s * ctx->pages_per_seq + k;
+        upd.page[upd.n] = pg.back();
+        if (++upd.n == kPageUpdMax) {
+          CK(launch_page_updates(upd, ctx->d_page_table, stream));
+          upd.n = 0;
+        }
+      }
+    }
+    CK(launch_page_updates(upd, ctx->d_page_table, stream));
+  }
 
   const int H = c.hidden, d = c.head_dim, nq = c.n_heads, nkv = c.n_kv_heads, F = c.ffn;
   const int M = n_seq * B;
@@ -925,8 +1055,8 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
   const double attn_bytes = ctx_tokens * nkv * d * 4 + 1.0 * M * nkv * d * 4 + 1.0 * M * nq * d * 2;
   {
     ProfScope ps(ctx, DFLASH_K_NORM, stream, 8.0 * M * H, 0);
-    CK(launch_embed(ctx->w.embed, anchor_ids, c.mask_id, c.vocab, meta, H, ctx->layers[0].g_attn, ctx->x, ctx->hg,
-                    ctx->ssA, ctx->d_status, stream));
+    CK(launch_embed(ctx->w.embed, anchor_ids, c.mask_id, tgt ? tgt->block_ids : nullptr, c.vocab, meta, H,
+                    ctx->layers[0].g_attn, ctx->x, ctx->hg, ctx->ssA, ctx->d_status, stream));
   }
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = ctx->layers[l];
@@ -949,6 +1079,10 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
       ProfScope ps(ctx, DFLASH_K_QKV, stream, gemm_bytes(M, nw, H, nw, 2), 2.0 * M * nw * H);
       CK(launch_gemm(am, rg, *hmap_qkv, M, n_qkv, H, 0, e, work, ctx->num_sms, stream));
     }
+    if (tgt) {   // the block's K/V into the target's own cache
+      ProfScope ps(ctx, DFLASH_K_OTHER, stream, 4.0 * M * nkv * d * 2, 0);
+      CK(launch_block_kv_append(meta, ss, l, ctx->kb, ctx->vb, ctx->pool, c.max_pages, nkv, d, ctx->d_status, stream));
+    }
     {  // non-causal attention over the injected context and the block
       AttnArgs a;
       std::memset(&a, 0, sizeof(a));
@@ -964,6 +1098,7 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
       a.items_cap = ctx->items_cap;
       a.rows_pad = 16 * ceil_div((nq / nkv) * B, 16);
       a.spread = (nq / nkv) * B <= 64;
+      a.causal = tgt ? 1 : 0;
       a.q = ctx->q;
       a.pool = ctx->pool;
       a.part_o = ctx->part_o;
@@ -1023,11 +1158,45 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
       ProfScope ps(ctx, DFLASH_K_DOWN, stream, gemm_bytes(M, H, F, H, 10), 2.0 * M * H * F);
       CK(launch_gemm(am, stacked({H}), *fmap, M, H, F, 0, e, work, ctx->num_sms, stream));
     }
+    if (tgt && tgt->feats && ctx->feat_slot[l] >= 0) {   // this layer's output is a feature
+      ProfScope ps(ctx, DFLASH_K_OTHER, stream, 6.0 * M * H, 0);
+      CK(launch_feat_copy(ctx->x, M, H, tgt->feats, ctx->n_feat * H, ctx->feat_slot[l] * H, stream));
+    }
   }
   ctx->last_rows = M;
-  ctx->last_draft_rows = n_seq * (B - 1);
-  ctx->last_sel_rows = ctx->sel_on && !samp ? n_seq * (B - 1) : 0;
-  if (B > 1 && samp) {
+  ctx->last_draft_rows = tgt ? M : n_seq * (B - 1);
+  ctx->last_sel_rows = ctx->sel_on && !samp && !tgt ? n_seq * (B - 1) : 0;
+  if (tgt) {
+    // LM head with the argmax at every block position (final norm folded in)
+    AMaps am;
+    am.m[0] = ctx->m_lm;
+    GemmEpi e = base_epi(ctx, EPI_ARGMAX);
+    e.keys = ctx->keys;
+    e.done = ctx->done;
+    e.out_ids = tgt->target_ids;
+    e.out_logit = ctx->top_logit;
+    e.argmax_skip_B = 0;
+    e.in_ss = ctx->ssA;
+    e.in_ss_parts = parts;
+    e.in_ss_ld = rows_ld;
+    {
+      ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(M, c.vocab, H, 1, 8), 2.0 * M * c.vocab * H);
+      CK(launch_gemm(am, stacked({c.vocab}), *hmap_lm, M, c.vocab, H, 0, e, work, ctx->num_sms, stream));
+    }
+    // the block's tokens become pending (verify commits tau) or committed
+    {
+      ProfScope ps(ctx, DFLASH_K_OTHER, stream, 8.0 * n_seq, 0);
+      CK(launch_fuse_advance(meta, ss, tgt->pending, stream));
+    }
+    for (int i = 0; i < n_seq; ++i) {
+      const int s = meta.slot[i];
+      if (tgt->pending) ctx->pend[s] += B;
+      else {
+        ctx->len_ub[s] += B;
+        ctx->added_since[s] += B;
+      }
+    }
+  } else if (B > 1 && samp) {
     // LM head into fp32 rows (final RMSNorm scale applied), then the 32
     // largest logits of every masked row, the filter and the draw
     const int Md = n_seq * (B - 1);
@@ -1288,6 +1457,7 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
                                        const uint16_t* w_h, int dim, void* stream_v) {
   ApiRange nvtx_range("dflash_set_path_selector");
   if (!ctx) return DFLASH_EINVAL;
+  if (ctx->target) return fail(ctx, DFLASH_EINVAL, "the path selector belongs to a drafter context");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const dflash_config& c = ctx->cfg;
   const int H = c.hidden;

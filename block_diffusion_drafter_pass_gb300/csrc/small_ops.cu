@@ -36,13 +36,15 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return r;
 }
 
-// Block rows [anchor, MASK x (B-1)] per sequence -> fp32 residual x, the
-// first layer's RMSNorm input bf16(x * gain) and sum(x^2) per row (the GEMM
-// that consumes the row applies 1/sqrt(mean + eps)). One CTA per row,
-// 16-byte loads of the bf16 embedding row.
+// Block rows [anchor, MASK x (B-1)] per sequence (drafter), or the caller's
+// block ids (target pass: ids[m] for row m) -> fp32 residual x, the first
+// layer's RMSNorm input bf16(x * gain) and sum(x^2) per row (the GEMM that
+// consumes the row applies 1/sqrt(mean + eps)). One CTA per row, 16-byte
+// loads of the bf16 embedding row.
 __global__ void __launch_bounds__(kRowThreads) embed_kernel(const uint16_t* __restrict__ embed,
                                                             const int32_t* __restrict__ anchors, int mask_id,
-                                                            int vocab, const __grid_constant__ SeqMeta meta, int H,
+                                                            const int32_t* __restrict__ ids, int vocab,
+                                                            const __grid_constant__ SeqMeta meta, int H,
                                                             const uint16_t* __restrict__ gain, float* __restrict__ x,
                                                             uint16_t* __restrict__ hg, float* __restrict__ ss,
                                                             int* status) {
@@ -51,7 +53,7 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const uint16_t* __re
   grid_dep_launch();
   const int m = blockIdx.x;
   const int i = m / meta.B, j = m - i * meta.B;
-  int id = j == 0 ? anchors[i] : mask_id;
+  int id = ids ? ids[m] : (j == 0 ? anchors[i] : mask_id);
   if (id < 0 || id >= vocab) {
     if (threadIdx.x == 0) latch_status(status, kDevBounds);
     id = 0;
@@ -118,6 +120,50 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, int* status) {
   mbar_init(&bar, 1);
   fence_mbar_init();
   if (!mbar_wait_for(&bar, 0, limit_ns)) latch_status(status, kDevTimeout);
+}
+
+// Target pass: the block's keys (rotated) and values of one layer, from the
+// projection's block buffers (keys [row][n_kv][d], values transposed
+// [sequence][n_kv][d][64 slots]), appended to the paged pool at positions
+// len + j, the slots after the sequence's committed tokens. One CTA per block
+// row.
+__global__ void block_kv_append_kernel(const __grid_constant__ SeqMeta meta, SeqState st, int layer,
+                                       const uint16_t* __restrict__ kb, const uint16_t* __restrict__ vb,
+                                       uint16_t* __restrict__ pool, int pool_pages, int n_kv, int d, int* status) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int m = blockIdx.x;
+  const int i = m / meta.B, j = m - i * meta.B;
+  const int slot = meta.slot[i];
+  const int pos = st.len[slot] + j;
+  const int pi = pos / kPage, s64 = pos - pi * kPage;
+  const int page = pi < st.pages_per_seq ? st.page_table[static_cast<size_t>(slot) * st.pages_per_seq + pi] : -1;
+  if (page < 0 || page >= pool_pages) {
+    if (threadIdx.x == 0) latch_status(status, kDevBounds);
+    return;
+  }
+  const size_t base = (static_cast<size_t>(layer) * pool_pages + page) * 2 * n_kv * kPage * d;
+  for (int e = threadIdx.x; e < n_kv * d; e += blockDim.x) {
+    const int h = e / d, di = e - h * d;
+    pool[base + (static_cast<size_t>(h) * kPage + s64) * d + di] = kb[(static_cast<size_t>(m) * n_kv + h) * d + di];
+    pool[base + static_cast<size_t>(n_kv) * kPage * d + (static_cast<size_t>(h) * d + di) * kPage + s64] =
+        vb[((static_cast<size_t>(i) * n_kv + h) * d + di) * kPage + j];
+  }
+}
+
+// Target pass: the residual stream after a feature layer, x [M][H] fp32, to
+// columns col0 .. col0+H-1 of the feature rows feats [M][ld] bf16.
+__global__ void feat_copy_kernel(const float* __restrict__ x, int H, uint16_t* __restrict__ feats, int ld, int col0) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int m = blockIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(m) * H);
+  uint2* fr = reinterpret_cast<uint2*>(feats + static_cast<size_t>(m) * ld + col0);
+  for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
+    const float4 v = xr[c];
+    fr[c] = make_uint2(static_cast<uint32_t>(f32_to_bf16(v.x)) | (static_cast<uint32_t>(f32_to_bf16(v.y)) << 16),
+                       static_cast<uint32_t>(f32_to_bf16(v.z)) | (static_cast<uint32_t>(f32_to_bf16(v.w)) << 16));
+  }
 }
 
 __global__ void fuse_advance_kernel(const __grid_constant__ SeqMeta meta, SeqState st, int pending) {
@@ -313,12 +359,26 @@ cudaError_t launch_argmax_kc(const uint16_t* logits, int rows, int cols, int32_t
 
 }  // namespace
 
-cudaError_t launch_embed(const uint16_t* embed, const int32_t* anchors, int mask_id, int vocab, const SeqMeta& meta,
-                         int H, const uint16_t* gain, float* x, uint16_t* hg, float* ss, int* status, cudaStream_t s) {
+cudaError_t launch_embed(const uint16_t* embed, const int32_t* anchors, int mask_id, const int32_t* ids, int vocab,
+                         const SeqMeta& meta, int H, const uint16_t* gain, float* x, uint16_t* hg, float* ss,
+                         int* status, cudaStream_t s) {
   const int rows = meta.n_seq * meta.B;
   if (rows == 0) return cudaSuccess;
-  return launch_pdl(embed_kernel, dim3(rows), dim3(kRowThreads), 0, s, embed, anchors, mask_id, vocab, meta, H, gain,
-                    x, hg, ss, status);
+  return launch_pdl(embed_kernel, dim3(rows), dim3(kRowThreads), 0, s, embed, anchors, mask_id, ids, vocab, meta, H,
+                    gain, x, hg, ss, status);
+}
+
+cudaError_t launch_block_kv_append(const SeqMeta& meta, SeqState st, int layer, const uint16_t* kb, const uint16_t* vb,
+                                   uint16_t* pool, int pool_pages, int n_kv, int d, int* status, cudaStream_t s) {
+  const int rows = meta.n_seq * meta.B;
+  if (rows == 0) return cudaSuccess;
+  return launch_pdl(block_kv_append_kernel, dim3(rows), dim3(256), 0, s, meta, st, layer, kb, vb, pool, pool_pages,
+                    n_kv, d, status);
+}
+
+cudaError_t launch_feat_copy(const float* x, int M, int H, uint16_t* feats, int ld, int col0, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  return launch_pdl(feat_copy_kernel, dim3(M), dim3(256), 0, s, x, H, feats, ld, col0);
 }
 
 cudaError_t launch_verify(const SeqMeta& meta, SeqState st, const int32_t* drafts, const int32_t* targets,

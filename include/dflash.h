@@ -175,6 +175,56 @@ dflash_status dflash_verify(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, 
                             const int32_t* draft_ids, const int32_t* target_ids,
                             int32_t* tau, int32_t* bonus, void* stream);
 
+/* ---- the target side of the cycle: a target-shaped verify pass ----
+ * The DFlash notes' decoding cycle (4.5, "The Decoding Loop"): the target LLM
+ * computes logits for all positions of the drafted block in one batched
+ * forward pass, its greedy choice after each position feeds the acceptance
+ * check, and (4.2, 6.1 "Setup") the hidden states of 5 of its layers,
+ * uniformly sampled between layer 2 and the third-to-last, are the drafter's
+ * features. The time of that pass is T_verify of the speedup formula (2.2);
+ * the same pass over one token is a plain decoding step (L_target).
+ *
+ * A target context is a dflash_ctx built by dflash_target_create: the
+ * drafter's pre-norm layer (RMSNorm, rotate-half RoPE, GQA, SwiGLU; no
+ * QK-norm) with causal attention, caching its own K/V in the same paged
+ * layout. dflash_verify, dflash_seq_len, dflash_seq_reset, dflash_sync and
+ * the inspection hooks work on it as on a drafter; dflash_fuse_ctx,
+ * dflash_draft, dflash_draft_sample and dflash_set_path_selector return
+ * EINVAL. */
+
+/* The default feature layers: out[k] = (0-based) index of 1-based layer
+ * round(2 + k (n_layers - 4) / (n_feat - 1)), k < n_feat (n_feat = 1: layer
+ * 2); for 36 layers and 5 features, 1-based layers 2, 10, 18, 26, 34.
+ * Host only. Errors: EINVAL (n_layers < 5, n_feat outside 1..min(16,
+ * n_layers - 3), out NULL). */
+dflash_status dflash_target_feature_layers(int n_layers, int n_feat, int32_t* out);
+
+/* Create a target context. cfg as for dflash_create, except: n_layers up to
+ * 64; n_feat_layers = number of feature layers (0..16); mask_id and
+ * max_fuse_tokens unused. w as for dflash_create without the fusion weights
+ * (w_c, g_c ignored). feat_layers: host [n_feat_layers] strictly increasing
+ * 0-based layer indices (may be NULL when n_feat_layers is 0).
+ * Errors: as dflash_create. */
+dflash_status dflash_target_create(const dflash_config* cfg, const dflash_weights* w, const int32_t* feat_layers,
+                                   dflash_ctx** out);
+
+/* One target pass per sequence over block_ids (B tokens at positions
+ * committed .. committed+B-1; the sequence must have no pending tokens):
+ * causal attention over its cached tokens and the block, the block's K/V
+ * appended to its cache (pending = 1: speculative until dflash_verify, which
+ * commits the first min(tau, B); pending = 0: committed at once, as in
+ * prefill), and the argmax of the logits at every block position.
+ *  block_ids  device [n_seq, B] int32
+ *  B          1..max_block
+ *  target_ids device [n_seq, B] int32 output: t_j, the greedy token after
+ *             block position j (dflash_verify's target_ids)
+ *  feats      device [n_seq * B, n_feat_layers * H] bf16 output, 16-byte
+ *             aligned, or NULL: each block position's residual stream after
+ *             each feature layer, layer-major (dflash_fuse_ctx's feats)
+ * Errors: EINVAL, ENOMEM (page pool exhausted; nothing enqueued). */
+dflash_status dflash_target_forward(dflash_ctx* t, const int32_t* seq_ids, int n_seq, const int32_t* block_ids, int B,
+                                    int pending, int32_t* target_ids, uint16_t* feats, void* stream);
+
 /* Row-wise argmax of bf16 logits (lowest index on ties): the target's greedy
  * ids that dflash_verify consumes. Stateless.
  *  logits device [rows, cols] bf16 (row pitch = cols); out device [rows] int32.

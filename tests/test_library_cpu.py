@@ -63,3 +63,14 @@ def test_stateless_calls_validate_arguments(lib):
     assert lib.dflash_rows_argmax_bf16(None, 4, 0, None, None) == dfl.DFLASH_EINVAL
     assert lib.dflash_rows_argmax_bf16(None, -1, 8, None, None) == dfl.DFLASH_EINVAL
     assert lib.dflash_debug_gemm(None, None, None, 1, 1, 8, 0, None) == dfl.DFLASH_EINVAL
+
+
+def test_target_feature_layers_follow_the_oracle(lib):
+    """The library's default feature layers (host code) are the oracle's
+    reading of the setup table for every depth and count it accepts."""
+    from oracle import target_pass
+    for L in (5, 8, 12, 28, 36, 40, 64):
+        for n in range(1, min(16, L - 3) + 1):
+            assert dfl.target_feature_layers(L, n) == target_pass.feature_layers(L, n), (L, n)
+    out = (ctypes.c_int32 * 5)()
+    assert lib.dflash_target_feature_layers(4, 5, out) == dfl.DFLASH_EINVAL
