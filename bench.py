@@ -51,9 +51,10 @@ DEFAULT_WORKLOAD = "qwen3_8b_b1_ctx4096"
 L2_NOTE = "no flush: each step streams more than 3.4 GB of weights and KV (> 129 MB L2)"
 
 
-def workload_config(workload, batch, B, ctx, spread, layers, world, sampling=False, path_selector=False):
+def workload_config(workload, batch, B, ctx, spread, layers, world, sampling=False, path_selector=False,
+                    kv_format="bf16"):
     """The `config` object of a bench line, the same for both arms."""
-    return {"workload": workload,
+    return {"workload": workload, "kv_format": kv_format,
             "model": f"Qwen3-8B-shaped DFlash drafter ({layers} layers, H 4096, 32/8 heads x 128, FFN 12288, "
                      "V 151936, 5 fused target layers)",
             "batch_per_gpu": batch, "block": B,
@@ -200,7 +201,8 @@ def ncu_traffic(workload: str):
 class Cycle:
     """Device-resident inputs and outputs of the benchmarked speculative cycle."""
 
-    def __init__(self, dfl, shape, batch, ctx_lens, B, steps_total, seed, dev, max_fuse=4096, weights=None):
+    def __init__(self, dfl, shape, batch, ctx_lens, B, steps_total, seed, dev, max_fuse=4096, weights=None,
+                 kv_format=0):
         import torch
         from synth import make_weights_torch
         self.torch = torch
@@ -215,7 +217,7 @@ class Cycle:
         max_ctx = max(ctx_lens) + steps_total * B + 2 * B + 64
         pages = sum((c + steps_total * B + 2 * B + 63) // 64 + 1 for c in ctx_lens)
         self.d = dfl.Drafter(shape, self.weights, max_seqs=batch, max_batch=batch, max_block=B,
-                             max_ctx=max_ctx, max_pages=pages, max_fuse_tokens=max_fuse)
+                             max_ctx=max_ctx, max_pages=pages, max_fuse_tokens=max_fuse, kv_format=kv_format)
         g = torch.Generator(device=dev)
         g.manual_seed(seed + 1)
         # fill every sequence's committed context, one chunk at a time
@@ -479,7 +481,8 @@ def run_ours(args):
     # start short of the nominal length so the timed region is centred on it
     start_lens = [max(0, c - W - K // 2) for c in lens]
     shape = QWEN3_8B.with_layers(args.layers)
-    cyc = Cycle(dfl, shape, batch, start_lens, B, total_steps, seed=1000 * rank, dev=dev)
+    kvf = 1 if args.kv_format == "q8_0" else 0
+    cyc = Cycle(dfl, shape, batch, start_lens, B, total_steps, seed=1000 * rank, dev=dev, kv_format=kvf)
     sel = selector_weights(shape, dev, seed=7 + rank)
     if args.path_selector:
         cyc.d.set_path_selector(**sel)
@@ -551,13 +554,15 @@ def run_ours(args):
 
     targets = None
     weights = cyc.weights
-    if args.targets and not args.path_selector and not args.sampling and args.workload == DEFAULT_WORKLOAD:
+    if (args.targets and not args.path_selector and not args.sampling and args.workload == DEFAULT_WORKLOAD
+            and args.kv_format == "bf16"):
         cyc.close()
         cyc = None
         torch.cuda.empty_cache()
         targets = run_targets(args, dfl, shape, weights, dev, world)
     target_cycle = None
-    if args.targets and not args.path_selector and not args.sampling and args.workload == DEFAULT_WORKLOAD:
+    if (args.targets and not args.path_selector and not args.sampling and args.workload == DEFAULT_WORKLOAD
+            and args.kv_format == "bf16"):
         target_cycle = run_target_cycle(args, dfl, shape, weights, dev, world)
     if rank != 0:
         return None
@@ -595,7 +600,7 @@ def run_ours(args):
     g_ms_in_step = share * ms_step if share else None
     achieved = (g_bytes / K) / (g_ms_in_step / 1e3) / 1e9 if g_ms_in_step else None
     cfg = workload_config(args.workload, batch, B, ctx, spread, args.layers, world, args.sampling,
-                          args.path_selector)
+                          args.path_selector, args.kv_format)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -1198,6 +1203,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=5,
                     help="drafter depth (5 = the benchmarked drafter; fewer only for small profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-format", choices=("bf16", "q8_0"), default="bf16",
+                    help="cached context K/V: bf16, or 8-bit blocks (the q8_0 format)")
     ap.add_argument("--no-targets", dest="targets", action="store_false",
                     help="skip the context-32768 and batch-32 measurements that the default workload adds")
     ap.add_argument("--path-selector", action="store_true",

@@ -31,6 +31,7 @@ EXPORTED = (
     "dflash_block_sched_create", "dflash_block_sched_destroy", "dflash_block_sched_observe",
     "dflash_block_sched_set_cost", "dflash_block_sched_expected_tau", "dflash_block_sched_choose",
     "dflash_debug_wait_timeout", "dflash_target_feature_layers", "dflash_target_create", "dflash_target_forward",
+    "dflash_debug_read_kv_q8",
 )
 SAMPLE_WIDTH = 32   # DFLASH_SAMPLE_WIDTH
 
@@ -50,7 +51,7 @@ class dflash_config(ctypes.Structure):
                                             "n_layers", "n_feat_layers")] + [
         ("rope_base", ctypes.c_float), ("rms_eps", ctypes.c_float)] + [
         (n, ctypes.c_int) for n in ("mask_id", "max_seqs", "max_batch", "max_block", "max_ctx", "max_pages",
-                                    "max_fuse_tokens")]
+                                    "max_fuse_tokens", "kv_format")]
 
 
 class dflash_layer_weights(ctypes.Structure):
@@ -93,6 +94,7 @@ def load_library() -> ctypes.CDLL:
         "dflash_rows_argmax_bf16": ([VP, I, I, VP, VP], I),
         "dflash_sync": ([VP], I),
         "dflash_debug_read_kv": ([VP, I, I, I, I, VP, VP], I),
+        "dflash_debug_read_kv_q8": ([VP, I, I, I, I, VP, VP, VP, VP], I),
         "dflash_debug_last_draft": ([VP, VP, VP], I),
         "dflash_debug_gemm": ([VP, VP, VP, I, I, I, I, VP], I),
         "dflash_debug_profile": ([VP, I], I),
@@ -230,7 +232,7 @@ class Drafter:
 
     def __init__(self, shape, weights, *, max_seqs: int = 4, max_batch: int = 4, max_block: int = 16,
                  max_ctx: int = 4096, max_pages: Optional[int] = None, max_fuse_tokens: int = 1024,
-                 _feat_layers=None):
+                 kv_format: int = 0, _feat_layers=None):
         import torch
         lib = load_library()
         self.shape = shape
@@ -245,7 +247,7 @@ class Drafter:
         self.cfg = dflash_config(shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
                                  shape.vocab, shape.n_layers, shape.n_feat_layers, shape.rope_base,
                                  shape.rms_eps, shape.mask_id, max_seqs, max_batch, max_block, max_ctx,
-                                 max_pages, max_fuse_tokens)
+                                 max_pages, max_fuse_tokens, kv_format)
         layers = (dflash_layer_weights * shape.n_layers)()
         for i, lw in enumerate(weights["layers"]):
             layers[i] = dflash_layer_weights(*[_ptr(lw[k]) for k in ("w_q", "w_k", "w_v", "w_o", "w_gate",
@@ -408,6 +410,20 @@ class Drafter:
                self.ctx)
         f = lambda a: (a.astype(np.uint32) << 16).view(np.float32)
         return f(k), f(v)
+
+    def read_kv_q8(self, layer: int, seq: int, pos0: int, n: int):
+        """The stored 8-bit blocks (kv_format 1): K codes, K scales, V codes,
+        V scales; codes int8 [n, n_kv, d], scales float32 [n, n_kv, d/32]
+        (the stored fp16 values)."""
+        import numpy as np
+        sh = self.shape
+        kc = np.empty((n, sh.n_kv_heads, sh.head_dim), dtype=np.int8)
+        vc = np.empty_like(kc)
+        ks = np.empty((n, sh.n_kv_heads, sh.head_dim // 32), dtype=np.uint16)
+        vs = np.empty_like(ks)
+        _check(load_library().dflash_debug_read_kv_q8(self.ctx, layer, seq, pos0, n, kc.ctypes.data, ks.ctypes.data,
+                                                      vc.ctypes.data, vs.ctypes.data), self.ctx)
+        return kc, ks.view(np.float16).astype(np.float32), vc, vs.view(np.float16).astype(np.float32)
 
     def profile(self, enable: bool) -> None:
         """Event-time every kernel launch (on its launch stream) while enabled."""

@@ -33,6 +33,7 @@
 // Query row r of an item is (block position j, head g of the group) with
 // r = j*G + g (the order the 3D query box lands in shared memory).
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -44,31 +45,46 @@ namespace {
 constexpr int kKeyTile = 64;
 constexpr float kRescaleLog2 = 8.f;   // rescale O when the row max grows by more than 2^8
 constexpr int kThreads = 224;         // producer, MMA, 4 softmax warps, L2 prefetch warp
+constexpr int kConvWarps = 4;         // 8-bit pages: warps 7..10 convert the codes to fp16 tiles
+                                      // (one per SM sub-partition)
+template <bool Q8>
+constexpr int attn_threads() { return Q8 ? kThreads + 32 * kConvWarps : kThreads; }
 constexpr int kPrefetchSteps = 4;     // the prefetch warp runs this many steps ahead of the producer
 
 // Rows of the block's own key box: B rounded up to 16 or 32.
 __host__ __device__ __forceinline__ int block_rows(int B) { return B <= 16 ? 16 : 32; }
 
-template <int D>
+template <int D, bool Q8 = false>
 struct ACfg {
   // One pipeline stage holds one step: two 64-key units (context pages or the
   // block) as [K dim-box 0: 128 keys x 128 B]...[K dim-box D/64-1][V^T unit 0]
   // [V^T unit 1], so S = Q K^T of a step is one N = 128 product per K slice.
-  static constexpr int kStages = D == 128 ? 3 : 6;
+  // 8-bit pages: the raw loader brings each context unit as a raw region
+  // (codes and scales, q8_head_bytes) into one of kRawSlots unit slots, as
+  // far ahead as free slots allow, and the converter warps write the fp16
+  // stage from them.
+  static constexpr int kStages = Q8 ? (D == 128 ? 2 : 4) : (D == 128 ? 3 : 6);
   static constexpr int kUnitBox = 64 * 128;               // 64 rows x 128 bytes
   static constexpr int kKBox = 2 * kUnitBox;              // 128 key rows of one 64-dim slice
   static constexpr int kKBytes = (D / 64) * kKBox;
   static constexpr int kVUnit = (D / 64) * kUnitBox;      // values transposed [D][64] of one unit
   static constexpr int kStageBytes = kKBytes + 2 * kVUnit;
-  static constexpr int kSmem = kStages * kStageBytes + 1024;
+  static constexpr int kRawUnit = static_cast<int>(q8_head_bytes(D));
+  // as many unit slots as the shared memory left by the stages holds (4 KB
+  // under the 227 KB a block may use, kept for the static shared variables)
+  static constexpr int kRawSlots = Q8 ? (227 * 1024 - 4096 - 1024 - kStages * kStageBytes) / kRawUnit : 0;
+  static constexpr int kSmem = kStages * kStageBytes + kRawSlots * kRawUnit + 1024;
+  static_assert(!Q8 || kRawSlots >= 4, "8-bit pages need at least two steps of raw slots");
   // TMEM columns: S buffers at 0 and 128 (P overwrites the first 64 columns
   // of its own S as packed bf16), Q at 256 (D/2 columns of packed bf16), O after it.
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCols = 2 * kKeyTile;
   static constexpr uint32_t kQCol = 2 * kSCols;
   static constexpr uint32_t kOCol = kQCol + D / 2;
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 2 * kKeyTile);
-  static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D);
+  // 8-bit pages run the products in fp16 (Q, P and the decoded K/V tiles),
+  // so that a code pair decodes in three packed instructions
+  static constexpr uint32_t kIdescS = Q8 ? idesc_f16_f32(128, 2 * kKeyTile) : idesc_bf16_f32(128, 2 * kKeyTile);
+  static constexpr uint32_t kIdescO = Q8 ? idesc_f16_f32(128, D) : idesc_bf16_f32(128, D);
 };
 
 // D[tmem] (+)= A[tmem] * B[smem]^T: A (M rows in TMEM lanes, K packed two bf16
@@ -92,6 +108,12 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
@@ -251,6 +273,110 @@ __device__ __forceinline__ float row_max(const float (&v)[N]) {
   return max3(m0, m2, max3(v[N - 2], v[N - 1], -INFINITY));
 }
 
+// 8-bit pages: two codes of an offset-binary word (code + 128 per byte),
+// selected by `sel`, decoded in fp16 and scaled by the fp16 pair s2. The
+// byte under an fp16 exponent of 2^10 reads as 1024 + code + 128 exactly; one
+// exact subtraction gives the code, one multiply applies the scale (rounded
+// to fp16).
+__device__ __forceinline__ uint32_t q8_pair_f16(uint32_t ub, uint32_t sel, uint32_t s2) {
+  const uint32_t h = __byte_perm(ub, 0x64646464u, sel);
+  const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6480),
+                                                                                  __ushort_as_half(0x6480)));
+  const __half2 r = __hmul2(q, *reinterpret_cast<const __half2*>(&s2));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// 16 codes (one 16-byte word) with their fp16 scales (one pair per code pair)
+// -> 8 fp16 pairs.
+__device__ __forceinline__ void q8_decode16(const uint4& cw, const uint32_t (&s2)[8], uint32_t (&o)[8]) {
+  const uint32_t w[4] = {cw.x ^ 0x80808080u, cw.y ^ 0x80808080u, cw.z ^ 0x80808080u, cw.w ^ 0x80808080u};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    o[2 * k] = q8_pair_f16(w[k], 0x4140u, s2[2 * k]);
+    o[2 * k + 1] = q8_pair_f16(w[k], 0x4342u, s2[2 * k + 1]);
+  }
+}
+
+// Shared-memory accesses by 32-bit shared-window address (the stage and raw
+// ring pointers are realigned through an integer, which hides their state
+// space from the compiler; generic accesses would cost 64-bit address math
+// and the long scoreboard).
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
+// One 64-key context unit: raw region (K codes [64][D], V codes [D][64], K
+// scales [64][D/32], V scales [D/32][64]) -> unit u of an fp16 stage in the
+// 128-byte-swizzled layout the MMAs read (keys: row u*64 + k of each 64-dim
+// slice box; transposed values: row r of box r/64 of the unit's V^T tile).
+// Thread ct of NCT takes tasks ct + j*NCT, all in one unrolled round: the
+// loads of every task first, then decode and stores (a converter warp is
+// latency-bound, so its tasks must be independent in flight). raw and stage
+// are shared-window addresses.
+template <int D, int NCT, int kKBox, int kKBytes, int kVUnit, int kUnitBox>
+__device__ __forceinline__ void q8_convert_unit(uint32_t raw, uint32_t stage, int u, int ct) {
+  // keys: tasks (key k, 16-dim group g); values: tasks (dim r, 16-key group kg)
+  constexpr int kTK = 64 * (D / 16), kTV = D * 4, kIlp = (kTK + kTV) / NCT;
+  static_assert(kTK % NCT == 0 && kTV % NCT == 0, "each round takes only keys or only values");
+  const uint32_t ksc = raw + static_cast<uint32_t>(q8_kscale_off(D));
+  const uint32_t vsc = raw + static_cast<uint32_t>(q8_vscale_off(D));
+  const uint32_t vcd = raw + static_cast<uint32_t>(q8_vcode_off(D));
+  uint4 cw[kIlp];
+  uint32_t s2[kIlp][8];
+#pragma unroll
+  for (int j = 0; j < kIlp; ++j) {
+    const int task = ct + j * NCT;
+    if (j * NCT < kTK) {
+      const int k = task / (D / 16), g = task % (D / 16);
+      cw[j] = lds128(raw + k * D + g * 16);
+      const uint32_t s1 = lds16(ksc + (k * (D / 32) + (g >> 1)) * 2);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) s2[j][c] = s1 | (s1 << 16);
+    } else {
+      const int r = (task - kTK) >> 2, kg = (task - kTK) & 3;
+      cw[j] = lds128(vcd + r * 64 + kg * 16);
+      // the 16 keys' scales of this dim's block: 8 fp16 pairs, 32 contiguous bytes
+      const uint32_t sp = vsc + ((r >> 5) * 64 + kg * 16) * 2;
+      const uint4 sa = lds128(sp), sb = lds128(sp + 16);
+      s2[j][0] = sa.x; s2[j][1] = sa.y; s2[j][2] = sa.z; s2[j][3] = sa.w;
+      s2[j][4] = sb.x; s2[j][5] = sb.y; s2[j][6] = sb.z; s2[j][7] = sb.w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kIlp; ++j) {
+    const int task = ct + j * NCT;
+    uint32_t o[8];
+    q8_decode16(cw[j], s2[j], o);
+    const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
+    if (j * NCT < kTK) {
+      const int k = task / (D / 16), g = task % (D / 16);
+      const int row = u * 64 + k, c0 = (g & 3) * 2;
+      const uint32_t rowp = stage + (g >> 2) * kKBox + row * 128;
+      // lanes g and g + 4 of one key write the same chunks of two boxes (one
+      // bank set); opposite store orders keep each store conflict-free
+      const int flip = (g >> 2) & 1;
+      sts128(rowp + (((c0 + flip) ^ (row & 7)) << 4), flip ? hi : lo);
+      sts128(rowp + (((c0 + 1 - flip) ^ (row & 7)) << 4), flip ? lo : hi);
+    } else {
+      const int r = (task - kTK) >> 2, kg = (task - kTK) & 3;
+      const int row = r & 63, c0 = kg * 2;
+      const uint32_t rowp = stage + kKBytes + u * kVUnit + (r >> 6) * kUnitBox + row * 128;
+      sts128(rowp + ((c0 ^ (row & 7)) << 4), lo);
+      sts128(rowp + (((c0 + 1) ^ (row & 7)) << 4), hi);
+    }
+  }
+}
+
 // Work decomposition shared by the three roles and the combine kernel.
 struct SeqSplit {
   int len;        // committed context tokens
@@ -279,15 +405,18 @@ struct Item {
 // Units are 64-key tiles: context pages 0 .. n_ctx-1, then the block (unit
 // n_ctx). An item covers units [tb, te) with tb even; a step takes units
 // (tb + 2j, tb + 2j + 1), the second possibly absent.
-template <int D, bool SPREAD>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool SPREAD, bool Q8>
+__global__ void __launch_bounds__(attn_threads<Q8>(), 1)
     attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ AttnArgs a,
                 const __grid_constant__ AttnSched sched) {
-  using C = ACfg<D>;
+  using C = ACfg<D, Q8>;
   constexpr int S = C::kStages;
+  constexpr int RS = Q8 ? C::kRawSlots : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* raw_ring = smem + S * C::kStageBytes;   // 8-bit pages: kRawSlots raw unit slots
   __shared__ __align__(8) uint64_t kv_full[S], kv_empty[S];
+  __shared__ __align__(8) uint64_t raw_full[RS], raw_empty[RS];
   __shared__ __align__(8) uint64_t q_ready, mma_done, o_full, o_free;
   __shared__ __align__(8) uint64_t s_full[2], p_full[2];
   __shared__ uint32_t tmem_slot;
@@ -305,8 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_full[s], Q8 ? 1 + kConvWarps : 1);   // producer (+ converter warps)
       mbar_init(&kv_empty[s], 1);
+    }
+    for (int r = 0; r < RS; ++r) {
+      mbar_init(&raw_full[r], 1);
+      mbar_init(&raw_empty[r], kConvWarps);
     }
     mbar_init(&q_ready, 4);
     mbar_init(&mma_done, 1);
@@ -409,13 +542,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + s * C::kStageBytes;
           const int nu = min(2, it.te - t0);
           uint32_t bytes = 0;
-          for (int u = 0; u < nu; ++u) bytes += (t0 + u < nctx ? C::kVUnit : (D / 64) * Bb * 128) + C::kVUnit;
+          for (int u = 0; u < nu; ++u) {
+            if (t0 + u < nctx) bytes += Q8 ? 0 : 2 * C::kVUnit;
+            else bytes += (D / 64) * Bb * 128 + C::kVUnit;
+          }
           mbar_arrive_expect_tx(&kv_full[s], bytes);
           for (int u = 0; u < nu; ++u) {
             const int t = t0 + u;
             uint8_t* ku = st + u * C::kUnitBox;
             uint8_t* vu = st + C::kKBytes + u * C::kVUnit;
             if (t < nctx) {
+              if constexpr (Q8) continue;   // written by the converter warps
               int page = u == 0 ? cur0 : cur1;
               if (page < 0 || page >= a.pool_pages) {
                 latch_status(a.status, kDevBounds);
@@ -522,6 +659,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every issued MMA completes before TMEM and shared memory are released
       tc_commit(&mma_done);
       mbar_wait(&mma_done, 0);
+    }
+  } else if (Q8 && warp >= 7) {
+    // ---------------- 8-bit page converters ----------------
+    // Walk the producer's steps: wait for a free stage; per context unit of
+    // the step, wait for its raw slot (context units are numbered in walk
+    // order, as the raw loader issues them), decode it into the stage and free
+    // the slot; then make the stores visible to the tensor cores and arrive on
+    // the stage (the producer's arrival counts the block unit's copies).
+    const int ct = threadIdx.x - 7 * 32;
+    int q = 0, qu = 0;
+    bool dead = false;
+    for (int rk = rec_begin; rk < rec_end && !dead; rk = next_rec(rk + 1)) {
+      const Item it = decode(rk);
+      const int nctx = s_nctx[it.i];
+      for (int t0 = it.tb; t0 < it.te && !dead; t0 += 2, ++q) {
+        const int s = q % S;
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[s], ((q / S) & 1) ^ 1, &abort_flag))) {
+          give_up();
+          dead = true;
+          break;
+        }
+        const int nu = min(2, it.te - t0);
+        for (int u = 0; u < nu; ++u) {
+          if (t0 + u >= nctx) continue;
+          const int r = qu % RS;
+          if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[r], (qu / RS) & 1, &abort_flag))) {
+            give_up();
+            dead = true;
+            break;
+          }
+          q8_convert_unit<D, 32 * kConvWarps, C::kKBox, C::kKBytes, C::kVUnit, C::kUnitBox>(
+              smem_u32(raw_ring + r * C::kRawUnit), smem_u32(smem + s * C::kStageBytes), u, ct);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&raw_empty[r]);
+          ++qu;
+        }
+        if (dead) break;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_full[s]);
+      }
+    }
+  } else if (Q8 && warp == 6) {
+    // ---------------- 8-bit page raw loader ----------------
+    // Walks the same context units in the same order and brings each raw
+    // region (codes and scales of one page and kv head) into the next unit
+    // slot with one bulk copy, as soon as the converters have freed it.
+    if (lane == 0) {
+      int qu = 0;
+      bool dead = false;
+      for (int rk = rec_begin; rk < rec_end && !dead; rk = next_rec(rk + 1)) {
+        const Item it = decode(rk);
+        const int slot = a.meta.slot[it.i], nctx = s_nctx[it.i];
+        const int* ptab = a.seqs.page_table + static_cast<size_t>(slot) * a.seqs.pages_per_seq;
+        const int t_end = min(it.te, nctx);
+        for (int t = it.tb; t < t_end; ++t, ++qu) {
+          const int r = qu % RS;
+          if (!mbar_wait(&raw_empty[r], ((qu / RS) & 1) ^ 1, &abort_flag)) {
+            give_up();
+            dead = true;
+            break;
+          }
+          int page = t < a.seqs.pages_per_seq ? ptab[t] : -1;
+          if (page < 0 || page >= a.pool_pages) {
+            latch_status(a.status, kDevBounds);
+            page = 0;
+          }
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.pool) +
+                               ((static_cast<size_t>(a.layer) * a.pool_pages + page) * nkv + it.kvh) * C::kRawUnit;
+          mbar_arrive_expect_tx(&raw_full[r], C::kRawUnit);
+          bulk_load(raw_ring + r * C::kRawUnit, src, C::kRawUnit, &raw_full[r]);
+        }
+      }
+      // copies still in flight complete before shared memory is released
+      for (int j = max(0, qu - RS); j < qu; ++j) mbar_wait(&raw_full[j % RS], (j / RS) & 1);
     }
   } else if (warp == 6) {
     // ---------------- L2 prefetch ----------------
@@ -655,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float p0 = ex2(fmaf(sv[2 * c], sl2, -m));
         const float p1 = ex2(fmaf(sv[2 * c + 1], sl2, -m));
         s4[c & 3] += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
+        pk[c] = Q8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
       }
       return (s4[0] + s4[1]) + (s4[2] + s4[3]);
     };
@@ -912,26 +1124,31 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const 
   for (int e = 0; e < kPer; ++e) out[e] = f32_to_bf16(acc[e] * inv);
 }
 
-template <int D, bool SPREAD>
+template <int D, bool SPREAD, bool Q8>
 cudaError_t launch_main(const AttnMaps& maps, const AttnArgs& a, const AttnSched& sched, int grid,
                         cudaStream_t stream) {
-  using C = ACfg<D>;
+  using C = ACfg<D, Q8>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(attn_kernel<D, SPREAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaFuncSetAttribute(attn_kernel<D, SPREAD, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(attn_kernel<D, SPREAD>, dim3(grid), dim3(kThreads), C::kSmem, stream, maps, a, sched);
+  return launch_pdl(attn_kernel<D, SPREAD, Q8>, dim3(grid), dim3(attn_threads<Q8>()), C::kSmem, stream, maps, a,
+                    sched);
 }
 
 template <int D>
 cudaError_t launch_d(const AttnMaps& maps, const AttnArgs& a, const AttnSched& sched, int grid, int part,
                      cudaStream_t stream) {
-  if (part == 0)
-    return a.spread ? launch_main<D, true>(maps, a, sched, grid, stream)
-                    : launch_main<D, false>(maps, a, sched, grid, stream);
+  if (part == 0) {
+    if (a.q8)
+      return a.spread ? launch_main<D, true, true>(maps, a, sched, grid, stream)
+                      : launch_main<D, false, true>(maps, a, sched, grid, stream);
+    return a.spread ? launch_main<D, true, false>(maps, a, sched, grid, stream)
+                    : launch_main<D, false, false>(maps, a, sched, grid, stream);
+  }
   const dim3 grid_c(a.n_q_heads, a.meta.n_seq, (a.meta.B + kCombineWarps - 1) / kCombineWarps);
   const dim3 block_c(32 * kCombineWarps);
   if (a.max_chunks <= 8) return launch_pdl(attn_combine_kernel<D, 8>, grid_c, block_c, 0, stream, a);
@@ -943,14 +1160,19 @@ cudaError_t launch_d(const AttnMaps& maps, const AttnArgs& a, const AttnSched& s
 
 int attention_block_rows(int B) { return block_rows(B); }
 
-int attention_ctas_per_sm(int head_dim) {
+int attention_ctas_per_sm(int head_dim, bool q8) {
   int n = 0;
-  auto q = [&](auto kern, int smem) {
+  auto q = [&](auto kern, int smem, int threads) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess) n = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) n = 1;
   };
-  if (head_dim == 128) q(attn_kernel<128, true>, ACfg<128>::kSmem);
-  else q(attn_kernel<64, true>, ACfg<64>::kSmem);
+  if (q8) {
+    if (head_dim == 128) q(attn_kernel<128, true, true>, ACfg<128, true>::kSmem, attn_threads<true>());
+    else q(attn_kernel<64, true, true>, ACfg<64, true>::kSmem, attn_threads<true>());
+  } else {
+    if (head_dim == 128) q(attn_kernel<128, true, false>, ACfg<128>::kSmem, kThreads);
+    else q(attn_kernel<64, true, false>, ACfg<64>::kSmem, kThreads);
+  }
   return n < 1 ? 1 : n;
 }
 

@@ -29,6 +29,7 @@
 // per 16-column chunk.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -616,9 +617,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
       // one sequence, written as two 16-byte stores
       const int i = (m0 + c0) / e.meta.B, j0 = (m0 + c0) - i * e.meta.B;
       uint32_t w[8];
+      const bool h16 = e.qkv_f16 != 0;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        w[c] = static_cast<uint32_t>(f32_to_bf16(v[2 * c])) | (static_cast<uint32_t>(f32_to_bf16(v[2 * c + 1])) << 16);
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t lo = h16 ? f32_to_f16(v[2 * c]) : f32_to_bf16(v[2 * c]);
+        const uint32_t hi = h16 ? f32_to_f16(v[2 * c + 1]) : f32_to_bf16(v[2 * c + 1]);
+        w[c] = lo | (hi << 16);
+      }
       uint4* dstv = reinterpret_cast<uint4*>(
           e.out_v + ((static_cast<size_t>(i) * e.n_kv_heads + hd) * d + di) * kPage + j0);
       dstv[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -640,11 +645,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
       for (int c = 1; c < 16; ++c) run = run && posv[c] == posv[0] + c;
       float2 cs = rope ? sh.rope_base[c0 >> 4][fi] : make_float2(1.f, 0.f);
       uint16_t ov[16];
+      float xf[16];
       const float sg = lo ? -1.f : 1.f;   // rotate-half sign of this row
       if (run) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          ov[c] = f32_to_bf16(fmaf(sg * other[c], cs.y, v[c] * cs.x));
+          xf[c] = fmaf(sg * other[c], cs.y, v[c] * cs.x);
           cs = make_float2(cs.x * rot.x - cs.y * rot.y, cs.y * rot.x + cs.x * rot.y);
         }
       } else {
@@ -656,9 +662,92 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
             const float2 t = pos >= 0 ? e.rope[static_cast<size_t>(pos) * half + fi] : make_float2(1.f, 0.f);
             x = fmaf(sg * other[c], t.y, x * t.x);
           }
-          ov[c] = f32_to_bf16(x);
+          xf[c] = x;
         }
       }
+      if (kind == EPI_QKV_ROPE && e.qkv_f16) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) ov[c] = f32_to_f16(xf[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) ov[c] = f32_to_bf16(xf[c]);
+      }
+      if (kind == EPI_KV_APPEND && e.kv_q8) {
+        // 8-bit pages: the 32 lanes of this warp are 32 consecutive values of
+        // one head row (tile rows 32q .. 32q+31 of a K or V region), i.e. one
+        // block per token (column). Scale d = max|x| / 127, codes round(x / d)
+        // halves away from zero, d stored as fp16 by lane c for column c.
+        const int layer = e.layer0 + (reg >> 1), blk = di >> 5, nb = d >> 5;
+        const bool is_v = (reg & 1) != 0;
+        const size_t hb = q8_head_bytes(d);
+        uint8_t* pb = reinterpret_cast<uint8_t*>(e.pool);
+        float amax[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) amax[c] = fabsf(xf[c]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) amax[c] = fmaxf(amax[c], __shfl_xor_sync(0xffffffffu, amax[c], o));
+        }
+        uint32_t qb[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float dd = amax[c] / 127.f;
+          float t = dd > 0.f ? xf[c] / dd : 0.f;
+          t = fminf(fmaxf(truncf(t + copysignf(0.5f, t)), -127.f), 127.f);
+          qb[c] = static_cast<uint32_t>(static_cast<int>(t)) & 0xFFu;
+        }
+        auto region = [&](int dst) {   // byte offset of this head's region of the token's page
+          const int page = dst / (2 * e.n_kv_heads * kPage);
+          return ((static_cast<size_t>(layer) * e.pool_pages + page) * e.n_kv_heads + hd) * hb;
+        };
+        // the chunk's 16 tokens at consecutive slots of one page
+        bool qrun = dstv[0] >= 0 && (dstv[0] & (kPage - 1)) + 16 <= kPage;
+#pragma unroll
+        for (int c = 1; c < 16; ++c) qrun = qrun && dstv[c] == dstv[0] + c;
+        if (is_v && qrun) {   // one row of the transposed code tile: 16 contiguous bytes
+          const int slot0 = dstv[0] & (kPage - 1);
+          uint8_t* p = pb + region(dstv[0]) + q8_vcode_off(d) + static_cast<size_t>(di) * kPage + slot0;
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            w[k] = qb[4 * k] | (qb[4 * k + 1] << 8) | (qb[4 * k + 2] << 16) | (qb[4 * k + 3] << 24);
+          if ((slot0 & 15) == 0) {
+            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else if ((slot0 & 3) == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) reinterpret_cast<uint32_t*>(p)[k] = w[k];
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) p[c] = static_cast<uint8_t>(qb[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int dst = dstv[c];
+            if (dst < 0) continue;
+            const int slot = dst & (kPage - 1);
+            pb[region(dst) + (is_v ? q8_vcode_off(d) + static_cast<size_t>(di) * kPage + slot
+                                   : static_cast<size_t>(slot) * d + di)] = static_cast<uint8_t>(qb[c]);
+          }
+        }
+        // lane c stores column c's scale
+        float my_amax = 0.f;
+        int my_dst = -1;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (lane == c) {
+            my_amax = amax[c];
+            my_dst = dstv[c];
+          }
+        }
+        if (lane < 16 && my_dst >= 0) {
+          const int slot = my_dst & (kPage - 1);
+          const size_t so = is_v ? q8_vscale_off(d) + (static_cast<size_t>(blk) * kPage + slot) * 2
+                                 : q8_kscale_off(d) + (static_cast<size_t>(slot) * nb + blk) * 2;
+          *reinterpret_cast<__half*>(pb + region(my_dst) + so) = __float2half_rn(my_amax / 127.f);
+        }
+      } else {
       // KV append, value rows: the chunk's 16 tokens at consecutive slots of
       // one page are 32 contiguous bytes of this row of the transposed value
       // tile, written with the widest aligned stores (the per-token path
@@ -729,6 +818,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
                                        : (static_cast<size_t>(hd) * kPage + slot) * d + di;
           e.pool[lp + off] = ov[c];
         }
+      }
       }
     }
 #pragma unroll

@@ -52,6 +52,16 @@ constexpr int kPage = 64;          // tokens per KV page
 constexpr int kMaxBatch = 64;      // sequences per call
 constexpr int kMaxBlock = 32;      // block size B
 constexpr int kMaxTargetLayers = 64;   // layers of a target context
+
+// 8-bit context pages (kv_format 1): per (layer, page, kv head) one region of
+//   [K codes: 64 slots][d] int8 | [V codes: d][64 slots] int8 (transposed)
+//   | [K scales: 64 slots][d/32] fp16 | [V scales: d/32][64 slots] fp16,
+// 136 d bytes, regions ordered (layer, page, kv head). A scale covers 32
+// consecutive values of one token's head row.
+__host__ __device__ constexpr size_t q8_head_bytes(int d) { return static_cast<size_t>(136) * d; }
+__host__ __device__ constexpr size_t q8_vcode_off(int d) { return static_cast<size_t>(64) * d; }
+__host__ __device__ constexpr size_t q8_kscale_off(int d) { return static_cast<size_t>(128) * d; }
+__host__ __device__ constexpr size_t q8_vscale_off(int d) { return static_cast<size_t>(132) * d; }
 constexpr int kMaxAMaps = 12;      // weight tensor maps per GEMM launch
 
 // device status bits (dflash_sync maps them to ETIMEOUT / EDEVICE)
@@ -127,6 +137,8 @@ struct GemmEpi {
   uint16_t* pool;
   int pool_pages;
   int layer0;                       // layer of region 0
+  int kv_q8;                        // 1: the pool holds 8-bit pages (q8_head_bytes regions)
+  int qkv_f16;                      // QKV_ROPE: q, k, v stored as fp16 (the 8-bit pages' fp16 attention)
   // ARGMAX
   unsigned long long* keys;         // [M] running max keys (zero between calls)
   int* done;                        // CTA completion counter (zero between calls)
@@ -197,6 +209,7 @@ struct AttnArgs {
   int rows_pad;              // row stride of the partial buffers (>= G*B)
   int spread;                // 1: G*B <= 64, query rows spread 16 per TMEM lane quarter
   int causal;                // 1: block position j sees block keys 0..j only (target pass)
+  int q8;                    // 1: context pages in the 8-bit block format
   const uint16_t* q;         // [n_seq*B][n_q*d] bf16 (RoPE applied)
   const uint16_t* pool;      // the KV pool (read directly only for L2 prefetches)
   float* part_o;             // [items][rows_pad][d]
@@ -229,7 +242,7 @@ struct AttnMaps {
 cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& a, const AttnSched& sched, int grid, int part,
                              cudaStream_t stream);
 int attention_block_rows(int B);   // key-box height used for the block's own keys
-int attention_ctas_per_sm(int head_dim);   // resident attention CTAs per SM
+int attention_ctas_per_sm(int head_dim, bool q8);   // resident attention CTAs per SM
 
 // ----------------------------------------------------------------------------
 // Small kernels

@@ -284,6 +284,7 @@ GemmEpi base_epi(dflash_ctx* ctx, int kind) {
   e.seqs = seq_state(ctx);
   e.pool = ctx->pool;
   e.pool_pages = ctx->cfg.max_pages;
+  e.kv_q8 = ctx->cfg.kv_format == 1;
   e.status = ctx->d_status;
   e.inv_hidden = 1.0f / ctx->cfg.hidden;
   e.eps = ctx->cfg.rms_eps;
@@ -410,10 +411,16 @@ dflash_status create_impl(const dflash_config* cfg_in, const dflash_weights* w, 
   if (c.max_seqs < 1 || c.max_ctx < 1 || c.max_pages < 1 || c.max_fuse_tokens < 1)
     return fail(nullptr, DFLASH_EINVAL, "capacities must be positive");
   if (!(c.rms_eps >= 0.f) || !(c.rope_base > 1.f)) return fail(nullptr, DFLASH_EINVAL, "bad rms_eps or rope_base");
+  if (c.kv_format != 0 && c.kv_format != 1) return fail(nullptr, DFLASH_EINVAL, "kv_format must be 0 or 1");
+  if (c.kv_format == 1 && target) return fail(nullptr, DFLASH_EINVAL, "8-bit K/V pages are for drafter contexts");
+  const bool q8 = c.kv_format == 1;
   const long long pool_rows = 1LL * c.n_layers * c.max_pages * 2 * c.n_kv_heads * kPage;
   // the pool is also read as rows of 64 elements (transposed values)
-  if (pool_rows * (d / 64) >= (1LL << 31))
+  if (!q8 && pool_rows * (d / 64) >= (1LL << 31))
     return fail(nullptr, DFLASH_EINVAL, "KV pool too large for 32-bit TMA coordinates");
+  // 8-bit pages: 136 d bytes per (layer, page, kv head), held as 16-bit elements
+  const size_t pool_elems = q8 ? 1ull * c.n_layers * c.max_pages * c.n_kv_heads * q8_head_bytes(d) / 2
+                               : static_cast<size_t>(pool_rows) * d;
   const void* ptrs[] = {w->embed, w->lm_head, w->g_final, target ? w->embed : w->w_c, target ? w->embed : w->g_c};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return fail(nullptr, DFLASH_EINVAL, "weight pointer null or not 16-byte aligned");
@@ -463,8 +470,8 @@ dflash_status create_impl(const dflash_config* cfg_in, const dflash_weights* w, 
     if (e_ != cudaSuccess) return bad(e_, what); \
   } while (0)
 
-  CA(dalloc(&ctx->pool, static_cast<size_t>(pool_rows) * d), "KV pool");
-  CA(cudaMemset(ctx->pool, 0, static_cast<size_t>(pool_rows) * d * 2), "KV pool");
+  CA(dalloc(&ctx->pool, pool_elems), "KV pool");
+  CA(cudaMemset(ctx->pool, 0, pool_elems * 2), "KV pool");
   CA(dalloc(&ctx->rope, static_cast<size_t>(ctx->rope_positions) * (d / 2)), "RoPE table");
   CA(dalloc(&ctx->d_len, c.max_seqs), "lengths");
   CA(dalloc(&ctx->d_pend, c.max_seqs), "lengths");
@@ -522,8 +529,8 @@ dflash_status create_impl(const dflash_config* cfg_in, const dflash_weights* w, 
   const int wb = kWeightBoxRows;
   bool ok = encode_2d(&ctx->m_lm, w->lm_head, c.vocab, H, wb) &&
             (target || encode_2d(&ctx->m_wc, w->w_c, H, static_cast<uint64_t>(c.n_feat_layers) * H, wb)) &&
-            encode_2d(&ctx->m_pool, ctx->pool, pool_rows, d, 64) &&
-            encode_2d(&ctx->m_pool_vt, ctx->pool, static_cast<uint64_t>(pool_rows) * (d / 64), 64, 64) &&
+            (q8 || encode_2d(&ctx->m_pool, ctx->pool, pool_rows, d, 64)) &&
+            (q8 || encode_2d(&ctx->m_pool_vt, ctx->pool, static_cast<uint64_t>(pool_rows) * (d / 64), 64, 64)) &&
             encode_2d(&ctx->m_vblk, ctx->vb, static_cast<uint64_t>(c.max_batch) * nkv * d, 64, 64);
   ctx->m_wq.resize(c.n_layers);
   ctx->m_wk.resize(c.n_layers);
@@ -750,7 +757,8 @@ dflash_status dflash_fuse_ctx(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq
       e.in_ss_parts = parts;
       e.in_ss_ld = c.max_fuse_tokens;
       const double nw = 2.0 * nl * nkv * d;
-      ProfScope ps(ctx, DFLASH_K_FUSE_KV, stream, gemm_bytes(M, nw, H, nw, 2), 2.0 * M * nw * H);
+      const double out_b = c.kv_format == 1 ? 2.125 / 4.0 * 2 : 2;   // bytes per output value
+      ProfScope ps(ctx, DFLASH_K_FUSE_KV, stream, gemm_bytes(M, nw, H, nw, out_b), 2.0 * M * nw * H);
       CK(launch_gemm(am, rg, *xm, M, 2 * nl * tiles * 128, H, 0, e, work, ctx->num_sms, stream));
     }
   }
@@ -954,7 +962,7 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
   // (batch 1) keep one chunk per CTA; rows of mixed lengths get several
   // shorter chunks, and the short row tails fill the gaps.
   int& per_sm = ctx->attn_ctas_per_sm;
-  if (per_sm == 0) per_sm = attention_ctas_per_sm(d);
+  if (per_sm == 0) per_sm = attention_ctas_per_sm(d, c.kv_format == 1);
   const int grid_full = std::min(per_sm * ctx->num_sms, kSchedCtas);
   const long long item_cap = std::min<long long>(ctx->items_cap, kSchedItems);
   auto items_for = [&](int ch) {
@@ -1052,7 +1060,9 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
     ctx_tokens += ctx->len_ub[meta.slot[i]];
     attn_flops += 4.0 * B * nq * d * (ctx->len_ub[meta.slot[i]] + B);
   }
-  const double attn_bytes = ctx_tokens * nkv * d * 4 + 1.0 * M * nkv * d * 4 + 1.0 * M * nq * d * 2;
+  // context K/V per token and kv head: 4 d bytes (bf16) or 2 d codes + 2 d/32 fp16 scales (8-bit pages)
+  const double kv_token_head = c.kv_format == 1 ? 2.125 * d : 4.0 * d;
+  const double attn_bytes = ctx_tokens * nkv * kv_token_head + 1.0 * M * nkv * d * 4 + 1.0 * M * nq * d * 2;
   {
     ProfScope ps(ctx, DFLASH_K_NORM, stream, 8.0 * M * H, 0);
     CK(launch_embed(ctx->w.embed, anchor_ids, c.mask_id, tgt ? tgt->block_ids : nullptr, c.vocab, meta, H,
@@ -1068,6 +1078,7 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
       ARegions rg = stacked({nq * d, nkv * d, nkv * d});
       rg.pair = d / 2;
       GemmEpi e = base_epi(ctx, EPI_QKV_ROPE);
+      e.qkv_f16 = c.kv_format == 1;   // the 8-bit pages' attention runs in fp16
       e.out_q = ctx->q;
       e.out_k = ctx->kb;
       e.out_v = ctx->vb;
@@ -1099,6 +1110,7 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
       a.rows_pad = 16 * ceil_div((nq / nkv) * B, 16);
       a.spread = (nq / nkv) * B <= 64;
       a.causal = tgt ? 1 : 0;
+      a.q8 = c.kv_format == 1;
       a.q = ctx->q;
       a.pool = ctx->pool;
       a.part_o = ctx->part_o;
@@ -1360,6 +1372,32 @@ dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0
   CK(cudaMemcpy(&pend, ctx->d_pend + seq, sizeof(int), cudaMemcpyDeviceToHost));
   if (pos0 + n > len + pend) return fail(ctx, DFLASH_EINVAL, "positions beyond the cached tokens");
   const int d = c.head_dim, nkv = c.n_kv_heads;
+  if (c.kv_format == 1) {   // decoded 8-bit blocks, rounded to bf16
+    std::vector<int8_t> kc(static_cast<size_t>(n) * nkv * d), vc(kc.size());
+    std::vector<uint16_t> ks(static_cast<size_t>(n) * nkv * (d / 32)), vs(ks.size());
+    dflash_status st = dflash_debug_read_kv_q8(ctx, layer, seq, pos0, n, kc.data(), ks.data(), vc.data(), vs.data());
+    if (st != DFLASH_OK) return st;
+    auto h2f = [](uint16_t h) {   // fp16 -> fp32
+      const uint32_t sgn = (h & 0x8000u) << 16, ex = (h >> 10) & 0x1Fu, mant = h & 0x3FFu;
+      float v;
+      if (ex == 0) v = std::ldexp(static_cast<float>(mant), -24);
+      else if (ex == 31) v = mant ? NAN : INFINITY;
+      else v = std::ldexp(static_cast<float>(mant | 0x400u), static_cast<int>(ex) - 25);
+      return sgn ? -v : v;
+    };
+    auto f2bf = [](float f) {   // round to nearest even
+      uint32_t u;
+      std::memcpy(&u, &f, 4);
+      u += 0x7FFFu + ((u >> 16) & 1u);
+      return static_cast<uint16_t>(u >> 16);
+    };
+    for (size_t e = 0; e < kc.size(); ++e) {
+      const size_t blk = e / 32;
+      if (k_out) k_out[e] = f2bf(static_cast<float>(kc[e]) * h2f(ks[blk]));
+      if (v_out) v_out[e] = f2bf(static_cast<float>(vc[e]) * h2f(vs[blk]));
+    }
+    return DFLASH_OK;
+  }
   const size_t page_elems = static_cast<size_t>(2) * nkv * kPage * d;
   std::vector<uint16_t> buf(page_elems);
   int cur_page = -1;
@@ -1381,6 +1419,53 @@ dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0
       if (k_out) std::memcpy(k_out + (static_cast<size_t>(t) * nkv + h) * d, ks, d * 2);
       if (v_out)
         for (int di = 0; di < d; ++di) v_out[(static_cast<size_t>(t) * nkv + h) * d + di] = vs[static_cast<size_t>(di) * kPage];
+    }
+  }
+  return DFLASH_OK;
+}
+
+dflash_status dflash_debug_read_kv_q8(dflash_ctx* ctx, int layer, int seq, int pos0, int n, int8_t* k_codes,
+                                      uint16_t* k_scales, int8_t* v_codes, uint16_t* v_scales) {
+  if (!ctx) return DFLASH_EINVAL;
+  const dflash_config& c = ctx->cfg;
+  if (c.kv_format != 1) return fail(ctx, DFLASH_EINVAL, "the cache is not in the 8-bit format");
+  if (layer < 0 || layer >= c.n_layers || seq < 0 || seq >= c.max_seqs || pos0 < 0 || n < 0)
+    return fail(ctx, DFLASH_EINVAL, "argument out of range");
+  CK(cudaDeviceSynchronize());
+  int len = 0, pend = 0;
+  CK(cudaMemcpy(&len, ctx->d_len + seq, sizeof(int), cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(&pend, ctx->d_pend + seq, sizeof(int), cudaMemcpyDeviceToHost));
+  if (pos0 + n > len + pend) return fail(ctx, DFLASH_EINVAL, "positions beyond the cached tokens");
+  const int d = c.head_dim, nkv = c.n_kv_heads, nb = d / 32;
+  const size_t hb = q8_head_bytes(d);
+  std::vector<uint8_t> buf(hb * nkv);
+  const uint8_t* pool = reinterpret_cast<const uint8_t*>(ctx->pool);
+  int cur_page = -1;
+  for (int t = 0; t < n; ++t) {
+    const int pos = pos0 + t;
+    const int pi = pos / kPage;
+    if (pi >= static_cast<int>(ctx->pages[seq].size())) return fail(ctx, DFLASH_EINVAL, "position not paged");
+    const int page = ctx->pages[seq][pi];
+    if (page != cur_page) {
+      CK(cudaMemcpy(buf.data(), pool + (static_cast<size_t>(layer) * c.max_pages + page) * nkv * hb, hb * nkv,
+                    cudaMemcpyDeviceToHost));
+      cur_page = page;
+    }
+    const int slot = pos % kPage;
+    for (int h = 0; h < nkv; ++h) {
+      const uint8_t* r = buf.data() + h * hb;
+      const uint16_t* ksc = reinterpret_cast<const uint16_t*>(r + q8_kscale_off(d));
+      const uint16_t* vsc = reinterpret_cast<const uint16_t*>(r + q8_vscale_off(d));
+      for (int di = 0; di < d; ++di) {
+        const size_t o = (static_cast<size_t>(t) * nkv + h) * d + di;
+        if (k_codes) k_codes[o] = static_cast<int8_t>(r[slot * d + di]);
+        if (v_codes) v_codes[o] = static_cast<int8_t>(r[q8_vcode_off(d) + static_cast<size_t>(di) * kPage + slot]);
+      }
+      for (int b = 0; b < nb; ++b) {
+        const size_t o = (static_cast<size_t>(t) * nkv + h) * nb + b;
+        if (k_scales) k_scales[o] = ksc[slot * nb + b];
+        if (v_scales) v_scales[o] = vsc[b * kPage + slot];
+      }
     }
   }
   return DFLASH_OK;

@@ -73,6 +73,9 @@ typedef struct {
   int max_ctx;         /* most cached tokens per sequence (committed + pending)      */
   int max_pages;       /* KV pool size in 64-token pages (shared by all sequences)   */
   int max_fuse_tokens; /* most feature rows in one dflash_fuse_ctx call               */
+  int kv_format;       /* cached context K/V: 0 bf16; 1 8-bit blocks (q8_0: per head
+                          row, blocks of 32 values, int8 codes round(x/d) halves away
+                          from zero, d = max|x|/127 stored as fp16); drafter only  */
 } dflash_config;
 
 /* One drafter layer's weights, device pointers to bf16 (nn.Linear layout). */
@@ -355,10 +358,18 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
 /* ---- inspection hooks (used by the parity tests; they synchronise) ---- */
 
 /* Copy `n` cached tokens of layer `layer` of `seq`, starting at position
- * `pos0`, to host buffers k_out / v_out, each [n, n_kv_heads, d] bf16.
+ * `pos0`, to host buffers k_out / v_out, each [n, n_kv_heads, d] bf16
+ * (kv_format 1: the decoded values code * scale, rounded to bf16).
  * Positions may reach into the pending tokens. */
 dflash_status dflash_debug_read_kv(dflash_ctx* ctx, int layer, int seq, int pos0, int n,
                                    uint16_t* k_out, uint16_t* v_out);
+
+/* kv_format 1 only: the stored 8-bit blocks of `n` cached tokens, host
+ * outputs (any may be NULL): k_codes, v_codes [n, n_kv_heads, d] int8;
+ * k_scales, v_scales [n, n_kv_heads, d/32] fp16 bit patterns.
+ * EINVAL for a bf16 cache. */
+dflash_status dflash_debug_read_kv_q8(dflash_ctx* ctx, int layer, int seq, int pos0, int n, int8_t* k_codes,
+                                      uint16_t* k_scales, int8_t* v_codes, uint16_t* v_scales);
 
 /* State of the last dflash_draft call: the final residual stream
  * [n_seq*B, H] fp32 (before the final RMSNorm), and the winning logit of each

@@ -38,8 +38,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match_the_header(lib):
-    # 15 ints + 2 floats; 9 pointers; 5 pointers + 1 pointer
-    assert ctypes.sizeof(dfl.dflash_config) == 17 * 4
+    # 16 ints + 2 floats; 9 pointers; 5 pointers + 1 pointer
+    assert ctypes.sizeof(dfl.dflash_config) == 18 * 4
     assert ctypes.sizeof(dfl.dflash_layer_weights) == 9 * ctypes.sizeof(ctypes.c_void_p)
     assert ctypes.sizeof(dfl.dflash_weights) == 6 * ctypes.sizeof(ctypes.c_void_p)
 
