@@ -551,6 +551,22 @@ def run_ours(args):
     ms_sel, ms_plain = (ms_draft, ms_other) if args.path_selector else (ms_other, ms_draft)
     st_sel = stats if args.path_selector else st_other
     n_sel = K if args.path_selector else kd
+    # the drafter pass with the DFlash 2 two-tap convolutions (four sites per
+    # layer, rank CONV_RANK) against the plain pass
+    conv_raw = None
+    if not args.path_selector and not args.sampling and shape.hidden % 128 == 0:
+        cw = conv_weights(shape, dev, seed=11 + rank)
+        cyc.d.set_conv(cw, CONV_RANK)
+        for _ in range(3):
+            cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts)
+        ms_conv = timed(lambda k: cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts), kd, world, dev)
+        cyc.d.profile_read()
+        cyc.d.profile(True)
+        timed(lambda k: cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts), kd, world, dev)
+        cyc.d.profile(False)
+        conv_raw = (cyc.d.profile_read(), ms_conv / kd, ms_draft / kd)
+        cyc.d.set_conv(None)
+        del cw
 
     targets = None
     weights = cyc.weights
@@ -633,6 +649,8 @@ def run_ours(args):
         "latency_model": latency_model(ms_draft / kd, ms_step, peaks["hbm_gbs"], B, target_cycle),
         "kernels": kernels,
         "path_selector": selector_summary(st_sel, n_sel, ms_sel / kd, ms_plain / kd, peaks, peak_kind, batch, world),
+        "conv": (conv_summary(conv_raw[0], kd, conv_raw[1], conv_raw[2], stats, K, peaks, peak_kind, batch, world)
+                 if conv_raw else None),
         "sampling": samp_out,
     }
     if targets is not None:
@@ -872,6 +890,42 @@ def sampling_summary(cyc, kd: int, world: int, dev, ms_plain_total):
     if ms_plain_total:
         out["draft_plain_ms_per_pass"] = ms_plain_total / kd
         out["draft_sample_overhead_ms"] = (ms_ds - ms_plain_total) / kd
+    return out
+
+
+CONV_RANK = 80   # the two-tap convolutions' correction rank (the reading of the DFlash 2 parameter count)
+
+
+def conv_weights(shape, dev, seed: int):
+    """Seeded two-tap convolution weights of every layer on the device."""
+    import torch
+    from synth import make_conv_weights_np
+    cv = lambda a: torch.from_numpy(a).to(torch.bfloat16).to(dev)
+    return [{site: {k: cv(v) for k, v in c.items()} for site, c in layer.items()}
+            for layer in make_conv_weights_np(shape, rank=CONV_RANK, seed=seed)]
+
+
+def conv_summary(st, n, ms_conv: float, ms_plain: float, st_plain, n_plain, peaks, peak_kind: str, batch: int,
+                 world: int):
+    """The drafter pass with the two-tap convolutions against the plain pass:
+    the overhead, the apply kernels against the HBM roofline, and the O/down
+    projections' growth (their 2r extra rows carry the output sites'
+    products). The notes put the convolutions at 0.7 % of their latency."""
+    cv = st.get("conv", {})
+    out = {"rank": CONV_RANK, "sites_per_layer": 4, "batch": batch,
+           "passes_per_s": whole_job_rate(1, world, ms_conv) if ms_conv else None, "ms_per_pass": ms_conv,
+           "plain_ms_per_pass": ms_plain, "overhead_ms": ms_conv - ms_plain, "overhead_frac": ms_conv / ms_plain - 1.0,
+           "pages_overhead_frac": 0.007}
+    if cv.get("launches") and cv.get("ms"):
+        gbs = cv["bytes"] / (cv["ms"] / 1e3) / 1e9
+        out.update({"conv_us_per_pass": 1e3 * cv["ms"] / n, "conv_launches_per_pass": cv["launches"] / n,
+                    "conv_GB_per_pass": cv["bytes"] / n / 1e9,
+                    "conv_roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_kind} hbm_gbs"}})
+    od = [st.get(k, {}).get("ms", 0.0) for k in ("o", "down")]
+    od_plain = [st_plain.get(k, {}).get("ms", 0.0) for k in ("o", "down")]
+    out["o_down_us_per_pass"] = 1e3 * sum(od) / n
+    out["o_down_plain_us_per_pass"] = 1e3 * sum(od_plain) / n_plain
     return out
 
 

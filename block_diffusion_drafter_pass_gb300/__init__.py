@@ -31,13 +31,13 @@ EXPORTED = (
     "dflash_block_sched_create", "dflash_block_sched_destroy", "dflash_block_sched_observe",
     "dflash_block_sched_set_cost", "dflash_block_sched_expected_tau", "dflash_block_sched_choose",
     "dflash_debug_wait_timeout", "dflash_target_feature_layers", "dflash_target_create", "dflash_target_forward",
-    "dflash_debug_read_kv_q8",
+    "dflash_debug_read_kv_q8", "dflash_set_conv",
 )
 SAMPLE_WIDTH = 32   # DFLASH_SAMPLE_WIDTH
 
 # Kernel classes of the per-kernel accounting (DFLASH_K_* in include/dflash.h).
 KERNEL_CLASSES = ("qkv", "attn", "attn_combine", "o", "gateup", "down", "lmhead", "fuse_wc", "fuse_kv", "norm",
-                  "verify", "other", "select", "sample")
+                  "verify", "other", "select", "sample", "conv")
 
 
 class DFlashError(RuntimeError):
@@ -57,6 +57,13 @@ class dflash_config(ctypes.Structure):
 class dflash_layer_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down",
                                                "g_attn", "g_ffn")]
+
+
+class dflash_conv_site(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("base", "u", "v")]
+
+
+CONV_SITES = ("ai", "ao", "fi", "fo")   # per layer: attention in/out, feed-forward in/out
 
 
 class dflash_kernel_stat(ctypes.Structure):
@@ -101,6 +108,7 @@ def load_library() -> ctypes.CDLL:
         "dflash_debug_profile_read": ([VP, P(dflash_kernel_stat), I], I),
         "dflash_gemm_noalloc": ([VP, VP, VP, I, I, I, I, VP], I),
         "dflash_set_path_selector": ([VP, VP, VP, VP, I, VP], I),
+        "dflash_set_conv": ([VP, VP, I, VP], I),
         "dflash_debug_last_selection": ([VP, VP, VP, VP], I),
         "dflash_draft_sample": ([VP, i32p, I, VP, I, ctypes.c_float, I, ctypes.c_float, VP, VP, VP, VP, VP], I),
         "dflash_sample_filter": ([VP, VP, I, I, ctypes.c_float, I, ctypes.c_float, VP, VP, VP, VP, VP], I),
@@ -327,6 +335,31 @@ class Drafter:
         _check(load_library().dflash_set_path_selector(self.ctx, _ptr(w_a), _ptr(w_b), _ptr(w_h), w_a.shape[0],
                                                        _stream(stream)), self.ctx)
         self._sel = ws   # W_H is read by every draft
+
+    def set_conv(self, sites=None, rank: int = 0, stream=None) -> None:
+        """Install the DFlash 2 two-tap convolutions: `sites` is a list over
+        layers of dicts {"ai", "ao", "fi", "fo"} of dicts {"base" [2, H],
+        "U" [2, H, r], "V" [2, r, H]} (contiguous bf16 CUDA tensors); None
+        removes them."""
+        import torch
+        if sites is None:
+            _check(load_library().dflash_set_conv(self.ctx, None, 0, _stream(stream)), self.ctx)
+            self._conv = None
+            return
+        arr = (dflash_conv_site * (4 * len(sites)))()
+        keep = []
+        for l, layer in enumerate(sites):
+            for k, name in enumerate(CONV_SITES):
+                c = layer[name]
+                for key in ("base", "U", "V"):
+                    t = c[key]
+                    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                        raise DFlashError(DFLASH_EINVAL, "conv arrays must be contiguous bf16 CUDA tensors")
+                    keep.append(t)
+                arr[4 * l + k] = dflash_conv_site(_ptr(c["base"]), _ptr(c["U"]), _ptr(c["V"]))
+        _check(load_library().dflash_set_conv(self.ctx, ctypes.cast(arr, ctypes.c_void_p), rank, _stream(stream)),
+               self.ctx)
+        self._conv = keep   # borrowed by every draft
 
     # temperature sampling ------------------------------------------------------
     def draft_sample(self, seq_ids, anchor_ids, B: int, temperature: float, top_k: int, top_p: float, uniforms,

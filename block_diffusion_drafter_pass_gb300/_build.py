@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdflash.so")
 SOURCES = ["runtime.cu", "gemm_tc.cu", "gemm_ec_f32.cu", "gemm_ec_norm.cu", "gemm_ec_rope.cu", "gemm_ec_swiglu.cu",
-           "gemm_ec_argmax.cu", "attention.cu", "small_ops.cu", "noalloc.cu", "path_selector.cu", "sampling.cu", "block_sched.cu"]
+           "gemm_ec_argmax.cu", "attention.cu", "small_ops.cu", "noalloc.cu", "path_selector.cu", "sampling.cu", "block_sched.cu", "conv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC] + ARCH
 

@@ -276,6 +276,52 @@ cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStre
 cudaError_t launch_rows_argmax_bf16(const uint16_t* logits, int rows, int cols, int32_t* out, cudaStream_t s);
 
 // ----------------------------------------------------------------------------
+// Two-tap dynamic convolution (DFlash 2): one apply kernel per site, CTAs of
+// kConvCols columns x 16 rows. Rows are n_seq blocks of B positions; row m's
+// predecessor is m - 1 unless m % B == 0.
+// Input site (out_h set): x_t = rms_scale(ss, m) * xin[m] * gin; P = P[m]
+//   (times the row's scale unless p_scaled); out_h[m] = bf16(Conv(x)_m); the
+//   CTAs zero `zero` ([M][2r], may be null) between them.
+// Output site (out_h null): x_t = y[m][0..H), P = y[m][H..H+2r);
+//   x[m] += Conv(y)_m, out_hg = bf16(x * gain), out_ss[H / kConvCols parts][m]
+//   = sum over the part's columns of x^2; with vt set, pacc[m][j] (zero
+//   before) += the next input site's V_next (x * gain) over the CTA's columns.
+// ----------------------------------------------------------------------------
+constexpr int kConvMaxRank = 128;
+constexpr int kConvCols = 32;      // columns per CTA = columns per sums-of-squares part
+struct ConvArgs {
+  int M, H, r, B;
+  const uint16_t* base;   // [2][H] bf16
+  const uint16_t* U;      // [2][H][r] bf16
+  // input site
+  const float* xin;       // [M][H] residual stream
+  const uint16_t* gin;    // [H] the RMSNorm gain
+  const float* ss;        // [ss_parts][ss_ld] sums of x^2
+  int ss_parts, ss_ld;
+  float inv_hidden, eps;
+  const float* P;         // [M][2r]
+  int p_scaled;           // P already carries the RMSNorm scale
+  uint16_t* out_h;        // [M][H]
+  float* zero;            // [M][2r] accumulator to clear, or null
+  // output site
+  const float* y;         // [M][ld_y]: the sublayer output, then its 2r products with V
+  int ld_y;
+  float* x;               // [M][H] residual stream
+  uint16_t* out_hg;       // [M][H]
+  const uint16_t* gain;   // [H] the next RMSNorm's gain
+  float* out_ss;          // [H/kConvCols][out_ss_ld]
+  int out_ss_ld;
+  const uint16_t* vt;     // [H][2r] the next input site's V, transposed (null: none)
+  float* pacc;            // [M][2r] accumulator of the next input site's products
+  int* status;
+};
+cudaError_t launch_conv_apply(const ConvArgs& a, cudaStream_t s);
+size_t conv_smem_bytes(int r);   // dynamic shared memory of the apply kernel at rank r (upper bound)
+// Install time: F[j][c] = sum_h V[j][h] W[h][c] (bf16, fp32 sums); transpose of a bf16 matrix.
+cudaError_t launch_conv_fold(const uint16_t* V, const uint16_t* W, int J, int H, int K, uint16_t* F, cudaStream_t s);
+cudaError_t launch_transpose_bf16(const uint16_t* in, int rows, int cols, uint16_t* out, cudaStream_t s);
+
+// ----------------------------------------------------------------------------
 // Path selector (DFlash 2): top-16 candidates per draft row, 16 x 16 pair
 // scores per adjacent pair of positions, greedy walk per sequence.
 // ----------------------------------------------------------------------------

@@ -131,6 +131,19 @@ struct dflash_ctx {
   unsigned long long* samp_part = nullptr; // [max_rows][64][32] sampling slice lists
   int* sel_tickets = nullptr;              // [max_batch]
 
+  // two-tap convolutions (installed by dflash_set_conv)
+  bool conv_on = false;
+  int conv_rank = 0, conv_alloc_rank = 0;
+  std::vector<dflash_conv_site> conv_sites;   // [n_layers][ai, ao, fi, fo]
+  uint16_t* conv_fold = nullptr;   // per layer: V_ao W_o [2r][n_q d], then V_fo W_d [2r][F]
+  uint16_t* conv_vt = nullptr;     // per layer: V_ai^T, then V_fi^T, each [H][2r]
+  float* conv_yp = nullptr;        // [max_rows][H + 2r] sublayer output | its products with V
+  uint16_t* conv_h = nullptr;      // [max_rows][H] convolved input of QKV / gate-up
+  float* conv_p = nullptr;         // [max_rows][2r] layer 0's V_ai products (scaled)
+  float* conv_acc = nullptr;       // [2][max_rows][2r] accumulators of an input site's products
+  std::vector<CUtensorMap> m_fold_o, m_fold_d;
+  CUtensorMap m_vai0{};
+
   // weight descriptors
   std::vector<CUtensorMap> m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd;
   CUtensorMap m_lm{}, m_wc{}, m_pool{}, m_pool_vt{}, m_vblk{};
@@ -360,7 +373,8 @@ dflash_status dflash_destroy(dflash_ctx* ctx) {
                   ctx->part_o, ctx->part_ml, ctx->split_ws, ctx->tickets, ctx->keys, ctx->done, ctx->top_logit,
                   ctx->sel_table, ctx->sel_logits, ctx->sel_part, ctx->sel_scores, ctx->sel_cand, ctx->sel_cand_u,
                   ctx->sel_tickets, ctx->sel_next,
-                  ctx->samp_part};
+                  ctx->samp_part, ctx->conv_fold, ctx->conv_vt, ctx->conv_yp, ctx->conv_h, ctx->conv_p,
+                  ctx->conv_acc};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (ctx->h_snap) cudaFreeHost(ctx->h_snap);
@@ -485,8 +499,9 @@ dflash_status create_impl(const dflash_config* cfg_in, const dflash_weights* w, 
   const int parts = ceil_div(H, 128);
   CA(dalloc(&ctx->x, rows * H), "workspace");
   CA(dalloc(&ctx->hg, rows * H), "workspace");
-  CA(dalloc(&ctx->ssA, rows * parts), "workspace");
-  CA(dalloc(&ctx->ssB, rows * parts), "workspace");
+  // sums-of-squares parts: 128-column GEMM tiles, or the convolutions' 32-column parts
+  CA(dalloc(&ctx->ssA, rows * ceil_div(H, kConvCols)), "workspace");
+  CA(dalloc(&ctx->ssB, rows * ceil_div(H, kConvCols)), "workspace");
   CA(dalloc(&ctx->q, rows * nq * d), "workspace");
   CA(dalloc(&ctx->kb, rows * nkv * d), "workspace");
   const size_t vb_elems = static_cast<size_t>(c.max_batch) * nkv * d * kPage;
@@ -1045,10 +1060,80 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
   const CUtensorMap* hmap_lm = act_map(ctx, ctx->hg, M, H, gemm_act_rows(M, c.vocab, H, sms));
   const int parts = ceil_div(H, 128);
   const int rows_ld = ctx->max_rows();
-  const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, gemm_act_rows(M, H, nq * d, sms));
-  const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, gemm_act_rows(M, H, F, sms));
+  // two-tap convolutions: the O and down projections carry 2r extra rows
+  // (V W of the output sites), QKV and gate/up read the convolved rows
+  const bool conv = ctx->conv_on && !tgt;
+  const int r2c = conv ? 2 * ctx->conv_rank : 0;
+  const CUtensorMap* amap = act_map(ctx, ctx->attn, M, nq * d, gemm_act_rows(M, H + r2c, nq * d, sms));
+  const CUtensorMap* fmap = act_map(ctx, ctx->act, M, F, gemm_act_rows(M, H + r2c, F, sms));
   if (!km || !hmap_qkv || !hmap_gu || !hmap_lm || !amap || !fmap)
     return fail(ctx, DFLASH_ECUDA, "activation descriptor encode failed");
+  const CUtensorMap *cmap_qkv = nullptr, *cmap_gu = nullptr, *hmap_p0 = nullptr;
+  if (conv) {
+    cmap_qkv = act_map(ctx, ctx->conv_h, M, H, gemm_act_rows(M, n_qkv, H, sms));
+    cmap_gu = act_map(ctx, ctx->conv_h, M, H, gemm_act_rows(M, n_gu, H, sms));
+    hmap_p0 = act_map(ctx, ctx->hg, M, H, gemm_act_rows(M, r2c, H, sms));
+    if (!cmap_qkv || !cmap_gu || !hmap_p0) return fail(ctx, DFLASH_ECUDA, "conv descriptor encode failed");
+  }
+  auto conv_args = [&](int l, int site) {
+    ConvArgs ca;
+    std::memset(&ca, 0, sizeof(ca));
+    const dflash_conv_site& cs = ctx->conv_sites[4 * l + site];
+    ca.M = M;
+    ca.H = H;
+    ca.r = ctx->conv_rank;
+    ca.B = B;
+    ca.base = cs.base;
+    ca.U = cs.u;
+    ca.inv_hidden = 1.0f / H;
+    ca.eps = c.rms_eps;
+    ca.status = ctx->d_status;
+    return ca;
+  };
+  // apply kernel traffic: U (and the next V^T) slices, the rows in and out
+  const double conv_w_bytes = 2.0 * H * r2c * 2;
+  const size_t acc_elems = static_cast<size_t>(rows_ld) * r2c;
+  // sums-of-squares parts the apply kernels write (32-column parts)
+  const int conv_parts = ceil_div(H, kConvCols);
+  auto conv_in_site = [&](int l, int site, const uint16_t* gain, const float* ss, int ss_parts, const float* P,
+                          bool p_scaled, float* zero) -> dflash_status {
+    ConvArgs ca = conv_args(l, site);
+    ca.xin = ctx->x;
+    ca.gin = gain;
+    ca.ss = ss;
+    ca.ss_parts = ss_parts;
+    ca.ss_ld = rows_ld;
+    ca.P = P;
+    ca.p_scaled = p_scaled ? 1 : 0;
+    ca.zero = zero;
+    ca.out_h = ctx->conv_h;
+    ProfScope ps(ctx, DFLASH_K_CONV, stream, conv_w_bytes / 2 + 6.0 * M * H + 4.0 * M * r2c,
+                 2.0 * M * H * r2c + 3.0 * M * H);
+    CK(launch_conv_apply(ca, stream));
+    return DFLASH_OK;
+  };
+  auto conv_out_site = [&](int l, int site, const uint16_t* gain, float* out_ss, const uint16_t* vt,
+                           float* pacc) -> dflash_status {
+    ConvArgs ca = conv_args(l, site);
+    ca.y = ctx->conv_yp;
+    ca.ld_y = H + r2c;
+    ca.x = ctx->x;
+    ca.out_hg = ctx->hg;
+    ca.gain = gain;
+    ca.out_ss = out_ss;
+    ca.out_ss_ld = rows_ld;
+    ca.vt = vt;
+    ca.pacc = pacc;
+    ProfScope ps(ctx, DFLASH_K_CONV, stream,
+                 (vt ? conv_w_bytes : conv_w_bytes / 2) + 1.0 * M * (H + r2c) * 4 + 10.0 * M * H +
+                     (vt ? 4.0 * M * r2c : 0),
+                 2.0 * M * H * r2c * (vt ? 1.5 : 1.0) + 6.0 * M * H);
+    CK(launch_conv_apply(ca, stream));
+    return DFLASH_OK;
+  };
+  auto vt_of = [&](int l, int which) {   // which 0: V_ai^T, 1: V_fi^T
+    return ctx->conv_vt + static_cast<size_t>(2 * l + which) * H * r2c;
+  };
   AttnMaps attn_maps;
   attn_maps.pool_k = ctx->m_pool;
   attn_maps.pool_vt = ctx->m_pool_vt;
@@ -1070,6 +1155,26 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
   }
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = ctx->layers[l];
+    if (conv) {   // h = Conv_ai(RMSNorm(x)); layer 0's products V_ai x from one GEMM over the embedding rows
+      if (l == 0) {
+        AMaps am;
+        am.m[0] = ctx->m_vai0;
+        GemmEpi e = base_epi(ctx, EPI_F32_STORE);
+        e.out_f32 = ctx->conv_p;
+        e.ld_out = r2c;
+        e.in_ss = ctx->ssA;
+        e.in_ss_parts = 1;
+        e.in_ss_ld = rows_ld;
+        ProfScope ps(ctx, DFLASH_K_CONV, stream, gemm_bytes(M, r2c, H, r2c, 4), 2.0 * M * r2c * H);
+        CK(launch_gemm(am, stacked({r2c}), *hmap_p0, M, r2c, H, 0, e, work, ctx->num_sms, stream));
+      }
+      // P: layer 0's from the GEMM (scaled); later layers' accumulated by the
+      // previous layer's feed-forward output site (accumulator 1). Clears
+      // accumulator 0 for this layer's attention output site.
+      const dflash_status st = conv_in_site(l, 0, L.g_attn, ctx->ssA, l == 0 ? 1 : conv_parts,
+                                            l == 0 ? ctx->conv_p : ctx->conv_acc + acc_elems, l == 0, ctx->conv_acc);
+      if (st != DFLASH_OK) return st;
+    }
     {  // q, k, v with RoPE at positions len .. len+B-1
       AMaps am;
       am.m[0] = ctx->m_wq[l];
@@ -1083,12 +1188,12 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
       e.out_k = ctx->kb;
       e.out_v = ctx->vb;
       e.meta = meta;
-      e.in_ss = ctx->ssA;
+      e.in_ss = conv ? nullptr : ctx->ssA;   // the convolved rows are normalised already
       e.in_ss_parts = l == 0 ? 1 : parts;
       e.in_ss_ld = rows_ld;
       const double nw = 1.0 * (nq + 2 * nkv) * d;
       ProfScope ps(ctx, DFLASH_K_QKV, stream, gemm_bytes(M, nw, H, nw, 2), 2.0 * M * nw * H);
-      CK(launch_gemm(am, rg, *hmap_qkv, M, n_qkv, H, 0, e, work, ctx->num_sms, stream));
+      CK(launch_gemm(am, rg, conv ? *cmap_qkv : *hmap_qkv, M, n_qkv, H, 0, e, work, ctx->num_sms, stream));
     }
     if (tgt) {   // the block's K/V into the target's own cache
       ProfScope ps(ctx, DFLASH_K_OTHER, stream, 4.0 * M * nkv * d * 2, 0);
@@ -1126,7 +1231,22 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
         CK(launch_attention(attn_maps, a, sched, attn_grid, 1, stream));
       }
     }
-    {  // x += attn W_o^T; the FFN's RMSNorm input is folded into the epilogue
+    if (conv) {   // [attn W_o^T | attn (V_ao W_o)^T], then x += Conv_ao, then h = Conv_fi(RMSNorm(x))
+      AMaps am;
+      am.m[0] = ctx->m_wo[l];
+      am.m[1] = ctx->m_fold_o[l];
+      GemmEpi e = base_epi(ctx, EPI_F32_STORE);
+      e.out_f32 = ctx->conv_yp;
+      e.ld_out = H + r2c;
+      {
+        ProfScope ps(ctx, DFLASH_K_O, stream, gemm_bytes(M, H + r2c, nq * d, H + r2c, 4), 2.0 * M * (H + r2c) * nq * d);
+        CK(launch_gemm(am, stacked({H, r2c}), *amap, M, H + r2c, nq * d, 0, e, work, ctx->num_sms, stream));
+      }
+      dflash_status st = conv_out_site(l, 1, L.g_ffn, ctx->ssB, vt_of(l, 1), ctx->conv_acc);
+      if (st == DFLASH_OK)
+        st = conv_in_site(l, 2, L.g_ffn, ctx->ssB, conv_parts, ctx->conv_acc, false, ctx->conv_acc + acc_elems);
+      if (st != DFLASH_OK) return st;
+    } else {  // x += attn W_o^T; the FFN's RMSNorm input is folded into the epilogue
       AMaps am;
       am.m[0] = ctx->m_wo[l];
       GemmEpi e = base_epi(ctx, EPI_RESID);
@@ -1151,13 +1271,28 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
       GemmEpi e = base_epi(ctx, EPI_SWIGLU);
       e.out_act = ctx->act;
       e.n_valid = F;
-      e.in_ss = ctx->ssB;
+      e.in_ss = conv ? nullptr : ctx->ssB;
       e.in_ss_parts = parts;
       e.in_ss_ld = rows_ld;
       ProfScope ps(ctx, DFLASH_K_GATEUP, stream, gemm_bytes(M, 2.0 * F, H, F, 2), 4.0 * M * F * H);
-      CK(launch_gemm(am, rg, *hmap_gu, M, n_gu, H, 0, e, work, ctx->num_sms, stream));
+      CK(launch_gemm(am, rg, conv ? *cmap_gu : *hmap_gu, M, n_gu, H, 0, e, work, ctx->num_sms, stream));
     }
-    {  // x += act W_down^T; the next RMSNorm (next layer's input, or the final norm) is folded in
+    if (conv) {   // [act W_down^T | act (V_fo W_down)^T], then x += Conv_fo (+ the next layer's V_ai products)
+      AMaps am;
+      am.m[0] = ctx->m_wd[l];
+      am.m[1] = ctx->m_fold_d[l];
+      GemmEpi e = base_epi(ctx, EPI_F32_STORE);
+      e.out_f32 = ctx->conv_yp;
+      e.ld_out = H + r2c;
+      {
+        ProfScope ps(ctx, DFLASH_K_DOWN, stream, gemm_bytes(M, H + r2c, F, H + r2c, 4), 2.0 * M * (H + r2c) * F);
+        CK(launch_gemm(am, stacked({H, r2c}), *fmap, M, H + r2c, F, 0, e, work, ctx->num_sms, stream));
+      }
+      const bool last = l + 1 == c.n_layers;
+      const dflash_status st = conv_out_site(l, 3, last ? ctx->w.g_final : ctx->layers[l + 1].g_attn, ctx->ssA,
+                                             last ? nullptr : vt_of(l + 1, 0), ctx->conv_acc + acc_elems);
+      if (st != DFLASH_OK) return st;
+    } else {  // x += act W_down^T; the next RMSNorm (next layer's input, or the final norm) is folded in
       AMaps am;
       am.m[0] = ctx->m_wd[l];
       GemmEpi e = base_epi(ctx, EPI_RESID);
@@ -1189,7 +1324,7 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
     e.out_logit = ctx->top_logit;
     e.argmax_skip_B = 0;
     e.in_ss = ctx->ssA;
-    e.in_ss_parts = parts;
+    e.in_ss_parts = conv ? conv_parts : parts;
     e.in_ss_ld = rows_ld;
     {
       ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(M, c.vocab, H, 1, 8), 2.0 * M * c.vocab * H);
@@ -1220,7 +1355,7 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
     e.out_f32 = ctx->sel_logits;
     e.ld_out = ctx->sel_ld;
     e.in_ss = ctx->ssA;
-    e.in_ss_parts = parts;
+    e.in_ss_parts = conv ? conv_parts : parts;
     e.in_ss_ld = rows_ld;
     {
       ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(M, c.vocab, H, c.vocab, 4), 2.0 * M * c.vocab * H);
@@ -1254,7 +1389,7 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
     e.out_f32 = ctx->sel_logits;
     e.ld_out = ctx->sel_ld;
     e.in_ss = ctx->ssA;
-    e.in_ss_parts = parts;
+    e.in_ss_parts = conv ? conv_parts : parts;
     e.in_ss_ld = rows_ld;
     {
       ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(M, n_out, H, n_out, 4), 2.0 * M * n_out * H);
@@ -1299,7 +1434,7 @@ dflash_status draft_impl(dflash_ctx* ctx, const int32_t* seq_ids, int n_seq, con
     e.out_logit = ctx->top_logit;
     e.argmax_skip_B = B;
     e.in_ss = ctx->ssA;
-    e.in_ss_parts = parts;
+    e.in_ss_parts = conv ? conv_parts : parts;
     e.in_ss_ld = rows_ld;
     ProfScope ps(ctx, DFLASH_K_LMHEAD, stream, gemm_bytes(Md, c.vocab, H, 1, 8), 2.0 * Md * c.vocab * H);
     CK(launch_gemm(am, stacked({c.vocab}), *hmap_lm, M, c.vocab, H, 0, e, work, ctx->num_sms, stream));
@@ -1608,6 +1743,71 @@ dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, con
   }
   CK(cudaStreamSynchronize(stream));
   ctx->sel_on = true;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_set_conv(dflash_ctx* ctx, const dflash_conv_site* sites, int rank, void* stream_v) {
+  ApiRange nvtx_range("dflash_set_conv");
+  if (!ctx) return DFLASH_EINVAL;
+  if (ctx->target) return fail(ctx, DFLASH_EINVAL, "the two-tap convolutions belong to a drafter context");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const dflash_config& c = ctx->cfg;
+  const int H = c.hidden, nl = c.n_layers, ko = c.n_heads * c.head_dim, F = c.ffn;
+  if (!sites) {
+    ctx->conv_on = false;
+    return DFLASH_OK;
+  }
+  if (rank < 8 || rank > kConvMaxRank || rank % 8 != 0)
+    return fail(ctx, DFLASH_EINVAL, "conv rank must be a multiple of 8 in [8, 128]");
+  if (H % 128 != 0) return fail(ctx, DFLASH_EINVAL, "the two-tap convolutions need hidden % 128 == 0");
+  for (int i = 0; i < 4 * nl; ++i) {
+    const dflash_conv_site& cs = sites[i];
+    if (!cs.base || !cs.u || !cs.v) return fail(ctx, DFLASH_EINVAL, "a conv site has a NULL array");
+    if (!aligned16(cs.base) || !aligned16(cs.u) || !aligned16(cs.v))
+      return fail(ctx, DFLASH_EINVAL, "conv arrays must be 16-byte aligned");
+  }
+  const int r2 = 2 * rank;
+  const size_t rows = ctx->max_rows();
+  ctx->conv_on = false;
+  if (ctx->conv_alloc_rank != rank) {
+    void* old[] = {ctx->conv_fold, ctx->conv_vt, ctx->conv_yp, ctx->conv_h, ctx->conv_p, ctx->conv_acc};
+    for (void* p : old)
+      if (p) cudaFree(p);
+    ctx->conv_fold = ctx->conv_h = ctx->conv_vt = nullptr;
+    ctx->conv_yp = ctx->conv_p = ctx->conv_acc = nullptr;
+    ctx->conv_alloc_rank = 0;
+    cudaError_t e = dalloc(&ctx->conv_fold, static_cast<size_t>(nl) * r2 * (ko + F));
+    if (e == cudaSuccess) e = dalloc(&ctx->conv_vt, static_cast<size_t>(nl) * 2 * H * r2);
+    if (e == cudaSuccess) e = dalloc(&ctx->conv_yp, rows * (H + r2));
+    if (e == cudaSuccess) e = dalloc(&ctx->conv_h, rows * H);
+    if (e == cudaSuccess) e = dalloc(&ctx->conv_p, rows * r2);
+    if (e == cudaSuccess) e = dalloc(&ctx->conv_acc, 2 * rows * r2);
+    if (e != cudaSuccess)
+      return fail(ctx, e == cudaErrorMemoryAllocation ? DFLASH_ENOMEM : DFLASH_ECUDA,
+                  std::string("conv buffers: ") + cudaGetErrorString(e));
+    ctx->conv_alloc_rank = rank;
+  }
+  ctx->m_fold_o.assign(nl, CUtensorMap{});
+  ctx->m_fold_d.assign(nl, CUtensorMap{});
+  for (int l = 0; l < nl; ++l) {
+    const dflash_layer_weights& L = ctx->layers[l];
+    uint16_t* fo = ctx->conv_fold + static_cast<size_t>(l) * r2 * (ko + F);
+    uint16_t* fd = fo + static_cast<size_t>(r2) * ko;
+    CK(launch_conv_fold(sites[4 * l + 1].v, L.w_o, r2, H, ko, fo, stream));
+    CK(launch_conv_fold(sites[4 * l + 3].v, L.w_down, r2, H, F, fd, stream));
+    CK(launch_transpose_bf16(sites[4 * l + 0].v, r2, H, ctx->conv_vt + static_cast<size_t>(2 * l) * H * r2, stream));
+    CK(launch_transpose_bf16(sites[4 * l + 2].v, r2, H, ctx->conv_vt + static_cast<size_t>(2 * l + 1) * H * r2,
+                             stream));
+    if (!encode_2d(&ctx->m_fold_o[l], fo, r2, ko, kWeightBoxRows) ||
+        !encode_2d(&ctx->m_fold_d[l], fd, r2, F, kWeightBoxRows))
+      return fail(ctx, DFLASH_ECUDA, "conv fold descriptor encode failed");
+  }
+  if (!encode_2d(&ctx->m_vai0, sites[0].v, r2, H, kWeightBoxRows))
+    return fail(ctx, DFLASH_ECUDA, "conv V descriptor encode failed");
+  CK(cudaStreamSynchronize(stream));
+  ctx->conv_sites.assign(sites, sites + 4 * nl);
+  ctx->conv_rank = rank;
+  ctx->conv_on = true;
   return DFLASH_OK;
 }
 

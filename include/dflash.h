@@ -355,6 +355,43 @@ dflash_status dflash_block_sched_choose(const dflash_block_sched* s, int* B_out)
 dflash_status dflash_set_path_selector(dflash_ctx* ctx, const uint16_t* w_a, const uint16_t* w_b,
                                        const uint16_t* w_h, int dim, void* stream);
 
+/* One site of the DFlash 2 two-tap dynamic convolution ("DFlash 2" notes,
+ * "Solution - Two-Tap Dynamic Convolution"): over the block positions t of
+ * each sequence,
+ *     Conv(x)_t = k_{t,0} * x_t + k_{t,1} * x_{t-1}     (* elementwise),
+ *     k_{t,i}   = base_i + U_i (V_i x_t),
+ * x_{-1} = 0 for the block's first position (the anchor); the first masked
+ * position reads the anchor. The correction is a rank-`rank` map of the
+ * position's own input (the notes leave its form open; 20 sites of two such
+ * taps at rank 80 and hidden 2560 give the 16.5M parameters they state).
+ * All three device arrays are bf16, 16-byte aligned, and borrowed like the
+ * model weights:
+ *   base  [2][hidden]          tap 0 (position t), tap 1 (position t - 1)
+ *   u     [2][hidden][rank]
+ *   v     [2][rank][hidden] */
+typedef struct {
+  const uint16_t* base;
+  const uint16_t* u;
+  const uint16_t* v;
+} dflash_conv_site;
+
+/* Install (or remove) the two-tap convolutions of a drafter context: four
+ * sites per layer, in the order
+ *     ai  on the attention input       h = Conv_ai(RMSNorm(x))
+ *     ao  on the attention output      x += Conv_ao(Attn(h) W_o^T)
+ *     fi  on the feed-forward input    h = Conv_fi(RMSNorm(x))
+ *     fo  on the feed-forward output   x += Conv_fo(FFN(h))
+ * `sites` is a host array of 4 * n_layers entries (layer-major); NULL
+ * removes the convolutions. The injected context K/V do not pass through
+ * them. The library keeps, per layer, V_ao W_o and V_fo W_d (the output
+ * sites' products come out of the O and down projections as 2 * rank extra
+ * rows) and V_ai, V_fi transposed: 2 * rank * (2 * hidden + n_q * d + ffn)
+ * bf16 per layer, plus row buffers for max_batch * max_block rows.
+ * Enqueued on `stream`, then waits for it. Errors: EINVAL (target context,
+ * rank not a multiple of 8 in [8, 128], hidden not a multiple of 128, a NULL
+ * or misaligned pointer), ENOMEM, ECUDA. */
+dflash_status dflash_set_conv(dflash_ctx* ctx, const dflash_conv_site* sites, int rank, void* stream);
+
 /* ---- inspection hooks (used by the parity tests; they synchronise) ---- */
 
 /* Copy `n` cached tokens of layer `layer` of `seq`, starting at position
@@ -446,6 +483,7 @@ enum {
   DFLASH_K_OTHER,         /* bookkeeping kernels                        */
   DFLASH_K_SELECT,        /* path selector: top-16, pair scores, walk   */
   DFLASH_K_SAMPLE,        /* top-32 lists, filter and draw              */
+  DFLASH_K_CONV,          /* two-tap convolutions (apply kernels)       */
   DFLASH_K_COUNT
 };
 

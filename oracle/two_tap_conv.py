@@ -1,8 +1,8 @@
 """CPU oracle of the DFlash 2 two-tap dynamic convolution.
 
-TEST INFRASTRUCTURE. Only the tests may import this module. The CUDA library
-does not implement the convolution yet; when it does, it shares no code with
-this module.
+TEST INFRASTRUCTURE. Only the tests, the smoke check and the bench's CPU
+baseline leg may import this module. The CUDA library (conv.cu and the draft
+pass) shares no code, table or helper with it and never calls it.
 
 What it computes ("DFlash 2" notes, "Solution - Two-Tap Dynamic
 Convolution"): a short depthwise convolution reaching one block position back,
@@ -86,8 +86,9 @@ def draft_block_conv(weights, shape, conv_weights: Sequence[Dict[str, Dict[str, 
     if B > 1:
         logits = hf[1:] @ weights["lm_head"].T
         return {"draft": od.rows_argmax(logits), "hidden": x, "top1": np.max(logits, axis=-1),
-                "gap": od.top2_gap(logits)}
-    return {"draft": np.zeros(0, dtype=np.int64), "hidden": x, "top1": np.zeros(0), "gap": np.zeros(0)}
+                "gap": od.top2_gap(logits), "logits": logits}
+    return {"draft": np.zeros(0, dtype=np.int64), "hidden": x, "top1": np.zeros(0), "gap": np.zeros(0),
+            "logits": np.zeros((0, weights["lm_head"].shape[0]))}
 
 
 def identity_conv(H: int, r: int, dtype=np.float64) -> Dict[str, np.ndarray]:

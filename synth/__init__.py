@@ -13,6 +13,7 @@ from .generators import (  # noqa: F401
     bits_to_f32,
     make_weights_np,
     make_selector_weights_np,
+    make_conv_weights_np,
     make_weights_torch,
     torch_weights_to_np,
     make_features_np,

@@ -198,6 +198,30 @@ def make_selector_weights_np(shape: DrafterShape, seed: int = 0, dim: int = 256,
     return {k: _normal(rng, (dim, H), std) for k in ("w_a", "w_b", "w_h")}
 
 
+def make_conv_weights_np(shape: DrafterShape, rank: int = 80, seed: int = 0, corr: float = 0.2,
+                         base_jitter: float = 0.1, tap1_std: float = 0.3):
+    """Two-tap convolution weights for every layer: a list over layers of
+    dicts {"ai", "ao", "fi", "fo"} -> {"base" [2, H], "U" [2, H, r],
+    "V" [2, r, H]}, float32 arrays of bf16 values.
+
+    base tap 0 ~ 1 + N(0, base_jitter^2), tap 1 ~ N(0, tap1_std^2); U and V
+    entries N(0, s^2) with s^2 = corr / sqrt(r H), so that for inputs of unit
+    RMS the rank-r correction U V x has RMS about corr.
+    """
+    H = shape.hidden
+    s = float(np.sqrt(corr / np.sqrt(rank * H)))
+    rng = np.random.Generator(np.random.PCG64(seed))
+    layers = []
+    for _ in range(shape.n_layers):
+        sites = {}
+        for name in ("ai", "ao", "fi", "fo"):
+            base = np.stack([1.0 + rng.standard_normal(H) * base_jitter, rng.standard_normal(H) * tap1_std])
+            sites[name] = {"base": bf16_round(base.astype(np.float32)),
+                           "U": _normal(rng, (2, H, rank), s), "V": _normal(rng, (2, rank, H), s)}
+        layers.append(sites)
+    return layers
+
+
 def make_features_np(n_tokens: int, width: int, seed: int) -> np.ndarray:
     """Concatenated target features [n, L_f*H], N(0, 1) per element, bf16 values."""
     rng = np.random.Generator(np.random.PCG64(seed))
