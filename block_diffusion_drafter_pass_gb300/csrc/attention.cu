@@ -273,7 +273,7 @@ __device__ __forceinline__ float row_max(const float (&v)[N]) {
   return max3(m0, m2, max3(v[N - 2], v[N - 1], -INFINITY));
 }
 
-// 8-bit pages: two codes of an offset-binary word (code + 128 per byte),
+// 8-bit pages: two codes of a stored offset-binary word (code + 128 per byte),
 // selected by `sel`, decoded in fp16 and scaled by the fp16 pair s2. The
 // byte under an fp16 exponent of 2^10 reads as 1024 + code + 128 exactly; one
 // exact subtraction gives the code, one multiply applies the scale (rounded
@@ -289,7 +289,7 @@ __device__ __forceinline__ uint32_t q8_pair_f16(uint32_t ub, uint32_t sel, uint3
 // 16 codes (one 16-byte word) with their fp16 scales (one pair per code pair)
 // -> 8 fp16 pairs.
 __device__ __forceinline__ void q8_decode16(const uint4& cw, const uint32_t (&s2)[8], uint32_t (&o)[8]) {
-  const uint32_t w[4] = {cw.x ^ 0x80808080u, cw.y ^ 0x80808080u, cw.z ^ 0x80808080u, cw.w ^ 0x80808080u};
+  const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};   // stored offset-binary
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     o[2 * k] = q8_pair_f16(w[k], 0x4140u, s2[2 * k]);
@@ -323,6 +323,25 @@ __device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
 // loads of every task first, then decode and stores (a converter warp is
 // latency-bound, so its tasks must be independent in flight). raw and stage
 // are shared-window addresses.
+// Key task -> (key k, 16-dim group g). The eight tasks of one 16-byte access
+// phase of a warp take two keys, the first key's four groups of one 64-dim
+// box and the second key's four of the other box (d = 64: one box, the two
+// keys 64 bytes apart): their code loads cover the two halves of the banks,
+// and their swizzled stores land in distinct chunks (even and odd rows).
+template <int D>
+__device__ __forceinline__ void q8_key_task(int task, int& k, int& g) {
+  if constexpr (D == 128) {
+    const int kp = task >> 4, b = (task >> 3) & 1, w = task & 7, par = w >> 2;
+    k = 2 * kp + par;
+    g = ((b ^ par) << 2) + (w & 3);
+  } else {
+    static_assert(D == 64, "head dims 64 and 128");
+    const int kp = task >> 3, w = task & 7;
+    k = 2 * kp + (w >> 2);
+    g = w & 3;
+  }
+}
+
 template <int D, int NCT, int kKBox, int kKBytes, int kVUnit, int kUnitBox>
 __device__ __forceinline__ void q8_convert_unit(uint32_t raw, uint32_t stage, int u, int ct) {
   // keys: tasks (key k, 16-dim group g); values: tasks (dim r, 16-key group kg)
@@ -337,7 +356,8 @@ __device__ __forceinline__ void q8_convert_unit(uint32_t raw, uint32_t stage, in
   for (int j = 0; j < kIlp; ++j) {
     const int task = ct + j * NCT;
     if (j * NCT < kTK) {
-      const int k = task / (D / 16), g = task % (D / 16);
+      int k, g;
+      q8_key_task<D>(task, k, g);
       cw[j] = lds128(raw + k * D + g * 16);
       const uint32_t s1 = lds16(ksc + (k * (D / 32) + (g >> 1)) * 2);
 #pragma unroll
@@ -359,14 +379,12 @@ __device__ __forceinline__ void q8_convert_unit(uint32_t raw, uint32_t stage, in
     q8_decode16(cw[j], s2[j], o);
     const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
     if (j * NCT < kTK) {
-      const int k = task / (D / 16), g = task % (D / 16);
+      int k, g;
+      q8_key_task<D>(task, k, g);
       const int row = u * 64 + k, c0 = (g & 3) * 2;
       const uint32_t rowp = stage + (g >> 2) * kKBox + row * 128;
-      // lanes g and g + 4 of one key write the same chunks of two boxes (one
-      // bank set); opposite store orders keep each store conflict-free
-      const int flip = (g >> 2) & 1;
-      sts128(rowp + (((c0 + flip) ^ (row & 7)) << 4), flip ? hi : lo);
-      sts128(rowp + (((c0 + 1 - flip) ^ (row & 7)) << 4), flip ? lo : hi);
+      sts128(rowp + ((c0 ^ (row & 7)) << 4), lo);
+      sts128(rowp + (((c0 + 1) ^ (row & 7)) << 4), hi);
     } else {
       const int r = (task - kTK) >> 2, kg = (task - kTK) & 3;
       const int row = r & 63, c0 = kg * 2;

@@ -676,7 +676,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         // 8-bit pages: the 32 lanes of this warp are 32 consecutive values of
         // one head row (tile rows 32q .. 32q+31 of a K or V region), i.e. one
         // block per token (column). Scale d = max|x| / 127, codes round(x / d)
-        // halves away from zero, d stored as fp16 by lane c for column c.
+        // halves away from zero (stored as the byte code + 128), d stored as
+        // fp16 by lane c for column c.
         const int layer = e.layer0 + (reg >> 1), blk = di >> 5, nb = d >> 5;
         const bool is_v = (reg & 1) != 0;
         const size_t hb = q8_head_bytes(d);
@@ -695,7 +696,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
           const float dd = amax[c] / 127.f;
           float t = dd > 0.f ? xf[c] / dd : 0.f;
           t = fminf(fmaxf(truncf(t + copysignf(0.5f, t)), -127.f), 127.f);
-          qb[c] = static_cast<uint32_t>(static_cast<int>(t)) & 0xFFu;
+          qb[c] = static_cast<uint32_t>(static_cast<int>(t) + 128);   // stored offset-binary: code + 128
         }
         auto region = [&](int dst) {   // byte offset of this head's region of the token's page
           const int page = dst / (2 * e.n_kv_heads * kPage);

@@ -54,7 +54,8 @@ constexpr int kMaxBlock = 32;      // block size B
 constexpr int kMaxTargetLayers = 64;   // layers of a target context
 
 // 8-bit context pages (kv_format 1): per (layer, page, kv head) one region of
-//   [K codes: 64 slots][d] int8 | [V codes: d][64 slots] int8 (transposed)
+//   [K codes: 64 slots][d] | [V codes: d][64 slots] (transposed), each code
+//   stored as the byte code + 128 (offset binary, so the decode needs no sign fix)
 //   | [K scales: 64 slots][d/32] fp16 | [V scales: d/32][64 slots] fp16,
 // 136 d bytes, regions ordered (layer, page, kv head). A scale covers 32
 // consecutive values of one token's head row.

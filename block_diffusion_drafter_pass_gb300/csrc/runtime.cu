@@ -1593,8 +1593,10 @@ dflash_status dflash_debug_read_kv_q8(dflash_ctx* ctx, int layer, int seq, int p
       const uint16_t* vsc = reinterpret_cast<const uint16_t*>(r + q8_vscale_off(d));
       for (int di = 0; di < d; ++di) {
         const size_t o = (static_cast<size_t>(t) * nkv + h) * d + di;
-        if (k_codes) k_codes[o] = static_cast<int8_t>(r[slot * d + di]);
-        if (v_codes) v_codes[o] = static_cast<int8_t>(r[q8_vcode_off(d) + static_cast<size_t>(di) * kPage + slot]);
+        // stored offset-binary (code + 128)
+        if (k_codes) k_codes[o] = static_cast<int8_t>(static_cast<int>(r[slot * d + di]) - 128);
+        if (v_codes)
+          v_codes[o] = static_cast<int8_t>(static_cast<int>(r[q8_vcode_off(d) + static_cast<size_t>(di) * kPage + slot]) - 128);
       }
       for (int b = 0; b < nb; ++b) {
         const size_t o = (static_cast<size_t>(t) * nkv + h) * nb + b;
