@@ -45,10 +45,16 @@ namespace {
 constexpr int kKeyTile = 64;
 constexpr float kRescaleLog2 = 8.f;   // rescale O when the row max grows by more than 2^8
 constexpr int kThreads = 224;         // producer, MMA, 4 softmax warps, L2 prefetch warp
-constexpr int kConvWarps = 4;         // 8-bit pages: warps 7..10 convert the codes to fp16 tiles
-                                      // (one per SM sub-partition)
+constexpr int kConvWarps = 8;         // 8-bit pages: warps 8..15 (two warpgroups) convert the codes
+                                      // to fp16 tiles; warp 7 idles
 template <bool Q8>
-constexpr int attn_threads() { return Q8 ? kThreads + 32 * kConvWarps : kThreads; }
+constexpr int attn_threads() { return Q8 ? 256 + 32 * kConvWarps : kThreads; }
+// 8-bit pages: the block is launched at 128 registers a thread (512 threads,
+// the whole register file); warpgroups 0-1 (producer, MMA, softmax, loader)
+// raise theirs to 168 and warpgroups 2-3 (converters) drop to 88, which sum
+// to the launch's 65536.
+constexpr uint32_t kQ8RegsMain = 168, kQ8RegsConv = 88;
+static_assert(256 * kQ8RegsMain + 256 * kQ8RegsConv == 512 * 128, "register split of the 8-bit kernel");
 constexpr int kPrefetchSteps = 4;     // the prefetch warp runs this many steps ahead of the producer
 
 // Rows of the block's own key box: B rounded up to 16 or 32.
@@ -533,6 +539,53 @@ __global__ void __launch_bounds__(attn_threads<Q8>(), 1)
     latch_status(a.status, kDevTimeout);
   };
 
+  // The converter warpgroups and the rest each change their register count
+  // once, at the top of their branch (every warp of a warpgroup executes the
+  // same instruction), so each role is compiled against its own budget.
+  if (Q8 && warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kQ8RegsConv) : "memory");
+    // ---------------- 8-bit page converters ----------------
+    // Walk the producer's steps: wait for a free stage; per context unit of
+    // the step, wait for its raw slot (context units are numbered in walk
+    // order, as the raw loader issues them), decode it into the stage and free
+    // the slot; then make the stores visible to the tensor cores and arrive on
+    // the stage (the producer's arrival counts the block unit's copies).
+    const int ct = threadIdx.x - 8 * 32;
+    int q = 0, qu = 0;
+    bool dead = false;
+    for (int rk = rec_begin; rk < rec_end && !dead; rk = next_rec(rk + 1)) {
+      const Item it = decode(rk);
+      const int nctx = s_nctx[it.i];
+      for (int t0 = it.tb; t0 < it.te && !dead; t0 += 2, ++q) {
+        const int s = q % S;
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[s], ((q / S) & 1) ^ 1, &abort_flag))) {
+          give_up();
+          dead = true;
+          break;
+        }
+        const int nu = min(2, it.te - t0);
+        for (int u = 0; u < nu; ++u) {
+          if (t0 + u >= nctx) continue;
+          const int r = qu % RS;
+          if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[r], (qu / RS) & 1, &abort_flag))) {
+            give_up();
+            dead = true;
+            break;
+          }
+          q8_convert_unit<D, 32 * kConvWarps, C::kKBox, C::kKBytes, C::kVUnit, C::kUnitBox>(
+              smem_u32(raw_ring + r * C::kRawUnit), smem_u32(smem + s * C::kStageBytes), u, ct);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&raw_empty[r]);
+          ++qu;
+        }
+        if (dead) break;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_full[s]);
+      }
+    }
+  } else {
+    if constexpr (Q8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kQ8RegsMain) : "memory");
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -678,47 +731,7 @@ __global__ void __launch_bounds__(attn_threads<Q8>(), 1)
       tc_commit(&mma_done);
       mbar_wait(&mma_done, 0);
     }
-  } else if (Q8 && warp >= 7) {
-    // ---------------- 8-bit page converters ----------------
-    // Walk the producer's steps: wait for a free stage; per context unit of
-    // the step, wait for its raw slot (context units are numbered in walk
-    // order, as the raw loader issues them), decode it into the stage and free
-    // the slot; then make the stores visible to the tensor cores and arrive on
-    // the stage (the producer's arrival counts the block unit's copies).
-    const int ct = threadIdx.x - 7 * 32;
-    int q = 0, qu = 0;
-    bool dead = false;
-    for (int rk = rec_begin; rk < rec_end && !dead; rk = next_rec(rk + 1)) {
-      const Item it = decode(rk);
-      const int nctx = s_nctx[it.i];
-      for (int t0 = it.tb; t0 < it.te && !dead; t0 += 2, ++q) {
-        const int s = q % S;
-        if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[s], ((q / S) & 1) ^ 1, &abort_flag))) {
-          give_up();
-          dead = true;
-          break;
-        }
-        const int nu = min(2, it.te - t0);
-        for (int u = 0; u < nu; ++u) {
-          if (t0 + u >= nctx) continue;
-          const int r = qu % RS;
-          if (!__all_sync(0xffffffffu, mbar_wait(&raw_full[r], (qu / RS) & 1, &abort_flag))) {
-            give_up();
-            dead = true;
-            break;
-          }
-          q8_convert_unit<D, 32 * kConvWarps, C::kKBox, C::kKBytes, C::kVUnit, C::kUnitBox>(
-              smem_u32(raw_ring + r * C::kRawUnit), smem_u32(smem + s * C::kStageBytes), u, ct);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&raw_empty[r]);
-          ++qu;
-        }
-        if (dead) break;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&kv_full[s]);
-      }
-    }
+  } else if (Q8 && warp == 7) {   // idle: the converters take whole warpgroups
   } else if (Q8 && warp == 6) {
     // ---------------- 8-bit page raw loader ----------------
     // Walks the same context units in the same order and brings each raw
@@ -1008,6 +1021,7 @@ __global__ void __launch_bounds__(attn_threads<Q8>(), 1)
       if (lane == 0) mbar_arrive(&o_free);
       q += ns;
     }
+  }
   }
   tc_fence_before();
   __syncthreads();
