@@ -212,3 +212,35 @@ def test_qwen3_8b_width_q8_two_layers(dfl):
         for B in (16, 8):
             total += _draft_q8(d, orc, [0, 1], anchors, B, f"8B q8 B={B}")
         assert total > 0
+
+
+def test_q8_long_positions_262144(dfl):
+    """The longest configuration in 8-bit pages: 262144 injected tokens, one
+    key/value head of d = 128 at tiny width (the fp64 oracle holds the whole
+    cache). Every stored block of the context is checked against the format
+    and the oracle's blocks (RoPE angles up to 2.6e5 rad before quantising),
+    then drafts at B = 8, 16 and 32 over the whole quantised context: 4096
+    context units per pass through the raw loader's slots and the converter
+    warps, thousands of chunks in the combine."""
+    sh = replace(TINY, n_heads=2, n_kv_heads=1, head_dim=128)
+    wn = make_weights_np(sh, seed=461, gamma="jitter", std=0.05)
+    orc = oracle.OracleDrafter(sh, wn)
+    width = sh.n_feat_layers * sh.hidden
+    C, chunk = 262144, 32768
+    with dfl.Drafter(sh, np_weights_to_device(wn, DEV), max_seqs=1, max_batch=1, max_block=32, max_ctx=C + 64,
+                     max_fuse_tokens=chunk, kv_format=1) as d:
+        for i in range(C // chunk):
+            f = make_features_np(chunk, width, seed=462 + i)
+            d.fuse_ctx([0], [chunk], bf16_dev(f, DEV), pending=False)
+            orc.fuse_ctx([0], [chunk], f, pending=False)
+            del f
+        d.sync()
+        assert d.seq_len(0) == (C, 0)
+        assert _check_codes(d, orc, 0, [0], "C=262144") == 2 * C * 4
+        anchors = make_anchor_ids_np(1, sh.vocab, seed=470)
+        # every row: residual stream, winning logit and the near-top check;
+        # at this length the oracle's own quantisation effect on the logits
+        # puts the id-exact threshold (0.1 + twice that effect) above every
+        # row's top-1/top-2 gap, so no row is required to match bit for bit
+        for B in (8, 16, 32):
+            _draft_q8(d, orc, [0], anchors, B, f"q8 C=262144 B={B}", ROW_REL_HIGH_GAIN)
