@@ -394,30 +394,33 @@ class BlasThreads:
             self.set(int(n))
 
 
-def _oracle_cycles(orc, shape, ctx_len: int, B: int, budget_s: float, max_cycles: int = 50):
+def _oracle_cycles(orc, shape, ctx_lens, B: int, budget_s: float, max_cycles: int = 50):
     """Full speculative cycles of the oracle (argmax of the target's block
-    logits, fuse B features pending, verify, draft) over a committed context
-    of ctx_len tokens, until budget_s has passed. Inputs are drawn before the
-    timed loop."""
+    logits, fuse B features pending, verify, draft) for one sequence per
+    entry of ctx_lens, each over a committed context of that many tokens,
+    until budget_s has passed. Inputs are drawn before the timed loop."""
     import numpy as np
     import oracle
     rng = np.random.Generator(np.random.PCG64(7))
-    st = orc._state(0)
-    for l in range(shape.n_layers):   # synthetic committed context (an input, not computed)
-        st["k"][l] = rng.standard_normal((ctx_len, shape.n_kv_heads, shape.head_dim), dtype=np.float32)
-        st["v"][l] = rng.standard_normal((ctx_len, shape.n_kv_heads, shape.head_dim), dtype=np.float32)
-    st["len"], st["pend"] = ctx_len, 0
+    seqs = list(range(len(ctx_lens)))
+    for s, c in zip(seqs, ctx_lens):
+        st = orc._state(s)
+        for l in range(shape.n_layers):   # synthetic committed context (an input, not computed)
+            st["k"][l] = rng.standard_normal((c, shape.n_kv_heads, shape.head_dim), dtype=np.float32)
+            st["v"][l] = rng.standard_normal((c, shape.n_kv_heads, shape.head_dim), dtype=np.float32)
+        st["len"], st["pend"] = c, 0
     width = shape.n_feat_layers * shape.hidden
-    ring = [(rng.standard_normal((B, width), dtype=np.float32),
-             (rng.standard_normal((B, shape.vocab), dtype=np.float32) * 3)) for _ in range(2)]
-    drafts = np.zeros((1, B - 1), dtype=np.int64)
+    ns = len(seqs)
+    ring = [(rng.standard_normal((ns * B, width), dtype=np.float32),
+             (rng.standard_normal((ns, B, shape.vocab), dtype=np.float32) * 3)) for _ in range(2)]
+    drafts = np.zeros((ns, B - 1), dtype=np.int64)
     n, t0 = 0, time.perf_counter()
     while True:
         f, lg = ring[n % 2]
-        t = oracle.rows_argmax(lg)[None, :]
-        orc.fuse_ctx([0], [B], f, pending=True)
-        _, bonus = orc.verify([0], B, drafts, t)
-        drafts = orc.draft([0], bonus, B)[0]["draft"][None, :]
+        t = np.stack([oracle.rows_argmax(lg[i]) for i in range(ns)])
+        orc.fuse_ctx(seqs, [B] * ns, f, pending=True)
+        _, bonus = orc.verify(seqs, B, drafts, t)
+        drafts = np.stack([r["draft"] for r in orc.draft(seqs, bonus, B)])
         n += 1
         el = time.perf_counter() - t0
         if el > budget_s or n >= max_cycles:
@@ -425,11 +428,18 @@ def _oracle_cycles(orc, shape, ctx_len: int, B: int, budget_s: float, max_cycles
     return n, el
 
 
-def cpu_baseline(shape, weights_dev, ctx_len: int, B: int, budget_s: float = 10.0):
+def cpu_baseline(shape, weights_dev, ctx_lens, B: int, budget_s: float = 10.0, max_seqs: int = 4):
     """The oracle as it stands, timed on this host's cores on a bounded
     sample: full speculative cycles of the same drafter at the same context
-    length, once on every core (BLAS at its default thread count) and once on
-    one core (affinity to one CPU, one BLAS thread)."""
+    lengths, once on every core (BLAS at its default thread count) and once
+    on one core (affinity to one CPU, one BLAS thread). A batch of more than
+    max_seqs sequences is sampled by its first max_seqs (at their own
+    lengths) and the rate scaled by the slice's share of the batch, since a
+    pass covers every sequence of the batch."""
+    ctx_lens = [int(c) for c in ctx_lens]
+    batch = len(ctx_lens)
+    sl = ctx_lens[:max_seqs]
+    scale = len(sl) / batch
     import numpy as np
     import oracle
     from synth import torch_weights_to_np
@@ -438,20 +448,22 @@ def cpu_baseline(shape, weights_dev, ctx_len: int, B: int, budget_s: float = 10.
     blas = BlasThreads()
     threads_all = blas.threads()
     all_cpus = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
-    n, el = _oracle_cycles(orc, shape, ctx_len, B, budget_s)
-    out = {"value": n / el, "unit": UNIT, "cores": len(all_cpus) if all_cpus else os.cpu_count(),
+    n, el = _oracle_cycles(orc, shape, sl, B, budget_s)
+    ctx_txt = f"context {sl[0]}" if len(sl) == 1 else f"{len(sl)} sequences at contexts {sl}"
+    slice_txt = "" if batch == len(sl) else f"; {len(sl)} of the batch's {batch} sequences, rate scaled by {len(sl)}/{batch}"
+    out = {"value": scale * n / el, "unit": UNIT, "cores": len(all_cpus) if all_cpus else os.cpu_count(),
            "cpu_count": os.cpu_count(), "blas": blas.lib, "blas_threads": threads_all, "kind": "oracle",
            "sample": f"{n} full cycles (argmax of the target's block logits + fuse {B} features + verify + draft, "
-                     f"{shape.n_layers} layers, context {ctx_len}, fp32 numpy) in {el:.1f} s"}
+                     f"{shape.n_layers} layers, {ctx_txt}, fp32 numpy) in {el:.1f} s{slice_txt}"}
     if all_cpus and blas.set:
         one = min(all_cpus)
         try:
             os.sched_setaffinity(0, {one})
             blas.limit(1)
             orc.seqs.clear()
-            n1, el1 = _oracle_cycles(orc, shape, ctx_len, B, budget_s)
-            out["one_core"] = {"value": n1 / el1, "unit": UNIT, "cores": 1, "blas_threads": blas.threads(),
-                               "sample": f"{n1} full cycles on CPU {one} in {el1:.1f} s"}
+            n1, el1 = _oracle_cycles(orc, shape, sl, B, budget_s)
+            out["one_core"] = {"value": scale * n1 / el1, "unit": UNIT, "cores": 1, "blas_threads": blas.threads(),
+                               "sample": f"{n1} full cycles on CPU {one} in {el1:.1f} s{slice_txt}"}
         finally:
             blas.limit(threads_all)
             os.sched_setaffinity(0, all_cpus)
@@ -658,7 +670,7 @@ def run_ours(args):
     if target_cycle is not None:
         out["target_cycle"] = target_cycle
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(shape, weights, lens[0], B)
+        out["cpu_baseline"] = cpu_baseline(shape, weights, lens, B)
     return out
 
 
