@@ -9,9 +9,9 @@
 // (128 CTAs per 16 rows at hidden 4096, so a batch-1 block spreads over the
 // GPU); its slices of U and of the next site's V^T arrive by bulk copies
 // issued before the wait on the previous kernel (the pass never writes
-// weights). It forms the rank-r products U_i P_t in fp32 (P_t = V x_t, 2r
-// values per row, made before: by the GEMM that produced the site's input,
-// or by the previous apply kernel), the two-tap combination and then either
+// weights). It forms the rank-r products U_i P_t (P_t = V x_t, 2r values per
+// row, made before: by the GEMM that produced the site's input, or by the
+// previous apply kernel), the two-tap combination and then either
 //   input sites  (before a sublayer): bf16 Conv(RMSNorm(x)) -> the sublayer's
 //                GEMM input, RMSNorm(x) from the fp32 residual stream;
 //   output sites (after a sublayer):  x += Conv(y); bf16(x * g) and the row's

@@ -387,6 +387,9 @@ typedef struct {
  * sites' products come out of the O and down projections as 2 * rank extra
  * rows) and V_ai, V_fi transposed: 2 * rank * (2 * hidden + n_q * d + ffn)
  * bf16 per layer, plus row buffers for max_batch * max_block rows.
+ * While installed, each output site adds the next input site's products
+ * over its columns with float atomics, so repeated drafts agree only up to
+ * the order of those sums (the plain pass is bit-reproducible).
  * Enqueued on `stream`, then waits for it. Errors: EINVAL (target context,
  * rank not a multiple of 8 in [8, 128], hidden not a multiple of 128, a NULL
  * or misaligned pointer), ENOMEM, ECUDA. */
