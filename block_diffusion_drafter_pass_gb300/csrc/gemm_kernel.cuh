@@ -279,18 +279,39 @@ __device__ __forceinline__ void load_resid(const GemmArgs& a, const GemmEpi& e, 
   }
 }
 
-// Park a tile's partial sum: TMEM columns [0, BN) of this thread's lane to
-// dst[column * 128] (column-major, so each warp store covers 128 bytes), 32
-// columns per TMEM load.
+// Partial tiles hold column runs of four: value (column c, row r) sits at
+// float ((c / 4) * 128 + r) * 4 + c % 4 of the slot, so a row's four columns
+// are one 16-byte access and a warp's access covers 512 contiguous bytes.
+// part_row(slot, r) is row r's first run; run j is 512 floats further.
+constexpr int kPartRun = kTileN * 4;
+__device__ __forceinline__ float* part_row(float* slot, int r) { return slot + 4 * r; }
+__device__ __forceinline__ const float* part_row(const float* slot, int r) { return slot + 4 * r; }
+
+// 16 partial values of one row: columns c0 .. c0 + 15 (c0 a multiple of 4).
+__device__ __forceinline__ void part_load16(const float* row, int c0, float (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 t = __ldcg(reinterpret_cast<const float4*>(row + static_cast<size_t>((c0 >> 2) + j) * kPartRun));
+    v[4 * j] = t.x;
+    v[4 * j + 1] = t.y;
+    v[4 * j + 2] = t.z;
+    v[4 * j + 3] = t.w;
+  }
+}
+
+// Park a tile's partial sum: TMEM columns [cb, ce) of this thread's lane to
+// its row of the slot (row = part_row(slot, lane)), 16 or 32 columns per TMEM load.
 template <int BN>
-__device__ __forceinline__ void park_partial(uint32_t tb, float* dst, int cb = 0, int ce = BN) {
+__device__ __forceinline__ void park_partial(uint32_t tb, float* row, int cb = 0, int ce = BN) {
   if constexpr (BN < 32) {
 #pragma unroll
     for (int c0 = cb; c0 < ce; c0 += 16) {
       float v[16];
       tmem_ld16(tb + c0, v);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) dst[static_cast<size_t>(c0 + c) * kTileN] = v[c];
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float4*>(row + static_cast<size_t>((c0 >> 2) + j) * kPartRun) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
   } else {
 #pragma unroll 1
@@ -298,9 +319,46 @@ __device__ __forceinline__ void park_partial(uint32_t tb, float* dst, int cb = 0
       float v[32];
       tmem_ld32(tb + c0, v);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) dst[static_cast<size_t>(c0 + c) * kTileN] = v[c];
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(row + static_cast<size_t>((c0 >> 2) + j) * kPartRun) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
   }
+}
+
+// Per-lane epilogue inputs read from memory that do not depend on the
+// accumulator: the row's RMSNorm gain (RESID, NORMSRC) and its RoPE rotation
+// (the table's position 1). Read before the accumulator wait, so their
+// latency overlaps the MMAs instead of opening the epilogue.
+struct EpiPre {
+  float gain;
+  float2 rot;
+};
+
+template <int EC>
+__device__ __forceinline__ EpiPre epi_pre(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int tile, int r) {
+  EpiPre p;
+  p.gain = 0.f;
+  p.rot = make_float2(1.f, 0.f);
+  const int kind = class_kind<EC>(e.kind);
+  const int tn = tile / a.m_tiles;
+  if (kind == EPI_RESID || kind == EPI_NORMSRC) {
+    const int n = tn * kTileN + r;
+    if (n < a.N) p.gain = bf16_to_f32(e.gain[n]);
+  } else if (kind == EPI_QKV_ROPE || kind == EPI_KV_APPEND) {
+    int reg = 0, rf = r;
+    if (!rg.paired) {
+      reg = region_of(rg, tn);
+      rf = (tn - rg.tile_begin[reg]) * kTileN + r;
+    }
+    const bool rope = kind == EPI_QKV_ROPE ? reg < 2 : (reg & 1) == 0;
+    if (rope) {
+      const int d = e.head_dim > 0 ? e.head_dim : 1, half = d >> 1;
+      const int di = rf % d;
+      p.rot = e.rope[half + ((r & rg.pair) == 0 ? di : di - half)];
+    }
+  }
+  return p;
 }
 
 // Drain one finished tile from TMEM (plus the other workers' partial tiles)
@@ -315,9 +373,9 @@ __device__ __forceinline__ void park_partial(uint32_t tb, float* dst, int cb = 0
 template <int BN, int EC, int G = 1>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions& rg, const GemmEpi& e, int g,
                                               int tile, int first, int last, uint32_t tb, int r, EpiShared& sh,
-                                              float* stg, uint32_t pre, const float (&rpre)[16], int cbeg,
-                                              int cend, const float* speer, long long tile_u0, int cstep = 1,
-                                              int cbase = 0, int grp = 0) {
+                                              float* stg, uint32_t pre, const float (&rpre)[16], const EpiPre& pp,
+                                              int cbeg, int cend, const float* speer, long long tile_u0,
+                                              int cstep = 1, int cbase = 0, int grp = 0) {
   const int kind = class_kind<EC>(e.kind);
   const int q = r >> 5, lane = r & 31;
   const int tn = tile / a.m_tiles, tm = tile - tn * a.m_tiles;
@@ -341,7 +399,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   if (kind == EPI_QKV_ROPE) rope = reg < 2;
   if (kind == EPI_KV_APPEND) rope = (reg & 1) == 0;
   const int fi = lo ? di : di - half;           // RoPE frequency index of the pair
-  const float gain = (kind == EPI_RESID || kind == EPI_NORMSRC) && n < a.N ? bf16_to_f32(e.gain[n]) : 0.f;
+  const float gain = pp.gain;
 
   // Other CTAs holding partial sums of this tile. A one-chunk tile reads up
   // to kRound of them in one round of loads; wider tiles read one a chunk
@@ -353,7 +411,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   const bool first_in_slot1 = unit_begin(first, a) < tile_u0;
   auto partial_src = [&](int o) {
     const int side = (o == first && first_in_slot1) ? 1 : 0;
-    return a.partial + (static_cast<size_t>(o * cstep + cbase) * 2 + side) * slot_elems + r;
+    return part_row(a.partial + (static_cast<size_t>(o * cstep + cbase) * 2 + side) * slot_elems, r);
   };
   // wider tiles: the first kAhead other pieces, in CTA order, are read one
   // chunk ahead, all in one round of loads (256-token tiles: two, the most a
@@ -370,8 +428,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
   auto partial_load = [&](int c0, float (&p0)[kAhead][16]) {
 #pragma unroll
     for (int k = 0; k < kAhead; ++k) {
+      if (psrc[k]) {
+        part_load16(psrc[k], c0, p0[k]);
+      } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) p0[k][c] = psrc[k] ? __ldcg(psrc[k] + static_cast<size_t>(c0 + c) * kTileN) : 0.f;
+        for (int c = 0; c < 16; ++c) p0[k][c] = 0.f;
+      }
     }
   };
   // RoPE: when a chunk's 16 positions are consecutive (one sequence's block),
@@ -395,7 +457,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
       load_resid(a, e, m0, cbeg + 16, n, rb);
     }
   }
-  if (rope) rot = e.rope[half + fi];
+  if (rope) rot = pp.rot;
   float pc0[kAhead][16];
   if constexpr (BN > 16) {
     if (n_oth) partial_load(cbeg, pc0);
@@ -433,9 +495,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
 #pragma unroll
       for (int k = 0; k < kRound; ++k) {
         const int o = first + k + (first + k >= g ? 1 : 0);
-        const float* src = o <= last ? partial_src(o) : nullptr;
+        if (o <= last) {
+          part_load16(partial_src(o), 0, pv[k]);
+        } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pv[k][c] = src ? __ldcg(src + static_cast<size_t>(c) * kTileN) : 0.f;
+          for (int c = 0; c < 16; ++c) pv[k][c] = 0.f;
+        }
       }
       float sum[16];
 #pragma unroll
@@ -470,9 +535,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
             }
           }
         } else {
-          const float* src = partial_src(o);
+          float pv[16];
+          part_load16(partial_src(o), c0, pv);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) sum[c] += __ldcg(src + static_cast<size_t>(c0 + c) * kTileN);
+          for (int c = 0; c < 16; ++c) sum[c] += pv[c];
         }
       }
 #pragma unroll
@@ -1013,6 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cbeg = a.csplit ? (g & 1) * (BN / 2) : 0;
       const int cend = a.csplit ? cbeg + BN / 2 : BN;
       tile_cols_prepare<BN, EC>(a, e, m0, r, esh);
+      const EpiPre pp = epi_pre<EC>(a, rg, e, t, r);
       float rpre[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) rpre[c] = 0.f;
@@ -1086,7 +1153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (!whole) {
         // park this segment's partial sum in the CTA's slot, then take a ticket
         const int side = (u == u0) ? 0 : 1;
-        park_partial<BN>(tb, a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems + r);
+        park_partial<BN>(tb, part_row(a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems, r));
         first = cta_of(static_cast<long long>(t) * kb, a);
         last = cta_of(static_cast<long long>(t + 1) * kb - 1, a);
         __threadfence();
@@ -1101,7 +1168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (finish) __threadfence();
       }
       if (finish) {
-        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre, rpre, cbeg, cend, speer,
+        epilogue_tile<BN, EC>(a, rg, e, g, t, first, last, tb, r, esh, stg, pre, rpre, pp, cbeg, cend, speer,
                               static_cast<long long>(t) * kb);
         if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, (a.csplit ? 2 : 1) * a.n_tiles * a.m_tiles);
       }
@@ -1380,6 +1447,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const int t = tn * a.m_tiles + tm;   // this CTA's tile
       const int buf = j & 1;
       tile_cols_prepare<BN, EC>(a, e, tm * BN, r, esh, gcb, gce, grp);
+      const EpiPre pp = epi_pre<EC>(a, rg, e, t, r);
       float rpre[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) rpre[c] = 0.f;
@@ -1455,7 +1523,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           if (!finish) {
             // park this segment's partial sum in the CTA's slot, then take a ticket
             const int side = (seg_u == su0) ? 0 : 1;
-            park_partial<BN>(tb, a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems + r, gcb, gce);
+            park_partial<BN>(tb, part_row(a.partial + (static_cast<size_t>(g) * 2 + side) * slot_elems, r), gcb, gce);
             first = cta_of(tu0, a);
             last = cta_of(tu0 + kb - 1, a);
             __threadfence();
@@ -1471,14 +1539,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           }
         }
         if (finish) {
-          epilogue_tile<BN, EC, kEpiGroups>(a, rg, e, pair, t, first, last, tb, r, esh, gstg, 0u, rpre, gcb, gce,
+          epilogue_tile<BN, EC, kEpiGroups>(a, rg, e, pair, t, first, last, tb, r, esh, gstg, 0u, rpre, pp, gcb, gce,
                                             nullptr, tu0, 2, static_cast<int>(member), grp);
           if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, kEpiGroups * a.n_tiles * a.m_tiles, grp);
         }
       } else {
         // a pair's second weight tile past N (odd tile count) has no rows to store
         if (tn < a.n_tiles)
-          epilogue_tile<BN, EC, kEpiGroups>(a, rg, e, g, t, g, g, tb, r, esh, gstg, pre, rpre, gcb, gce, speer,
+          epilogue_tile<BN, EC, kEpiGroups>(a, rg, e, g, t, g, g, tb, r, esh, gstg, pre, rpre, pp, gcb, gce, speer,
                                             static_cast<long long>(t) * kb, 1, 0, grp);
         if constexpr (EC == kEcArgmax) argmax_tile_done(a, e, esh, r, kEpiGroups * KS * 2 * pair_tiles, grp);
       }
