@@ -1045,18 +1045,21 @@ template <int D, int NC>
 __global__ void __launch_bounds__(32 * kCombineWarps) attn_combine_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int kPer = D / 32;                 // dims per lane: 4 (D = 128) or 2 (D = 64)
   static_assert(NC >= 1 && NC <= 32, "one chunk per lane at most");
-  grid_dep_wait();
-  grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.x, i = blockIdx.y;
   const int j = blockIdx.z * kCombineWarps + warp;
   const int B = a.meta.B;
   const int nkv = a.n_kv_heads, G = a.n_q_heads / nkv;
   const int kvh = hq / G, gh = hq - kvh * G;
+  // The lengths are final before any kernel of the pass starts (as for the
+  // attention kernel's pages), so the row's chunk base is read before the
+  // wait; the partials, written by the attention kernel, after it.
   int base = 0;
   for (int s = 0; s < i; ++s) base += nkv * seq_split(a, s).n_chunks;
   const int nch = seq_split(a, i).n_chunks;
   base += kvh * nch;
+  grid_dep_wait();
+  grid_dep_launch();
   if (j >= B || base + nch > a.items_cap) {
     if (j < B && lane == 0) latch_status(a.status, kDevBounds);
     return;

@@ -28,7 +28,13 @@ DEV = "cuda:0"
     (256, 16, 256, 1),        # one tile
     (384, 5, 1024, 0),        # ragged tokens, automatic split-K
     (100, 33, 200, 0),        # ragged everything, K not a multiple of 64
-    (4096, 16, 4096, 0),      # batch-1 weight streaming shape
+    (4096, 16, 4096, 0),      # batch-1 weight streaming shape (O): stream-K over all SMs
+    (6144, 16, 4096, 0),      # batch-1 QKV shape
+    (4096, 5, 4096, 0),       # the same with a ragged token tile
+    (4256, 16, 4096, 0),      # a ragged last weight tile (34 tiles)
+    (2048, 16, 1000, 0),      # 16 k-blocks, the last one ragged
+    (2048, 16, 1088, 0),      # 17 k-blocks: pieces of uneven length
+    (4096, 16, 12288, 0),     # batch-1 down shape
     (1024, 300, 512, 1),      # two 256-token tiles with a ragged tail
     (640, 64, 2048, 3),       # explicit split-K
     (256, 128, 128, 2),
