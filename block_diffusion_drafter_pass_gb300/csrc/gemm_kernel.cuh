@@ -361,6 +361,30 @@ __device__ __forceinline__ EpiPre epi_pre(const GemmArgs& a, const ARegions& rg,
   return p;
 }
 
+// Stores one 16-token chunk of bf16 rows whose 128 tile rows are contiguous
+// features of each token's output row (q / k rows, the keys of a page slot):
+// each thread puts its row's 16 values into a free 128 x 16 staging buffer
+// (token-major), and after a barrier writes 32 contiguous bytes of one
+// token, so a warp writes four tokens' 256-byte runs instead of sixteen
+// 64-byte pieces. dst(token) is the token's first output element for tile
+// row 0 (rows of one head stay within 16-row segments), or null to skip it.
+// Ends with a barrier, so the buffer can be reused.
+template <typename Dst>
+__device__ __forceinline__ void store_chunk_transposed(const uint16_t (&ov)[16], int r, float* buf, int grp, Dst dst) {
+  uint16_t* t = reinterpret_cast<uint16_t*>(buf);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) t[c * 128 + r] = ov[c];
+  epi_bar(grp);
+  const int c = r >> 3, seg = (r & 7) * 16;
+  uint16_t* p = dst(c, seg);
+  if (p) {
+    const uint4* src = reinterpret_cast<const uint4*>(t + c * 128 + seg);
+    reinterpret_cast<uint4*>(p)[0] = src[0];
+    reinterpret_cast<uint4*>(p)[1] = src[1];
+  }
+  epi_bar(grp);
+}
+
 // Drain one finished tile from TMEM (plus the other workers' partial tiles)
 // and run the epilogue. r = TMEM lane of this thread (0..127). g, first and
 // last are stream-K workers; worker w's partial slots belong to CTA
@@ -699,13 +723,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
       // value computed, before the chunk's first global store: loads placed
       // after a store would wait for it.
       int posv[16], dstv[16];
-      bool allpos = true;
+      bool allpos = true, alldst = true;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         posv[c] = sh.row_pos[c0 + c];
         dstv[c] = kind == EPI_KV_APPEND ? sh.row_dst[c0 + c] : 0;
         allpos = allpos && posv[c] >= 0;
+        alldst = alldst && dstv[c] >= 0;
       }
+      // staging buffer free in this chunk: the other chunk parity's (its
+      // readers all passed the previous chunk's closing barrier), or the
+      // group's own one after its exchange reads
+      float* tbuf = G == 1 ? stg + (buf ^ 1) * (128 * 17) : sb;
       bool run = rope && posv[0] >= 0;   // all 16 positions consecutive
 #pragma unroll
       for (int c = 1; c < 16; ++c) run = run && posv[c] == posv[0] + c;
@@ -853,12 +882,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const ARegions&
         }
       } else if (kind == EPI_QKV_ROPE && reg != 2 && allpos && m0 + c0 + 16 <= a.M) {   // whole chunk of q or k
         const size_t ld = static_cast<size_t>(reg == 0 ? e.n_q_heads : e.n_kv_heads) * d;
-        uint16_t* p = (reg == 0 ? e.out_q : e.out_k) + static_cast<size_t>(m0 + c0) * ld + rf;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          *p = ov[c];
-          p += ld;
-        }
+        uint16_t* p0 = (reg == 0 ? e.out_q : e.out_k) + static_cast<size_t>(m0 + c0) * ld + (rf - f);
+        store_chunk_transposed(ov, r, tbuf, grp, [&](int c, int seg) { return p0 + static_cast<size_t>(c) * ld + seg; });
+      } else if (kind == EPI_KV_APPEND && !(reg & 1) && alldst) {   // keys of 16 tokens: [slot][d] rows of pages
+        const int layer = e.layer0 + (reg >> 1), rf0 = rf - f;
+        store_chunk_transposed(ov, r, tbuf, grp, [&](int c, int seg) -> uint16_t* {
+          const int dst = sh.row_dst[c0 + c], slot = dst & (kPage - 1);
+          const int hk = (rf0 + seg) / d, dk = rf0 + seg - hk * d;
+          const size_t lp = (static_cast<size_t>(layer) * e.pool_pages * 2 * e.n_kv_heads * kPage +
+                             static_cast<size_t>(dst - slot)) * d;
+          return e.pool + lp + (static_cast<size_t>(hk) * kPage + slot) * d + dk;
+        });
       } else
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
