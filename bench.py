@@ -239,9 +239,14 @@ class Cycle:
         del logits
         self.targets = torch.empty(batch, B, dtype=torch.int32, device=dev)
         self.sampling = None
-        self.drafts = torch.empty(batch, B - 1, dtype=torch.int32, device=dev)
-        self.tau = torch.empty(batch, dtype=torch.int32, device=dev)
-        self.bonus = torch.randint(0, shape.vocab - 1, (batch,), generator=g, device=dev, dtype=torch.int32)
+        # the step's results (drafts, tau, bonus) in one buffer, as a caller
+        # that reads them back each step would keep them: one copy per step
+        nd = batch * (B - 1)
+        self.results = torch.empty(nd + 2 * batch, dtype=torch.int32, device=dev)
+        self.drafts = self.results[:nd].view(batch, B - 1)
+        self.tau = self.results[nd:nd + batch]
+        self.bonus = self.results[nd + batch:]
+        self.bonus.copy_(torch.randint(0, shape.vocab - 1, (batch,), generator=g, device=dev, dtype=torch.int32))
         torch.cuda.synchronize()
         # first block so that step 0 has drafts to verify
         self.d.draft(self.seqs, self.bonus, B, out=self.drafts)
@@ -322,9 +327,7 @@ class Cycle:
         if k + 1 < host["steps"]:
             self._copy_inputs(k + 1, host)
         self._verify_and_draft(k % self.ring)
-        host["drafts"].copy_(self.drafts, non_blocking=True)
-        host["tau"].copy_(self.tau, non_blocking=True)
-        host["bonus"].copy_(self.bonus, non_blocking=True)
+        host["results"].copy_(self.results, non_blocking=True)   # drafts, tau and bonus
 
     def _copy_inputs(self, k: int, host) -> None:
         torch = self.torch
@@ -529,9 +532,7 @@ def run_ours(args):
         "ring": ring,
         "feats": cyc.feats[:ring].cpu().pin_memory(),
         "logits": cyc.logits[:ring].cpu().pin_memory(),
-        "drafts": torch.empty_like(cyc.drafts, device="cpu").pin_memory(),
-        "tau": torch.empty_like(cyc.tau, device="cpu").pin_memory(),
-        "bonus": torch.empty_like(cyc.bonus, device="cpu").pin_memory(),
+        "results": torch.empty_like(cyc.results, device="cpu").pin_memory(),
         "stream": torch.cuda.Stream(),
         "copied": [torch.cuda.Event(), torch.cuda.Event()],
         "consumed": [torch.cuda.Event(), torch.cuda.Event()],
@@ -540,7 +541,7 @@ def run_ours(args):
     ms_e2e = timed(lambda k: cyc.step_e2e(k, host), K, world, dev)
     e2e_value = whole_job_rate(K, world, reduce_max(ms_e2e, world, dev))
     h2d = host["feats"][0].numel() * 2 + host["logits"][0].numel() * 2
-    d2h = (host["drafts"].numel() + host["tau"].numel() + host["bonus"].numel()) * 4
+    d2h = host["results"].numel() * 4
     # the drafter pass alone (anchor + B-1 masks through all layers and the LM head)
     kd = min(K, 200)
     ms_draft = timed(lambda k: cyc.d.draft(cyc.seqs, cyc.bonus, B, out=cyc.drafts), kd, world, dev)
